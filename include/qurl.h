@@ -1,0 +1,193 @@
+/*
+ * qurl.h -- C ABI of libqurl, the W8A8 linear layer of QuRL's quantized
+ * rollout actor on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: Paper-Notes ICLR2026, "QuRL: Efficient Reinforcement
+ * Learning with Quantized Rollout":
+ *   [UAQ]   section "方法详解 > 关键设计 > 更新感知量化 (UAQ)": W X = (W/s)(sX);
+ *           s is applied column-wise to W and row-wise to the preceding
+ *           activation, and can be folded into the preceding norm gain.
+ *   [LOSS]  section "损失函数 / 训练策略": per-channel (output channel) weight
+ *           quantization and per-token activation quantization, INT8 or FP8;
+ *           UAQ factor s = 1.5.
+ *   [SYS]   section "系统集成与工程实现": UAQ is a one-time preprocessing of
+ *           the weights; the rollout runs INT8/FP8 matrix-multiply kernels.
+ *   [FRAME] section "方法详解 > 整体框架": every RL step quantizes the current
+ *           weights theta_old for the rollout.
+ *
+ * Conventions (all entry points):
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *     allocates no device memory on any of these calls and keeps no pointer
+ *     after a call returns.
+ *   - Row-major layouts.  M = tokens, K = in-features, N = out-features.
+ *     X: [M, K] bf16 with row stride ldx (elements).  W / Wq: [N, K] (the
+ *     torch Linear layout, K contiguous).  Y: [M, N] bf16 with row stride ldy.
+ *     Codes (Xq, Wq) are one byte each: int8 two's complement (QURL_INT8) or
+ *     OCP FP8 E4M3 "e4m3fn" (QURL_FP8_E4M3), densely packed with stride K.
+ *     Scales (sx [M], sw [N]) are fp32.
+ *   - Quantization is symmetric absmax per row: scale = absmax / qmax (IEEE
+ *     fp32 division, qmax = 127 for INT8, 448 for FP8), code = v / scale
+ *     (IEEE division) rounded to nearest even and clamped to [-127, 127]
+ *     (INT8) or converted with round-to-nearest-even and saturation to
+ *     +-448 (FP8).  An all-zero row has scale 1 and zero codes.  NaN inputs
+ *     are outside the domain.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and may be captured in a CUDA graph.  They validate
+ *     their arguments on the host BEFORE any launch and return QURL_OK or an
+ *     error code; nothing is launched when an error is returned.  They never
+ *     throw and never abort.
+ *   - Device-side failures (a bounded wait inside a kernel that ran out, ~1 s)
+ *     are latched in a per-device status word; qurl_check_device_status()
+ *     synchronises the stream and returns (and clears) it.
+ *   - Alignment: every pointer passed as a tensor must be 16-byte aligned and
+ *     every row stride must be a multiple of 16 bytes; K must be a multiple
+ *     of 16.  Violations return QURL_ERR_ALIGNMENT / QURL_ERR_UNSUPPORTED.
+ *   - Sizes: M, N, K in [1, 2^31); M*K, N*K, M*N below 2^40.
+ */
+#ifndef QURL_H_
+#define QURL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QURL_OK = 0,
+    QURL_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, unknown enum, bad stride */
+    QURL_ERR_UNSUPPORTED = 2, /* shape the kernels do not cover (e.g. K % 16 != 0) */
+    QURL_ERR_ALIGNMENT = 3,   /* pointer or row stride not 16-byte aligned */
+    QURL_ERR_WORKSPACE = 4,   /* reserved */
+    QURL_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed */
+    QURL_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out */
+} qurl_status;
+
+typedef enum { QURL_INT8 = 0, QURL_FP8_E4M3 = 1 } qurl_qtype;
+typedef enum { QURL_BF16 = 0, QURL_FP32 = 1 } qurl_ftype;
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* qurl_stream_t;
+
+/*
+ * UAQ weight preparation + per-output-channel weight quantization
+ * ([UAQ], [LOSS], [SYS], [FRAME]).
+ *
+ *   W'[n,k]     = W[n,k] / s          (IEEE fp32 division; the same scalar s
+ *                                      on every input column)
+ *   gamma'[k]   = gamma[k] * s        (the preceding RMSNorm gain, fp32)
+ *   sw[n]       = max_k |W'[n,k]| / qmax
+ *   Wq[n,k]     = quantize(W'[n,k] / sw[n])
+ *
+ * Called once with s = 1.5 at set-up (the fold), then every RL step with the
+ * trained W' and s = 1 (re-quantization of the current weights).
+ *
+ *   W            [N, K] bf16 or fp32 (w_type), row stride ldw elements.
+ *   gamma        [K] fp32 or NULL (no norm to fold into).
+ *   s            > 0, finite.
+ *   Wq           [N, K] codes (out).        sw [N] fp32 (out).
+ *   gamma_folded [K] fp32 (out) or NULL; required when gamma is given.
+ *   W_scaled     [N, K] fp32 (out) or NULL: W', the new training master.
+ *                May alias W when w_type == QURL_FP32 and ldw == K.
+ */
+qurl_status qurl_prepare_weights(const void* W, qurl_ftype w_type, int N, int K, int ldw, const float* gamma,
+                                 float s, qurl_qtype qt, void* Wq, float* sw, float* gamma_folded,
+                                 float* W_scaled, qurl_stream_t stream);
+
+/*
+ * Per-token dynamic activation quantization ([LOSS]).
+ *   v[m,k] = fp32(X[m,k]) * pre_scale;  sx[m] = max_k |v| / qmax;
+ *   Xq[m,k] = quantize(v[m,k] / sx[m]).
+ * pre_scale carries the UAQ factor s into an activation that has no norm to
+ * fold it into ([UAQ]: "row-wise on the preceding activation"); pass 1.0f
+ * otherwise.  X [M, K] bf16 with row stride ldx; Xq [M, K] (stride K); sx [M].
+ */
+qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale, qurl_qtype qt, void* Xq,
+                           float* sx, qurl_stream_t stream);
+
+/*
+ * RMSNorm with the folded gain gamma' = gamma * s, then per-token quantization
+ * ([UAQ] fold into the norm, [LOSS]).
+ *   ms[m] = (sum_k x^2) / K (fp32, the kernel's own reduction order);
+ *   r = 1 / sqrt(ms + eps) (correctly rounded fp32 sqrt and division);
+ *   v[m,k] = (x * r) * gamma'[k] (two fp32 products); then as qurl_quant_act.
+ * ms_out [M] fp32 or NULL receives ms (lets a checker reproduce the codes).
+ */
+qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float* gamma_folded, float eps,
+                               qurl_qtype qt, void* Xq, float* sx, float* ms_out, qurl_stream_t stream);
+
+/*
+ * SiLU(gate) * up, then per-token quantization: the MLP activation between
+ * the fused gate_up and the down projection.  GU [M, 2I] bf16, row stride
+ * ldgu; columns [0, I) are the gate g, [I, 2I) the up projection u.
+ *   h = (g / (1 + exp(-g))) * u (fp32);  v = h * pre_scale;  quantize rows.
+ * Xq [M, I] (stride I), sx [M]; h_out [M, I] fp32 or NULL receives h.
+ * I must be a multiple of 16.
+ */
+qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pre_scale, qurl_qtype qt,
+                                void* Xq, float* sx, float* h_out, qurl_stream_t stream);
+
+/*
+ * Bytes of workspace qurl_w8a8_linear / qurl_w8a8_gemm_acc /
+ * qurl_rmsnorm_quant_linear use for this shape at full speed (split-K
+ * partial sums).  A smaller workspace (or none) is accepted: the kernels then
+ * split K into fewer parts.
+ */
+size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
+
+/*
+ * The W8A8 linear layer ([SYS], [LOSS]):
+ *   acc[m,n] = sum_k Xq[m,k] * Wq[n,k]   (INT8: exact int32; FP8: fp32)
+ *   Y[m,n]   = bf16_RNE( (fp32(acc) * sx[m]) * sw[n] )
+ * Xq [M, K], Wq [N, K] codes; sx [M], sw [N] fp32; Y [M, N] bf16, row stride
+ * ldy.  workspace: device scratch of ws_bytes (may be NULL / 0).
+ * INT8 runs on the fp16 tensor path with integer-exact partial sums (see the
+ * design notes); its int32 accumulator and bf16 Y are exact.
+ */
+qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N,
+                             int K, qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
+                             qurl_stream_t stream);
+
+/*
+ * The raw accumulator of the 8-bit GEMM, acc [M, N] (stride N): int32 for
+ * INT8 (exact), fp32 for FP8.  For checking the GEMM on its own.
+ */
+qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int K, qurl_qtype qt, void* acc,
+                               void* workspace, size_t ws_bytes, qurl_stream_t stream);
+
+/*
+ * Fused entry: RMSNorm(gamma') -> per-token quantization -> W8A8 linear
+ * ([UAQ]: s lives in gamma', so Y = W (RMSNorm_gamma(X)) up to quantization).
+ * Xq_scratch [M, K] codes and sx_scratch [M] fp32 are caller-provided
+ * intermediate buffers (they hold the quantized activation afterwards).
+ */
+qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma_folded, float eps,
+                                      const void* Wq, const float* sw, int M, int N, int K, qurl_qtype qt,
+                                      void* Y, int ldy, void* Xq_scratch, float* sx_scratch, void* workspace,
+                                      size_t ws_bytes, qurl_stream_t stream);
+
+/*
+ * Weight-update probe ([UAQ]: the quantization error shrinks by s while the
+ * update grows by s): *count (device, uint64) = number of byte positions where
+ * the code buffers a and b (n bytes each) differ.  *count is overwritten.
+ */
+qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,
+                            qurl_stream_t stream);
+
+/* Synchronise `stream`, then return and clear the device status word of the
+ * current device (QURL_OK, or QURL_ERR_TIMEOUT from a kernel's bounded wait),
+ * or QURL_ERR_CUDA if the synchronisation itself failed. */
+qurl_status qurl_check_device_status(qurl_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* qurl_status_string(qurl_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+int qurl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QURL_H_ */

@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point the
+public header declares, and rejects bad arguments on the host before any launch
+(no compute call is made here)."""
+import ctypes
+import re
+
+import pytest
+
+import w8a8_precision_gemm_gb300 as q
+from w8a8_precision_gemm_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return q.load()
+
+
+def test_header_declares_the_boundary():
+    names = q.exported_names()
+    for required in ("qurl_prepare_weights", "qurl_quant_act", "qurl_w8a8_linear", "qurl_rmsnorm_quant_linear",
+                     "qurl_rmsnorm_quant", "qurl_silu_mul_quant", "qurl_w8a8_gemm_acc", "qurl_count_diff",
+                     "qurl_workspace_size", "qurl_check_device_status", "qurl_status_string", "qurl_version"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in q.exported_names():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_header_entry_points_are_extern_c():
+    text = open(q.HEADER).read()
+    assert 'extern "C"' in text
+    # no torch / C++ types in the declarations (comments stripped)
+    code = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    assert not re.search(r"\b(torch|at::|std::|Tensor)\b", code)
+
+
+def test_status_strings_and_version(L):
+    assert L.qurl_status_string(0) == b"QURL_OK"
+    assert L.qurl_status_string(6) == b"QURL_ERR_TIMEOUT"
+    assert L.qurl_status_string(99) == b"QURL_ERR_UNKNOWN"
+    assert L.qurl_version() == 100
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced: calls fail validation first
+FAKE_ODD = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+
+
+def test_quant_act_validation(L):
+    assert L.qurl_quant_act(None, 4, 256, 256, 1.0, 0, FAKE, FAKE, None) == 1       # null X
+    assert L.qurl_quant_act(FAKE, 0, 256, 256, 1.0, 0, FAKE, FAKE, None) == 1       # M = 0
+    assert L.qurl_quant_act(FAKE, 4, 256, 128, 1.0, 0, FAKE, FAKE, None) == 1       # ldx < K
+    assert L.qurl_quant_act(FAKE, 4, 250, 256, 1.0, 0, FAKE, FAKE, None) == 2       # K % 16
+    assert L.qurl_quant_act(FAKE_ODD, 4, 256, 256, 1.0, 0, FAKE, FAKE, None) == 3   # alignment
+    assert L.qurl_quant_act(FAKE, 4, 256, 260, 1.0, 0, FAKE, FAKE, None) == 3       # row stride not 16 B
+    assert L.qurl_quant_act(FAKE, 4, 256, 256, 1.0, 7, FAKE, FAKE, None) == 1       # bad qtype
+    assert L.qurl_quant_act(FAKE, 4, 256, 256, float("nan"), 0, FAKE, FAKE, None) == 1
+
+
+def test_linear_validation(L):
+    f = L.qurl_w8a8_linear
+    assert f(None, FAKE, FAKE, FAKE, 4, 8, 256, 0, FAKE, 8, None, 0, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 250, 0, FAKE, 8, None, 0, None) == 2
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 0, FAKE, 4, None, 0, None) == 1     # ldy < N
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 0, FAKE_ODD, 8, None, 0, None) == 3
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 0, FAKE, 12, None, 0, None) == 3    # ldy * 2 % 16
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 0, FAKE, 8, None, 64, None) == 1    # ws bytes without ws
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 2, FAKE, 8, None, 0, None) == 1     # bad qtype
+    assert L.qurl_w8a8_gemm_acc(FAKE, FAKE, 4, 8, 256, 0, None, None, 0, None) == 1
+
+
+def test_prepare_weights_validation(L):
+    f = L.qurl_prepare_weights
+    assert f(FAKE, 0, 8, 256, 256, None, 0.0, 0, FAKE, FAKE, None, None, None) == 1     # s = 0
+    assert f(FAKE, 0, 8, 256, 256, None, float("inf"), 0, FAKE, FAKE, None, None, None) == 1
+    assert f(FAKE, 0, 8, 256, 256, FAKE, 1.5, 0, FAKE, FAKE, None, None, None) == 1     # gamma without out
+    assert f(FAKE, 3, 8, 256, 256, None, 1.5, 0, FAKE, FAKE, None, None, None) == 1     # bad w_type
+    assert f(FAKE, 0, 8, 248, 248, None, 1.5, 0, FAKE, FAKE, None, None, None) == 2     # K % 16
+    assert f(FAKE, 0, 8, 256, 260, None, 1.5, 0, FAKE, FAKE, None, None, None) == 3     # bf16 ldw
+    # W' may alias W only for a dense fp32 W
+    assert f(FAKE, 0, 8, 256, 256, None, 1.5, 0, FAKE, FAKE, None, FAKE, None) == 1
+
+
+def test_other_validation(L):
+    assert L.qurl_silu_mul_quant(FAKE, 4, 100, 200, 1.0, 0, FAKE, FAKE, None, None) == 2   # I % 16
+    assert L.qurl_silu_mul_quant(FAKE, 4, 128, 200, 1.0, 0, FAKE, FAKE, None, None) == 1   # ld < 2I
+    assert L.qurl_rmsnorm_quant(FAKE, 4, 256, 256, None, 1e-6, 0, FAKE, FAKE, None, None) == 1
+    assert L.qurl_rmsnorm_quant(FAKE, 4, 256, 256, FAKE, -1.0, 0, FAKE, FAKE, None, None) == 1
+    assert L.qurl_count_diff(FAKE, None, 16, FAKE, None) == 1
+    assert L.qurl_count_diff(FAKE_ODD, FAKE, 16, FAKE, None) == 3
+    assert L.qurl_rmsnorm_quant_linear(FAKE, 256, FAKE, 1e-6, FAKE, FAKE, 4, 8, 256, 0, FAKE, 8, FAKE, None,
+                                       None, 0, None) == 1
+
+
+def test_workspace_size_without_gpu(L):
+    # sized for the SM count of the device (or the largest target when none is visible)
+    assert L.qurl_workspace_size(0, 8, 256, 0) == 0
+    ws = L.qurl_workspace_size(64, 4608, 3584, 1)
+    assert ws % (64 * 4608 * 4) == 0
+    assert L.qurl_workspace_size(8192, 55296, 5120, 1) == 0  # prefill fills the GPU without splitting K

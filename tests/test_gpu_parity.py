@@ -1,0 +1,375 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: quantized codes and scales (activation, weight, RMSNorm and SiLU
+quantizers), INT8 int32 accumulators and INT8 bf16 outputs, flip counts.
+FP8: fp32 accumulators within an accumulation-error bound, bf16 outputs within
+max-abs-rel 1e-2 (the accumulation order differs from the exact fp64 oracle).
+
+Sizes: small cases the oracle runs in seconds that still span several tiles,
+K-splits and ragged tails; the full projection shapes of the 7B- and 32B-class
+models in the launch configuration the benchmark uses, checked on a seeded
+sample of output rows / channels.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_precision_gemm_gb300 as q
+from w8a8_precision_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+NT = os.cpu_count() or 1
+QTS = [q.INT8, q.FP8_E4M3]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    q.load()
+    yield
+    q.qurl_check_device_status()
+
+
+def oqt(qt):
+    return oracle.INT8 if qt == q.INT8 else oracle.FP8_E4M3
+
+
+def codes(t):
+    return t.contiguous().cpu().view(torch.uint8).numpy()
+
+
+def f32(t):
+    return t.cpu().numpy()
+
+
+def bits(t):
+    return synth.bf16_bits(t.cpu())
+
+
+def max_abs_rel(y, ref):
+    y = y.astype(np.float64)
+    ref = ref.astype(np.float64)
+    return float(np.abs(y - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def sync_ok():
+    torch.cuda.synchronize()
+    q.qurl_check_device_status()
+
+
+# ------------------------------------------------------------------ quantizers
+
+ACT_SHAPES = [(16, 256), (1, 16), (17, 3584), (129, 5120), (3, 18944), (64, 27648), (2, 70000)]
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M,K", ACT_SHAPES)
+def test_quant_act_exact(qt, M, K):
+    X = synth.activations(f"gpu/act/{M}/{K}", M, K)
+    X[0, : K // 2] = 0  # a half-zero row
+    if M > 2:
+        X[2] = 0  # an all-zero row: scale 1, codes 0
+    for pre in (1.0, 1.5):
+        Xq, sx = q.quant_act(X.cuda(), qt, pre_scale=pre)
+        sync_ok()
+        qo, so = oracle.quant_act(bits(X), oqt(qt), pre_scale=pre)
+        np.testing.assert_array_equal(codes(Xq), qo)
+        np.testing.assert_array_equal(f32(sx), so)
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_quant_act_strided_rows(qt):
+    """The o_proj input is a column slice of the qkv output (row stride 4608)."""
+    big = synth.activations("gpu/act/strided", 37, 4608)
+    X = big[:, :3584]
+    Xq, sx = q.quant_act(big.cuda()[:, :3584], qt, pre_scale=1.5)
+    sync_ok()
+    qo, so = oracle.quant_act(bits(X.contiguous()), oqt(qt), pre_scale=1.5)
+    np.testing.assert_array_equal(codes(Xq), qo)
+    np.testing.assert_array_equal(f32(sx), so)
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M,K", [(16, 256), (33, 3584), (7, 5120), (4, 70000)])
+def test_rmsnorm_quant(qt, M, K):
+    X = synth.activations(f"gpu/rms/{M}/{K}", M, K)
+    g = synth.gamma(f"gpu/rms/g/{K}", K) * 1.5
+    Xq, sx, ms = q.rmsnorm_quant(X.cuda(), g.cuda(), qt, eps=1e-6, want_ms=True)
+    sync_ok()
+    ms_d = f32(ms)
+    ms_o = oracle.rms_ms(bits(X))
+    np.testing.assert_allclose(ms_d, ms_o, rtol=2e-6)
+    # codes and scales are exact given the kernel's mean of squares
+    qo, so, _, _ = oracle.rmsnorm_quant(bits(X), g.numpy(), oqt(qt), eps=1e-6, ms_given=ms_d)
+    np.testing.assert_array_equal(codes(Xq), qo)
+    np.testing.assert_array_equal(f32(sx), so)
+    # rows where the kernel's fp32 ms equals the oracle's own are exact with no input from the kernel
+    q2, s2, ms2, _ = oracle.rmsnorm_quant(bits(X), g.numpy(), oqt(qt), eps=1e-6)
+    same = ms2 == ms_d
+    assert same.mean() > 0.3
+    np.testing.assert_array_equal(codes(Xq)[same], q2[same])
+    np.testing.assert_array_equal(f32(sx)[same], s2[same])
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M,I", [(16, 256), (9, 18944), (3, 4096)])
+def test_silu_mul_quant(qt, M, I):
+    GU = synth.activations(f"gpu/silu/{M}/{I}", M, 2 * I, outlier_gain=4.0)
+    GU[0, :4] = torch.tensor([0.0, -90.0, 60.0, -3.0])
+    Xq, sx, h = q.silu_mul_quant(GU.cuda(), qt, pre_scale=1.5, want_h=True)
+    sync_ok()
+    _, _, ho = oracle.silu_mul_quant(bits(GU), oqt(qt), pre_scale=1.5)
+    hd = f32(h)
+    np.testing.assert_allclose(hd, ho, rtol=2e-6, atol=1e-35)
+    qo, so, _ = oracle.silu_mul_quant(bits(GU), oqt(qt), pre_scale=1.5, h_given=hd)
+    np.testing.assert_array_equal(codes(Xq), qo)
+    np.testing.assert_array_equal(f32(sx), so)
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("wtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("N,K", [(512, 256), (136, 3584), (3, 27648), (5, 70000)])
+def test_prepare_weights_exact(qt, wtype, N, K):
+    W = synth.weights(f"gpu/w/{N}/{K}", N, K)
+    W[1, :] = 0  # an all-zero output channel
+    g = synth.gamma(f"gpu/w/g/{K}", K)
+    Wi = W if wtype == "fp32" else W.to(torch.bfloat16)
+    for s in (1.5, 1.0):
+        Wq, sw, gf, Ws = q.prepare_weights(Wi.cuda(), qt, s=s, gamma=g.cuda())
+        sync_ok()
+        Wo, swo, gfo, Wso = oracle.prepare_weights(Wi.float().numpy(), oqt(qt), s=s, gamma=g.numpy())
+        np.testing.assert_array_equal(codes(Wq), Wo)
+        np.testing.assert_array_equal(f32(sw), swo)
+        np.testing.assert_array_equal(f32(gf), gfo)
+        np.testing.assert_array_equal(f32(Ws), Wso)
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_prepare_weights_in_place_master(qt):
+    """W' may overwrite the fp32 master in place (the per-step re-quantization
+    writes nothing new, but the set-up fold replaces W by W/s)."""
+    W = synth.weights("gpu/w/inplace", 64, 3584)
+    Wd = W.cuda()
+    Wq = torch.empty((64, 3584), dtype=q.code_dtype(qt), device="cuda")
+    sw = torch.empty(64, dtype=torch.float32, device="cuda")
+    q.qurl_prepare_weights(Wd, None, 1.5, qt, Wq, sw, None, Wd)
+    sync_ok()
+    Wo, swo, _, Wso = oracle.prepare_weights(W.numpy(), oqt(qt), s=1.5)
+    np.testing.assert_array_equal(codes(Wq), Wo)
+    np.testing.assert_array_equal(f32(Wd), Wso)
+
+
+# ------------------------------------------------------------------ GEMM
+
+GEMM_SHAPES = [
+    (16, 512, 256),     # the tiny layer
+    (1, 136, 16),       # a single token, one k-block, ragged channel tile
+    (17, 520, 4096),    # ragged tokens and channels, several INT8 chunks
+    (64, 4608, 3584),   # 7B qkv decode: split-K
+    (200, 1000, 1024),  # swap with two INT8 token tiles, ragged
+    (300, 520, 2048),   # prefill orientation, ragged
+    (129, 384, 1040),   # K not a multiple of the k-block (zero-filled tail)
+    (512, 768, 3072),   # prefill, several tiles each way
+]
+
+
+def random_codes(qt, shape, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    if qt == q.INT8:
+        return g.integers(-127, 128, size=shape).astype(np.int8).view(np.uint8)
+    # codes of Gaussian values: the magnitudes a quantized layer sees
+    v = g.standard_normal(shape).astype(np.float32) * np.float32(100.0)
+    return oracle.e4m3_encode(np.clip(v, -448, 448))
+
+
+def to_dev(codes_u8, qt):
+    t = torch.from_numpy(np.ascontiguousarray(codes_u8)).cuda()
+    return t.view(q.code_dtype(qt))
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("with_ws", [True, False])
+def test_gemm_acc_int8_exact(M, N, K, with_ws):
+    xq = random_codes(q.INT8, (M, K), M * 7 + K)
+    wq = random_codes(q.INT8, (N, K), N * 13 + K)
+    ws = q.workspace(M, N, K, q.INT8) if with_ws else None
+    acc = q.gemm_acc(to_dev(xq, q.INT8), to_dev(wq, q.INT8), q.INT8, ws)
+    sync_ok()
+    ref = oracle.gemm_i8(xq, wq, nthreads=NT)
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+
+
+def test_gemm_int8_worst_case_magnitude():
+    """|acc| = 127^2 * 27648 = 445,934,592: far beyond fp32's 2^24 exact range,
+    exact only through the chunked int32 accumulation."""
+    K = 27648
+    xq = np.full((3, K), 127, np.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127
+    wq = np.full((256, K), 127, np.int8)
+    wq[1::2] = -127
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
+                     q.workspace(3, 256, K, q.INT8))
+    sync_ok()
+    a = acc.cpu().numpy()
+    assert a[0, 0] == 445_934_592 and a[0, 1] == -445_934_592 and a[1, 0] == -445_934_592
+    assert a[2, 0] == 0
+    np.testing.assert_array_equal(a, oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT))
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_acc_fp8(M, N, K):
+    xq = random_codes(q.FP8_E4M3, (M, K), M * 7 + K)
+    wq = random_codes(q.FP8_E4M3, (N, K), N * 13 + K)
+    acc = q.gemm_acc(to_dev(xq, q.FP8_E4M3), to_dev(wq, q.FP8_E4M3), q.FP8_E4M3, q.workspace(M, N, K, q.FP8_E4M3))
+    sync_ok()
+    ref = oracle.gemm_fp8(xq, wq, nthreads=NT)
+    absref = oracle.gemm_fp8(xq & np.uint8(0x7F), wq & np.uint8(0x7F), nthreads=NT)  # sum_k |x w|, exact
+    err = np.abs(acc.cpu().numpy().astype(np.float64) - ref)
+    # fp32 accumulation: a few units of 2^-24 per term at worst, bounded by K
+    bound = absref * (K * 2.0 ** -23) + 1e-30
+    assert np.all(err <= bound), float((err / bound).max())
+    assert float((err / (absref + 1e-30)).max()) < 1e-4
+
+
+def _layer(qt, M, N, K, tag, s=1.0):
+    """Oracle-quantized inputs of one projection (oracle computes every input)."""
+    X = synth.activations(f"{tag}/X", M, K)
+    W = synth.weights(f"{tag}/W", N, K)
+    Xq, sx = oracle.quant_act(bits(X), oqt(qt))
+    Wq, sw, _, _ = oracle.prepare_weights(W.numpy(), oqt(qt), s=s)
+    return Xq, sx, Wq, sw
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_linear(qt, M, N, K):
+    Xq, sx, Wq, sw = _layer(qt, M, N, K, f"gpu/lin/{M}/{N}/{K}")
+    Y = q.linear(to_dev(Xq, qt), torch.from_numpy(sx).cuda(), to_dev(Wq, qt), torch.from_numpy(sw).cuda(), qt,
+                 q.workspace(M, N, K, qt))
+    sync_ok()
+    Yo, _ = oracle.w8a8_linear(Xq, sx, Wq, sw, oqt(qt), nthreads=NT)
+    yd = bits(Y)
+    if qt == q.INT8:
+        np.testing.assert_array_equal(yd, Yo)
+    else:
+        assert max_abs_rel(oracle.bf16_decode(yd), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_linear_output_row_stride(qt):
+    """Y written into a wider buffer (row stride > N) leaves the gap untouched."""
+    M, N, K = 40, 264, 512
+    Xq, sx, Wq, sw = _layer(qt, M, N, K, "gpu/lin/ldy")
+    Ybig = torch.full((M, N + 24), 7.0, dtype=torch.bfloat16, device="cuda")
+    Y = Ybig[:, :N]
+    q.qurl_w8a8_linear(to_dev(Xq, qt), torch.from_numpy(sx).cuda(), to_dev(Wq, qt), torch.from_numpy(sw).cuda(),
+                       qt, Y, q.workspace(M, N, K, qt))
+    sync_ok()
+    Yo, _ = oracle.w8a8_linear(Xq, sx, Wq, sw, oqt(qt), nthreads=NT)
+    assert torch.all(Ybig[:, N:] == 7.0)
+    if qt == q.INT8:
+        np.testing.assert_array_equal(bits(Y.contiguous()), Yo)
+    else:
+        assert max_abs_rel(oracle.bf16_decode(bits(Y.contiguous())), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_fused_rmsnorm_quant_linear(qt):
+    M, N, K = 48, 4608, 3584
+    X = synth.activations("gpu/fused/X", M, K)
+    W = synth.weights("gpu/fused/W", N, K)
+    g = synth.gamma("gpu/fused/g", K)
+    Wq, sw, gf, _ = q.prepare_weights(W.cuda(), qt, s=1.5, gamma=g.cuda())
+    Xd = X.cuda()
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Xqs = torch.empty((M, K), dtype=q.code_dtype(qt), device="cuda")
+    sxs = torch.empty(M, dtype=torch.float32, device="cuda")
+    q.qurl_rmsnorm_quant_linear(Xd, gf, 1e-6, Wq, sw, qt, Y, Xqs, sxs, q.workspace(M, N, K, qt))
+    # the same steps as separate calls give the same bits
+    Xq2, sx2, ms = q.rmsnorm_quant(Xd, gf, qt, eps=1e-6, want_ms=True)
+    Y2 = q.linear(Xq2, sx2, Wq, sw, qt, q.workspace(M, N, K, qt))
+    sync_ok()
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    # against the oracle: UAQ-folded weights and gain, layer output within 1e-2
+    Wo, swo, gfo, _ = oracle.prepare_weights(W.numpy(), oqt(qt), s=1.5, gamma=g.numpy())
+    qo, so, _, _ = oracle.rmsnorm_quant(bits(X), gfo, oqt(qt), eps=1e-6)
+    Yo, _ = oracle.w8a8_linear(qo, so, Wo, swo, oqt(qt), nthreads=NT)
+    assert max_abs_rel(oracle.bf16_decode(bits(Y)), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+# ------------------------------------------------------------------ full-size projections (sampled)
+
+FULL = [
+    # (model, proj, M, qtype): the 7B decode set is the benchmark workload
+    ("7b", "qkv", 64, q.INT8), ("7b", "gate_up", 64, q.INT8), ("7b", "down", 64, q.INT8),
+    ("7b", "qkv", 256, q.INT8), ("7b", "o_proj", 256, q.INT8), ("7b", "gate_up", 256, q.INT8),
+    ("7b", "down", 256, q.INT8),
+    ("7b", "gate_up", 256, q.FP8_E4M3), ("7b", "down", 64, q.FP8_E4M3), ("7b", "qkv", 4096, q.FP8_E4M3),
+    ("32b", "gate_up", 1024, q.INT8), ("32b", "down", 256, q.FP8_E4M3), ("32b", "o_proj", 8192, q.FP8_E4M3),
+    ("32b", "qkv", 8192, q.INT8),
+]
+
+
+@pytest.mark.parametrize("model,proj,M,qt", FULL)
+def test_full_size_projection_sampled(model, proj, M, qt):
+    K, N = (synth.SHAPES_7B if model == "7b" else synth.SHAPES_32B)[proj]
+    tag = f"gpu/full/{model}/{proj}/{M}"
+    X = synth.activations(f"{tag}/X", M, K)
+    W = synth.weights(f"{tag}/W", N, K)
+    Wq, sw, _, _ = q.prepare_weights(W.cuda(), qt, s=1.5, keep_scaled=False)
+    Xq, sx = q.quant_act(X.cuda(), qt)
+    Y = q.linear(Xq, sx, Wq, sw, qt, q.workspace(M, N, K, qt))
+    sync_ok()
+    g = np.random.Generator(np.random.PCG64(M * 31 + N))
+    rows = np.sort(g.choice(M, size=min(M, 96), replace=False))
+    cols = np.sort(g.choice(N, size=160, replace=False))
+    # oracle inputs from the oracle: the sampled weight rows and token rows
+    Wo, swo, _, _ = oracle.prepare_weights(W.numpy()[cols], oqt(qt), s=1.5)
+    Xo, sxo = oracle.quant_act(bits(X[rows]), oqt(qt))
+    np.testing.assert_array_equal(codes(Wq)[cols], Wo)  # the GPU inputs equal the oracle's
+    np.testing.assert_array_equal(codes(Xq)[rows], Xo)
+    Yo, _ = oracle.w8a8_linear(Xo, sxo, Wo, swo, oqt(qt), nthreads=NT)
+    yd = bits(Y)[np.ix_(rows, cols)]
+    if qt == q.INT8:
+        np.testing.assert_array_equal(yd, Yo)
+    else:
+        assert max_abs_rel(oracle.bf16_decode(yd), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+# ------------------------------------------------------------------ flip probe
+
+@pytest.mark.parametrize("n", [16, 100_003, 1 << 22])
+def test_count_diff_exact(n):
+    g = np.random.Generator(np.random.PCG64(n))
+    a = g.integers(0, 256, size=n, dtype=np.uint8)
+    b = a.copy()
+    idx = g.choice(n, size=max(1, n // 97), replace=False)
+    b[idx] ^= np.uint8(0x41)
+    c = q.count_diff(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    sync_ok()
+    assert int(c.item()) == oracle.count_diff(a, b) == len(idx)
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_flip_probe_matches_oracle(qt):
+    """Re-quantize W' and W' + dW' on the GPU and count flipped codes: the count
+    equals the oracle's, and UAQ (s = 1.5) flips more codes than s = 1."""
+    N, K = 1024, 3584
+    W = synth.weights("gpu/flip/W", N, K)
+    dW = synth.update("gpu/flip/dW", N, K)
+    counts = {}
+    for s in (1.0, 1.5):
+        Wq0, _, _, Ws = q.prepare_weights(W.cuda(), qt, s=s)
+        Ws1 = Ws + float(s) * dW.cuda()  # SGD view: the update lands in W' space scaled by s
+        Wq1, _, _, _ = q.prepare_weights(Ws1, qt, s=1.0, keep_scaled=False)
+        c = int(q.count_diff(Wq0, Wq1).item())
+        sync_ok()
+        a0, _, _, Wso = oracle.prepare_weights(W.numpy(), oqt(qt), s=s)
+        a1, _, _, _ = oracle.prepare_weights(Wso + np.float32(s) * dW.numpy(), oqt(qt), s=1.0)
+        assert c == oracle.count_diff(a0, a1)
+        counts[s] = c
+    assert counts[1.5] > 1.5 * counts[1.0]

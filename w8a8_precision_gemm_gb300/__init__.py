@@ -1,0 +1,258 @@
+"""W8A8 linear layer of QuRL's quantized rollout actor on one GB300 (sm_103a).
+
+A thin binding over the C ABI of ``libqurl.so`` (``include/qurl.h``).  Every
+function named ``qurl_*`` has the C entry point's name and arguments, with
+torch tensors in place of device pointers; it only marshals arguments -- every
+step of the computation runs in the library's CUDA kernels.  The convenience
+helpers at the bottom allocate outputs with torch and call those functions.
+
+There is no CPU fallback: if the CUDA library has not been built, or no CUDA
+device is present, the calls raise.
+
+Method: Paper-Notes ICLR2026, "QuRL: Efficient Reinforcement Learning with
+Quantized Rollout" -- UAQ invariant scaling W X = (W/s)(sX) with s folded into
+the preceding norm gain (section "更新感知量化 (UAQ)"), per-channel weight and
+per-token activation INT8 / FP8 quantization, s = 1.5 (section "损失函数 /
+训练策略"), INT8/FP8 matmul in the rollout (section "系统集成与工程实现").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import _build
+
+INT8 = 0
+FP8_E4M3 = 1
+BF16 = 0
+FP32 = 1
+
+STATUS = {0: "QURL_OK", 1: "QURL_ERR_INVALID_ARG", 2: "QURL_ERR_UNSUPPORTED", 3: "QURL_ERR_ALIGNMENT",
+          4: "QURL_ERR_WORKSPACE", 5: "QURL_ERR_CUDA", 6: "QURL_ERR_TIMEOUT"}
+
+HEADER = os.path.join(_build.ROOT, "include", "qurl.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QurlError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def exported_names() -> list[str]:
+    """Entry points declared in include/qurl.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(qurl_[a-z0-9_]+)\s*\(", text)))
+
+
+def load() -> ctypes.CDLL:
+    """Load libqurl.so (built by ``_build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is not built; run `python -m w8a8_precision_gemm_gb300._build` "
+                               "(or __graft_entry__.build()) first -- this package has no CPU fallback")
+        L = ctypes.CDLL(_build.LIB)
+        P, i, f, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "qurl_prepare_weights": [P, i, i, i, i, P, f, i, P, P, P, P, P],
+            "qurl_quant_act": [P, i, i, i, f, i, P, P, P],
+            "qurl_rmsnorm_quant": [P, i, i, i, P, f, i, P, P, P, P],
+            "qurl_silu_mul_quant": [P, i, i, i, f, i, P, P, P, P],
+            "qurl_w8a8_linear": [P, P, P, P, i, i, i, i, P, i, P, z, P],
+            "qurl_w8a8_gemm_acc": [P, P, i, i, i, i, P, P, z, P],
+            "qurl_rmsnorm_quant_linear": [P, i, P, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
+            "qurl_count_diff": [P, P, z, P, P],
+            "qurl_check_device_status": [P],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.qurl_workspace_size.argtypes = [i, i, i, i]
+        L.qurl_workspace_size.restype = ctypes.c_size_t
+        L.qurl_status_string.argtypes = [ctypes.c_int]
+        L.qurl_status_string.restype = ctypes.c_char_p
+        L.qurl_version.argtypes = []
+        L.qurl_version.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libqurl takes device tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ok(rc: int, where: str):
+    if rc != 0:
+        raise QurlError(rc, where)
+
+
+def _ld(t) -> int:
+    return t.stride(0)
+
+
+# ---------------------------------------------------------------- the C ABI, by name
+
+def qurl_prepare_weights(W, gamma, s, qt, Wq, sw, gamma_folded=None, W_scaled=None, stream=None):
+    wt = FP32 if W.dtype == torch.float32 else BF16
+    N, K = W.shape
+    _ok(load().qurl_prepare_weights(_ptr(W), wt, N, K, _ld(W), _ptr(gamma), float(s), qt, _ptr(Wq), _ptr(sw),
+                                    _ptr(gamma_folded), _ptr(W_scaled), _stream(stream)), "qurl_prepare_weights")
+
+
+def qurl_quant_act(X, pre_scale, qt, Xq, sx, stream=None):
+    M, K = X.shape
+    _ok(load().qurl_quant_act(_ptr(X), M, K, _ld(X), float(pre_scale), qt, _ptr(Xq), _ptr(sx), _stream(stream)),
+        "qurl_quant_act")
+
+
+def qurl_rmsnorm_quant(X, gamma_folded, eps, qt, Xq, sx, ms_out=None, stream=None):
+    M, K = X.shape
+    _ok(load().qurl_rmsnorm_quant(_ptr(X), M, K, _ld(X), _ptr(gamma_folded), float(eps), qt, _ptr(Xq), _ptr(sx),
+                                  _ptr(ms_out), _stream(stream)), "qurl_rmsnorm_quant")
+
+
+def qurl_silu_mul_quant(GU, pre_scale, qt, Xq, sx, h_out=None, stream=None):
+    M, I2 = GU.shape
+    _ok(load().qurl_silu_mul_quant(_ptr(GU), M, I2 // 2, _ld(GU), float(pre_scale), qt, _ptr(Xq), _ptr(sx),
+                                   _ptr(h_out), _stream(stream)), "qurl_silu_mul_quant")
+
+
+def qurl_workspace_size(M, N, K, qt) -> int:
+    return int(load().qurl_workspace_size(M, N, K, qt))
+
+
+def qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, workspace=None, stream=None):
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(load().qurl_w8a8_linear(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), M, N, K, qt, _ptr(Y), _ld(Y),
+                                _ptr(workspace), ws_bytes, _stream(stream)), "qurl_w8a8_linear")
+
+
+def qurl_w8a8_gemm_acc(Xq, Wq, qt, acc, workspace=None, stream=None):
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(load().qurl_w8a8_gemm_acc(_ptr(Xq), _ptr(Wq), M, N, K, qt, _ptr(acc), _ptr(workspace), ws_bytes,
+                                  _stream(stream)), "qurl_w8a8_gemm_acc")
+
+
+def qurl_rmsnorm_quant_linear(X, gamma_folded, eps, Wq, sw, qt, Y, Xq_scratch, sx_scratch, workspace=None,
+                              stream=None):
+    M, K = X.shape
+    N = Wq.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(load().qurl_rmsnorm_quant_linear(_ptr(X), _ld(X), _ptr(gamma_folded), float(eps), _ptr(Wq), _ptr(sw), M, N,
+                                         K, qt, _ptr(Y), _ld(Y), _ptr(Xq_scratch), _ptr(sx_scratch),
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "qurl_rmsnorm_quant_linear")
+
+
+def qurl_count_diff(a, b, count, stream=None):
+    n = a.numel() * a.element_size()
+    assert b.numel() * b.element_size() == n
+    _ok(load().qurl_count_diff(_ptr(a), _ptr(b), n, _ptr(count), _stream(stream)), "qurl_count_diff")
+
+
+def qurl_check_device_status(stream=None):
+    _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
+
+
+def qurl_status_string(s: int) -> str:
+    return load().qurl_status_string(s).decode()
+
+
+def qurl_version() -> int:
+    return int(load().qurl_version())
+
+
+# ---------------------------------------------------------------- allocating helpers
+
+def code_dtype(qt):
+    return torch.int8 if qt == INT8 else torch.float8_e4m3fn
+
+
+def prepare_weights(W, qt, s=1.5, gamma=None, keep_scaled=True, stream=None):
+    """UAQ fold + per-channel quantization.  Returns (Wq, sw, gamma', W')."""
+    N, K = W.shape
+    dev = W.device
+    Wq = torch.empty((N, K), dtype=code_dtype(qt), device=dev)
+    sw = torch.empty(N, dtype=torch.float32, device=dev)
+    gf = None if gamma is None else torch.empty(K, dtype=torch.float32, device=dev)
+    Ws = torch.empty((N, K), dtype=torch.float32, device=dev) if keep_scaled else None
+    qurl_prepare_weights(W, gamma, s, qt, Wq, sw, gf, Ws, stream)
+    return Wq, sw, gf, Ws
+
+
+def quant_act(X, qt, pre_scale=1.0, stream=None):
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=code_dtype(qt), device=X.device)
+    sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    qurl_quant_act(X, pre_scale, qt, Xq, sx, stream)
+    return Xq, sx
+
+
+def rmsnorm_quant(X, gamma_folded, qt, eps=1e-6, want_ms=False, stream=None):
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=code_dtype(qt), device=X.device)
+    sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    ms = torch.empty(M, dtype=torch.float32, device=X.device) if want_ms else None
+    qurl_rmsnorm_quant(X, gamma_folded, eps, qt, Xq, sx, ms, stream)
+    return (Xq, sx, ms) if want_ms else (Xq, sx)
+
+
+def silu_mul_quant(GU, qt, pre_scale=1.0, want_h=False, stream=None):
+    M, I2 = GU.shape
+    Xq = torch.empty((M, I2 // 2), dtype=code_dtype(qt), device=GU.device)
+    sx = torch.empty(M, dtype=torch.float32, device=GU.device)
+    h = torch.empty((M, I2 // 2), dtype=torch.float32, device=GU.device) if want_h else None
+    qurl_silu_mul_quant(GU, pre_scale, qt, Xq, sx, h, stream)
+    return (Xq, sx, h) if want_h else (Xq, sx)
+
+
+def workspace(M, N, K, qt, device="cuda"):
+    nbytes = qurl_workspace_size(M, N, K, qt)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
+
+
+def linear(Xq, sx, Wq, sw, qt, ws=None, stream=None):
+    M, N = Xq.shape[0], Wq.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, ws, stream)
+    return Y
+
+
+def gemm_acc(Xq, Wq, qt, ws=None, stream=None):
+    M, N = Xq.shape[0], Wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32 if qt == INT8 else torch.float32, device=Xq.device)
+    qurl_w8a8_gemm_acc(Xq, Wq, qt, acc, ws, stream)
+    return acc
+
+
+def count_diff(a, b, stream=None) -> torch.Tensor:
+    c = torch.empty(1, dtype=torch.int64, device=a.device)
+    qurl_count_diff(a, b, c, stream)
+    return c

@@ -1,0 +1,366 @@
+// api.cu -- the C ABI of libqurl (include/qurl.h): host-side validation,
+// per-device state (SM count, status word), TMA tensor maps, and dispatch to
+// the kernels.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "qurl.h"
+
+namespace {
+
+// Per-device status word: kernels latch a bounded-wait timeout here.
+__device__ int g_qurl_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of g_qurl_status on that device
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+
+qurl_status cuda_fail(cudaError_t e) {
+  (void)e;
+  cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  return QURL_ERR_CUDA;
+}
+
+// State of the current device, initialised on first use.
+qurl_status device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return QURL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_qurl_status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    d.ready = true;
+  }
+  *out = &d;
+  return QURL_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  long long rows, cols, ld;
+  int box_cols, box_rows, swizzle;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_cols == o.box_cols &&
+           box_rows == o.box_rows && swizzle == o.swizzle;
+  }
+};
+
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used = false;
+};
+
+constexpr int kMapCache = 128;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+// 2-D map over a row-major byte matrix [rows, cols] with row pitch ld bytes;
+// boxes of box_rows x box_cols bytes; out-of-range rows/columns read as 0.
+qurl_status byte_map(const void* ptr, long long rows, long long cols, long long ld, int box_cols, int box_rows,
+                     bool swizzle128, CUtensorMap* out) {
+  const MapKey key{ptr, rows, cols, ld, box_cols, box_rows, swizzle128 ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& e : g_maps)
+      if (e.used && e.key == key) {
+        *out = e.map;
+        return QURL_OK;
+      }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return QURL_ERR_CUDA;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return QURL_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    MapEntry& e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.key = key;
+    e.map = m;
+    e.used = true;
+  }
+  *out = m;
+  return QURL_OK;
+}
+
+// ------------------------------------------------------------------ validation
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_qt(int qt) { return qt == QURL_INT8 || qt == QURL_FP8_E4M3; }
+bool valid_dim(int x) { return x > 0; }
+
+// X-like bf16 activation [M, K] with row stride ld (elements).
+qurl_status check_act(const void* X, int M, int K, int ld) {
+  if (!X) return QURL_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_dim(K) || ld < K) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(X) || (static_cast<long long>(ld) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
+  return QURL_OK;
+}
+
+qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int qt, const void* ws, size_t ws_bytes) {
+  if (!Xq || !Wq) return QURL_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt)) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(Xq) || !aligned16(Wq)) return QURL_ERR_ALIGNMENT;
+  if (ws_bytes > 0 && !ws) return QURL_ERR_INVALID_ARG;
+  if (ws && !aligned16(ws)) return QURL_ERR_ALIGNMENT;
+  return QURL_OK;
+}
+
+#define QURL_TRY(expr)                    \
+  do {                                    \
+    const qurl_status _s = (expr);        \
+    if (_s != QURL_OK) return _s;         \
+  } while (0)
+
+#define QURL_CUDA(expr)                   \
+  do {                                    \
+    const cudaError_t _e = (expr);        \
+    if (_e != cudaSuccess) return cuda_fail(_e); \
+  } while (0)
+
+// Run the GEMM; mode bf16 -> Y, otherwise raw accumulators -> acc_out.
+qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
+                     void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
+  const bool int8 = (qt == QURL_INT8);
+  const long long a_rows = p.swap ? N : M;
+  const long long b_rows = p.swap ? M : N;
+  const void* a_ptr = p.swap ? Wq : Xq;
+  const void* b_ptr = p.swap ? Xq : Wq;
+  CUtensorMap ta, tb;
+  QURL_TRY(byte_map(a_ptr, a_rows, K, K, p.bk, 128, !int8, &ta));
+  QURL_TRY(byte_map(b_ptr, b_rows, K, K, p.bk, p.bn, !int8, &tb));
+  qurl::GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_kb = p.num_kb;
+  a.kb_per_split = p.kb_per_split;
+  a.sx = sx;
+  a.sw = sw;
+  a.Y = reinterpret_cast<__nv_bfloat16*>(Y);
+  a.ldy = ldy;
+  a.status = dev->status;
+  const bool split = p.splits > 1;
+  if (Y && !split) {
+    a.mode = qurl::kModeBf16;
+  } else {
+    a.mode = qurl::kModeAcc;
+    a.part = split ? ws : acc_out;
+  }
+  const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
+  QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
+                 : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
+  if (split)
+    QURL_CUDA(qurl::launch_splitk_reduce(qt, ws, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
+                                         dev->num_sms, st));
+  return QURL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qurl_status_string(qurl_status s) {
+  switch (s) {
+    case QURL_OK: return "QURL_OK";
+    case QURL_ERR_INVALID_ARG: return "QURL_ERR_INVALID_ARG";
+    case QURL_ERR_UNSUPPORTED: return "QURL_ERR_UNSUPPORTED";
+    case QURL_ERR_ALIGNMENT: return "QURL_ERR_ALIGNMENT";
+    case QURL_ERR_WORKSPACE: return "QURL_ERR_WORKSPACE";
+    case QURL_ERR_CUDA: return "QURL_ERR_CUDA";
+    case QURL_ERR_TIMEOUT: return "QURL_ERR_TIMEOUT";
+  }
+  return "QURL_ERR_UNKNOWN";
+}
+
+int qurl_version(void) { return 100; }
+
+qurl_status qurl_prepare_weights(const void* W, qurl_ftype w_type, int N, int K, int ldw, const float* gamma,
+                                 float s, qurl_qtype qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
+                                 qurl_stream_t stream) {
+  if (!W || !Wq || !sw) return QURL_ERR_INVALID_ARG;
+  if (w_type != QURL_BF16 && w_type != QURL_FP32) return QURL_ERR_INVALID_ARG;
+  if (!valid_dim(N) || !valid_dim(K) || ldw < K || !valid_qt(qt)) return QURL_ERR_INVALID_ARG;
+  if (!(s > 0.0f) || !std::isfinite(s)) return QURL_ERR_INVALID_ARG;
+  if (gamma && !gamma_folded) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  const int esize = (w_type == QURL_FP32) ? 4 : 2;
+  if (!aligned16(W) || (static_cast<long long>(ldw) * esize) % 16 != 0 || !aligned16(Wq) ||
+      (W_scaled && !aligned16(W_scaled)))
+    return QURL_ERR_ALIGNMENT;
+  if (W_scaled && reinterpret_cast<const void*>(W_scaled) == W && !(w_type == QURL_FP32 && ldw == K))
+    return QURL_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  (void)dev;
+  QURL_CUDA(qurl::launch_prepare_weights(W, w_type == QURL_FP32, N, K, ldw, gamma, s, qt, Wq, sw, gamma_folded,
+                                         W_scaled, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale, qurl_qtype qt, void* Xq,
+                           float* sx, qurl_stream_t stream) {
+  QURL_TRY(check_act(X, M, K, ldx));
+  if (!Xq || !sx || !valid_qt(qt) || !std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Xq)) return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float* gamma_folded, float eps,
+                               qurl_qtype qt, void* Xq, float* sx, float* ms_out, qurl_stream_t stream) {
+  QURL_TRY(check_act(X, M, K, ldx));
+  if (!gamma_folded || !Xq || !sx || !valid_qt(qt) || !(eps >= 0.0f) || !std::isfinite(eps))
+    return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Xq) || !aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pre_scale, qurl_qtype qt, void* Xq,
+                                float* sx, float* h_out, qurl_stream_t stream) {
+  if (!GU || !Xq || !sx || !valid_qt(qt) || !std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_dim(I) || ldgu < 2LL * I) return QURL_ERR_INVALID_ARG;
+  if (I % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0 || !aligned16(Xq) ||
+      (h_out && !aligned16(h_out)))
+    return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt) {
+  if (!valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt)) return 0;
+  int sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 160;  // no device visible: size for the largest SM count this library targets
+  }
+  return qurl::plan_gemm(M, N, K, qt, sms, static_cast<size_t>(-1)).ws_bytes;
+}
+
+qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K,
+                             qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
+                             qurl_stream_t stream) {
+  QURL_TRY(check_gemm(Xq, Wq, M, N, K, qt, workspace, ws_bytes));
+  if (!sx || !sw || !Y || ldy < N) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
+  return run_gemm(Xq, sx, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int K, qurl_qtype qt, void* acc,
+                               void* workspace, size_t ws_bytes, qurl_stream_t stream) {
+  QURL_TRY(check_gemm(Xq, Wq, M, N, K, qt, workspace, ws_bytes));
+  if (!acc) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(acc)) return QURL_ERR_ALIGNMENT;
+  return run_gemm(Xq, nullptr, Wq, nullptr, M, N, K, qt, nullptr, N, acc, workspace, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma_folded, float eps, const void* Wq,
+                                      const float* sw, int M, int N, int K, qurl_qtype qt, void* Y, int ldy,
+                                      void* Xq_scratch, float* sx_scratch, void* workspace, size_t ws_bytes,
+                                      qurl_stream_t stream) {
+  QURL_TRY(check_act(X, M, K, ldx));
+  QURL_TRY(check_gemm(Xq_scratch, Wq, M, N, K, qt, workspace, ws_bytes));
+  if (!gamma_folded || !sw || !Y || !sx_scratch || ldy < N || !(eps >= 0.0f) || !std::isfinite(eps))
+    return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0 || !aligned16(gamma_folded))
+    return QURL_ERR_ALIGNMENT;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, st));
+  return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st);
+}
+
+qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,
+                            qurl_stream_t stream) {
+  if (!a || !b || !count) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(count) & 7u) != 0) return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_count_diff(a, b, n, count, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_check_device_status(qurl_stream_t stream) {
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int v = 0;
+  QURL_CUDA(cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v != 0) {
+    const int zero = 0;
+    QURL_CUDA(cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
+    return v == qurl::kDevTimeout ? QURL_ERR_TIMEOUT : QURL_ERR_CUDA;
+  }
+  return QURL_OK;
+}
+
+}  // extern "C"

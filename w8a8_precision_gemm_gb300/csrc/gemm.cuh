@@ -1,0 +1,474 @@
+// gemm.cuh -- the W8A8 GEMM with dequantizing epilogue on the sm_103a
+// tensor cores (tcgen05 / TMEM, fed by TMA).
+//
+//   acc[m,n] = sum_k Xq[m,k] * Wq[n,k];   Y[m,n] = bf16((fp32(acc) * sx[m]) * sw[n])
+//
+// One CTA computes a 128 x BN tile of the accumulator for one range of K
+// k-blocks ("split").  Warp roles:
+//   warp 0      TMA producer: streams A and B tiles into a STAGES-deep ring.
+//   warp 1      MMA issuer (one thread) and TMEM owner.
+//   warps 2-5   epilogue: TMEM -> registers -> scales -> bf16 (or raw partials).
+//   warps 6-9   (INT8 only) converters: int8 tiles -> fp16 tiles in the 128-byte
+//               swizzled K-major layout the MMA reads.
+//
+// FP8-E4M3 runs tcgen05.mma kind::f8f6f4 directly on the TMA-loaded codes,
+// fp32 accumulation in TMEM.
+//
+// INT8: this toolchain has no tcgen05 kind::i8 for sm_103a, so the int8 codes
+// are widened to fp16 (every integer of magnitude <= 2048 is exact in fp16)
+// and multiplied with kind::f16 into fp32 TMEM accumulators.  Each product is
+// an integer of magnitude <= 127^2 and every partial sum over a chunk of 1024
+// k stays below 1024 * 127^2 = 16,516,096 < 2^24, so the fp32 accumulation
+// of one chunk is exact; the epilogue warps drain each chunk from TMEM,
+// convert it to int32 and add it to an int32 running sum that also lives in
+// TMEM.  Two TMEM partial buffers let the MMA fill one chunk while the other
+// is drained.  The int32 result is therefore exact.
+//
+// Orientation: with SWAP the weight tile is the MMA's M side (128 output
+// channels per CTA) and the tokens are its N side (BN <= 256) -- the layout for
+// small-M decode, where every weight byte is read once.  Without SWAP the
+// tokens are the M side (prefill).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qurl {
+
+template <int QT, bool SWAP, int BN, int STAGES>
+struct GemmCfg {
+  static constexpr bool kInt8 = (QT == 0);
+  static constexpr int BM = 128;                        // MMA M (rows of the A tile)
+  static constexpr int BK = kInt8 ? 64 : 128;           // k per k-block (= bytes per code row)
+  static constexpr int CSTAGES = kInt8 ? 3 : 0;         // fp16 stages (INT8)
+  static constexpr int A_STAGE = BM * BK;               // bytes of a staged code tile
+  static constexpr int B_STAGE = BN * BK;
+  static constexpr int A_CONV = BM * 128;               // fp16 tile: rows x 64 halves
+  static constexpr int B_CONV = BN * 128;
+  static constexpr int SMEM_TILES = CSTAGES * (A_CONV + B_CONV) + STAGES * (A_STAGE + B_STAGE);
+  static constexpr int SMEM_BYTES = SMEM_TILES + 1024;  // slack for 1024-byte alignment
+  static constexpr int NUM_THREADS = kInt8 ? 320 : 192;
+  static constexpr int TMEM_USED = kInt8 ? 3 * BN : BN;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                   : TMEM_USED <= 64  ? 64
+                                   : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256
+                                                      : 512;
+  static constexpr int CHUNK_KB = kInt8 ? (1024 / BK) : (1 << 30);  // k-blocks per exact chunk
+  static constexpr int MMA_K_BYTES = 32;                // k per MMA: 32 e4m3 or 16 f16
+  static constexpr int MMAS_PER_KB = 128 / MMA_K_BYTES; // a k-block row is 128 bytes in smem
+  static constexpr uint32_t IDESC = umma_idesc_f32acc(0, 0, BM, BN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(TMEM_USED <= 512, "TMEM has 512 columns");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+template <int STAGES, int CSTAGES>
+struct GemmBarriers {
+  uint64_t full[STAGES];    // TMA -> consumer (tx bytes)
+  uint64_t empty[STAGES];   // consumer -> TMA
+  uint64_t cfull[CSTAGES > 0 ? CSTAGES : 1];   // converters -> MMA
+  uint64_t cempty[CSTAGES > 0 ? CSTAGES : 1];  // MMA -> converters
+  uint64_t pfull[2];        // MMA -> epilogue (accumulator chunk ready)
+  uint64_t pempty[2];       // epilogue -> MMA (TMEM buffer drained)
+  uint64_t done;            // MMA drain on the error path
+  uint32_t tmem_base;
+};
+
+// Wait (bounded, ignoring latched errors) for async copies/MMAs a thread has
+// issued itself, so nothing is in flight when the CTA leaves.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, kDevOk, kDevTimeout);
+      return;
+    }
+  }
+}
+
+// Warp-uniform bounded wait: every lane polls, then the warp agrees.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status) {
+  const bool ok = mbar_wait(bar, parity, status);
+  return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
+// 16 int8 codes -> 16 fp16 values, exactly: with u = c + 128 in [0, 255], the
+// fp16 with bits 0x6400 | u is 1024 + u; subtracting 1152 leaves c.
+__device__ __forceinline__ void i8x16_to_f16x16(const uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+  uint32_t o[8];
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p0 = __byte_perm(w[i], 0x64646464u, 0x4140);
+    const uint32_t p1 = __byte_perm(w[i], 0x64646464u, 0x4342);
+    __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), bias);
+    __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&p1), bias);
+    o[2 * i] = *reinterpret_cast<uint32_t*>(&h0);
+    o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&h1);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Widen a staged int8 tile (rows x 64 bytes, row-major, unswizzled) into an
+// fp16 tile of rows x 128 bytes in the 128-byte swizzled K-major layout: the
+// 16-byte chunk c of row r lives at (r/8)*1024 + (r%8)*128 + ((c ^ (r%8))*16).
+// 128 threads; thread t converts 16 codes (chunk t%4) of rows t/4, t/4+32, ...
+// A quarter-warp reads 128 contiguous bytes and writes 8 distinct chunk
+// positions, so neither side has bank conflicts.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows, int t) {
+  const int j = t & 3;
+  for (int r = t >> 2; r < rows; r += 32) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + r * 64 + j * 16);
+    uint4 lo, hi;
+    i8x16_to_f16x16(v, lo, hi);
+    uint8_t* row = dst + (r >> 3) * 1024 + (r & 7) * 128;
+    *reinterpret_cast<uint4*>(row + (((2 * j) ^ (r & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+  }
+}
+
+// Write 32 accumulator values of one tile row/column.  i = row of the A tile
+// (TMEM lane), columns c0..c0+31 of the B tile.
+template <bool SWAP, int BN, typename T>
+__device__ __forceinline__ void emit32(const GemmArgs& a, int a0, int b0, int i, int c0, const T (&v)[32]) {
+  const int M = a.M, N = a.N;
+  if (a.mode == kModeAcc) {
+    T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(blockIdx.z) * M * N;
+    if (SWAP) {
+      const int n = a0 + i;
+      if (n < N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int m = b0 + c0 + j;
+          if (c0 + j < BN && m < M) part[static_cast<size_t>(m) * N + n] = v[j];
+        }
+      }
+    } else {
+      const int m = a0 + i;
+      if (m < M) {
+        T* dst = part + static_cast<size_t>(m) * N + (b0 + c0);
+        const int nvalid = min(32, min(BN - c0, N - (b0 + c0)));
+        if (nvalid == 32 && (N & 3) == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<uint4*>(dst + j) =
+                make_uint4(*reinterpret_cast<const uint32_t*>(&v[j]),
+                           *reinterpret_cast<const uint32_t*>(&v[j + 1]),
+                           *reinterpret_cast<const uint32_t*>(&v[j + 2]),
+                           *reinterpret_cast<const uint32_t*>(&v[j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid) dst[j] = v[j];
+        }
+      }
+    }
+    return;
+  }
+  // dequantizing epilogue: y = bf16((fp32(acc) * sx[m]) * sw[n])
+  if (SWAP) {
+    const int n = a0 + i;
+    if (n >= N) return;
+    const float swn = __ldg(a.sw + n);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int m = b0 + c0 + j;
+      if (c0 + j < BN && m < M) {
+        const float accf = static_cast<float>(v[j]);
+        const float y = __fmul_rn(__fmul_rn(accf, __ldg(a.sx + m)), swn);
+        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
+      }
+    }
+  } else {
+    const int m = a0 + i;
+    if (m >= M) return;
+    const float sxm = __ldg(a.sx + m);
+    __nv_bfloat16* dst = a.Y + static_cast<size_t>(m) * a.ldy + (b0 + c0);
+    const int nvalid = min(32, min(BN - c0, N - (b0 + c0)));
+    if (nvalid == 32) {
+      uint32_t packed[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float y0 = __fmul_rn(__fmul_rn(static_cast<float>(v[j]), sxm), __ldg(a.sw + b0 + c0 + j));
+        const float y1 = __fmul_rn(__fmul_rn(static_cast<float>(v[j + 1]), sxm), __ldg(a.sw + b0 + c0 + j + 1));
+        __nv_bfloat162 p = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+        packed[j / 2] = *reinterpret_cast<uint32_t*>(&p);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4*>(dst)[q] =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nvalid) {
+          const float y = __fmul_rn(__fmul_rn(static_cast<float>(v[j]), sxm), __ldg(a.sw + b0 + c0 + j));
+          dst[j] = __float2bfloat16_rn(y);
+        }
+    }
+  }
+}
+
+template <int QT, bool SWAP, int BN, int STAGES>
+__global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
+    w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args) {
+  using C = GemmCfg<QT, SWAP, BN, STAGES>;
+  __shared__ GemmBarriers<STAGES, C::CSTAGES> bars;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* convA = smem;                                   // [CSTAGES][A_CONV]  (INT8)
+  uint8_t* convB = convA + C::CSTAGES * C::A_CONV;         // [CSTAGES][B_CONV]  (INT8)
+  uint8_t* stA = convB + C::CSTAGES * C::B_CONV;           // [STAGES][A_STAGE]
+  uint8_t* stB = stA + STAGES * C::A_STAGE;                // [STAGES][B_STAGE]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int a_tile = SWAP ? blockIdx.y : blockIdx.x;
+  const int b_tile = SWAP ? blockIdx.x : blockIdx.y;
+  const int a0 = a_tile * C::BM;
+  const int b0 = b_tile * BN;
+  const int kb0 = blockIdx.z * args.kb_per_split;
+  const int nkb = min(args.num_kb - kb0, args.kb_per_split);  // >= 1 by construction
+  int* status = args.status;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], C::kInt8 ? 128 : 1);
+    }
+#pragma unroll
+    for (int s = 0; s < (C::CSTAGES > 0 ? C::CSTAGES : 1); ++s) {
+      mbar_init(&bars.cfull[s], 128);
+      mbar_init(&bars.cempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.pfull[b], 1);
+      mbar_init(&bars.pempty[b], 128);
+    }
+    mbar_init(&bars.done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
+      int issued = 0;
+      bool ok = true;
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(&bars.empty[s], ph ^ 1, status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars.full[s], C::A_STAGE + C::B_STAGE);
+        const int kc = (kb0 + it) * C::BK;
+        tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, a0, &bars.full[s], polA);
+        tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, b0, &bars.full[s], polB);
+        ++issued;
+      }
+      if (!ok) {  // let the copies still in flight land before the CTA leaves
+        for (int it = max(0, issued - STAGES); it < issued; ++it)
+          mbar_wait_drain(&bars.full[it % STAGES], (it / STAGES) & 1, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      if constexpr (!C::kInt8) {
+        for (int it = 0; it < nkb; ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&bars.full[s], (it / STAGES) & 1, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(stA + s * C::A_STAGE);
+          const uint32_t sb = smem_addr(stB + s * C::B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
+            umma_f8f6f4(tmem, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
+                        C::IDESC, (it | kk) != 0);
+          umma_commit(&bars.empty[s]);
+        }
+        if (ok) umma_commit(&bars.pfull[0]);
+      } else {  // INT8
+        for (int it = 0; it < nkb; ++it) {
+          const int c = it / C::CHUNK_KB;
+          const int kin = it % C::CHUNK_KB;
+          const int buf = c & 1;
+          if (kin == 0 && c >= 2) {
+            if (!mbar_wait(&bars.pempty[buf], ((c >> 1) - 1) & 1, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const int cs = it % C::CSTAGES;
+          if (!mbar_wait(&bars.cfull[cs], (it / C::CSTAGES) & 1, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(convA + cs * C::A_CONV);
+          const uint32_t sb = smem_addr(convB + cs * C::B_CONV);
+          const uint32_t d = tmem + buf * BN;
+#pragma unroll
+          for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
+            umma_f16(d, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
+                     C::IDESC, (kin | kk) != 0);
+          umma_commit(&bars.cempty[cs]);
+          if (kin == C::CHUNK_KB - 1 || it == nkb - 1) umma_commit(&bars.pfull[buf]);
+        }
+      }
+      if (!ok) {  // no MMA may still be writing TMEM when it is released
+        umma_commit(&bars.done);
+        mbar_wait_drain(&bars.done, 0, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM lane quadrant this warp may access
+    const int i = q * 32 + lane;          // row of the A tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    if constexpr (!C::kInt8) {
+      if (warp_wait(&bars.pfull[0], 0, status)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + c0, r);
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          emit32<SWAP, BN, float>(args, a0, b0, i, c0, v);
+        }
+      }
+    } else {
+      const int nch = (nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
+      const uint32_t tR = lane_base + 2 * BN;  // int32 running sum
+      for (int c = 0; c < nch; ++c) {
+        const int buf = c & 1;
+        if (!warp_wait(&bars.pfull[buf], (c >> 1) & 1, status)) break;
+        tc_fence_after();
+        const bool last = (c == nch - 1);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t p[32];
+          tmem_ld32(lane_base + buf * BN + c0, p);
+          int v[32];
+          if (c > 0) {
+            uint32_t rs[32];
+            tmem_ld32(tR + c0, rs);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
+          }
+          if (!last) {
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = static_cast<uint32_t>(v[j]);
+            tmem_st32(tR + c0, w);
+          } else {
+            emit32<SWAP, BN, int>(args, a0, b0, i, c0, v);
+          }
+        }
+        if (!last) tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.pempty[buf]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ converters (INT8)
+    if constexpr (C::kInt8) {
+      const int t = threadIdx.x - 192;
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % STAGES;
+        if (!warp_wait(&bars.full[s], (it / STAGES) & 1, status)) break;
+        const int cs = it % C::CSTAGES;
+        if (!warp_wait(&bars.cempty[cs], ((it / C::CSTAGES) & 1) ^ 1, status)) break;
+        convert_tile(stA + s * C::A_STAGE, convA + cs * C::A_CONV, C::BM, t);
+        convert_tile(stB + s * C::B_STAGE, convB + cs * C::B_CONV, BN, t);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.empty[s]);
+        mbar_arrive(&bars.cfull[cs]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Split-K reduction in a fixed order (z = 0, 1, ...), then either the
+// dequantizing epilogue (Y != nullptr) or the raw sum (acc_out).
+template <typename T>
+__global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
+                                     const float* __restrict__ sx, const float* __restrict__ sw,
+                                     __nv_bfloat16* __restrict__ Y, long long ldy, T* __restrict__ acc_out) {
+  const size_t total = static_cast<size_t>(M) * N;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    T s = part[idx];
+    for (int z = 1; z < splits; ++z) s += part[static_cast<size_t>(z) * total + idx];
+    const int m = static_cast<int>(idx / N);
+    const int n = static_cast<int>(idx - static_cast<size_t>(m) * N);
+    if (Y != nullptr) {
+      const float y = __fmul_rn(__fmul_rn(static_cast<float>(s), __ldg(sx + m)), __ldg(sw + n));
+      Y[static_cast<size_t>(m) * ldy + n] = __float2bfloat16_rn(y);
+    } else {
+      acc_out[idx] = s;
+    }
+  }
+}
+
+// Host-side launch of one instantiation.
+template <int QT, bool SWAP, int BN, int STAGES>
+cudaError_t launch_gemm_inst(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, dim3 grid,
+                             cudaStream_t stream) {
+  using C = GemmCfg<QT, SWAP, BN, STAGES>;
+  auto kern = w8a8_gemm_kernel<QT, SWAP, BN, STAGES>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, args);
+  return cudaGetLastError();
+}
+
+}  // namespace qurl

@@ -1,0 +1,66 @@
+// gemm_common.cu -- tile planning and the split-K reduction of the W8A8 GEMM.
+#include <algorithm>
+
+#include "gemm.cuh"
+
+namespace qurl {
+
+// Decode (M <= 256): weights on the MMA M side, tokens padded to a power of two
+// >= 16 on the N side (<= 256 for FP8, <= 128 for INT8, whose TMEM holds two
+// partial buffers and an int32 running sum).  Prefill: 128-token tiles x 256
+// (FP8) or 128 (INT8) channels.  When the tiles do not fill the SMs, K is split
+// so that tiles x splits is close to the SM count, each split at least 4 (FP8)
+// or 8 (INT8) k-blocks deep, as far as the workspace allows.
+GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
+  GemmPlan p{};
+  const bool int8 = (qt == kQInt8);
+  p.bk = int8 ? 64 : 128;
+  p.num_kb = (K + p.bk - 1) / p.bk;
+  p.swap = (M <= 256);
+  if (p.swap) {
+    const int max_bn = int8 ? 128 : 256;
+    int bn = 16;
+    while (bn < M && bn < max_bn) bn *= 2;
+    p.bn = bn;
+    p.tiles_tok = (M + bn - 1) / bn;
+    p.tiles_ch = (N + 127) / 128;
+  } else {
+    p.bn = int8 ? 128 : 256;
+    p.tiles_tok = (M + 127) / 128;
+    p.tiles_ch = (N + p.bn - 1) / p.bn;
+  }
+  const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
+  int splits = 1;
+  if (num_sms > 0 && tiles < num_sms) {
+    const int min_kb = int8 ? 8 : 4;
+    const int want = static_cast<int>(num_sms / tiles);
+    const int cap = std::max(1, p.num_kb / min_kb);
+    splits = std::max(1, std::min(want, cap));
+  }
+  const size_t per_split = static_cast<size_t>(M) * N * 4;
+  if (splits > 1 && ws_avail < static_cast<size_t>(splits) * per_split)
+    splits = std::max(1, static_cast<int>(std::min<size_t>(ws_avail / per_split, 1 << 20)));
+  p.kb_per_split = (p.num_kb + splits - 1) / splits;
+  p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
+  return p;
+}
+
+cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
+                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
+                                 cudaStream_t st) {
+  const size_t total = static_cast<size_t>(M) * N;
+  size_t blocks = (total + 255) / 256;
+  blocks = std::min<size_t>(blocks, static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8);
+  blocks = std::max<size_t>(blocks, 1);
+  auto* y = reinterpret_cast<__nv_bfloat16*>(Y);
+  if (qt == kQInt8)
+    splitk_reduce_kernel<int><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        reinterpret_cast<const int*>(part), splits, M, N, sx, sw, y, ldy, reinterpret_cast<int*>(acc_out));
+  else
+    splitk_reduce_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        reinterpret_cast<const float*>(part), splits, M, N, sx, sw, y, ldy, reinterpret_cast<float*>(acc_out));
+  return cudaGetLastError();
+}
+
+}  // namespace qurl

@@ -1,0 +1,76 @@
+// internal.h -- declarations shared by the translation units of libqurl
+// (not part of the public ABI; the public header is include/qurl.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace qurl {
+
+// Status codes written by kernels into the per-device status word.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 6;  // QURL_ERR_TIMEOUT
+
+constexpr int kQInt8 = 0;  // QURL_INT8
+constexpr int kQFp8 = 1;   // QURL_FP8_E4M3
+
+constexpr int kModeBf16 = 0;  // GEMM epilogue dequantizes and writes Y
+constexpr int kModeAcc = 1;   // GEMM writes the raw accumulator of its split to part
+
+struct GemmArgs {
+  int M, N, K;       // tokens, output channels, depth
+  int num_kb;        // k-blocks covering K
+  int kb_per_split;  // k-blocks per split (grid.z = number of splits)
+  int mode;
+  const float* sx;   // [M]
+  const float* sw;   // [N]
+  __nv_bfloat16* Y;  // [M, ldy]
+  long long ldy;
+  void* part;        // [splits][M][N] int32 (INT8) or fp32 (FP8), mode kModeAcc
+  int* status;       // device status word
+};
+
+// quant.cu
+cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
+                             cudaStream_t st);
+cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
+                                 int qt, void* Xq, float* sx, float* ms_out, cudaStream_t st);
+cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
+                                  float* sx, float* h_out, cudaStream_t st);
+cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
+                                   float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
+                                   cudaStream_t st);
+cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned long long* count, int num_sms,
+                              cudaStream_t st);
+
+// How one GEMM call is cut into CTAs.
+struct GemmPlan {
+  bool swap;         // weights on the MMA M side (decode)
+  int bn;            // MMA N (tile width on the B side)
+  int bk;            // k per k-block
+  int tiles_tok;     // grid.x
+  int tiles_ch;      // grid.y
+  int splits;        // grid.z
+  int num_kb;
+  int kb_per_split;
+  size_t ws_bytes;   // workspace the split-K partials need (0 if splits == 1)
+};
+
+// gemm_plan.cu
+GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
+
+// gemm_fp8.cu / gemm_i8.cu: launch the instantiation matching (swap, bn).
+cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                            dim3 grid, cudaStream_t st);
+cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                           dim3 grid, cudaStream_t st);
+// split-K reduction: T = int (INT8) or float (FP8)
+cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
+                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
+                                 cudaStream_t st);
+
+}  // namespace qurl

@@ -1,0 +1,407 @@
+// quant.cu -- the memory-bound kernels of the W8A8 path:
+//   * per-token activation quantization (optionally with a UAQ pre-scale),
+//   * RMSNorm with the UAQ-folded gain -> per-token quantization,
+//   * SiLU(gate) * up -> per-token quantization,
+//   * UAQ weight fold W' = W/s + per-output-channel weight quantization,
+//   * gain fold gamma' = gamma * s,
+//   * code-flip count of two code buffers.
+//
+// Method: Paper-Notes ICLR2026, "QuRL: Efficient Reinforcement Learning with
+// Quantized Rollout", sections "更新感知量化 (UAQ)" (W X = (W/s)(sX), s folded
+// into the norm gain) and "损失函数 / 训练策略" (per-channel weight and
+// per-token activation INT8/FP8 quantization, s = 1.5).
+//
+// Every row (token or output channel) is one CTA: 16-byte vector loads, the
+// row cached in registers between the absmax pass and the code pass, a
+// warp-shuffle + shared-memory block reduction.  Arithmetic that decides a
+// code is IEEE fp32 with explicit rounding intrinsics (no contraction):
+//   scale = absmax / qmax (absmax == 0 -> 1);  code = RNE(v / scale)
+//   clamped to +-127 (INT8), or e4m3 RNE with saturation (FP8).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace qurl {
+namespace {
+
+constexpr int kVPT = 8;  // 16-byte vectors cached per thread
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Block-wide reduction (max or sum); every thread gets the result.
+template <bool kMax>
+__device__ __forceinline__ float block_reduce(float v, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  v = kMax ? warp_max(v) : warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < nw ? red[lane] : 0.0f;
+    t = kMax ? warp_max(t) : warp_sum(t);
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  const float r = red[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float row_scale(float amax, int qt) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, qt == kQInt8 ? 127.0f : 448.0f);
+}
+
+__device__ __forceinline__ uint8_t encode(float v, float scale, int qt) {
+  const float r = __fdiv_rn(v, scale);
+  if (qt == kQInt8) {
+    int q = __float2int_rn(r);
+    q = max(-127, min(127, q));
+    return static_cast<uint8_t>(static_cast<int8_t>(q));
+  }
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
+}
+
+// 8 values -> 8 code bytes packed in a uint2 (little-endian byte order = k order).
+__device__ __forceinline__ uint2 encode8(const float (&v)[8], float scale, int qt) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) lo |= static_cast<uint32_t>(encode(v[e], scale, qt)) << (8 * e);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) hi |= static_cast<uint32_t>(encode(v[4 + e], scale, qt)) << (8 * e);
+  return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+// Visit the 16-byte vectors idx = threadIdx.x + c * blockDim.x of a row: the
+// first kVPT from the register cache (fully unrolled, so the cache stays in
+// registers), the rest (rows longer than kVPT * blockDim vectors) from memory.
+template <int NC, typename F>
+__device__ __forceinline__ void for_vectors(const uint4* row, int nvec, const uint4 (&cache)[NC], F&& f) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    if (idx < nvec) f(cache[c], idx);
+  }
+  for (int idx = threadIdx.x + NC * blockDim.x; idx < nvec; idx += blockDim.x) f(__ldg(row + idx), idx);
+}
+
+template <int NC>
+__device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&cache)[NC]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    if (idx < nvec) cache[c] = __ldg(row + idx);
+  }
+}
+
+// ------------------------------------------------------------------ activation quant
+
+__global__ void quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
+                                 uint8_t* __restrict__ Xq, float* __restrict__ sx) {
+  __shared__ float red[33];
+  const int m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
+  const int nvec = K >> 3;
+  uint4 cache[kVPT];
+  fill_cache(row, nvec, cache);
+  float amax = 0.0f;
+  for_vectors(row, nvec, cache, [&](const uint4 u, int) {
+    float x[8];
+    bf16x8_to_f32(u, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(x[e], pre)));
+  });
+  amax = block_reduce<true>(amax, red);
+  const float scale = row_scale(amax, qt);
+  if (threadIdx.x == 0) sx[m] = scale;
+  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * K);
+  for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
+    float x[8];
+    bf16x8_to_f32(u, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
+    out[idx] = encode8(x, scale, qt);
+  });
+}
+
+// ------------------------------------------------------------------ RMSNorm -> quant
+
+__global__ void rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
+                                     const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
+                                     float* __restrict__ sx, float* __restrict__ ms_out) {
+  __shared__ float red[33];
+  const int m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  const int nvec = K >> 3;
+  uint4 cache[kVPT];
+  fill_cache(row, nvec, cache);
+  // mean of squares (fp32; this kernel's own, fixed reduction order)
+  float ss = 0.0f;
+  for_vectors(row, nvec, cache, [&](const uint4 u, int) {
+    float x[8];
+    bf16x8_to_f32(u, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
+  });
+  ss = block_reduce<false>(ss, red);
+  const float ms = __fdiv_rn(ss, static_cast<float>(K));
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  if (threadIdx.x == 0 && ms_out) ms_out[m] = ms;
+  // v = (x * r) * gamma'
+  auto normed = [&](const uint4 u, int idx, float (&x)[8]) {
+    bf16x8_to_f32(u, x);
+    const float4 ga = __ldg(g4 + 2 * idx), gb = __ldg(g4 + 2 * idx + 1);
+    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(__fmul_rn(x[e], r), g[e]);
+  };
+  float amax = 0.0f;
+  for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
+    float x[8];
+    normed(u, idx, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  });
+  amax = block_reduce<true>(amax, red);
+  const float scale = row_scale(amax, qt);
+  if (threadIdx.x == 0) sx[m] = scale;
+  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * K);
+  for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
+    float x[8];
+    normed(u, idx, x);
+    out[idx] = encode8(x, scale, qt);
+  });
+}
+
+// ------------------------------------------------------------------ SiLU * up -> quant
+
+__device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float (&h)[8]) {
+  float g[8], u[8];
+  bf16x8_to_f32(gu, g);
+  bf16x8_to_f32(uu, u);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float den = __fadd_rn(1.0f, expf(-g[e]));
+    h[e] = __fmul_rn(__fdiv_rn(g[e], den), u[e]);
+  }
+}
+
+__global__ void silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
+                                      int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
+                                      float* __restrict__ h_out) {
+  __shared__ float red[33];
+  const int m = blockIdx.x;
+  const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
+  const uint4* urow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu + I);
+  const int nvec = I >> 3;
+  uint4 cg[kVPT / 2], cu[kVPT / 2];
+  fill_cache(grow, nvec, cg);
+  fill_cache(urow, nvec, cu);
+  // visit (gate, up) vector pairs: cached ones unrolled, the rest from memory
+  auto visit = [&](auto&& f) {
+#pragma unroll
+    for (int c = 0; c < kVPT / 2; ++c) {
+      const int idx = threadIdx.x + c * blockDim.x;
+      if (idx < nvec) f(cg[c], cu[c], idx);
+    }
+    for (int idx = threadIdx.x + (kVPT / 2) * blockDim.x; idx < nvec; idx += blockDim.x)
+      f(__ldg(grow + idx), __ldg(urow + idx), idx);
+  };
+  float amax = 0.0f;
+  visit([&](const uint4 g, const uint4 u, int idx) {
+    float h[8];
+    silu_mul8(g, u, h);
+    if (h_out) {
+      float4* ho = reinterpret_cast<float4*>(h_out + static_cast<size_t>(m) * I) + 2 * idx;
+      ho[0] = make_float4(h[0], h[1], h[2], h[3]);
+      ho[1] = make_float4(h[4], h[5], h[6], h[7]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(h[e], pre)));
+  });
+  amax = block_reduce<true>(amax, red);
+  const float scale = row_scale(amax, qt);
+  if (threadIdx.x == 0) sx[m] = scale;
+  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * I);
+  visit([&](const uint4 g, const uint4 u, int idx) {
+    float h[8];
+    silu_mul8(g, u, h);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
+    out[idx] = encode8(h, scale, qt);
+  });
+}
+
+// ------------------------------------------------------------------ weight fold + quant
+
+// Loads 8 consecutive weights of a row as fp32 (bf16 or fp32 storage).
+template <bool kF32>
+__device__ __forceinline__ void load_w8(const void* row, int idx, float (&w)[8]) {
+  if (kF32) {
+    const float4* p = reinterpret_cast<const float4*>(row) + 2 * idx;
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else {
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(row) + idx), w);
+  }
+}
+
+template <bool kF32>
+__global__ void prepare_weights_kernel(const void* __restrict__ W, int K, long long ldw, float s, int qt,
+                                       uint8_t* __restrict__ Wq, float* __restrict__ sw, float* W_scaled) {
+  __shared__ float red[33];
+  const int n = blockIdx.x;
+  const char* row = reinterpret_cast<const char*>(W) + static_cast<size_t>(n) * ldw * (kF32 ? 4 : 2);
+  const int nvec = K >> 3;
+  // pass 1: absmax of W' = W / s (reads only)
+  float amax = 0.0f;
+  for (int idx = threadIdx.x; idx < nvec; idx += blockDim.x) {
+    float w[8];
+    load_w8<kF32>(row, idx, w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fdiv_rn(w[e], s)));
+  }
+  amax = block_reduce<true>(amax, red);
+  const float scale = row_scale(amax, qt);
+  if (threadIdx.x == 0) sw[n] = scale;
+  // pass 2: codes; W' is written here, after the row has been read (each
+  // thread rewrites only the vectors it has just read, so W_scaled may alias W)
+  uint2* out = reinterpret_cast<uint2*>(Wq + static_cast<size_t>(n) * K);
+  for (int idx = threadIdx.x; idx < nvec; idx += blockDim.x) {
+    float w[8];
+    load_w8<kF32>(row, idx, w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = __fdiv_rn(w[e], s);
+    if (W_scaled) {
+      float4* o = reinterpret_cast<float4*>(W_scaled + static_cast<size_t>(n) * K) + 2 * idx;
+      o[0] = make_float4(w[0], w[1], w[2], w[3]);
+      o[1] = make_float4(w[4], w[5], w[6], w[7]);
+    }
+    out[idx] = encode8(w, scale, qt);
+  }
+}
+
+__global__ void fold_gamma_kernel(const float* __restrict__ gamma, int K, float s, float* __restrict__ out) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k < K) out[k] = __fmul_rn(gamma[k], s);
+}
+
+// ------------------------------------------------------------------ code-flip count
+
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
+  x |= x >> 4;
+  x |= x >> 2;
+  x |= x >> 1;
+  return __popc(x & 0x01010101u);
+}
+
+__global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b, size_t n,
+                                  unsigned long long* __restrict__ count) {
+  const size_t nv = n >> 4;
+  const uint4* a4 = reinterpret_cast<const uint4*>(a);
+  const uint4* b4 = reinterpret_cast<const uint4*>(b);
+  unsigned long long c = 0;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nv;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 x = __ldg(a4 + i), y = __ldg(b4 + i);
+    c += nonzero_bytes(x.x ^ y.x) + nonzero_bytes(x.y ^ y.y) + nonzero_bytes(x.z ^ y.z) +
+         nonzero_bytes(x.w ^ y.w);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < (n & 15)) {
+    const size_t i = (nv << 4) + threadIdx.x;
+    c += (a[i] != b[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(count, c);
+}
+
+// Threads per row-CTA: enough that kVPT vectors per thread cover the row.
+int row_threads(int nvec) {
+  int t = 32;
+  while (t < 1024 && t * kVPT < nvec) t *= 2;
+  return t;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
+                             cudaStream_t st) {
+  quant_act_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre,
+                                                       qt, reinterpret_cast<uint8_t*>(Xq), sx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
+                                 int qt, void* Xq, float* sx, float* ms_out, cudaStream_t st) {
+  rmsnorm_quant_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx,
+                                                           gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq), sx,
+                                                           ms_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
+                                  float* sx, float* h_out, cudaStream_t st) {
+  // two vectors (gate, up) are cached per position: use twice the threads
+  int t = 32;
+  while (t < 1024 && t * (kVPT / 2) < I / 8) t *= 2;
+  silu_mul_quant_kernel<<<M, t, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt,
+                                         reinterpret_cast<uint8_t*>(Xq), sx, h_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
+                                   float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
+                                   cudaStream_t st) {
+  const int t = row_threads(K / 8);
+  if (w_f32)
+    prepare_weights_kernel<true><<<N, t, 0, st>>>(W, K, ldw, s, qt, reinterpret_cast<uint8_t*>(Wq), sw, W_scaled);
+  else
+    prepare_weights_kernel<false><<<N, t, 0, st>>>(W, K, ldw, s, qt, reinterpret_cast<uint8_t*>(Wq), sw, W_scaled);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (gamma) {
+    fold_gamma_kernel<<<(K + 255) / 256, 256, 0, st>>>(gamma, K, s, gamma_folded);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned long long* count, int num_sms,
+                              cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(unsigned long long), st);
+  if (e != cudaSuccess) return e;
+  const size_t nv = n >> 4;
+  size_t blocks = (nv + 255) / 256;
+  const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  count_diff_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(a),
+                                                                  reinterpret_cast<const uint8_t*>(b), n, count);
+  return cudaGetLastError();
+}
+
+}  // namespace qurl
