@@ -220,6 +220,32 @@ def test_gemm_int8_worst_case_magnitude():
     np.testing.assert_array_equal(a, oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT))
 
 
+def test_gemm_int8_chunk_edge_exactness():
+    """Partial sums of a 1024-deep chunk reach 1023 * 127^2 + 1 = 16,499,968 + 1, one
+    below the fp32 integer limit 2^24 in magnitude, with +-1 terms that only survive
+    if the tensor core's fp32 accumulation drops no low bit; more chunks follow
+    with the opposite sign so the int32 sum also crosses zero."""
+    K = 4096
+    M, N = 8, 128
+    xq = np.full((M, K), 127, np.int8)
+    wq = np.full((N, K), 127, np.int8)
+    g = np.random.Generator(np.random.PCG64(99))
+    for c in range(K // 1024):
+        lo, hi = c * 1024, (c + 1) * 1024
+        sign = 1 if c % 2 == 0 else -1
+        wq[:, lo:hi] *= sign
+        # the last entries of each chunk: small +-1 products in varying places
+        xq[:, hi - 8:hi] = g.choice(np.array([-1, 1], np.int8), size=(M, 8))
+        wq[:, hi - 8:hi] = g.choice(np.array([-1, 1], np.int8), size=(N, 8))
+    xq[1] = -xq[1]
+    xq[2, ::3] = 0
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8)
+    sync_ok()
+    ref = oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT)
+    assert np.abs(ref).max() < 2 ** 24 * 2  # per chunk below 2^24; the total is exact in int32 anyway
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
 def test_gemm_acc_fp8(M, N, K):
     xq = random_codes(q.FP8_E4M3, (M, K), M * 7 + K)

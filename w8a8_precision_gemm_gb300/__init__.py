@@ -111,12 +111,23 @@ def _ok(rc: int, where: str):
 
 
 def _ld(t) -> int:
+    """Row stride of a row-major matrix whose rows may be strided (X, GU, W, Y)."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
     return t.stride(0)
+
+
+def _dense(*ts):
+    """Code, scale and accumulator buffers are dense (row stride = row length)."""
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("code / scale / accumulator tensors must be contiguous")
 
 
 # ---------------------------------------------------------------- the C ABI, by name
 
 def qurl_prepare_weights(W, gamma, s, qt, Wq, sw, gamma_folded=None, W_scaled=None, stream=None):
+    _dense(gamma, Wq, sw, gamma_folded, W_scaled)
     wt = FP32 if W.dtype == torch.float32 else BF16
     N, K = W.shape
     _ok(load().qurl_prepare_weights(_ptr(W), wt, N, K, _ld(W), _ptr(gamma), float(s), qt, _ptr(Wq), _ptr(sw),
@@ -124,18 +135,21 @@ def qurl_prepare_weights(W, gamma, s, qt, Wq, sw, gamma_folded=None, W_scaled=No
 
 
 def qurl_quant_act(X, pre_scale, qt, Xq, sx, stream=None):
+    _dense(Xq, sx)
     M, K = X.shape
     _ok(load().qurl_quant_act(_ptr(X), M, K, _ld(X), float(pre_scale), qt, _ptr(Xq), _ptr(sx), _stream(stream)),
         "qurl_quant_act")
 
 
 def qurl_rmsnorm_quant(X, gamma_folded, eps, qt, Xq, sx, ms_out=None, stream=None):
+    _dense(gamma_folded, Xq, sx, ms_out)
     M, K = X.shape
     _ok(load().qurl_rmsnorm_quant(_ptr(X), M, K, _ld(X), _ptr(gamma_folded), float(eps), qt, _ptr(Xq), _ptr(sx),
                                   _ptr(ms_out), _stream(stream)), "qurl_rmsnorm_quant")
 
 
 def qurl_silu_mul_quant(GU, pre_scale, qt, Xq, sx, h_out=None, stream=None):
+    _dense(Xq, sx, h_out)
     M, I2 = GU.shape
     _ok(load().qurl_silu_mul_quant(_ptr(GU), M, I2 // 2, _ld(GU), float(pre_scale), qt, _ptr(Xq), _ptr(sx),
                                    _ptr(h_out), _stream(stream)), "qurl_silu_mul_quant")
@@ -146,6 +160,7 @@ def qurl_workspace_size(M, N, K, qt) -> int:
 
 
 def qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, workspace=None, stream=None):
+    _dense(Xq, sx, Wq, sw, workspace)
     M, K = Xq.shape
     N = Wq.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -154,6 +169,7 @@ def qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, workspace=None, stream=None):
 
 
 def qurl_w8a8_gemm_acc(Xq, Wq, qt, acc, workspace=None, stream=None):
+    _dense(Xq, Wq, acc, workspace)
     M, K = Xq.shape
     N = Wq.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -163,6 +179,7 @@ def qurl_w8a8_gemm_acc(Xq, Wq, qt, acc, workspace=None, stream=None):
 
 def qurl_rmsnorm_quant_linear(X, gamma_folded, eps, Wq, sw, qt, Y, Xq_scratch, sx_scratch, workspace=None,
                               stream=None):
+    _dense(gamma_folded, Wq, sw, Xq_scratch, sx_scratch, workspace)
     M, K = X.shape
     N = Wq.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -172,6 +189,7 @@ def qurl_rmsnorm_quant_linear(X, gamma_folded, eps, Wq, sw, qt, Y, Xq_scratch, s
 
 
 def qurl_count_diff(a, b, count, stream=None):
+    _dense(a, b, count)
     n = a.numel() * a.element_size()
     assert b.numel() * b.element_size() == n
     _ok(load().qurl_count_diff(_ptr(a), _ptr(b), n, _ptr(count), _stream(stream)), "qurl_count_diff")
