@@ -109,7 +109,10 @@ qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale
 /*
  * RMSNorm with the folded gain gamma' = gamma * s, then per-token quantization
  * ([UAQ] fold into the norm, [LOSS]).
- *   ms[m] = (sum_k x^2) / K (fp32, the kernel's own reduction order);
+ *   ms[m] = (sum_k x^2) / K: each x^2 is exact in fp32 and the sum is kept
+ *           as an error-free compensated pair, divided by K in fp64 and
+ *           rounded to fp32 -- the correctly rounded mean unless it lies
+ *           within ~2^-44 (relative) of an fp32 rounding midpoint;
  *   r = 1 / sqrt(ms + eps) (correctly rounded fp32 sqrt and division);
  *   v[m,k] = (x * r) * gamma'[k] (two fp32 products); then as qurl_quant_act.
  * ms_out [M] fp32 or NULL receives ms (lets a checker reproduce the codes).
@@ -129,10 +132,12 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
                                 void* Xq, float* sx, float* h_out, qurl_stream_t stream);
 
 /*
- * Bytes of workspace qurl_w8a8_linear / qurl_w8a8_gemm_acc /
- * qurl_rmsnorm_quant_linear use for this shape at full speed (split-K
- * partial sums).  A smaller workspace (or none) is accepted: the kernels then
- * split K into fewer parts.
+ * Bytes of workspace the linear entry points (qurl_w8a8_linear,
+ * qurl_w8a8_gemm_acc and the fused *_linear entries) use for this shape at
+ * full speed: split-K partial sums and, for INT8 with M <= 256, an fp16 copy
+ * of the activation codes.  A smaller workspace (or none) is accepted: the
+ * kernels then split K into fewer parts and INT8 widens the codes in shared
+ * memory instead (slower, same result).
  */
 size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
 
@@ -142,8 +147,10 @@ size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
  *   Y[m,n]   = bf16_RNE( (fp32(acc) * sx[m]) * sw[n] )
  * Xq [M, K], Wq [N, K] codes; sx [M], sw [N] fp32; Y [M, N] bf16, row stride
  * ldy.  workspace: device scratch of ws_bytes (may be NULL / 0).
- * INT8 runs on the fp16 tensor path with integer-exact partial sums (see the
- * design notes); its int32 accumulator and bf16 Y are exact.
+ * INT8 runs on the fp16 tensor path: the codes are widened to fp16 (exact),
+ * each 1024-deep chunk of k is accumulated in fp32 (exact: every partial sum
+ * is an integer below 1024 * 127^2 < 2^24) and the chunks are added in int32,
+ * so the int32 accumulator and the bf16 Y are exact.
  */
 qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N,
                              int K, qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
@@ -166,6 +173,23 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
                                       const void* Wq, const float* sw, int M, int N, int K, qurl_qtype qt,
                                       void* Y, int ldy, void* Xq_scratch, float* sx_scratch, void* workspace,
                                       size_t ws_bytes, qurl_stream_t stream);
+
+/*
+ * Fused entry: per-token quantization (with the UAQ pre-scale) -> W8A8 linear,
+ * for a projection with no norm in front of it (o_proj: s moves to the
+ * activation, [UAQ]).  Same arguments and scratch buffers as above.
+ */
+qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const void* Wq, const float* sw, int M,
+                                  int N, int K, qurl_qtype qt, void* Y, int ldy, void* Xq_scratch, float* sx_scratch,
+                                  void* workspace, size_t ws_bytes, qurl_stream_t stream);
+
+/*
+ * Fused entry: SiLU(gate) * up -> per-token quantization (pre-scale) -> W8A8
+ * linear (the down projection; K = I).  GU [M, 2I] bf16, row stride ldgu.
+ */
+qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale, const void* Wq, const float* sw,
+                                       int M, int N, int I, qurl_qtype qt, void* Y, int ldy, void* Xq_scratch,
+                                       float* sx_scratch, void* workspace, size_t ws_bytes, qurl_stream_t stream);
 
 /*
  * Weight-update probe ([UAQ]: the quantization error shrinks by s while the

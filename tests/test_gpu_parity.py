@@ -101,15 +101,16 @@ def test_rmsnorm_quant(qt, M, K):
     sync_ok()
     ms_d = f32(ms)
     ms_o = oracle.rms_ms(bits(X))
-    np.testing.assert_allclose(ms_d, ms_o, rtol=2e-6)
+    np.testing.assert_allclose(ms_d, ms_o, rtol=2e-7)
     # codes and scales are exact given the kernel's mean of squares
     qo, so, _, _ = oracle.rmsnorm_quant(bits(X), g.numpy(), oqt(qt), eps=1e-6, ms_given=ms_d)
     np.testing.assert_array_equal(codes(Xq), qo)
     np.testing.assert_array_equal(f32(sx), so)
-    # rows where the kernel's fp32 ms equals the oracle's own are exact with no input from the kernel
+    # the kernel's compensated mean of squares is the oracle's own fp32 value in (nearly) every
+    # row; those rows are exact with no input from the kernel
     q2, s2, ms2, _ = oracle.rmsnorm_quant(bits(X), g.numpy(), oqt(qt), eps=1e-6)
     same = ms2 == ms_d
-    assert same.mean() > 0.3
+    assert same.mean() >= 0.9, same.mean()
     np.testing.assert_array_equal(codes(Xq)[same], q2[same])
     np.testing.assert_array_equal(f32(sx)[same], s2[same])
 
@@ -325,6 +326,58 @@ def test_fused_rmsnorm_quant_linear(qt):
     qo, so, _, _ = oracle.rmsnorm_quant(bits(X), gfo, oqt(qt), eps=1e-6)
     Yo, _ = oracle.w8a8_linear(qo, so, Wo, swo, oqt(qt), nthreads=NT)
     assert max_abs_rel(oracle.bf16_decode(bits(Y)), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+@pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M", [64, 200, 300])
+def test_fused_quant_entries(qt, M):
+    """quant_act -> linear and SiLU*mul -> quant -> linear, fused, give the bits
+    of the separate calls (which the oracle checks above), and the layer output
+    stays within 1e-2 of the oracle's chain."""
+    K, N, I = 1024, 768, 2048
+    X = synth.activations(f"gpu/fq/X/{M}", M, K)
+    GU = synth.activations(f"gpu/fq/GU/{M}", M, 2 * I, outlier_gain=4.0)
+    W1 = synth.weights("gpu/fq/W1", N, K)
+    W2 = synth.weights("gpu/fq/W2", N, I)
+    Wq1, sw1, _, _ = q.prepare_weights(W1.cuda(), qt, s=1.5)
+    Wq2, sw2, _, _ = q.prepare_weights(W2.cuda(), qt, s=1.5)
+    cd = q.code_dtype(qt)
+    Y1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    xs1 = torch.empty((M, K), dtype=cd, device="cuda")
+    xs2 = torch.empty((M, I), dtype=cd, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    sx2 = torch.empty(M, dtype=torch.float32, device="cuda")
+    q.qurl_quant_act_linear(X.cuda(), 1.5, Wq1, sw1, qt, Y1, xs1, sx, q.workspace(M, N, K, qt))
+    q.qurl_silu_mul_quant_linear(GU.cuda(), 1.5, Wq2, sw2, qt, Y2, xs2, sx2, q.workspace(M, N, I, qt))
+    Xq1, s1 = q.quant_act(X.cuda(), qt, pre_scale=1.5)
+    R1 = q.linear(Xq1, s1, Wq1, sw1, qt)  # no workspace: the other INT8 kernel, same bits
+    Xq2, s2 = q.silu_mul_quant(GU.cuda(), qt, pre_scale=1.5)
+    R2 = q.linear(Xq2, s2, Wq2, sw2, qt, q.workspace(M, N, I, qt))
+    sync_ok()
+    assert torch.equal(Y1.view(torch.int16), R1.view(torch.int16))
+    assert torch.equal(Y2.view(torch.int16), R2.view(torch.int16))
+    Wo, swo, _, _ = oracle.prepare_weights(W1.numpy(), oqt(qt), s=1.5)
+    qo, so = oracle.quant_act(bits(X), oqt(qt), pre_scale=1.5)
+    Yo, _ = oracle.w8a8_linear(qo, so, Wo, swo, oqt(qt), nthreads=NT)
+    if qt == q.INT8:
+        np.testing.assert_array_equal(bits(Y1), Yo)
+    else:
+        assert max_abs_rel(oracle.bf16_decode(bits(Y1)), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 512, 256), (64, 4608, 3584), (256, 1000, 2048)])
+def test_linear_int8_with_and_without_workspace(M, N, K):
+    """INT8 decode runs the TMEM-operand kernel with a workspace and the
+    shared-memory widening kernel without one: the same exact bits."""
+    Xq, sx, Wq, sw = _layer(q.INT8, M, N, K, f"gpu/lin/ws/{M}/{N}/{K}")
+    args = (to_dev(Xq, q.INT8), torch.from_numpy(sx).cuda(), to_dev(Wq, q.INT8), torch.from_numpy(sw).cuda(), q.INT8)
+    Ya = q.linear(*args, q.workspace(M, N, K, q.INT8))
+    Yb = q.linear(*args, None)
+    sync_ok()
+    Yo, _ = oracle.w8a8_linear(Xq, sx, Wq, sw, oracle.INT8, nthreads=NT)
+    np.testing.assert_array_equal(bits(Ya), Yo)
+    np.testing.assert_array_equal(bits(Yb), Yo)
 
 
 # ------------------------------------------------------------------ full-size projections (sampled)

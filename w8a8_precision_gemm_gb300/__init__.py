@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
             "qurl_w8a8_linear": [P, P, P, P, i, i, i, i, P, i, P, z, P],
             "qurl_w8a8_gemm_acc": [P, P, i, i, i, i, P, P, z, P],
             "qurl_rmsnorm_quant_linear": [P, i, P, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
+            "qurl_quant_act_linear": [P, i, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
+            "qurl_silu_mul_quant_linear": [P, i, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
             "qurl_count_diff": [P, P, z, P, P],
             "qurl_check_device_status": [P],
         }
@@ -186,6 +188,26 @@ def qurl_rmsnorm_quant_linear(X, gamma_folded, eps, Wq, sw, qt, Y, Xq_scratch, s
     _ok(load().qurl_rmsnorm_quant_linear(_ptr(X), _ld(X), _ptr(gamma_folded), float(eps), _ptr(Wq), _ptr(sw), M, N,
                                          K, qt, _ptr(Y), _ld(Y), _ptr(Xq_scratch), _ptr(sx_scratch),
                                          _ptr(workspace), ws_bytes, _stream(stream)), "qurl_rmsnorm_quant_linear")
+
+
+def qurl_quant_act_linear(X, pre_scale, Wq, sw, qt, Y, Xq_scratch, sx_scratch, workspace=None, stream=None):
+    _dense(Wq, sw, Xq_scratch, sx_scratch, workspace)
+    M, K = X.shape
+    N = Wq.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(load().qurl_quant_act_linear(_ptr(X), _ld(X), float(pre_scale), _ptr(Wq), _ptr(sw), M, N, K, qt, _ptr(Y),
+                                     _ld(Y), _ptr(Xq_scratch), _ptr(sx_scratch), _ptr(workspace), ws_bytes,
+                                     _stream(stream)), "qurl_quant_act_linear")
+
+
+def qurl_silu_mul_quant_linear(GU, pre_scale, Wq, sw, qt, Y, Xq_scratch, sx_scratch, workspace=None, stream=None):
+    _dense(Wq, sw, Xq_scratch, sx_scratch, workspace)
+    M, I2 = GU.shape
+    N = Wq.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(load().qurl_silu_mul_quant_linear(_ptr(GU), _ld(GU), float(pre_scale), _ptr(Wq), _ptr(sw), M, N, I2 // 2,
+                                          qt, _ptr(Y), _ld(Y), _ptr(Xq_scratch), _ptr(sx_scratch), _ptr(workspace),
+                                          ws_bytes, _stream(stream)), "qurl_silu_mul_quant_linear")
 
 
 def qurl_count_diff(a, b, count, stream=None):

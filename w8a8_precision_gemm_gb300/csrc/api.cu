@@ -170,19 +170,27 @@ qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int 
   } while (0)
 
 // Run the GEMM; mode bf16 -> Y, otherwise raw accumulators -> acc_out.
+// x16_ready: the fp16 copy of Xq's codes is already at the start of the
+// workspace (written by a fused quantizer), so it is not widened again.
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
-                     void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+                     void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
+                     bool x16_ready = false) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
   const bool int8 = (qt == QURL_INT8);
-  const long long a_rows = p.swap ? N : M;
-  const long long b_rows = p.swap ? M : N;
-  const void* a_ptr = p.swap ? Wq : Xq;
-  const void* b_ptr = p.swap ? Xq : Wq;
   CUtensorMap ta, tb;
-  QURL_TRY(byte_map(a_ptr, a_rows, K, K, p.bk, 128, !int8, &ta));
-  QURL_TRY(byte_map(b_ptr, b_rows, K, K, p.bk, p.bn, !int8, &tb));
+  uint8_t* part_base = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
+  if (p.tmem_a) {
+    if (!x16_ready) QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, static_cast<size_t>(M) * K, dev->num_sms, st));
+    QURL_TRY(byte_map(Wq, N, K, K, 128, 128, true, &ta));
+    QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, p.bn, true, &tb));
+  } else {
+    const long long a_rows = p.swap ? N : M;
+    const long long b_rows = p.swap ? M : N;
+    QURL_TRY(byte_map(p.swap ? Wq : Xq, a_rows, K, K, p.bk, 128, !int8, &ta));
+    QURL_TRY(byte_map(p.swap ? Xq : Wq, b_rows, K, K, p.bk, p.bn, !int8, &tb));
+  }
   qurl::GemmArgs a{};
   a.M = M;
   a.N = N;
@@ -199,13 +207,16 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
     a.mode = qurl::kModeBf16;
   } else {
     a.mode = qurl::kModeAcc;
-    a.part = split ? ws : acc_out;
+    a.part = split ? static_cast<void*>(part_base) : acc_out;
   }
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
-  QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
-                 : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
+  if (p.tmem_a)
+    QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
+  else
+    QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
+                   : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
   if (split)
-    QURL_CUDA(qurl::launch_splitk_reduce(qt, ws, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
+    QURL_CUDA(qurl::launch_splitk_reduce(qt, part_base, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
                                          dev->num_sms, st));
   return QURL_OK;
 }
@@ -259,7 +270,8 @@ qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale
   if (!aligned16(Xq)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, reinterpret_cast<cudaStream_t>(stream)));
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr,
+                                   reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
 
@@ -271,7 +283,7 @@ qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float
   if (!aligned16(Xq) || !aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out,
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr,
                                        reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -286,7 +298,7 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
     return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out,
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
                                         reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -322,21 +334,65 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Where the GEMM plan reads an fp16 copy of the INT8 codes from the workspace,
+// the fused quantizer writes it there directly.
+void* fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+  DevState* dev = nullptr;
+  if (device_state(&dev) != QURL_OK) return nullptr;
+  const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
+  return p.tmem_a ? ws : nullptr;
+}
+
+qurl_status check_fused_out(const void* Wq, const float* sw, int M, int N, int K, int qt, void* Y, int ldy,
+                            const void* Xq_scratch, const float* sx_scratch, const void* ws, size_t ws_bytes) {
+  QURL_TRY(check_gemm(Xq_scratch, Wq, M, N, K, qt, ws, ws_bytes));
+  if (!sw || !Y || !sx_scratch || ldy < N) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
+  return QURL_OK;
+}
+
 qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma_folded, float eps, const void* Wq,
                                       const float* sw, int M, int N, int K, qurl_qtype qt, void* Y, int ldy,
                                       void* Xq_scratch, float* sx_scratch, void* workspace, size_t ws_bytes,
                                       qurl_stream_t stream) {
   QURL_TRY(check_act(X, M, K, ldx));
-  QURL_TRY(check_gemm(Xq_scratch, Wq, M, N, K, qt, workspace, ws_bytes));
-  if (!gamma_folded || !sw || !Y || !sx_scratch || ldy < N || !(eps >= 0.0f) || !std::isfinite(eps))
-    return QURL_ERR_INVALID_ARG;
-  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0 || !aligned16(gamma_folded))
-    return QURL_ERR_ALIGNMENT;
+  QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
+  if (!gamma_folded || !(eps >= 0.0f) || !std::isfinite(eps)) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  DevState* dev = nullptr;
-  QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, st));
-  return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st);
+  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, x16,
+                                       st));
+  return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
+                  x16 != nullptr);
+}
+
+qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const void* Wq, const float* sw, int M,
+                                  int N, int K, qurl_qtype qt, void* Y, int ldy, void* Xq_scratch, float* sx_scratch,
+                                  void* workspace, size_t ws_bytes, qurl_stream_t stream) {
+  QURL_TRY(check_act(X, M, K, ldx));
+  QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
+  if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, x16, st));
+  return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
+                  x16 != nullptr);
+}
+
+qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale, const void* Wq, const float* sw,
+                                       int M, int N, int I, qurl_qtype qt, void* Y, int ldy, void* Xq_scratch,
+                                       float* sx_scratch, void* workspace, size_t ws_bytes, qurl_stream_t stream) {
+  if (!GU || !valid_dim(M) || !valid_dim(I) || ldgu < 2LL * I || !std::isfinite(pre_scale))
+    return QURL_ERR_INVALID_ARG;
+  if (I % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
+  QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* x16 = fused_x16(M, N, I, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, x16, st));
+  return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
+                  x16 != nullptr);
 }
 
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,

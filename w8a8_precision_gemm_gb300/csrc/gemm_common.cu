@@ -14,9 +14,14 @@ namespace qurl {
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
-  p.bk = int8 ? 64 : 128;
-  p.num_kb = (K + p.bk - 1) / p.bk;
   p.swap = (M <= 256);
+  // INT8 decode prefers the TMEM-operand kernel, which needs an fp16 copy of
+  // the activation codes (2 M K bytes) in the workspace.
+  const size_t x16 = (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
+  p.tmem_a = int8 && p.swap && ws_avail >= x16;
+  p.x16_bytes = p.tmem_a ? x16 : 0;
+  p.bk = (int8 && !p.tmem_a) ? 64 : 128;
+  p.num_kb = (K + p.bk - 1) / p.bk;
   if (p.swap) {
     const int max_bn = int8 ? 128 : 256;
     int bn = 16;
@@ -32,17 +37,18 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
   int splits = 1;
   if (num_sms > 0 && tiles < num_sms) {
-    const int min_kb = int8 ? 8 : 4;
+    const int min_kb = (p.bk == 64) ? 8 : 4;
     const int want = static_cast<int>(num_sms / tiles);
     const int cap = std::max(1, p.num_kb / min_kb);
     splits = std::max(1, std::min(want, cap));
   }
   const size_t per_split = static_cast<size_t>(M) * N * 4;
-  if (splits > 1 && ws_avail < static_cast<size_t>(splits) * per_split)
-    splits = std::max(1, static_cast<int>(std::min<size_t>(ws_avail / per_split, 1 << 20)));
+  const size_t avail = ws_avail > p.x16_bytes ? ws_avail - p.x16_bytes : 0;
+  if (splits > 1 && avail < static_cast<size_t>(splits) * per_split)
+    splits = std::max(1, static_cast<int>(std::min<size_t>(avail / per_split, 1 << 20)));
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
-  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
+  p.ws_bytes = p.x16_bytes + (p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0);
   return p;
 }
 

@@ -34,13 +34,14 @@ struct GemmArgs {
   int* status;       // device status word
 };
 
-// quant.cu
+// quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
+// (the operand the INT8 decode GEMM reads), saving it a widening pass.
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             cudaStream_t st);
+                             void* x16, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, cudaStream_t st);
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, cudaStream_t st);
+                                  float* sx, float* h_out, void* x16, cudaStream_t st);
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st);
@@ -50,6 +51,8 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
 // How one GEMM call is cut into CTAs.
 struct GemmPlan {
   bool swap;         // weights on the MMA M side (decode)
+  bool tmem_a;       // INT8 decode: weights widened into TMEM, fp16 activation copy in the workspace
+  size_t x16_bytes;  // bytes of that fp16 copy at the start of the workspace (256-aligned)
   int bn;            // MMA N (tile width on the B side)
   int bk;            // k per k-block
   int tiles_tok;     // grid.x
@@ -57,7 +60,7 @@ struct GemmPlan {
   int splits;        // grid.z
   int num_kb;
   int kb_per_split;
-  size_t ws_bytes;   // workspace the split-K partials need (0 if splits == 1)
+  size_t ws_bytes;   // total workspace: fp16 activation copy + split-K partials
 };
 
 // gemm_plan.cu
@@ -68,6 +71,11 @@ cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUte
                             dim3 grid, cudaStream_t st);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                            dim3 grid, cudaStream_t st);
+// gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
+// int8 -> fp16 widening of the activation codes it reads.
+cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
+                            cudaStream_t st);
+cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st);
 // split-K reduction: T = int (INT8) or float (FP8)
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
                                  const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,

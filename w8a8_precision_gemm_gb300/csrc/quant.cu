@@ -18,6 +18,7 @@
 //   scale = absmax / qmax (absmax == 0 -> 1);  code = RNE(v / scale)
 //   clamped to +-127 (INT8), or e4m3 RNE with saturation (FP8).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -28,7 +29,8 @@
 namespace qurl {
 namespace {
 
-constexpr int kVPT = 8;  // 16-byte vectors cached per thread
+constexpr int kVPT = 8;           // 16-byte vectors cached per thread
+constexpr int kRowThreads = 512;  // most threads of a row CTA (register budget of the row kernels)
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -60,6 +62,52 @@ __device__ __forceinline__ float block_reduce(float v, float* red) {
   return r;
 }
 
+// s + c += y without rounding error in the pair (two-sum of s and y; the
+// rounding error goes to c).
+__device__ __forceinline__ void two_sum_acc(float& s, float& c, float y) {
+  const float t = __fadd_rn(s, y);
+  const float bp = __fsub_rn(t, s);
+  const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(y, bp));
+  s = t;
+  c = __fadd_rn(c, err);
+}
+
+// Block-wide sum of (s, c) pairs, compensated; every thread gets the result.
+__device__ __forceinline__ void block_reduce_pair(float& s, float& c, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float os = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    const float oc = __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    two_sum_acc(s, c, os);
+    c = __fadd_rn(c, oc);
+  }
+  if (lane == 0) {
+    red[2 * warp] = s;
+    red[2 * warp + 1] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float ts = lane < nw ? red[2 * lane] : 0.0f;
+    float tc = lane < nw ? red[2 * lane + 1] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float os = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+      const float oc = __shfl_xor_sync(0xFFFFFFFFu, tc, o);
+      two_sum_acc(ts, tc, os);
+      tc = __fadd_rn(tc, oc);
+    }
+    if (lane == 0) {
+      red[64] = ts;
+      red[65] = tc;
+    }
+  }
+  __syncthreads();
+  s = red[64];
+  c = red[65];
+  __syncthreads();
+}
+
 __device__ __forceinline__ float row_scale(float amax, int qt) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, qt == kQInt8 ? 127.0f : 448.0f);
 }
@@ -82,6 +130,26 @@ __device__ __forceinline__ uint2 encode8(const float (&v)[8], float scale, int q
 #pragma unroll
   for (int e = 0; e < 4; ++e) hi |= static_cast<uint32_t>(encode(v[4 + e], scale, qt)) << (8 * e);
   return make_uint2(lo, hi);
+}
+
+// Store 8 codes (and, for INT8 when x16 is given, the same 8 codes as fp16 --
+// exact, integers of magnitude <= 127 -- for the tensor-core GEMM to read).
+__device__ __forceinline__ void store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
+                                       const float (&v)[8], float scale, int qt) {
+  const uint2 c = encode8(v, scale, qt);
+  reinterpret_cast<uint2*>(q)[idx] = c;
+  if (x16 != nullptr) {
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t w = e < 2 ? c.x : c.y;
+      const int lo = static_cast<int8_t>((w >> (16 * (e & 1))) & 0xFF);
+      const int hi = static_cast<int8_t>((w >> (16 * (e & 1) + 8)) & 0xFF);
+      const __half2 p = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+      h[e] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    reinterpret_cast<uint4*>(x16)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
@@ -117,8 +185,8 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 
 // ------------------------------------------------------------------ activation quant
 
-__global__ void quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
-                                 uint8_t* __restrict__ Xq, float* __restrict__ sx) {
+__global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
+                                 uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16) {
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -135,38 +203,44 @@ __global__ void quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, lon
   amax = block_reduce<true>(amax, red);
   const float scale = row_scale(amax, qt);
   if (threadIdx.x == 0) sx[m] = scale;
-  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * K);
+  uint8_t* out = Xq + static_cast<size_t>(m) * K;
+  uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
     float x[8];
     bf16x8_to_f32(u, x);
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
-    out[idx] = encode8(x, scale, qt);
+    store8(out, out16, idx, x, scale, qt);
   });
 }
 
 // ------------------------------------------------------------------ RMSNorm -> quant
 
-__global__ void rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
-                                     float* __restrict__ sx, float* __restrict__ ms_out) {
-  __shared__ float red[33];
+                                     float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16) {
+  __shared__ float red[66];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(gamma);
   const int nvec = K >> 3;
   uint4 cache[kVPT];
   fill_cache(row, nvec, cache);
-  // mean of squares (fp32; this kernel's own, fixed reduction order)
-  float ss = 0.0f;
+  // mean of squares.  Each x^2 is exact in fp32 (a bf16 has an 8-bit
+  // significand); the sum is carried as an unevaluated pair s + c (error-free
+  // two-sum per term, Knuth) and divided by K in fp64, so ms is the fp32
+  // rounding of the mean to within ~2^-44 relative -- the same fp32 value a
+  // plain fp64 sum gives, except when the mean lies that close to a rounding
+  // midpoint.
+  float ss = 0.0f, sc = 0.0f;
   for_vectors(row, nvec, cache, [&](const uint4 u, int) {
     float x[8];
     bf16x8_to_f32(u, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
+    for (int e = 0; e < 8; ++e) two_sum_acc(ss, sc, __fmul_rn(x[e], x[e]));
   });
-  ss = block_reduce<false>(ss, red);
-  const float ms = __fdiv_rn(ss, static_cast<float>(K));
+  block_reduce_pair(ss, sc, red);
+  const float ms = static_cast<float>((static_cast<double>(ss) + static_cast<double>(sc)) / static_cast<double>(K));
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
   if (threadIdx.x == 0 && ms_out) ms_out[m] = ms;
   // v = (x * r) * gamma'
@@ -187,11 +261,12 @@ __global__ void rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K,
   amax = block_reduce<true>(amax, red);
   const float scale = row_scale(amax, qt);
   if (threadIdx.x == 0) sx[m] = scale;
-  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * K);
+  uint8_t* out = Xq + static_cast<size_t>(m) * K;
+  uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
     float x[8];
     normed(u, idx, x);
-    out[idx] = encode8(x, scale, qt);
+    store8(out, out16, idx, x, scale, qt);
   });
 }
 
@@ -208,9 +283,9 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
   }
 }
 
-__global__ void silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
+__global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
-                                      float* __restrict__ h_out) {
+                                      float* __restrict__ h_out, uint8_t* __restrict__ x16) {
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
@@ -244,13 +319,14 @@ __global__ void silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int 
   amax = block_reduce<true>(amax, red);
   const float scale = row_scale(amax, qt);
   if (threadIdx.x == 0) sx[m] = scale;
-  uint2* out = reinterpret_cast<uint2*>(Xq + static_cast<size_t>(m) * I);
+  uint8_t* out = Xq + static_cast<size_t>(m) * I;
+  uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
   visit([&](const uint4 g, const uint4 u, int idx) {
     float h[8];
     silu_mul8(g, u, h);
 #pragma unroll
     for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
-    out[idx] = encode8(h, scale, qt);
+    store8(out, out16, idx, h, scale, qt);
   });
 }
 
@@ -270,7 +346,7 @@ __device__ __forceinline__ void load_w8(const void* row, int idx, float (&w)[8])
 }
 
 template <bool kF32>
-__global__ void prepare_weights_kernel(const void* __restrict__ W, int K, long long ldw, float s, int qt,
+__global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void* __restrict__ W, int K, long long ldw, float s, int qt,
                                        uint8_t* __restrict__ Wq, float* __restrict__ sw, float* W_scaled) {
   __shared__ float red[33];
   const int n = blockIdx.x;
@@ -339,37 +415,39 @@ __global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* 
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(count, c);
 }
 
-// Threads per row-CTA: enough that kVPT vectors per thread cover the row.
+// Threads per row-CTA: enough that kVPT vectors per thread cover the row, at
+// most kRowThreads (longer rows stream their tail from L1/L2 in the code pass).
 int row_threads(int nvec) {
   int t = 32;
-  while (t < 1024 && t * kVPT < nvec) t *= 2;
+  while (t < kRowThreads && t * kVPT < nvec) t *= 2;
   return t;
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             cudaStream_t st) {
+                             void* x16, cudaStream_t st) {
   quant_act_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre,
-                                                       qt, reinterpret_cast<uint8_t*>(Xq), sx);
+                                                       qt, reinterpret_cast<uint8_t*>(Xq), sx,
+                                                       reinterpret_cast<uint8_t*>(x16));
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, cudaStream_t st) {
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st) {
   rmsnorm_quant_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx,
                                                            gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                                                           ms_out);
+                                                           ms_out, reinterpret_cast<uint8_t*>(x16));
   return cudaGetLastError();
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, cudaStream_t st) {
+                                  float* sx, float* h_out, void* x16, cudaStream_t st) {
   // two vectors (gate, up) are cached per position: use twice the threads
   int t = 32;
-  while (t < 1024 && t * (kVPT / 2) < I / 8) t *= 2;
+  while (t < kRowThreads && t * (kVPT / 2) < I / 8) t *= 2;
   silu_mul_quant_kernel<<<M, t, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt,
-                                         reinterpret_cast<uint8_t*>(Xq), sx, h_out);
+                                         reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
   return cudaGetLastError();
 }
 
