@@ -481,6 +481,30 @@ def run_ours(args):
     return 0
 
 
+def run_single(args):
+    """One projection's W8A8 linear call, repeated -- a small, fixed launch
+    sequence for profilers (e.g. ncu -k regex:w8a8_gemm -s 1 -c 1)."""
+    import w8a8_precision_gemm_gb300 as q
+    from w8a8_precision_gemm_gb300 import synth
+
+    model, proj = args.single.split(":")
+    K, N = (synth.SHAPES_7B if model == "7b" else synth.SHAPES_32B)[proj]
+    M = args.single_m
+    qt = q.INT8 if args.qtype == "int8" else q.FP8_E4M3
+    W = synth.weights(f"single/{model}/{proj}/W", N, K).cuda()
+    Wq, sw, _, _ = q.prepare_weights(W, qt, s=S_UAQ, keep_scaled=False)
+    del W
+    Xq, sx = q.quant_act(synth.activations(f"single/{model}/{proj}/X", M, K).cuda(), qt)
+    ws = q.workspace(M, N, K, qt)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.single_reps):
+        q.qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, ws)
+    torch.cuda.synchronize()
+    q.qurl_check_device_status()
+    print(json.dumps({"single": args.single, "M": M, "K": K, "N": N, "qtype": args.qtype, "reps": args.single_reps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,7 +516,12 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=32, help="tokens per oracle step (reference arm / sample)")
     ap.add_argument("--cpu-full-step", action="store_true", default=True,
                     help="time the oracle on one whole step (both batches) for cpu_baseline")
+    ap.add_argument("--single", default=None, help="model:proj, e.g. 7b:gate_up -- run one linear for profiling")
+    ap.add_argument("--single-m", type=int, default=256)
+    ap.add_argument("--single-reps", type=int, default=3)
     args = ap.parse_args()
+    if args.single:
+        return run_single(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -351,7 +351,9 @@ def test_fused_quant_entries(qt, M):
     q.qurl_quant_act_linear(X.cuda(), 1.5, Wq1, sw1, qt, Y1, xs1, sx, q.workspace(M, N, K, qt))
     q.qurl_silu_mul_quant_linear(GU.cuda(), 1.5, Wq2, sw2, qt, Y2, xs2, sx2, q.workspace(M, N, I, qt))
     Xq1, s1 = q.quant_act(X.cuda(), qt, pre_scale=1.5)
-    R1 = q.linear(Xq1, s1, Wq1, sw1, qt)  # no workspace: the other INT8 kernel, same bits
+    # INT8: no workspace runs the other INT8 kernel, with the same exact bits; FP8 sums in fp32, so
+    # the comparison keeps the same plan (same K split, same summation order)
+    R1 = q.linear(Xq1, s1, Wq1, sw1, qt, None if qt == q.INT8 else q.workspace(M, N, K, qt))
     Xq2, s2 = q.silu_mul_quant(GU.cuda(), qt, pre_scale=1.5)
     R2 = q.linear(Xq2, s2, Wq2, sw2, qt, q.workspace(M, N, I, qt))
     sync_ok()

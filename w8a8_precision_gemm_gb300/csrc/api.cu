@@ -172,9 +172,11 @@ qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int 
 // Run the GEMM; mode bf16 -> Y, otherwise raw accumulators -> acc_out.
 // x16_ready: the fp16 copy of Xq's codes is already at the start of the
 // workspace (written by a fused quantizer), so it is not widened again.
+// w_indep: the kernel launched just before the GEMM does not write Wq (a
+// quantizer of this library), so the GEMM may prefetch weights before it ends.
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                     bool x16_ready = false) {
+                     bool x16_ready = false, bool w_indep = false) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
@@ -202,6 +204,8 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.Y = reinterpret_cast<__nv_bfloat16*>(Y);
   a.ldy = ldy;
   a.status = dev->status;
+  // the widening kernel launched just below writes only the workspace
+  a.w_prefetch = (w_indep || (p.tmem_a && !x16_ready)) ? 1 : 0;
   const bool split = p.splits > 1;
   if (Y && !split) {
     a.mode = qurl::kModeBf16;
@@ -364,7 +368,7 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, x16,
                                        st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const void* Wq, const float* sw, int M,
@@ -377,7 +381,7 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
   QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, x16, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale, const void* Wq, const float* sw,
@@ -392,7 +396,7 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   void* x16 = fused_x16(M, N, I, qt, workspace, ws_bytes);
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, x16, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,

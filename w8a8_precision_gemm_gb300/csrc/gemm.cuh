@@ -268,23 +268,45 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  griddep_launch_dependents();
+  if (warp != 0) griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
       const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
+      // Weight tiles of the first stages may stream in while the previous
+      // kernel (which, per w_prefetch, does not write Wq) is finishing.
+      const int npre = args.w_prefetch ? min(STAGES, nkb) : 0;
+      for (int it = 0; it < npre; ++it) {
+        mbar_arrive_expect_tx(&bars.full[it], C::A_STAGE + C::B_STAGE);
+        const int kc = (kb0 + it) * C::BK;
+        if (SWAP)
+          tma_load_2d(stA + it * C::A_STAGE, &tmA, kc, a0, &bars.full[it], polA);
+        else
+          tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, b0, &bars.full[it], polB);
+      }
+      griddep_wait();
       int issued = 0;
       bool ok = true;
       for (int it = 0; it < nkb; ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
+        const int kc = (kb0 + it) * C::BK;
+        if (it < npre) {  // the weight half is in flight; add the activation half
+          if (SWAP)
+            tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, b0, &bars.full[s], polB);
+          else
+            tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, a0, &bars.full[s], polA);
+          ++issued;
+          continue;
+        }
         if (!mbar_wait(&bars.empty[s], ph ^ 1, status)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&bars.full[s], C::A_STAGE + C::B_STAGE);
-        const int kc = (kb0 + it) * C::BK;
         tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, a0, &bars.full[s], polA);
         tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, b0, &bars.full[s], polB);
         ++issued;
@@ -437,6 +459,8 @@ template <typename T>
 __global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
                                      const float* __restrict__ sx, const float* __restrict__ sw,
                                      __nv_bfloat16* __restrict__ Y, long long ldy, T* __restrict__ acc_out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const size_t total = static_cast<size_t>(M) * N;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
@@ -467,8 +491,7 @@ cudaError_t launch_gemm_inst(const CUtensorMap& ta, const CUtensorMap& tb, const
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, stream, ta, tb, args);
 }
 
 }  // namespace qurl

@@ -61,12 +61,12 @@ cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, in
   blocks = std::max<size_t>(blocks, 1);
   auto* y = reinterpret_cast<__nv_bfloat16*>(Y);
   if (qt == kQInt8)
-    splitk_reduce_kernel<int><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        reinterpret_cast<const int*>(part), splits, M, N, sx, sw, y, ldy, reinterpret_cast<int*>(acc_out));
-  else
-    splitk_reduce_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        reinterpret_cast<const float*>(part), splits, M, N, sx, sw, y, ldy, reinterpret_cast<float*>(acc_out));
-  return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel<int>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                      reinterpret_cast<const int*>(part), splits, M, N, sx, sw, y, ldy,
+                      reinterpret_cast<int*>(acc_out));
+  return launch_pdl(splitk_reduce_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    reinterpret_cast<const float*>(part), splits, M, N, sx, sw, y, ldy,
+                    reinterpret_cast<float*>(acc_out));
 }
 
 }  // namespace qurl

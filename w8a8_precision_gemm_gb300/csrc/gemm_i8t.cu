@@ -109,23 +109,35 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  griddep_launch_dependents();
+  if (warp != 0) griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t polW = l2_policy_evict_first();
       const uint64_t polX = l2_policy_evict_last();
+      // weight tiles of the first stages stream in while the previous kernel
+      // (which, per w_prefetch, does not write Wq) is finishing
+      const int npre = args.w_prefetch ? min(STAGES, nkb) : 0;
+      for (int it = 0; it < npre; ++it) {
+        mbar_arrive_expect_tx(&bars.full[it], C::W_STAGE + C::X_STAGE);
+        tma_load_2d(stW + it * C::W_STAGE, &tmW, (kb0 + it) * C::BK, a0, &bars.full[it], polW);
+      }
+      griddep_wait();
       int issued = 0;
       bool ok = true;
       for (int it = 0; it < nkb; ++it) {
         const int s = it % STAGES;
-        if (!mbar_wait(&bars.empty[s], ((it / STAGES) & 1) ^ 1, status)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars.full[s], C::W_STAGE + C::X_STAGE);
         const int kb = kb0 + it;
-        tma_load_2d(stW + s * C::W_STAGE, &tmW, kb * C::BK, a0, &bars.full[s], polW);
+        if (it >= npre) {
+          if (!mbar_wait(&bars.empty[s], ((it / STAGES) & 1) ^ 1, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.full[s], C::W_STAGE + C::X_STAGE);
+          tma_load_2d(stW + s * C::W_STAGE, &tmW, kb * C::BK, a0, &bars.full[s], polW);
+        }
         uint8_t* xs = stX + s * C::X_STAGE;
         tma_load_2d(xs, &tmX16, kb * C::BK * 2, b0, &bars.full[s], polX);
         tma_load_2d(xs + C::X_HALF, &tmX16, kb * C::BK * 2 + 128, b0, &bars.full[s], polX);
@@ -259,6 +271,8 @@ __global__ void __launch_bounds__(320, 1)
 
 // int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense.
 __global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec) {
+  griddep_launch_dependents();
+  griddep_wait();
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     uint4 lo, hi;
@@ -281,8 +295,7 @@ cudaError_t launch_i8t_inst(const CUtensorMap& tw, const CUtensorMap& tx, const 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, stream, tw, tx, args);
 }
 
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
@@ -303,9 +316,8 @@ cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, 
   const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  i8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint4*>(src),
-                                                                  reinterpret_cast<uint4*>(dst), nvec);
-  return cudaGetLastError();
+  return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec);
 }
 
 }  // namespace qurl

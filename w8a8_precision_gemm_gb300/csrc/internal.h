@@ -32,7 +32,30 @@ struct GemmArgs {
   long long ldy;
   void* part;        // [splits][M][N] int32 (INT8) or fp32 (FP8), mode kModeAcc
   int* status;       // device status word
+  int w_prefetch;    // the previous kernel in the stream does not write Wq: its first
+                     // stages may be loaded before waiting for that kernel
 };
+
+// Launch a kernel with programmatic stream serialization: it may start while
+// the previous kernel in the stream finishes; every kernel of this library
+// calls griddepcontrol.wait before it reads anything the previous kernel may
+// have written (weights excepted where the caller says they are not written
+// there, see GemmArgs::w_prefetch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
 // (the operand the INT8 decode GEMM reads), saving it a widening pass.

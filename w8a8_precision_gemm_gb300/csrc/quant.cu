@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace qurl {
 namespace {
@@ -187,6 +188,8 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
                                  uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -219,6 +222,8 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
                                      float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[66];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -286,6 +291,8 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
 __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
                                       float* __restrict__ h_out, uint8_t* __restrict__ x16) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
@@ -348,6 +355,8 @@ __device__ __forceinline__ void load_w8(const void* row, int idx, float (&w)[8])
 template <bool kF32>
 __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void* __restrict__ W, int K, long long ldw, float s, int qt,
                                        uint8_t* __restrict__ Wq, float* __restrict__ sw, float* W_scaled) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[33];
   const int n = blockIdx.x;
   const char* row = reinterpret_cast<const char*>(W) + static_cast<size_t>(n) * ldw * (kF32 ? 4 : 2);
@@ -381,6 +390,8 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
 }
 
 __global__ void fold_gamma_kernel(const float* __restrict__ gamma, int K, float s, float* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k < K) out[k] = __fmul_rn(gamma[k], s);
 }
@@ -396,6 +407,8 @@ __device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
 
 __global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b, size_t n,
                                   unsigned long long* __restrict__ count) {
+  griddep_launch_dependents();
+  griddep_wait();
   const size_t nv = n >> 4;
   const uint4* a4 = reinterpret_cast<const uint4*>(a);
   const uint4* b4 = reinterpret_cast<const uint4*>(b);
@@ -427,18 +440,16 @@ int row_threads(int nvec) {
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
                              void* x16, cudaStream_t st) {
-  quant_act_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre,
-                                                       qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                                                       reinterpret_cast<uint8_t*>(x16));
-  return cudaGetLastError();
+  return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
+                    reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
+                    reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
                                  int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st) {
-  rmsnorm_quant_kernel<<<M, row_threads(K / 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), K, ldx,
-                                                           gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                                                           ms_out, reinterpret_cast<uint8_t*>(x16));
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
+                    reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
+                    sx, ms_out, reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
@@ -446,25 +457,20 @@ cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, 
   // two vectors (gate, up) are cached per position: use twice the threads
   int t = 32;
   while (t < kRowThreads && t * (kVPT / 2) < I / 8) t *= 2;
-  silu_mul_quant_kernel<<<M, t, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt,
-                                         reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
-  return cudaGetLastError();
+  return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
+                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st) {
   const int t = row_threads(K / 8);
-  if (w_f32)
-    prepare_weights_kernel<true><<<N, t, 0, st>>>(W, K, ldw, s, qt, reinterpret_cast<uint8_t*>(Wq), sw, W_scaled);
-  else
-    prepare_weights_kernel<false><<<N, t, 0, st>>>(W, K, ldw, s, qt, reinterpret_cast<uint8_t*>(Wq), sw, W_scaled);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = w_f32 ? launch_pdl(prepare_weights_kernel<true>, dim3(N), dim3(t), 0, st, W, K, ldw, s, qt,
+                                     reinterpret_cast<uint8_t*>(Wq), sw, W_scaled)
+                        : launch_pdl(prepare_weights_kernel<false>, dim3(N), dim3(t), 0, st, W, K, ldw, s, qt,
+                                     reinterpret_cast<uint8_t*>(Wq), sw, W_scaled);
   if (e != cudaSuccess) return e;
-  if (gamma) {
-    fold_gamma_kernel<<<(K + 255) / 256, 256, 0, st>>>(gamma, K, s, gamma_folded);
-    e = cudaGetLastError();
-  }
+  if (gamma) e = launch_pdl(fold_gamma_kernel, dim3((K + 255) / 256), dim3(256), 0, st, gamma, K, s, gamma_folded);
   return e;
 }
 
@@ -477,9 +483,8 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
   const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 4;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  count_diff_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint8_t*>(a),
-                                                                  reinterpret_cast<const uint8_t*>(b), n, count);
-  return cudaGetLastError();
+  return launch_pdl(count_diff_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    reinterpret_cast<const uint8_t*>(a), reinterpret_cast<const uint8_t*>(b), n, count);
 }
 
 }  // namespace qurl
