@@ -8,7 +8,7 @@
 //   warp 0      TMA producer: streams A and B tiles into a STAGES-deep ring.
 //   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2-5   epilogue: TMEM -> registers -> scales -> bf16 (or raw partials).
-//   warps 6-9   (INT8 only) converters: int8 tiles -> fp16 tiles in the 128-byte
+//   warps 6-13  (INT8 only) converters: int8 tiles -> fp16 tiles in the 128-byte
 //               swizzled K-major layout the MMA reads.
 //
 // FP8-E4M3 runs tcgen05.mma kind::f8f6f4 directly on the TMA-loaded codes,
@@ -33,10 +33,83 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace qurl {
+
+// One work unit of a persistent GEMM CTA: a 128 x BN accumulator tile over
+// one K split.  Units are numbered token tile fastest, so CTAs running at the
+// same time share weight tiles (L2 reuse when there are several token tiles).
+struct Unit {
+  int a0, b0;    // first row of the A tile / of the B tile
+  int kb0, nkb;  // k-block range
+  int split;
+};
+
+template <bool SWAP, int BN>
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int u) {
+  const int tok = u % a.tiles_tok;
+  const int rest = u / a.tiles_tok;
+  const int ch = rest % a.tiles_ch;
+  const int sp = rest / a.tiles_ch;
+  Unit w;
+  w.a0 = (SWAP ? ch : tok) * 128;
+  w.b0 = (SWAP ? tok : ch) * BN;
+  w.kb0 = sp * a.kb_per_split;
+  w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
+  w.split = sp;
+  return w;
+}
+
+// The units one CTA processes: u, u + stride, ... < end.  Without clusters a
+// CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...; with an in-kernel
+// split-K reduction, cluster c takes tiles c, c + #clusters, ... and its CTA of
+// rank r the split r of each.
+struct UnitRange {
+  int u, stride, end;
+};
+
+__device__ __forceinline__ UnitRange unit_range(const GemmArgs& a) {
+  if (a.cluster_splits > 1) {
+    const int tiles = a.tiles_tok * a.tiles_ch;
+    const int rank = static_cast<int>(cluster_ctarank());
+    return {static_cast<int>(cluster_id_x()) + tiles * rank, static_cast<int>(cluster_count_x()),
+            tiles * (rank + 1)};
+  }
+  return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), a.tiles_tok * a.tiles_ch * a.splits};
+}
+
+// In-cluster split-K reduction of one decode tile (weights on the MMA M side):
+// every split's partial is in a.part; this CTA (rank r of S) sums, in split
+// order, the tokens j = r, r + S, ... of the tile for all of its 128 output
+// channels, then dequantizes to Y (or stores the raw sum to acc_out).  Thread
+// t (0..127) owns channel a0 + t, so a warp reads and writes 32 consecutive
+// channels.  Partials are read around L1 (another SM wrote them).
+template <int BN, typename T>
+__device__ __forceinline__ void cluster_reduce_tile(const GemmArgs& a, const Unit& w, int rank, int S, int t) {
+  const int n = w.a0 + t;
+  if (n >= a.N) return;
+  const size_t MN = static_cast<size_t>(a.M) * a.N;
+  const T* part = reinterpret_cast<const T*>(a.part);
+  const float swn = a.Y ? __ldg(a.sw + n) : 0.0f;
+  for (int j = rank; j < BN; j += S) {
+    const int m = w.b0 + j;
+    if (m >= a.M) break;
+    const size_t off = static_cast<size_t>(m) * a.N + n;
+    T acc = __ldcg(part + off);
+    for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
+    if (a.Y) {
+      const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), __ldg(a.sx + m)), swn);
+      a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
+    } else {
+      reinterpret_cast<T*>(a.acc_out)[off] = acc;
+    }
+  }
+}
 
 template <int QT, bool SWAP, int BN, int STAGES>
 struct GemmCfg {
@@ -50,8 +123,9 @@ struct GemmCfg {
   static constexpr int B_CONV = BN * 128;
   static constexpr int SMEM_TILES = CSTAGES * (A_CONV + B_CONV) + STAGES * (A_STAGE + B_STAGE);
   static constexpr int SMEM_BYTES = SMEM_TILES + 1024;  // slack for 1024-byte alignment
-  static constexpr int NUM_THREADS = kInt8 ? 320 : 192;
-  static constexpr int TMEM_USED = kInt8 ? 3 * BN : BN;
+  static constexpr int NUM_CONV = 256;                  // INT8 converter threads (warps 6-13)
+  static constexpr int NUM_THREADS = kInt8 ? 192 + NUM_CONV : 192;
+  static constexpr int TMEM_USED = kInt8 ? 3 * BN : 2 * BN;  // two accumulator buffers (+ int32 sum)
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                    : TMEM_USED <= 64  ? 64
                                    : TMEM_USED <= 128 ? 128
@@ -75,6 +149,7 @@ struct GemmBarriers {
   uint64_t pfull[2];        // MMA -> epilogue (accumulator chunk ready)
   uint64_t pempty[2];       // epilogue -> MMA (TMEM buffer drained)
   uint64_t done;            // MMA drain on the error path
+  uint64_t red_full;        // in-cluster split-K: every split's partial of the tile is written
   uint32_t tmem_base;
 };
 
@@ -118,12 +193,12 @@ __device__ __forceinline__ void i8x16_to_f16x16(const uint4 v, uint4& lo, uint4&
 // Widen a staged int8 tile (rows x 64 bytes, row-major, unswizzled) into an
 // fp16 tile of rows x 128 bytes in the 128-byte swizzled K-major layout: the
 // 16-byte chunk c of row r lives at (r/8)*1024 + (r%8)*128 + ((c ^ (r%8))*16).
-// 128 threads; thread t converts 16 codes (chunk t%4) of rows t/4, t/4+32, ...
-// A quarter-warp reads 128 contiguous bytes and writes 8 distinct chunk
-// positions, so neither side has bank conflicts.
-__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows, int t) {
+// nthreads threads; thread t converts 16 codes (chunk t%4) of rows t/4,
+// t/4 + nthreads/4, ...  A quarter-warp reads 128 contiguous bytes and writes 8
+// distinct chunk positions, so neither side has bank conflicts.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows, int t, int nthreads) {
   const int j = t & 3;
-  for (int r = t >> 2; r < rows; r += 32) {
+  for (int r = t >> 2; r < rows; r += nthreads >> 2) {
     const uint4 v = *reinterpret_cast<const uint4*>(src + r * 64 + j * 16);
     uint4 lo, hi;
     i8x16_to_f16x16(v, lo, hi);
@@ -136,10 +211,11 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
 // Write 32 accumulator values of one tile row/column.  i = row of the A tile
 // (TMEM lane), columns c0..c0+31 of the B tile.
 template <bool SWAP, int BN, typename T>
-__device__ __forceinline__ void emit32(const GemmArgs& a, int a0, int b0, int i, int c0, const T (&v)[32]) {
+__device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int b0, int split, int i, int c0,
+                                       const T (&v)[32]) {
   const int M = a.M, N = a.N;
-  if (a.mode == kModeAcc) {
-    T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(blockIdx.z) * M * N;
+  if (mode == kModeAcc) {
+    T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(split) * M * N;
     if (SWAP) {
       const int n = a0 + i;
       if (n < N) {
@@ -230,23 +306,20 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int a_tile = SWAP ? blockIdx.y : blockIdx.x;
-  const int b_tile = SWAP ? blockIdx.x : blockIdx.y;
-  const int a0 = a_tile * C::BM;
-  const int b0 = b_tile * BN;
-  const int kb0 = blockIdx.z * args.kb_per_split;
-  const int nkb = min(args.num_kb - kb0, args.kb_per_split);  // >= 1 by construction
+  const UnitRange R = unit_range(args);
+  const int S = args.cluster_splits;  // > 1: in-cluster split-K reduction
   int* status = args.status;
 
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.empty[s], C::kInt8 ? 128 : 1);
+      mbar_init(&bars.empty[s], C::kInt8 ? C::NUM_CONV : 1);
     }
+    mbar_init(&bars.red_full, S > 1 ? S * 128 : 1);
 #pragma unroll
     for (int s = 0; s < (C::CSTAGES > 0 ? C::CSTAGES : 1); ++s) {
-      mbar_init(&bars.cfull[s], 128);
+      mbar_init(&bars.cfull[s], C::NUM_CONV);
       mbar_init(&bars.cempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -267,6 +340,7 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (S > 1) cluster_sync();  // every CTA's barriers are initialised before remote arrives
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
@@ -278,41 +352,45 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
       const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
       // Weight tiles of the first stages may stream in while the previous
       // kernel (which, per w_prefetch, does not write Wq) is finishing.
-      const int npre = args.w_prefetch ? min(STAGES, nkb) : 0;
-      for (int it = 0; it < npre; ++it) {
-        mbar_arrive_expect_tx(&bars.full[it], C::A_STAGE + C::B_STAGE);
-        const int kc = (kb0 + it) * C::BK;
-        if (SWAP)
-          tma_load_2d(stA + it * C::A_STAGE, &tmA, kc, a0, &bars.full[it], polA);
-        else
-          tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, b0, &bars.full[it], polB);
+      int npre = 0;
+      if (args.w_prefetch && R.u < R.end) {
+        const Unit w = unit_of<SWAP, BN>(args, R.u);
+        npre = min(STAGES, w.nkb);
+        for (int it = 0; it < npre; ++it) {
+          mbar_arrive_expect_tx(&bars.full[it], C::A_STAGE + C::B_STAGE);
+          const int kc = (w.kb0 + it) * C::BK;
+          if (SWAP)
+            tma_load_2d(stA + it * C::A_STAGE, &tmA, kc, w.a0, &bars.full[it], polA);
+          else
+            tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, w.b0, &bars.full[it], polB);
+        }
       }
       griddep_wait();
-      int issued = 0;
+      int g = 0;  // k-blocks issued by this CTA (ring position)
       bool ok = true;
-      for (int it = 0; it < nkb; ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int kc = (kb0 + it) * C::BK;
-        if (it < npre) {  // the weight half is in flight; add the activation half
-          if (SWAP)
-            tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, b0, &bars.full[s], polB);
-          else
-            tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, a0, &bars.full[s], polA);
-          ++issued;
-          continue;
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<SWAP, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g) {
+          const int s = g % STAGES;
+          const int kc = (w.kb0 + it) * C::BK;
+          if (g < npre) {  // the weight half is in flight; add the activation half
+            if (SWAP)
+              tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, w.b0, &bars.full[s], polB);
+            else
+              tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, w.a0, &bars.full[s], polA);
+            continue;
+          }
+          if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.full[s], C::A_STAGE + C::B_STAGE);
+          tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, w.a0, &bars.full[s], polA);
+          tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, w.b0, &bars.full[s], polB);
         }
-        if (!mbar_wait(&bars.empty[s], ph ^ 1, status)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars.full[s], C::A_STAGE + C::B_STAGE);
-        tma_load_2d(stA + s * C::A_STAGE, &tmA, kc, a0, &bars.full[s], polA);
-        tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, b0, &bars.full[s], polB);
-        ++issued;
       }
       if (!ok) {  // let the copies still in flight land before the CTA leaves
-        for (int it = max(0, issued - STAGES); it < issued; ++it)
+        for (int it = max(0, g - STAGES); it < g; ++it)
           mbar_wait_drain(&bars.full[it % STAGES], (it / STAGES) & 1, status);
       }
     }
@@ -321,50 +399,53 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
-      if constexpr (!C::kInt8) {
-        for (int it = 0; it < nkb; ++it) {
-          const int s = it % STAGES;
-          if (!mbar_wait(&bars.full[s], (it / STAGES) & 1, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_addr(stA + s * C::A_STAGE);
-          const uint32_t sb = smem_addr(stB + s * C::B_STAGE);
-#pragma unroll
-          for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
-            umma_f8f6f4(tmem, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
-                        C::IDESC, (it | kk) != 0);
-          umma_commit(&bars.empty[s]);
-        }
-        if (ok) umma_commit(&bars.pfull[0]);
-      } else {  // INT8
-        for (int it = 0; it < nkb; ++it) {
-          const int c = it / C::CHUNK_KB;
+      int g = 0;   // k-blocks consumed
+      int cg = 0;  // accumulator chunks started (buffer cg & 1)
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<SWAP, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g) {
           const int kin = it % C::CHUNK_KB;
-          const int buf = c & 1;
-          if (kin == 0 && c >= 2) {
-            if (!mbar_wait(&bars.pempty[buf], ((c >> 1) - 1) & 1, status)) {
+          const int buf = cg & 1;
+          if (kin == 0 && cg >= 2) {  // the epilogue must have drained this buffer's previous chunk
+            if (!mbar_wait(&bars.pempty[buf], ((cg >> 1) - 1) & 1, status)) {
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t d = tmem + buf * BN;
+          if constexpr (!C::kInt8) {
+            const int s = g % STAGES;
+            if (!mbar_wait(&bars.full[s], (g / STAGES) & 1, status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-          }
-          const int cs = it % C::CSTAGES;
-          if (!mbar_wait(&bars.cfull[cs], (it / C::CSTAGES) & 1, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_addr(convA + cs * C::A_CONV);
-          const uint32_t sb = smem_addr(convB + cs * C::B_CONV);
-          const uint32_t d = tmem + buf * BN;
+            const uint32_t sa = smem_addr(stA + s * C::A_STAGE);
+            const uint32_t sb = smem_addr(stB + s * C::B_STAGE);
 #pragma unroll
-          for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
-            umma_f16(d, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
-                     C::IDESC, (kin | kk) != 0);
-          umma_commit(&bars.cempty[cs]);
-          if (kin == C::CHUNK_KB - 1 || it == nkb - 1) umma_commit(&bars.pfull[buf]);
+            for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
+              umma_f8f6f4(d, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
+                          C::IDESC, (kin | kk) != 0);
+            umma_commit(&bars.empty[s]);
+          } else {
+            const int cs = g % C::CSTAGES;
+            if (!mbar_wait(&bars.cfull[cs], (g / C::CSTAGES) & 1, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_addr(convA + cs * C::A_CONV);
+            const uint32_t sb = smem_addr(convB + cs * C::B_CONV);
+#pragma unroll
+            for (int kk = 0; kk < C::MMAS_PER_KB; ++kk)
+              umma_f16(d, umma_desc_sw128(sa + kk * C::MMA_K_BYTES), umma_desc_sw128(sb + kk * C::MMA_K_BYTES),
+                       C::IDESC, (kin | kk) != 0);
+            umma_commit(&bars.cempty[cs]);
+          }
+          if (kin == C::CHUNK_KB - 1 || it == w.nkb - 1) {
+            umma_commit(&bars.pfull[buf]);
+            ++cg;
+          }
         }
       }
       if (!ok) {  // no MMA may still be writing TMEM when it is released
@@ -378,69 +459,93 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     const int q = warp & 3;               // TMEM lane quadrant this warp may access
     const int i = q * 32 + lane;          // row of the A tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    if constexpr (!C::kInt8) {
-      if (warp_wait(&bars.pfull[0], 0, status)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + c0, r);
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          emit32<SWAP, BN, float>(args, a0, b0, i, c0, v);
+    const uint32_t tR = lane_base + 2 * BN;  // INT8: int32 running sum
+    const int emode = S > 1 ? kModeAcc : args.mode;  // a clustered split writes its partial first
+    int cg = 0, red_iter = 0;
+    bool ok = true;
+    for (int u = R.u; u < R.end && ok; u += R.stride) {
+      const Unit w = unit_of<SWAP, BN>(args, u);
+      const int nch = (w.nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
+      for (int c = 0; c < nch; ++c, ++cg) {
+        const int buf = cg & 1;
+        if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) {
+          ok = false;
+          break;
         }
-      }
-    } else {
-      const int nch = (nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
-      const uint32_t tR = lane_base + 2 * BN;  // int32 running sum
-      for (int c = 0; c < nch; ++c) {
-        const int buf = c & 1;
-        if (!warp_wait(&bars.pfull[buf], (c >> 1) & 1, status)) break;
         tc_fence_after();
         const bool last = (c == nch - 1);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t p[32];
           tmem_ld32(lane_base + buf * BN + c0, p);
-          int v[32];
-          if (c > 0) {
-            uint32_t rs[32];
-            tmem_ld32(tR + c0, rs);
+          if constexpr (!C::kInt8) {
+            float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
+            emit32<SWAP, BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
           } else {
+            int v[32];
+            if (c > 0) {
+              uint32_t rs[32];
+              tmem_ld32(tR + c0, rs);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
-          }
-          if (!last) {
-            uint32_t w[32];
+              for (int j = 0; j < 32; ++j)
+                v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = static_cast<uint32_t>(v[j]);
-            tmem_st32(tR + c0, w);
-          } else {
-            emit32<SWAP, BN, int>(args, a0, b0, i, c0, v);
+              for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
+            }
+            if (!last) {
+              uint32_t wv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) wv[j] = static_cast<uint32_t>(v[j]);
+              tmem_st32(tR + c0, wv);
+            } else {
+              emit32<SWAP, BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+            }
           }
         }
-        if (!last) tmem_wait_st();
+        if (C::kInt8 && !last) tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.pempty[buf]);
+      }
+      if (ok && SWAP && S > 1) {
+        // every split of this tile has written its partial: reduce this CTA's share
+        for (int r = 0; r < S; ++r) mbar_arrive_cluster(&bars.red_full, r);
+        if (!mbar_wait_cluster(&bars.red_full, red_iter & 1, status)) {
+          ok = false;
+          break;
+        }
+        ++red_iter;
+        cluster_reduce_tile<BN, typename std::conditional<C::kInt8, int, float>::type>(
+            args, w, static_cast<int>(cluster_ctarank()), S, threadIdx.x - 64);
       }
     }
   } else {
     // ------------------------------------------------------------ converters (INT8)
     if constexpr (C::kInt8) {
       const int t = threadIdx.x - 192;
-      for (int it = 0; it < nkb; ++it) {
-        const int s = it % STAGES;
-        if (!warp_wait(&bars.full[s], (it / STAGES) & 1, status)) break;
-        const int cs = it % C::CSTAGES;
-        if (!warp_wait(&bars.cempty[cs], ((it / C::CSTAGES) & 1) ^ 1, status)) break;
-        convert_tile(stA + s * C::A_STAGE, convA + cs * C::A_CONV, C::BM, t);
-        convert_tile(stB + s * C::B_STAGE, convB + cs * C::B_CONV, BN, t);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars.empty[s]);
-        mbar_arrive(&bars.cfull[cs]);
+      int g = 0;
+      bool ok = true;
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<SWAP, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g) {
+          const int s = g % STAGES;
+          if (!warp_wait(&bars.full[s], (g / STAGES) & 1, status)) {
+            ok = false;
+            break;
+          }
+          const int cs = g % C::CSTAGES;
+          if (!warp_wait(&bars.cempty[cs], ((g / C::CSTAGES) & 1) ^ 1, status)) {
+            ok = false;
+            break;
+          }
+          convert_tile(stA + s * C::A_STAGE, convA + cs * C::A_CONV, C::BM, t, C::NUM_CONV);
+          convert_tile(stB + s * C::B_STAGE, convB + cs * C::B_CONV, BN, t, C::NUM_CONV);
+          fence_proxy_async_smem();
+          mbar_arrive(&bars.empty[s]);
+          mbar_arrive(&bars.cfull[cs]);
+        }
       }
     }
   }
@@ -451,6 +556,7 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  if (S > 1) cluster_sync();  // no CTA leaves while the cluster may still signal it
 }
 
 // Split-K reduction in a fixed order (z = 0, 1, ...), then either the
@@ -478,20 +584,56 @@ __global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int
 }
 
 // Host-side launch of one instantiation.
-template <int QT, bool SWAP, int BN, int STAGES>
-cudaError_t launch_gemm_inst(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, dim3 grid,
-                             cudaStream_t stream) {
-  using C = GemmCfg<QT, SWAP, BN, STAGES>;
-  auto kern = w8a8_gemm_kernel<QT, SWAP, BN, STAGES>;
+// The unit grid (token tiles, channel tiles, splits) becomes a persistent
+// launch of one CTA per SM (fewer when there are fewer units).
+int persistent_ctas(const GemmArgs& a);
+
+// Launch a persistent GEMM kernel for grid = (token tiles, channel tiles,
+// splits).  With allow_cluster (decode tiles, K split in 2..8 parts) the splits
+// of each tile become one cluster that reduces in the kernel, provided every
+// tile gets a co-resident cluster in one round; the number of splits may be
+// lowered to the largest count for which that holds.
+template <typename Kern>
+cudaError_t launch_persistent(Kern kern, int threads, int smem, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const GemmArgs& args_in, dim3 grid, cudaStream_t stream, bool allow_cluster,
+                              bool* reduced) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  return launch_pdl(kern, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, stream, ta, tb, args);
+  GemmArgs args = args_in;
+  args.tiles_tok = grid.x;
+  args.tiles_ch = grid.y;
+  args.splits = grid.z;
+  args.cluster_splits = 0;
+  if (reduced) *reduced = false;
+  const int tiles = static_cast<int>(grid.x * grid.y);
+  if (allow_cluster && grid.z > 1) {
+    for (int S = std::min(static_cast<int>(grid.z), 8); S >= 2; --S) {
+      if (max_active_clusters(reinterpret_cast<const void*>(kern), S, threads, smem) < tiles) continue;
+      args.kb_per_split = (args.num_kb + S - 1) / S;
+      args.splits = (args.num_kb + args.kb_per_split - 1) / args.kb_per_split;
+      if (args.splits != S) continue;  // every rank of the cluster needs a non-empty split
+      args.cluster_splits = S;
+      if (reduced) *reduced = true;
+      return launch_pdl_cluster(kern, dim3(tiles * S), dim3(threads), smem, stream, S, ta, tb, args);
+    }
+    args.kb_per_split = args_in.kb_per_split;
+    args.splits = grid.z;
+  }
+  return launch_pdl(kern, dim3(persistent_ctas(args)), dim3(threads), smem, stream, ta, tb, args);
+}
+
+template <int QT, bool SWAP, int BN, int STAGES>
+cudaError_t launch_gemm_inst(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, dim3 grid,
+                             cudaStream_t stream, bool allow_cluster, bool* reduced) {
+  using C = GemmCfg<QT, SWAP, BN, STAGES>;
+  return launch_persistent(w8a8_gemm_kernel<QT, SWAP, BN, STAGES>, C::NUM_THREADS, C::SMEM_BYTES, ta, tb, args,
+                           grid, stream, allow_cluster && SWAP, reduced);
 }
 
 }  // namespace qurl

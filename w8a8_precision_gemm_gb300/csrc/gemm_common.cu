@@ -1,5 +1,6 @@
 // gemm_common.cu -- tile planning and the split-K reduction of the W8A8 GEMM.
 #include <algorithm>
+#include <mutex>
 
 #include "gemm.cuh"
 
@@ -50,6 +51,55 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.ws_bytes = p.x16_bytes + (p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0);
   return p;
+}
+
+int max_active_clusters(const void* kern, int cluster_x, int threads, int smem) {
+  struct Entry {
+    const void* kern;
+    int dev, cluster_x, value;
+  };
+  static std::mutex mu;
+  static Entry cache[256];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].kern == kern && cache[i].dev == dev && cache[i].cluster_x == cluster_x) return cache[i].value;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster_x * 64);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 256) cache[used++] = Entry{kern, dev, cluster_x, n};
+  return n;
+}
+
+int persistent_ctas(const GemmArgs& a) {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int n = (dev >= 0 && dev < 64) ? sms[dev] : 0;
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev >= 0 && dev < 64) sms[dev] = n;
+  }
+  const long long units = static_cast<long long>(a.tiles_tok) * a.tiles_ch * a.splits;
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(units, n)));
 }
 
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,

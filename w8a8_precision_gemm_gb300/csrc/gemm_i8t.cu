@@ -29,7 +29,7 @@ struct I8tCfg {
   static constexpr int X_HALF = BN * 128;                 // fp16 [BN][64] swizzled half
   static constexpr int X_STAGE = 2 * X_HALF;
   static constexpr int SMEM_BYTES = STAGES * (W_STAGE + X_STAGE) + 1024;
-  static constexpr int NUM_THREADS = 320;
+  static constexpr int NUM_THREADS = 448;  // TMA, MMA, 4 epilogue warps, 8 converter warps
   static constexpr int A_BASE = ((3 * BN + 63) / 64) * 64;  // TMEM column of the first A stage
   static constexpr int A_COLS = 64;                       // 128 fp16 per lane per k-block
   static constexpr int TMEM_USED = A_BASE + ASTAGES * A_COLS;
@@ -53,17 +53,18 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 template <int STAGES, int ASTAGES>
 struct I8tBarriers {
   uint64_t full[STAGES];     // TMA (weights + fp16 activations) landed
-  uint64_t empty[STAGES];    // converters read the weights (128) and the MMA read the activations (1)
+  uint64_t empty[STAGES];    // converters read the weights (256) and the MMA read the activations (1)
   uint64_t afull[ASTAGES];   // converters -> MMA: A stage written to TMEM
   uint64_t aempty[ASTAGES];  // MMA -> converters: A stage consumed
   uint64_t pfull[2];
   uint64_t pempty[2];
   uint64_t done;
+  uint64_t red_full;  // in-cluster split-K: every split's partial of the tile is written
   uint32_t tmem_base;
 };
 
 template <int BN, int STAGES, int ASTAGES>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     w8a8_gemm_i8t_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX16,
                          const GemmArgs args) {
   using C = I8tCfg<BN, STAGES, ASTAGES>;
@@ -75,19 +76,18 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int a0 = blockIdx.y * C::BM;  // first weight row (output channel)
-  const int b0 = blockIdx.x * BN;     // first token
-  const int kb0 = blockIdx.z * args.kb_per_split;
-  const int nkb = min(args.num_kb - kb0, args.kb_per_split);
+  const UnitRange R = unit_range(args);
+  const int S = args.cluster_splits;  // > 1: in-cluster split-K reduction
   int* status = args.status;
 
   if (threadIdx.x == 0) {
+    mbar_init(&bars.red_full, S > 1 ? S * 128 : 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.empty[s], 129);
+      mbar_init(&bars.empty[s], 257);  // 256 converter threads + the MMA's commit
     }
     for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(&bars.afull[s], 128);
+      mbar_init(&bars.afull[s], 256);
       mbar_init(&bars.aempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (S > 1) cluster_sync();  // every CTA's barriers are initialised before remote arrives
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
@@ -119,32 +120,38 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t polX = l2_policy_evict_last();
       // weight tiles of the first stages stream in while the previous kernel
       // (which, per w_prefetch, does not write Wq) is finishing
-      const int npre = args.w_prefetch ? min(STAGES, nkb) : 0;
-      for (int it = 0; it < npre; ++it) {
-        mbar_arrive_expect_tx(&bars.full[it], C::W_STAGE + C::X_STAGE);
-        tma_load_2d(stW + it * C::W_STAGE, &tmW, (kb0 + it) * C::BK, a0, &bars.full[it], polW);
+      int npre = 0;
+      if (args.w_prefetch && R.u < R.end) {
+        const Unit w = unit_of<true, BN>(args, R.u);
+        npre = min(STAGES, w.nkb);
+        for (int it = 0; it < npre; ++it) {
+          mbar_arrive_expect_tx(&bars.full[it], C::W_STAGE + C::X_STAGE);
+          tma_load_2d(stW + it * C::W_STAGE, &tmW, (w.kb0 + it) * C::BK, w.a0, &bars.full[it], polW);
+        }
       }
       griddep_wait();
-      int issued = 0;
+      int g = 0;
       bool ok = true;
-      for (int it = 0; it < nkb; ++it) {
-        const int s = it % STAGES;
-        const int kb = kb0 + it;
-        if (it >= npre) {
-          if (!mbar_wait(&bars.empty[s], ((it / STAGES) & 1) ^ 1, status)) {
-            ok = false;
-            break;
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<true, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g) {
+          const int s = g % STAGES;
+          const int kb = w.kb0 + it;
+          if (g >= npre) {
+            if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars.full[s], C::W_STAGE + C::X_STAGE);
+            tma_load_2d(stW + s * C::W_STAGE, &tmW, kb * C::BK, w.a0, &bars.full[s], polW);
           }
-          mbar_arrive_expect_tx(&bars.full[s], C::W_STAGE + C::X_STAGE);
-          tma_load_2d(stW + s * C::W_STAGE, &tmW, kb * C::BK, a0, &bars.full[s], polW);
+          uint8_t* xs = stX + s * C::X_STAGE;
+          tma_load_2d(xs, &tmX16, kb * C::BK * 2, w.b0, &bars.full[s], polX);
+          tma_load_2d(xs + C::X_HALF, &tmX16, kb * C::BK * 2 + 128, w.b0, &bars.full[s], polX);
         }
-        uint8_t* xs = stX + s * C::X_STAGE;
-        tma_load_2d(xs, &tmX16, kb * C::BK * 2, b0, &bars.full[s], polX);
-        tma_load_2d(xs + C::X_HALF, &tmX16, kb * C::BK * 2 + 128, b0, &bars.full[s], polX);
-        ++issued;
       }
       if (!ok) {
-        for (int it = max(0, issued - STAGES); it < issued; ++it)
+        for (int it = max(0, g - STAGES); it < g; ++it)
           mbar_wait_drain(&bars.full[it % STAGES], (it / STAGES) & 1, status);
       }
     }
@@ -153,35 +160,41 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
-      for (int it = 0; it < nkb; ++it) {
-        const int c = it / C::CHUNK_KB;
-        const int kin = it % C::CHUNK_KB;
-        const int buf = c & 1;
-        if (kin == 0 && c >= 2) {
-          if (!mbar_wait(&bars.pempty[buf], ((c >> 1) - 1) & 1, status)) {
+      int g = 0, cg = 0;
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<true, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g) {
+          const int kin = it % C::CHUNK_KB;
+          const int buf = cg & 1;
+          if (kin == 0 && cg >= 2) {
+            if (!mbar_wait(&bars.pempty[buf], ((cg >> 1) - 1) & 1, status)) {
+              ok = false;
+              break;
+            }
+          }
+          const int s = g % STAGES;
+          const int as = g % ASTAGES;
+          if (!mbar_wait(&bars.full[s], (g / STAGES) & 1, status) ||
+              !mbar_wait(&bars.afull[as], (g / ASTAGES) & 1, status)) {
             ok = false;
             break;
           }
-        }
-        const int s = it % STAGES;
-        const int as = it % ASTAGES;
-        if (!mbar_wait(&bars.full[s], (it / STAGES) & 1, status) ||
-            !mbar_wait(&bars.afull[as], (it / ASTAGES) & 1, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem + buf * BN;
-        const uint32_t a_t = tmem + C::A_BASE + as * C::A_COLS;
-        const uint32_t xs = smem_addr(stX + s * C::X_STAGE);
+          tc_fence_after();
+          const uint32_t d = tmem + buf * BN;
+          const uint32_t a_t = tmem + C::A_BASE + as * C::A_COLS;
+          const uint32_t xs = smem_addr(stX + s * C::X_STAGE);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t b_addr = xs + (kk >> 2) * C::X_HALF + (kk & 3) * 32;
-          umma_f16_tmem_a(d, a_t + kk * 8, umma_desc_sw128(b_addr), C::IDESC, (kin | kk) != 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t b_addr = xs + (kk >> 2) * C::X_HALF + (kk & 3) * 32;
+            umma_f16_tmem_a(d, a_t + kk * 8, umma_desc_sw128(b_addr), C::IDESC, (kin | kk) != 0);
+          }
+          umma_commit(&bars.empty[s]);
+          umma_commit(&bars.aempty[as]);
+          if (kin == C::CHUNK_KB - 1 || it == w.nkb - 1) {
+            umma_commit(&bars.pfull[buf]);
+            ++cg;
+          }
         }
-        umma_commit(&bars.empty[s]);
-        umma_commit(&bars.aempty[as]);
-        if (kin == C::CHUNK_KB - 1 || it == nkb - 1) umma_commit(&bars.pfull[buf]);
       }
       if (!ok) {
         umma_commit(&bars.done);
@@ -194,54 +207,80 @@ __global__ void __launch_bounds__(320, 1)
     const int q = warp & 3;
     const int i = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int nch = (nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
     const uint32_t tR = lane_base + 2 * BN;
-    for (int c = 0; c < nch; ++c) {
-      const int buf = c & 1;
-      if (!warp_wait(&bars.pfull[buf], (c >> 1) & 1, status)) break;
-      tc_fence_after();
-      const bool last = (c == nch - 1);
+    const int emode = S > 1 ? kModeAcc : args.mode;  // a clustered split writes its partial first
+    int cg = 0, red_iter = 0;
+    bool ok = true;
+    for (int u = R.u; u < R.end && ok; u += R.stride) {
+      const Unit w = unit_of<true, BN>(args, u);
+      const int nch = (w.nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
+      for (int c = 0; c < nch; ++c, ++cg) {
+        const int buf = cg & 1;
+        if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool last = (c == nch - 1);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t p[32];
-        tmem_ld32(lane_base + buf * BN + c0, p);
-        int v[32];
-        if (c > 0) {
-          uint32_t rs[32];
-          tmem_ld32(tR + c0, rs);
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t p[32];
+          tmem_ld32(lane_base + buf * BN + c0, p);
+          int v[32];
+          if (c > 0) {
+            uint32_t rs[32];
+            tmem_ld32(tR + c0, rs);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
-        } else {
+            for (int j = 0; j < 32; ++j) v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
+            for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
+          }
+          if (!last) {
+            uint32_t wv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) wv[j] = static_cast<uint32_t>(v[j]);
+            tmem_st32(tR + c0, wv);
+          } else {
+            emit32<true, BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+          }
         }
-        if (!last) {
-          uint32_t w[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) w[j] = static_cast<uint32_t>(v[j]);
-          tmem_st32(tR + c0, w);
-        } else {
-          emit32<true, BN, int>(args, a0, b0, i, c0, v);
-        }
+        if (!last) tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.pempty[buf]);
       }
-      if (!last) tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars.pempty[buf]);
+      if (ok && S > 1) {
+        // every split of this tile has written its partial: reduce this CTA's share
+        for (int r = 0; r < S; ++r) mbar_arrive_cluster(&bars.red_full, r);
+        if (!mbar_wait_cluster(&bars.red_full, red_iter & 1, status)) {
+          ok = false;
+          break;
+        }
+        ++red_iter;
+        cluster_reduce_tile<BN, int>(args, w, static_cast<int>(cluster_ctarank()), S, threadIdx.x - 64);
+      }
     }
   } else {
     // ------------------------------------------------------------ converters: weights -> fp16 in TMEM
+    // Two warps per TMEM lane quadrant: warps 6-9 widen codes 0-63 of their
+    // rows (TMEM columns 0-31 of the stage), warps 10-13 codes 64-127.
     const int q = warp & 3;
+    const int half = (warp - 6) >> 2;
     const int i = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    for (int it = 0; it < nkb; ++it) {
-      const int s = it % STAGES;
-      const int as = it % ASTAGES;
-      if (!warp_wait(&bars.full[s], (it / STAGES) & 1, status)) break;
-      if (!warp_wait(&bars.aempty[as], ((it / ASTAGES) & 1) ^ 1, status)) break;
-      const uint8_t* wrow = stW + s * C::W_STAGE + (i >> 3) * 1024 + (i & 7) * 128;
-      const uint32_t a_t = lane_base + C::A_BASE + as * C::A_COLS;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+    int g = 0;
+    bool ok = true;
+    for (int u = R.u; u < R.end && ok; u += R.stride) {
+      const Unit w = unit_of<true, BN>(args, u);
+      for (int it = 0; it < w.nkb; ++it, ++g) {
+        const int s = g % STAGES;
+        const int as = g % ASTAGES;
+        if (!warp_wait(&bars.full[s], (g / STAGES) & 1, status) ||
+            !warp_wait(&bars.aempty[as], ((g / ASTAGES) & 1) ^ 1, status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* wrow = stW + s * C::W_STAGE + (i >> 3) * 1024 + (i & 7) * 128;
         uint32_t v[32];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -252,12 +291,12 @@ __global__ void __launch_bounds__(320, 1)
           v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
           v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
         }
-        tmem_st32(a_t + half * 32, v);
+        tmem_st32(lane_base + C::A_BASE + as * C::A_COLS + half * 32, v);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.afull[as]);
+        mbar_arrive(&bars.empty[s]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars.afull[as]);
-      mbar_arrive(&bars.empty[s]);
     }
   }
 
@@ -267,6 +306,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  if (S > 1) cluster_sync();  // no CTA leaves while the cluster may still signal it
 }
 
 // int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense.
@@ -284,27 +324,19 @@ __global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restric
 
 template <int BN, int STAGES, int ASTAGES>
 cudaError_t launch_i8t_inst(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& args, dim3 grid,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool allow_cluster, bool* reduced) {
   using C = I8tCfg<BN, STAGES, ASTAGES>;
-  auto kern = w8a8_gemm_i8t_kernel<BN, STAGES, ASTAGES>;
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
-  }
-  return launch_pdl(kern, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, stream, tw, tx, args);
+  return launch_persistent(w8a8_gemm_i8t_kernel<BN, STAGES, ASTAGES>, C::NUM_THREADS, C::SMEM_BYTES, tw, tx, args,
+                           grid, stream, allow_cluster, reduced);
 }
 
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool allow_cluster, bool* reduced) {
   switch (bn) {
-    case 16: return launch_i8t_inst<16, 6, 4>(tw, tx16, a, grid, st);
-    case 32: return launch_i8t_inst<32, 6, 4>(tw, tx16, a, grid, st);
-    case 64: return launch_i8t_inst<64, 5, 4>(tw, tx16, a, grid, st);
-    case 128: return launch_i8t_inst<128, 4, 2>(tw, tx16, a, grid, st);
+    case 16: return launch_i8t_inst<16, 6, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
+    case 32: return launch_i8t_inst<32, 6, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
+    case 64: return launch_i8t_inst<64, 5, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
+    case 128: return launch_i8t_inst<128, 4, 2>(tw, tx16, a, grid, st, allow_cluster, reduced);
     default: break;
   }
   return cudaErrorInvalidValue;

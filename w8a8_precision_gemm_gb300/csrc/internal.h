@@ -24,7 +24,10 @@ constexpr int kModeAcc = 1;   // GEMM writes the raw accumulator of its split to
 struct GemmArgs {
   int M, N, K;       // tokens, output channels, depth
   int num_kb;        // k-blocks covering K
-  int kb_per_split;  // k-blocks per split (grid.z = number of splits)
+  int kb_per_split;  // k-blocks per split
+  int tiles_tok;     // work units = tiles_tok x tiles_ch x splits, token tile fastest;
+  int tiles_ch;      // a persistent CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+  int splits;
   int mode;
   const float* sx;   // [M]
   const float* sw;   // [N]
@@ -34,6 +37,9 @@ struct GemmArgs {
   int* status;       // device status word
   int w_prefetch;    // the previous kernel in the stream does not write Wq: its first
                      // stages may be loaded before waiting for that kernel
+  int cluster_splits;  // > 1: the K splits of a tile run as one thread-block cluster of this
+                       // many CTAs and reduce their partials in the kernel (decode tiles only)
+  void* acc_out;       // raw-accumulator output [M, N] when Y is null (cluster reduction)
 };
 
 // Launch a kernel with programmatic stream serialization: it may start while
@@ -56,6 +62,31 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
+
+// The same, as clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// How many clusters of cluster_x CTAs of this kernel can run at once on the
+// current device (0 if unknown); cached per kernel, size and device.
+int max_active_clusters(const void* kern, int cluster_x, int threads, int smem);
 
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
 // (the operand the INT8 decode GEMM reads), saving it a widening pass.
@@ -89,15 +120,20 @@ struct GemmPlan {
 // gemm_plan.cu
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
-// gemm_fp8.cu / gemm_i8.cu: launch the instantiation matching (swap, bn).
+// gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
+// (swap, bn).  grid = (token tiles, channel tiles, K splits).  With
+// allow_cluster and K split in several parts, the launcher may run the splits
+// of each tile as a thread-block cluster that reduces them in the kernel (if
+// every tile fits in one round of co-resident clusters); *reduced then says
+// so, and the caller must not launch the split-K reduction.
 cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                            dim3 grid, cudaStream_t st);
+                            dim3 grid, cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                           dim3 grid, cudaStream_t st);
+                           dim3 grid, cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
 // gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
-                            cudaStream_t st);
+                            cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
 cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st);
 // split-K reduction: T = int (INT8) or float (FP8)
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
