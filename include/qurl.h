@@ -59,7 +59,7 @@ typedef enum {
     QURL_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, unknown enum, bad stride */
     QURL_ERR_UNSUPPORTED = 2, /* shape the kernels do not cover (e.g. K % 16 != 0) */
     QURL_ERR_ALIGNMENT = 3,   /* pointer or row stride not 16-byte aligned */
-    QURL_ERR_WORKSPACE = 4,   /* reserved */
+    QURL_ERR_WORKSPACE = 4,   /* the shape needs more scratch than qurl_w8a8_linear_static_scratch holds */
     QURL_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed */
     QURL_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out */
 } qurl_status;
@@ -155,6 +155,36 @@ size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
 qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N,
                              int K, qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
                              qurl_stream_t stream);
+
+/*
+ * qurl_w8a8_linear without a caller-provided workspace and without allocating:
+ * the same computation and the same results as qurl_w8a8_linear given a
+ * workspace of qurl_workspace_size(M, N, K, qt) bytes, but its scratch is a
+ * 32 MiB buffer compiled into the library (a file-scope device array), so
+ * neither the caller nor the library has to allocate device memory for it.
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate: an engine that has already reserved all of
+ * HBM for its own pools (KV caches sized to fill the device), code paths that
+ * must not risk an allocation failure or the device-wide synchronisation a
+ * cudaMalloc / cudaFree can bring in the middle of a decode loop, and foreign
+ * callers that have no handle on the application's allocator.
+ *
+ *   - Limit: a shape whose qurl_workspace_size exceeds 32 MiB (33,554,432
+ *     bytes) returns QURL_ERR_WORKSPACE and launches nothing (every 7B / 32B
+ *     decode projection up to M = 256 fits).
+ *   - The buffer is held by every GPU on which this entry point is used, until
+ *     the process exits.  Its device address is looked up (cudaGetSymbolAddress)
+ *     on the first call made with that device current, so make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the buffer, and it keeps what the last call
+ *     left there (nothing in it needs to start at zero).  Calls whose kernels
+ *     overlap on the GPU -- e.g. issued on two streams without ordering between
+ *     them -- race on it; serialise them (one stream, or events).
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+qurl_status qurl_w8a8_linear_static_scratch(const void* Xq, const float* sx, const void* Wq, const float* sw,
+                                            int M, int N, int K, qurl_qtype qt, void* Y, int ldy,
+                                            qurl_stream_t stream);
 
 /*
  * The raw accumulator of the 8-bit GEMM, acc [M, N] (stride N): int32 for

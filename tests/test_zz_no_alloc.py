@@ -1,0 +1,68 @@
+"""qurl_w8a8_linear_static_scratch: the linear entry point that allocates
+nothing and needs no workspace from its caller (its scratch is a buffer compiled
+into the library), for callers that cannot allocate device memory.  Checked
+through the C ABI against qurl_w8a8_linear given a workspace, on two calls in a
+row -- the second reuses the scratch the first left behind."""
+import ctypes
+
+import pytest
+import torch
+
+import w8a8_precision_gemm_gb300 as q
+from w8a8_precision_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _quantized(qt, M, N, K, tag):
+    X = synth.activations(f"noalloc/{tag}/X", M, K).cuda()
+    W = synth.weights(f"noalloc/{tag}/W", N, K).cuda()
+    Wq, sw, _, _ = q.prepare_weights(W, qt, s=1.5, keep_scaled=False)
+    Xq, sx = q.quant_act(X, qt)
+    return Xq, sx, Wq, sw
+
+
+def _static_call(L, Xq, sx, Wq, sw, qt, Y):
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    return L.qurl_w8a8_linear_static_scratch(ctypes.c_void_p(Xq.data_ptr()), ctypes.c_void_p(sx.data_ptr()),
+                                             ctypes.c_void_p(Wq.data_ptr()), ctypes.c_void_p(sw.data_ptr()), M, N, K,
+                                             qt, ctypes.c_void_p(Y.data_ptr()), Y.stride(0),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def _close(a, b, qt):
+    if qt == q.INT8:
+        return torch.equal(a.view(torch.int16), b.view(torch.int16))
+    a, b = a.float(), b.float()
+    return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30)) <= 1e-2
+
+
+@pytest.mark.parametrize("qt", [q.INT8, q.FP8_E4M3])
+def test_static_scratch_matches_workspace_entry_twice(qt):
+    assert torch.cuda.is_available()
+    L = q.load()
+    # two different projections in a row: split K with fp16 codes in the scratch, then another shape
+    for M, N, K, tag in ((64, 4608, 3584, "qkv64"), (256, 3584, 18944, "down256")):
+        Xq, sx, Wq, sw = _quantized(qt, M, N, K, tag)
+        ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        q.qurl_w8a8_linear(Xq, sx, Wq, sw, qt, ref, q.workspace(M, N, K, qt))
+        Y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        assert _static_call(L, Xq, sx, Wq, sw, qt, Y) == 0
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+        assert _close(Y, ref, qt), (M, N, K)
+
+
+def test_static_scratch_rejects_shapes_beyond_its_size():
+    L = q.load()
+    M, N, K = 256, 512, 70000  # the fp16 activation codes alone need 35.8 MB > 32 MiB
+    assert q.qurl_workspace_size(M, N, K, q.INT8) > 32 * 1024 * 1024
+    Xq = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    Wq = torch.zeros((N, K), dtype=torch.int8, device="cuda")
+    sx = torch.ones(M, device="cuda")
+    sw = torch.ones(N, device="cuda")
+    Y = torch.full((M, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    assert _static_call(L, Xq, sx, Wq, sw, q.INT8, Y) == 4  # QURL_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(Y == 5.0)  # nothing was launched

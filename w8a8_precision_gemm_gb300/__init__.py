@@ -74,6 +74,7 @@ def load() -> ctypes.CDLL:
             "qurl_silu_mul_quant": [P, i, i, i, f, i, P, P, P, P],
             "qurl_w8a8_linear": [P, P, P, P, i, i, i, i, P, i, P, z, P],
             "qurl_w8a8_gemm_acc": [P, P, i, i, i, i, P, P, z, P],
+            "qurl_w8a8_linear_static_scratch": [P, P, P, P, i, i, i, i, P, i, P],
             "qurl_rmsnorm_quant_linear": [P, i, P, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
             "qurl_quant_act_linear": [P, i, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
             "qurl_silu_mul_quant_linear": [P, i, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
@@ -168,6 +169,16 @@ def qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Y, workspace=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ok(load().qurl_w8a8_linear(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), M, N, K, qt, _ptr(Y), _ld(Y),
                                 _ptr(workspace), ws_bytes, _stream(stream)), "qurl_w8a8_linear")
+
+
+def qurl_w8a8_linear_static_scratch(Xq, sx, Wq, sw, qt, Y, stream=None):
+    """qurl_w8a8_linear with the library's built-in scratch buffer instead of a
+    workspace: for callers that cannot allocate device memory."""
+    _dense(Xq, sx, Wq, sw)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    _ok(load().qurl_w8a8_linear_static_scratch(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), M, N, K, qt, _ptr(Y), _ld(Y),
+                                               _stream(stream)), "qurl_w8a8_linear_static_scratch")
 
 
 def qurl_w8a8_gemm_acc(Xq, Wq, qt, acc, workspace=None, stream=None):
