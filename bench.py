@@ -206,23 +206,6 @@ def chain(q, qt, L, B):
     q.qurl_silu_mul_quant_linear(B.y["gate_up"], S_UAQ, Wq, sw, qt, B.y["down"], B.xq, B.sx, B.ws["down"])
 
 
-def gemm_launches(q, qt, M, N, K, fused):
-    """Kernels one linear call launches: the GEMM, a split-K reduction when K is
-    split, and (INT8 decode, unfused) the fp16 widening of the activation codes."""
-    ws = q.qurl_workspace_size(M, N, K, qt)
-    x16 = (qt == q.INT8 and M <= 256)
-    split = ws > (((M * K * 2 + 255) // 256) * 256 if x16 else 0)
-    return 1 + int(split) + int(x16 and not fused)
-
-
-def launches_per_step(q, qt):
-    n = 0
-    for M in M_LIST:
-        for name, K, N in PROJ:
-            n += 1 + gemm_launches(q, qt, M, N, K, fused=True)  # quantizer + GEMM (+ reduction)
-    return n
-
-
 def step_ops():
     return sum(2 * M * N * K for M in M_LIST for _, K, N in PROJ)
 
@@ -314,8 +297,9 @@ def run_reference(args):
     return 0
 
 
-def graph_of(fn):
-    """Capture fn() (C-ABI calls on the current stream) into a CUDA graph."""
+def graph_of(fn, q):
+    """Capture fn() (C-ABI calls on the current stream) into a CUDA graph;
+    returns the graph and the number of the library's kernels it holds."""
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -323,10 +307,12 @@ def graph_of(fn):
         fn()  # one eager pass on the capture stream (first-use set-up happens outside capture)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    n0 = q.qurl_kernel_launches()
     with torch.cuda.graph(g):
         fn()
+    n = q.qurl_kernel_launches() - n0
     torch.cuda.synchronize()
-    return g
+    return g, n
 
 
 def time_graph(g, reps, stream):
@@ -373,8 +359,8 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     q.qurl_check_device_status()
-    g_step = graph_of(step)
-    g_e2e = graph_of(step_e2e)
+    g_step, launches_step = graph_of(step, q)
+    g_e2e, _ = graph_of(step_e2e, q)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         g_step.replay()
@@ -417,7 +403,7 @@ def run_ours(args):
                     Wq, sw, _ = layers[r % 2].w[name]
                     q.qurl_w8a8_linear(xin, B.sx, Wq, sw, qt, B.y[name], B.ws[name])
 
-            g = graph_of(calls)
+            g, nl = graph_of(calls, q)
             g.replay()
             us = time_graph(g, 4, stream) / R * 1e3
             M = B.M
@@ -426,7 +412,7 @@ def run_ours(args):
             t_roof = max(ops / (pk["bf16_tflops"] * (2 if qt == q.FP8_E4M3 else 1) * 1e12), nb / (pk["hbm_gbs"] * 1e9))
             per[f"{name}/M{M}"] = {"us": us, "TOPS": ops / (us * 1e-6) / 1e12, "GBps": nb / (us * 1e-6) / 1e9,
                                    "roofline_frac": t_roof / (us * 1e-6),
-                                   "launches": gemm_launches(q, qt, M, N, K, fused=False)}
+                                   "launches": nl // R}
     q.qurl_check_device_status()
 
     ops = step_ops()
@@ -463,7 +449,8 @@ def run_ours(args):
             "roofline": roof,
             "e2e": {"value": ops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": launches_per_step(q, qt) * args.steps,
+            "gpu_launches": launches_step * args.steps,
+            "launches_per_step": launches_step,
             "clocks": clocks.summary(),
             "per_gemm": per}
 

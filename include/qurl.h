@@ -234,11 +234,25 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
  * or QURL_ERR_CUDA if the synchronisation itself failed. */
 qurl_status qurl_check_device_status(qurl_stream_t stream);
 
+/* Fault injection, for testing the failure path: the next GEMM this process
+ * launches (any linear / gemm_acc entry) skips the first k-block load of each
+ * CTA, so a shared-memory stage is never filled; the waits on it run out
+ * after ~1 s, the kernel latches QURL_ERR_TIMEOUT in the device status word,
+ * lets its own copies land, frees its tensor memory and exits.  Its outputs
+ * are then undefined; qurl_check_device_status() returns QURL_ERR_TIMEOUT and
+ * clears the word, and later calls run normally.  One-shot; always QURL_OK. */
+qurl_status qurl_debug_inject_timeout(void);
+
 /* Static, human-readable name of a status code. */
 const char* qurl_status_string(qurl_status s);
 
 /* ABI version of this header (major * 100 + minor). */
 int qurl_version(void);
+
+/* Number of CUDA kernels this library has launched (or recorded into a graph
+ * under stream capture) in this process: lets a caller count the kernels one
+ * call, or one captured step, consists of.  Host-side counter; no device work. */
+unsigned long long qurl_kernel_launches(void);
 
 #ifdef __cplusplus
 }

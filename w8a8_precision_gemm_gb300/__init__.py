@@ -80,6 +80,7 @@ def load() -> ctypes.CDLL:
             "qurl_silu_mul_quant_linear": [P, i, f, P, P, i, i, i, i, P, i, P, P, P, z, P],
             "qurl_count_diff": [P, P, z, P, P],
             "qurl_check_device_status": [P],
+            "qurl_debug_inject_timeout": [],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
         L.qurl_status_string.restype = ctypes.c_char_p
         L.qurl_version.argtypes = []
         L.qurl_version.restype = ctypes.c_int
+        L.qurl_kernel_launches.argtypes = []
+        L.qurl_kernel_launches.restype = ctypes.c_ulonglong
         _lib = L
         return L
 
@@ -232,12 +235,21 @@ def qurl_check_device_status(stream=None):
     _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
 
 
+def qurl_debug_inject_timeout():
+    """Test hook: the next GEMM launch stalls on purpose and times out (~1 s)."""
+    _ok(load().qurl_debug_inject_timeout(), "qurl_debug_inject_timeout")
+
+
 def qurl_status_string(s: int) -> str:
     return load().qurl_status_string(s).decode()
 
 
 def qurl_version() -> int:
     return int(load().qurl_version())
+
+
+def qurl_kernel_launches() -> int:
+    return int(load().qurl_kernel_launches())
 
 
 # ---------------------------------------------------------------- allocating helpers

@@ -12,6 +12,14 @@
 #include "internal.h"
 #include "qurl.h"
 
+namespace qurl {
+std::atomic<unsigned long long> g_kernel_launches{0};
+}  // namespace qurl
+
+namespace {
+std::atomic<int> g_inject_timeout{0};  // one-shot test hook, see qurl_debug_inject_timeout
+}  // namespace
+
 namespace {
 
 // Per-device status word: kernels latch a bounded-wait timeout here.
@@ -213,13 +221,18 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
     a.mode = qurl::kModeAcc;
     a.part = split ? static_cast<void*>(part_base) : acc_out;
   }
+  a.acc_out = acc_out;
+  if (split) a.part = part_base;  // partials; a cluster-reduced call then writes Y / acc_out itself
+  a.fault = g_inject_timeout.exchange(0);
+  const bool clusters = (a.fault == 0);
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
+  bool reduced = false;
   if (p.tmem_a)
-    QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
+    QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st, clusters, &reduced));
   else
-    QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
-                   : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
-  if (split)
+    QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st, clusters, &reduced)
+                   : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st, clusters, &reduced));
+  if (split && !reduced)
     QURL_CUDA(qurl::launch_splitk_reduce(qt, part_base, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
                                          dev->num_sms, st));
   return QURL_OK;
@@ -293,6 +306,13 @@ const char* qurl_status_string(qurl_status s) {
 }
 
 int qurl_version(void) { return 100; }
+
+unsigned long long qurl_kernel_launches(void) { return qurl::g_kernel_launches.load(); }
+
+qurl_status qurl_debug_inject_timeout(void) {
+  g_inject_timeout.store(1);
+  return QURL_OK;
+}
 
 qurl_status qurl_prepare_weights(const void* W, qurl_ftype w_type, int N, int K, int ldw, const float* gamma,
                                  float s, qurl_qtype qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,

@@ -83,6 +83,36 @@ __device__ __forceinline__ UnitRange unit_range(const GemmArgs& a) {
   return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), a.tiles_tok * a.tiles_ch * a.splits};
 }
 
+// Walks the (unit, k-block) sequence of a CTA ahead of its loads and prefetches
+// the weight tiles into L2: the shared-memory ring holds only a few stages,
+// so without it the bytes a CTA has in flight to DRAM -- and with them its
+// share of the bandwidth -- are capped by shared memory.
+template <bool SWAP, int BN>
+struct WeightPrefetcher {
+  UnitRange r;
+  int u, it;   // next (unit, k-block) to prefetch
+  Unit w;
+  __device__ __forceinline__ void init(const GemmArgs& a, const UnitRange& range) {
+    r = range;
+    u = r.u;
+    it = 0;
+    if (u < r.end) w = unit_of<SWAP, BN>(a, u);
+  }
+  // Prefetch the next k-block's weight tile (tm, rows from w.a0 or w.b0).
+  __device__ __forceinline__ void step(const GemmArgs& a, const CUtensorMap* tm, int bk) {
+    if (u >= r.end) return;
+    const int row = SWAP ? w.a0 : w.b0;
+    tma_prefetch_l2_2d(tm, (w.kb0 + it) * bk, row);
+    if (++it == w.nkb) {
+      it = 0;
+      u += r.stride;
+      if (u < r.end) w = unit_of<SWAP, BN>(a, u);
+    }
+  }
+};
+
+constexpr int kPrefetchKB = 12;  // k-blocks of weights prefetched into L2 ahead of the loads
+
 // In-cluster split-K reduction of one decode tile (weights on the MMA M side):
 // every split's partial is in a.part; this CTA (rank r of S) sums, in split
 // order, the tokens j = r, r + S, ... of the tile for all of its 128 output
@@ -353,7 +383,7 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
       // Weight tiles of the first stages may stream in while the previous
       // kernel (which, per w_prefetch, does not write Wq) is finishing.
       int npre = 0;
-      if (args.w_prefetch && R.u < R.end) {
+      if (args.w_prefetch && !args.fault && R.u < R.end) {
         const Unit w = unit_of<SWAP, BN>(args, R.u);
         npre = min(STAGES, w.nkb);
         for (int it = 0; it < npre; ++it) {
@@ -365,6 +395,11 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
             tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, w.b0, &bars.full[it], polB);
         }
       }
+      // weights only (the activation tiles are small and stay in L2)
+      WeightPrefetcher<SWAP, BN> pf;
+      pf.init(args, R);
+      const CUtensorMap* tmW = SWAP ? &tmA : &tmB;
+      for (int j = 0; j < kPrefetchKB + npre; ++j) pf.step(args, tmW, C::BK);
       griddep_wait();
       int g = 0;  // k-blocks issued by this CTA (ring position)
       bool ok = true;
@@ -373,6 +408,8 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
         for (int it = 0; it < w.nkb; ++it, ++g) {
           const int s = g % STAGES;
           const int kc = (w.kb0 + it) * C::BK;
+          if (g >= npre) pf.step(args, tmW, C::BK);
+          if (args.fault && g == 0) continue;  // injected fault: this stage never fills
           if (g < npre) {  // the weight half is in flight; add the activation half
             if (SWAP)
               tma_load_2d(stB + s * C::B_STAGE, &tmB, kc, w.b0, &bars.full[s], polB);

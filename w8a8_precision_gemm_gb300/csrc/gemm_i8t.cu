@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(448, 1)
       // weight tiles of the first stages stream in while the previous kernel
       // (which, per w_prefetch, does not write Wq) is finishing
       int npre = 0;
-      if (args.w_prefetch && R.u < R.end) {
+      if (args.w_prefetch && !args.fault && R.u < R.end) {
         const Unit w = unit_of<true, BN>(args, R.u);
         npre = min(STAGES, w.nkb);
         for (int it = 0; it < npre; ++it) {
@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(448, 1)
           tma_load_2d(stW + it * C::W_STAGE, &tmW, (w.kb0 + it) * C::BK, w.a0, &bars.full[it], polW);
         }
       }
+      WeightPrefetcher<true, BN> pf;
+      pf.init(args, R);
+      for (int j = 0; j < kPrefetchKB + npre; ++j) pf.step(args, &tmW, C::BK);
       griddep_wait();
       int g = 0;
       bool ok = true;
@@ -137,7 +140,9 @@ __global__ void __launch_bounds__(448, 1)
         for (int it = 0; it < w.nkb; ++it, ++g) {
           const int s = g % STAGES;
           const int kb = w.kb0 + it;
+          if (args.fault && g == 0) continue;  // injected fault: this stage never fills
           if (g >= npre) {
+            pf.step(args, &tmW, C::BK);
             if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
               ok = false;
               break;

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -40,7 +41,12 @@ struct GemmArgs {
   int cluster_splits;  // > 1: the K splits of a tile run as one thread-block cluster of this
                        // many CTAs and reduce their partials in the kernel (decode tiles only)
   void* acc_out;       // raw-accumulator output [M, N] when Y is null (cluster reduction)
+  int fault;           // test hook: 1 = the producer skips its first k-block, so the consumer's
+                       // bounded wait runs out and the kernel latches a timeout
 };
+
+// Number of kernels this library has launched in the process (api.cu).
+extern std::atomic<unsigned long long> g_kernel_launches;
 
 // Launch a kernel with programmatic stream serialization: it may start while
 // the previous kernel in the stream finishes; every kernel of this library
@@ -60,6 +66,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
@@ -81,6 +88,7 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
