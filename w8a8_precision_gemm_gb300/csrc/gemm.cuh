@@ -33,7 +33,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <algorithm>
 #include <type_traits>
 
 #include "internal.h"
@@ -48,6 +47,7 @@ struct Unit {
   int a0, b0;    // first row of the A tile / of the B tile
   int kb0, nkb;  // k-block range
   int split;
+  int tile;      // token tile + tiles_tok * channel tile (the split-K counter index)
 };
 
 template <bool SWAP, int BN>
@@ -62,81 +62,74 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int u) {
   w.kb0 = sp * a.kb_per_split;
   w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
   w.split = sp;
+  w.tile = tok + a.tiles_tok * ch;
   return w;
 }
 
-// The units one CTA processes: u, u + stride, ... < end.  Without clusters a
-// CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...; with an in-kernel
-// split-K reduction, cluster c takes tiles c, c + #clusters, ... and its CTA of
-// rank r the split r of each.
+// The units one CTA processes: blockIdx.x, blockIdx.x + gridDim.x, ... < end.
 struct UnitRange {
   int u, stride, end;
 };
 
 __device__ __forceinline__ UnitRange unit_range(const GemmArgs& a) {
-  if (a.cluster_splits > 1) {
-    const int tiles = a.tiles_tok * a.tiles_ch;
-    const int rank = static_cast<int>(cluster_ctarank());
-    return {static_cast<int>(cluster_id_x()) + tiles * rank, static_cast<int>(cluster_count_x()),
-            tiles * (rank + 1)};
-  }
   return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), a.tiles_tok * a.tiles_ch * a.splits};
 }
 
-// Walks the (unit, k-block) sequence of a CTA ahead of its loads and prefetches
-// the weight tiles into L2: the shared-memory ring holds only a few stages,
-// so without it the bytes a CTA has in flight to DRAM -- and with them its
-// share of the bandwidth -- are capped by shared memory.
-template <bool SWAP, int BN>
-struct WeightPrefetcher {
-  UnitRange r;
-  int u, it;   // next (unit, k-block) to prefetch
-  Unit w;
-  __device__ __forceinline__ void init(const GemmArgs& a, const UnitRange& range) {
-    r = range;
-    u = r.u;
-    it = 0;
-    if (u < r.end) w = unit_of<SWAP, BN>(a, u);
+// Split-K fixup, run by the 128 epilogue threads (t = 0..127) of a CTA that
+// has just written the partial of its split of a tile to a.part:
+// every thread fences its writes, the CTA's threads meet at a named barrier,
+// one thread counts the split in the tile's counter, and the CTA that brings
+// the counter to a.splits sums all partials of the tile in split order
+// (0, 1, ...) and writes Y (or the raw sum to acc_out).  Partials written by
+// other SMs are read around L1.  Returns after the CTA's share is done.
+template <bool SWAP, int BN, typename T>
+__device__ __forceinline__ void split_fixup(const GemmArgs& a, const Unit& w, int t, int* flag_smem) {
+  __threadfence();
+  named_barrier(1, 128);
+  if (t == 0) {
+    const int old = atomicAdd(a.tile_count + w.tile, 1);
+    *flag_smem = (old == a.splits - 1);
   }
-  // Prefetch the next k-block's weight tile (tm, rows from w.a0 or w.b0).
-  __device__ __forceinline__ void step(const GemmArgs& a, const CUtensorMap* tm, int bk) {
-    if (u >= r.end) return;
-    const int row = SWAP ? w.a0 : w.b0;
-    tma_prefetch_l2_2d(tm, (w.kb0 + it) * bk, row);
-    if (++it == w.nkb) {
-      it = 0;
-      u += r.stride;
-      if (u < r.end) w = unit_of<SWAP, BN>(a, u);
-    }
-  }
-};
-
-constexpr int kPrefetchKB = 12;  // k-blocks of weights prefetched into L2 ahead of the loads
-
-// In-cluster split-K reduction of one decode tile (weights on the MMA M side):
-// every split's partial is in a.part; this CTA (rank r of S) sums, in split
-// order, the tokens j = r, r + S, ... of the tile for all of its 128 output
-// channels, then dequantizes to Y (or stores the raw sum to acc_out).  Thread
-// t (0..127) owns channel a0 + t, so a warp reads and writes 32 consecutive
-// channels.  Partials are read around L1 (another SM wrote them).
-template <int BN, typename T>
-__device__ __forceinline__ void cluster_reduce_tile(const GemmArgs& a, const Unit& w, int rank, int S, int t) {
-  const int n = w.a0 + t;
-  if (n >= a.N) return;
+  named_barrier(1, 128);
+  if (!*flag_smem) return;
+  __threadfence();
   const size_t MN = static_cast<size_t>(a.M) * a.N;
   const T* part = reinterpret_cast<const T*>(a.part);
-  const float swn = a.Y ? __ldg(a.sw + n) : 0.0f;
-  for (int j = rank; j < BN; j += S) {
-    const int m = w.b0 + j;
-    if (m >= a.M) break;
-    const size_t off = static_cast<size_t>(m) * a.N + n;
-    T acc = __ldcg(part + off);
-    for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
-    if (a.Y) {
-      const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), __ldg(a.sx + m)), swn);
-      a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
-    } else {
-      reinterpret_cast<T*>(a.acc_out)[off] = acc;
+  // thread t owns A-tile row t: an output channel (SWAP) or a token
+  const int r = w.a0 + t;
+  if (SWAP) {
+    const int n = r;
+    if (n >= a.N) return;
+    const float swn = a.Y ? __ldg(a.sw + n) : 0.0f;
+    for (int j = 0; j < BN; ++j) {
+      const int m = w.b0 + j;
+      if (m >= a.M) break;
+      const size_t off = static_cast<size_t>(m) * a.N + n;  // a warp covers 32 consecutive channels
+      T acc = __ldcg(part + off);
+      for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
+      if (a.Y) {
+        const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), __ldg(a.sx + m)), swn);
+        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
+      } else {
+        reinterpret_cast<T*>(a.acc_out)[off] = acc;
+      }
+    }
+  } else {
+    const int m = r;
+    if (m >= a.M) return;
+    const float sxm = a.Y ? __ldg(a.sx + m) : 0.0f;
+    for (int j = 0; j < BN; ++j) {
+      const int n = w.b0 + j;
+      if (n >= a.N) break;
+      const size_t off = static_cast<size_t>(m) * a.N + n;
+      T acc = __ldcg(part + off);
+      for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
+      if (a.Y) {
+        const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), sxm), __ldg(a.sw + n));
+        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
+      } else {
+        reinterpret_cast<T*>(a.acc_out)[off] = acc;
+      }
     }
   }
 }
@@ -179,8 +172,8 @@ struct GemmBarriers {
   uint64_t pfull[2];        // MMA -> epilogue (accumulator chunk ready)
   uint64_t pempty[2];       // epilogue -> MMA (TMEM buffer drained)
   uint64_t done;            // MMA drain on the error path
-  uint64_t red_full;        // in-cluster split-K: every split's partial of the tile is written
   uint32_t tmem_base;
+  int last_split;           // split-K: this CTA reduces the tile it just finished
 };
 
 // Wait (bounded, ignoring latched errors) for async copies/MMAs a thread has
@@ -337,7 +330,6 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const UnitRange R = unit_range(args);
-  const int S = args.cluster_splits;  // > 1: in-cluster split-K reduction
   int* status = args.status;
 
   if (threadIdx.x == 0) {
@@ -346,7 +338,6 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], C::kInt8 ? C::NUM_CONV : 1);
     }
-    mbar_init(&bars.red_full, S > 1 ? S * 128 : 1);
 #pragma unroll
     for (int s = 0; s < (C::CSTAGES > 0 ? C::CSTAGES : 1); ++s) {
       mbar_init(&bars.cfull[s], C::NUM_CONV);
@@ -370,7 +361,6 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (S > 1) cluster_sync();  // every CTA's barriers are initialised before remote arrives
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
@@ -395,11 +385,6 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
             tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, w.b0, &bars.full[it], polB);
         }
       }
-      // weights only (the activation tiles are small and stay in L2)
-      WeightPrefetcher<SWAP, BN> pf;
-      pf.init(args, R);
-      const CUtensorMap* tmW = SWAP ? &tmA : &tmB;
-      for (int j = 0; j < kPrefetchKB + npre; ++j) pf.step(args, tmW, C::BK);
       griddep_wait();
       int g = 0;  // k-blocks issued by this CTA (ring position)
       bool ok = true;
@@ -408,7 +393,6 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
         for (int it = 0; it < w.nkb; ++it, ++g) {
           const int s = g % STAGES;
           const int kc = (w.kb0 + it) * C::BK;
-          if (g >= npre) pf.step(args, tmW, C::BK);
           if (args.fault && g == 0) continue;  // injected fault: this stage never fills
           if (g < npre) {  // the weight half is in flight; add the activation half
             if (SWAP)
@@ -497,8 +481,8 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     const int i = q * 32 + lane;          // row of the A tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t tR = lane_base + 2 * BN;  // INT8: int32 running sum
-    const int emode = S > 1 ? kModeAcc : args.mode;  // a clustered split writes its partial first
-    int cg = 0, red_iter = 0;
+    const int emode = args.splits > 1 ? kModeAcc : args.mode;  // a split writes its partial first
+    int cg = 0;
     bool ok = true;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<SWAP, BN>(args, u);
@@ -546,17 +530,9 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars.pempty[buf]);
       }
-      if (ok && SWAP && S > 1) {
-        // every split of this tile has written its partial: reduce this CTA's share
-        for (int r = 0; r < S; ++r) mbar_arrive_cluster(&bars.red_full, r);
-        if (!mbar_wait_cluster(&bars.red_full, red_iter & 1, status)) {
-          ok = false;
-          break;
-        }
-        ++red_iter;
-        cluster_reduce_tile<BN, typename std::conditional<C::kInt8, int, float>::type>(
-            args, w, static_cast<int>(cluster_ctarank()), S, threadIdx.x - 64);
-      }
+      if (ok && args.splits > 1)
+        split_fixup<SWAP, BN, typename std::conditional<C::kInt8, int, float>::type>(args, w, threadIdx.x - 64,
+                                                                                     &bars.last_split);
     }
   } else {
     // ------------------------------------------------------------ converters (INT8)
@@ -593,48 +569,18 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (S > 1) cluster_sync();  // no CTA leaves while the cluster may still signal it
 }
 
-// Split-K reduction in a fixed order (z = 0, 1, ...), then either the
-// dequantizing epilogue (Y != nullptr) or the raw sum (acc_out).
-template <typename T>
-__global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
-                                     const float* __restrict__ sx, const float* __restrict__ sw,
-                                     __nv_bfloat16* __restrict__ Y, long long ldy, T* __restrict__ acc_out) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const size_t total = static_cast<size_t>(M) * N;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    T s = part[idx];
-    for (int z = 1; z < splits; ++z) s += part[static_cast<size_t>(z) * total + idx];
-    const int m = static_cast<int>(idx / N);
-    const int n = static_cast<int>(idx - static_cast<size_t>(m) * N);
-    if (Y != nullptr) {
-      const float y = __fmul_rn(__fmul_rn(static_cast<float>(s), __ldg(sx + m)), __ldg(sw + n));
-      Y[static_cast<size_t>(m) * ldy + n] = __float2bfloat16_rn(y);
-    } else {
-      acc_out[idx] = s;
-    }
-  }
-}
-
-// Host-side launch of one instantiation.
 // The unit grid (token tiles, channel tiles, splits) becomes a persistent
 // launch of one CTA per SM (fewer when there are fewer units).
 int persistent_ctas(const GemmArgs& a);
 
-// Launch a persistent GEMM kernel for grid = (token tiles, channel tiles,
-// splits).  With allow_cluster (decode tiles, K split in 2..8 parts) the splits
-// of each tile become one cluster that reduces in the kernel, provided every
-// tile gets a co-resident cluster in one round; the number of splits may be
-// lowered to the largest count for which that holds.
+// attr_done: the caller's per-instantiation flags (one per device) recording
+// that the kernel's dynamic shared-memory limit has been raised -- every kernel
+// needs its own, although many share this function's signature type.
 template <typename Kern>
 cudaError_t launch_persistent(Kern kern, int threads, int smem, const CUtensorMap& ta, const CUtensorMap& tb,
-                              const GemmArgs& args_in, dim3 grid, cudaStream_t stream, bool allow_cluster,
-                              bool* reduced) {
-  static bool attr_done[64] = {};
+                              const GemmArgs& args_in, dim3 grid, cudaStream_t stream, bool (&attr_done)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
@@ -646,31 +592,16 @@ cudaError_t launch_persistent(Kern kern, int threads, int smem, const CUtensorMa
   args.tiles_tok = grid.x;
   args.tiles_ch = grid.y;
   args.splits = grid.z;
-  args.cluster_splits = 0;
-  if (reduced) *reduced = false;
-  const int tiles = static_cast<int>(grid.x * grid.y);
-  if (allow_cluster && grid.z > 1) {
-    for (int S = std::min(static_cast<int>(grid.z), 8); S >= 2; --S) {
-      if (max_active_clusters(reinterpret_cast<const void*>(kern), S, threads, smem) < tiles) continue;
-      args.kb_per_split = (args.num_kb + S - 1) / S;
-      args.splits = (args.num_kb + args.kb_per_split - 1) / args.kb_per_split;
-      if (args.splits != S) continue;  // every rank of the cluster needs a non-empty split
-      args.cluster_splits = S;
-      if (reduced) *reduced = true;
-      return launch_pdl_cluster(kern, dim3(tiles * S), dim3(threads), smem, stream, S, ta, tb, args);
-    }
-    args.kb_per_split = args_in.kb_per_split;
-    args.splits = grid.z;
-  }
   return launch_pdl(kern, dim3(persistent_ctas(args)), dim3(threads), smem, stream, ta, tb, args);
 }
 
 template <int QT, bool SWAP, int BN, int STAGES>
 cudaError_t launch_gemm_inst(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, dim3 grid,
-                             cudaStream_t stream, bool allow_cluster, bool* reduced) {
+                             cudaStream_t stream) {
   using C = GemmCfg<QT, SWAP, BN, STAGES>;
+  static bool attr_done[64] = {};
   return launch_persistent(w8a8_gemm_kernel<QT, SWAP, BN, STAGES>, C::NUM_THREADS, C::SMEM_BYTES, ta, tb, args,
-                           grid, stream, allow_cluster && SWAP, reduced);
+                           grid, stream, attr_done);
 }
 
 }  // namespace qurl

@@ -1,6 +1,5 @@
 // gemm_common.cu -- tile planning and the split-K reduction of the W8A8 GEMM.
 #include <algorithm>
-#include <mutex>
 
 #include "gemm.cuh"
 
@@ -11,7 +10,8 @@ namespace qurl {
 // partial buffers and an int32 running sum).  Prefill: 128-token tiles x 256
 // (FP8) or 128 (INT8) channels.  When the tiles do not fill the SMs, K is split
 // so that tiles x splits is close to the SM count, each split at least 4 (FP8)
-// or 8 (INT8) k-blocks deep, as far as the workspace allows.
+// or 8 (INT8) k-blocks deep, as far as the workspace allows.  Workspace
+// layout: [fp16 activation codes (INT8 decode)][split partials][tile counters].
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
@@ -43,50 +43,17 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     const int cap = std::max(1, p.num_kb / min_kb);
     splits = std::max(1, std::min(want, cap));
   }
+  p.num_tiles = static_cast<int>(tiles);
   const size_t per_split = static_cast<size_t>(M) * N * 4;
-  const size_t avail = ws_avail > p.x16_bytes ? ws_avail - p.x16_bytes : 0;
+  const size_t counters = (static_cast<size_t>(p.num_tiles) * 4 + 255) & ~static_cast<size_t>(255);
+  const size_t avail = ws_avail > p.x16_bytes + counters ? ws_avail - p.x16_bytes - counters : 0;
   if (splits > 1 && avail < static_cast<size_t>(splits) * per_split)
     splits = std::max(1, static_cast<int>(std::min<size_t>(avail / per_split, 1 << 20)));
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
-  p.ws_bytes = p.x16_bytes + (p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0);
+  p.part_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
+  p.ws_bytes = p.x16_bytes + (p.splits > 1 ? p.part_bytes + counters : 0);
   return p;
-}
-
-int max_active_clusters(const void* kern, int cluster_x, int threads, int smem) {
-  struct Entry {
-    const void* kern;
-    int dev, cluster_x, value;
-  };
-  static std::mutex mu;
-  static Entry cache[256];
-  static int used = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-      if (cache[i].kern == kern && cache[i].dev == dev && cache[i].cluster_x == cluster_x) return cache[i].value;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster_x * 64);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (used < 256) cache[used++] = Entry{kern, dev, cluster_x, n};
-  return n;
 }
 
 int persistent_ctas(const GemmArgs& a) {
@@ -102,21 +69,14 @@ int persistent_ctas(const GemmArgs& a) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(units, n)));
 }
 
-cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
-                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
-                                 cudaStream_t st) {
-  const size_t total = static_cast<size_t>(M) * N;
-  size_t blocks = (total + 255) / 256;
-  blocks = std::min<size_t>(blocks, static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8);
-  blocks = std::max<size_t>(blocks, 1);
-  auto* y = reinterpret_cast<__nv_bfloat16*>(Y);
-  if (qt == kQInt8)
-    return launch_pdl(splitk_reduce_kernel<int>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                      reinterpret_cast<const int*>(part), splits, M, N, sx, sw, y, ldy,
-                      reinterpret_cast<int*>(acc_out));
-  return launch_pdl(splitk_reduce_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    reinterpret_cast<const float*>(part), splits, M, N, sx, sw, y, ldy,
-                    reinterpret_cast<float*>(acc_out));
+__global__ void zero_counters_kernel(int* p, int n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
+cudaError_t launch_zero_counters(int* p, int n, cudaStream_t st) {
+  return launch_pdl(zero_counters_kernel, dim3(1), dim3(256), 0, st, p, n);
 }
 
 }  // namespace qurl

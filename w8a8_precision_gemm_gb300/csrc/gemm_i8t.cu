@@ -59,8 +59,8 @@ struct I8tBarriers {
   uint64_t pfull[2];
   uint64_t pempty[2];
   uint64_t done;
-  uint64_t red_full;  // in-cluster split-K: every split's partial of the tile is written
   uint32_t tmem_base;
+  int last_split;  // split-K: this CTA reduces the tile it just finished
 };
 
 template <int BN, int STAGES, int ASTAGES>
@@ -77,11 +77,9 @@ __global__ void __launch_bounds__(448, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const UnitRange R = unit_range(args);
-  const int S = args.cluster_splits;  // > 1: in-cluster split-K reduction
   int* status = args.status;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars.red_full, S > 1 ? S * 128 : 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], 257);  // 256 converter threads + the MMA's commit
@@ -108,7 +106,6 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (S > 1) cluster_sync();  // every CTA's barriers are initialised before remote arrives
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
@@ -129,9 +126,6 @@ __global__ void __launch_bounds__(448, 1)
           tma_load_2d(stW + it * C::W_STAGE, &tmW, (w.kb0 + it) * C::BK, w.a0, &bars.full[it], polW);
         }
       }
-      WeightPrefetcher<true, BN> pf;
-      pf.init(args, R);
-      for (int j = 0; j < kPrefetchKB + npre; ++j) pf.step(args, &tmW, C::BK);
       griddep_wait();
       int g = 0;
       bool ok = true;
@@ -142,7 +136,6 @@ __global__ void __launch_bounds__(448, 1)
           const int kb = w.kb0 + it;
           if (args.fault && g == 0) continue;  // injected fault: this stage never fills
           if (g >= npre) {
-            pf.step(args, &tmW, C::BK);
             if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
               ok = false;
               break;
@@ -213,8 +206,8 @@ __global__ void __launch_bounds__(448, 1)
     const int i = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t tR = lane_base + 2 * BN;
-    const int emode = S > 1 ? kModeAcc : args.mode;  // a clustered split writes its partial first
-    int cg = 0, red_iter = 0;
+    const int emode = args.splits > 1 ? kModeAcc : args.mode;  // a split writes its partial first
+    int cg = 0;
     bool ok = true;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<true, BN>(args, u);
@@ -254,16 +247,7 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_before();
         mbar_arrive(&bars.pempty[buf]);
       }
-      if (ok && S > 1) {
-        // every split of this tile has written its partial: reduce this CTA's share
-        for (int r = 0; r < S; ++r) mbar_arrive_cluster(&bars.red_full, r);
-        if (!mbar_wait_cluster(&bars.red_full, red_iter & 1, status)) {
-          ok = false;
-          break;
-        }
-        ++red_iter;
-        cluster_reduce_tile<BN, int>(args, w, static_cast<int>(cluster_ctarank()), S, threadIdx.x - 64);
-      }
+      if (ok && args.splits > 1) split_fixup<true, BN, int>(args, w, threadIdx.x - 64, &bars.last_split);
     }
   } else {
     // ------------------------------------------------------------ converters: weights -> fp16 in TMEM
@@ -311,13 +295,16 @@ __global__ void __launch_bounds__(448, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (S > 1) cluster_sync();  // no CTA leaves while the cluster may still signal it
 }
 
-// int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense.
-__global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec) {
+// int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense; block 0 also
+// zeroes the following GEMM's split-K tile counters.
+__global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec, int* zero,
+                                 int nzero) {
   griddep_launch_dependents();
   griddep_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     uint4 lo, hi;
@@ -329,32 +316,34 @@ __global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restric
 
 template <int BN, int STAGES, int ASTAGES>
 cudaError_t launch_i8t_inst(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& args, dim3 grid,
-                            cudaStream_t stream, bool allow_cluster, bool* reduced) {
+                            cudaStream_t stream) {
   using C = I8tCfg<BN, STAGES, ASTAGES>;
+  static bool attr_done[64] = {};
   return launch_persistent(w8a8_gemm_i8t_kernel<BN, STAGES, ASTAGES>, C::NUM_THREADS, C::SMEM_BYTES, tw, tx, args,
-                           grid, stream, allow_cluster, reduced);
+                           grid, stream, attr_done);
 }
 
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
-                            cudaStream_t st, bool allow_cluster, bool* reduced) {
+                            cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_i8t_inst<16, 6, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
-    case 32: return launch_i8t_inst<32, 6, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
-    case 64: return launch_i8t_inst<64, 5, 4>(tw, tx16, a, grid, st, allow_cluster, reduced);
-    case 128: return launch_i8t_inst<128, 4, 2>(tw, tx16, a, grid, st, allow_cluster, reduced);
+    case 16: return launch_i8t_inst<16, 6, 4>(tw, tx16, a, grid, st);
+    case 32: return launch_i8t_inst<32, 6, 4>(tw, tx16, a, grid, st);
+    case 64: return launch_i8t_inst<64, 5, 4>(tw, tx16, a, grid, st);
+    case 128: return launch_i8t_inst<128, 4, 2>(tw, tx16, a, grid, st);
     default: break;
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st) {
+cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, int* zero, int nzero,
+                             cudaStream_t st) {
   const size_t nvec = n / 16;
   size_t blocks = (nvec + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec);
+                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec, zero, nzero);
 }
 
 }  // namespace qurl

@@ -38,9 +38,9 @@ struct GemmArgs {
   int* status;       // device status word
   int w_prefetch;    // the previous kernel in the stream does not write Wq: its first
                      // stages may be loaded before waiting for that kernel
-  int cluster_splits;  // > 1: the K splits of a tile run as one thread-block cluster of this
-                       // many CTAs and reduce their partials in the kernel (decode tiles only)
-  void* acc_out;       // raw-accumulator output [M, N] when Y is null (cluster reduction)
+  int* tile_count;     // split K: one counter per output tile (zeroed before the GEMM starts);
+                       // the split that brings it to `splits` reduces the tile's partials
+  void* acc_out;       // raw-accumulator output [M, N] when Y is null
   int fault;           // test hook: 1 = the producer skips its first k-block, so the consumer's
                        // bounded wait runs out and the kernel latches a timeout
 };
@@ -70,40 +70,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// The same, as clusters of cluster_x CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                               int cluster_x, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster_x;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
-
-// How many clusters of cluster_x CTAs of this kernel can run at once on the
-// current device (0 if unknown); cached per kernel, size and device.
-int max_active_clusters(const void* kern, int cluster_x, int threads, int smem);
-
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
 // (the operand the INT8 decode GEMM reads), saving it a widening pass.
+// zero / nzero (may be null / 0): also zero the following GEMM's split-K tile
+// counters (after this kernel's own wait for its predecessor).
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, cudaStream_t st);
+                             void* x16, int* zero, int nzero, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st);
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* zero, int nzero,
+                                 cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, cudaStream_t st);
+                                  float* sx, float* h_out, void* x16, int* zero, int nzero, cudaStream_t st);
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st);
@@ -122,30 +99,27 @@ struct GemmPlan {
   int splits;        // grid.z
   int num_kb;
   int kb_per_split;
-  size_t ws_bytes;   // total workspace: fp16 activation copy + split-K partials
+  size_t part_bytes;  // split-K partials (after the fp16 copy)
+  size_t ws_bytes;    // total workspace: fp16 activation copy + split-K partials + tile counters
+  int num_tiles;      // tiles_tok * tiles_ch (one split-K counter each)
 };
 
 // gemm_plan.cu
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
 // gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
-// (swap, bn).  grid = (token tiles, channel tiles, K splits).  With
-// allow_cluster and K split in several parts, the launcher may run the splits
-// of each tile as a thread-block cluster that reduces them in the kernel (if
-// every tile fits in one round of co-resident clusters); *reduced then says
-// so, and the caller must not launch the split-K reduction.
+// (swap, bn) as a persistent grid.  grid = (token tiles, channel tiles, K
+// splits); with K split, the kernel reduces the partials itself (tile_count).
 cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                            dim3 grid, cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
+                            dim3 grid, cudaStream_t st);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                           dim3 grid, cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
+                           dim3 grid, cudaStream_t st);
 // gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
-                            cudaStream_t st, bool allow_cluster = false, bool* reduced = nullptr);
-cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st);
-// split-K reduction: T = int (INT8) or float (FP8)
-cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
-                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
-                                 cudaStream_t st);
-
+                            cudaStream_t st);
+cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, int* zero, int nzero,
+                             cudaStream_t st);
+// zero n ints (the split-K tile counters) when no kernel of the call precedes the GEMM
+cudaError_t launch_zero_counters(int* p, int n, cudaStream_t st);
 }  // namespace qurl
