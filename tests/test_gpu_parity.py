@@ -383,11 +383,11 @@ def test_linear_int8_with_and_without_workspace(M, N, K):
 
 
 @pytest.mark.parametrize("qt", QTS)
-def test_split_k_reduction_in_kernel(qt):
-    """Decode shapes whose K is split across CTAs: the CTA that finishes a tile's
-    last split sums the partials in split order inside the GEMM kernel -- no
-    reduction kernel.  Per call: the GEMM, plus the kernel that zeroes the
-    tiles' counters (INT8: the activation widening does it)."""
+def test_split_k_reduction(qt):
+    """Decode shapes whose K is split across CTAs (4 to 300 channel tiles): each
+    split writes its partial and a reduction kernel sums them in split order.
+    Launches per call: the GEMM, the reduction when K is split, and for INT8 the
+    widening of the activation codes."""
     M, K = 64, 2048
     for tiles in (4, 36, 75, 150, 300):
         N = tiles * 128
@@ -401,7 +401,7 @@ def test_split_k_reduction_in_kernel(qt):
         acc = q.gemm_acc(args[0], args[2], qt, ws)
         sync_ok()
         split = ws is not None and ws.numel() > (((M * K * 2 + 255) // 256) * 256 if qt == q.INT8 else 0)
-        assert launches == (2 if (qt == q.INT8 or split) else 1), (tiles, launches)
+        assert launches == 1 + int(split) + int(qt == q.INT8), (tiles, launches)
         Yo, acco = oracle.w8a8_linear(Xq, sx, Wq, sw, oqt(qt), nthreads=NT)
         if qt == q.INT8:
             np.testing.assert_array_equal(bits(Y), Yo)

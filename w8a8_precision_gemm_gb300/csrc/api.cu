@@ -177,61 +177,34 @@ qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int 
     if (_e != cudaSuccess) return cuda_fail(_e); \
   } while (0)
 
-// Where the pieces of a call's workspace go (see plan_gemm).
-struct WsLayout {
-  void* x16;      // fp16 copy of the activation codes (INT8 decode) or null
-  void* part;     // split-K partials or null
-  int* counters;  // split-K tile counters or null
-  int ncounters;
-};
-
-WsLayout ws_layout(const qurl::GemmPlan& p, void* ws) {
-  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
-  WsLayout l{};
-  l.x16 = p.tmem_a ? base : nullptr;
-  if (p.splits > 1) {
-    l.part = base + p.x16_bytes;
-    l.counters = reinterpret_cast<int*>(base + p.x16_bytes + p.part_bytes);
-    l.ncounters = p.num_tiles;
-  }
-  return l;
-}
-
 // Run the GEMM; mode bf16 -> Y, otherwise raw accumulators -> acc_out.
-//   x16_ready:      the fp16 copy of Xq's codes is already in the workspace (a
-//                   fused quantizer wrote it), so it is not widened again;
-//   counters_ready: the split-K tile counters were zeroed by that quantizer;
-//   w_indep:        the kernel launched just before the GEMM does not write Wq,
-//                   so the GEMM may load weights before that kernel ends.
+// Workspace layout (see plan_gemm): [fp16 copy of the activation codes (INT8
+// decode)][split-K partials].
+//   x16_ready: the fp16 copy is already there (a fused quantizer wrote it);
+//   w_indep:   the kernel launched just before the GEMM does not write Wq, so
+//              the GEMM may load weights before that kernel ends.
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                     bool x16_ready = false, bool counters_ready = false, bool w_indep = false) {
+                     bool x16_ready = false, bool w_indep = false) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
-  const WsLayout l = ws_layout(p, ws);
   const bool int8 = (qt == QURL_INT8);
   const bool split = p.splits > 1;
-  bool prior_kernel = w_indep;  // a kernel of this library that writes no weights runs just before
+  uint8_t* part = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
   CUtensorMap ta, tb;
   if (p.tmem_a) {
     if (!x16_ready) {
-      QURL_CUDA(qurl::launch_i8_to_f16(Xq, l.x16, static_cast<size_t>(M) * K, dev->num_sms,
-                                       counters_ready ? nullptr : l.counters, counters_ready ? 0 : l.ncounters, st));
-      counters_ready = true;
-      prior_kernel = true;
+      QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, static_cast<size_t>(M) * K, dev->num_sms, st));
+      w_indep = true;  // the widening kernel writes only the workspace
     }
     QURL_TRY(byte_map(Wq, N, K, K, 128, 128, true, &ta));
-    QURL_TRY(byte_map(l.x16, M, 2LL * K, 2LL * K, 128, p.bn, true, &tb));
+    QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, p.bn, true, &tb));
   } else {
     const long long a_rows = p.swap ? N : M;
     const long long b_rows = p.swap ? M : N;
     QURL_TRY(byte_map(p.swap ? Wq : Xq, a_rows, K, K, p.bk, 128, !int8, &ta));
     QURL_TRY(byte_map(p.swap ? Xq : Wq, b_rows, K, K, p.bk, p.bn, !int8, &tb));
-  }
-  if (split && !counters_ready) {
-    QURL_CUDA(qurl::launch_zero_counters(l.counters, l.ncounters, st));
-    prior_kernel = true;
   }
   qurl::GemmArgs a{};
   a.M = M;
@@ -244,11 +217,10 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.Y = reinterpret_cast<__nv_bfloat16*>(Y);
   a.ldy = ldy;
   a.status = dev->status;
-  a.w_prefetch = prior_kernel ? 1 : 0;
-  a.mode = Y ? qurl::kModeBf16 : qurl::kModeAcc;
-  a.part = split ? l.part : acc_out;  // unsplit raw accumulators go straight to acc_out
+  a.w_prefetch = w_indep ? 1 : 0;
+  a.mode = (Y && !split) ? qurl::kModeBf16 : qurl::kModeAcc;
+  a.part = split ? static_cast<void*>(part) : acc_out;
   a.acc_out = acc_out;
-  a.tile_count = l.counters;
   a.fault = g_inject_timeout.exchange(0);
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
   if (p.tmem_a)
@@ -256,6 +228,9 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   else
     QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
                    : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
+  if (split)
+    QURL_CUDA(qurl::launch_splitk_reduce(qt, part, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
+                                         dev->num_sms, st));
   return QURL_OK;
 }
 
@@ -365,7 +340,7 @@ qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale
   if (!aligned16(Xq)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr, nullptr, 0,
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr,
                                    reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -378,7 +353,7 @@ qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float
   if (!aligned16(Xq) || !aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr, nullptr, 0,
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr,
                                        reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -393,7 +368,7 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
     return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr, nullptr, 0,
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
                                         reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -429,24 +404,13 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
-// What a fused quantizer writes for the GEMM after it: the fp16 copy of the
-// INT8 codes (when the plan reads one) and zeroed split-K counters.
-struct FusedPrep {
-  void* x16;
-  int* zero;
-  int nzero;
-};
-
-FusedPrep fused_prep(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+// Where the GEMM plan reads an fp16 copy of the INT8 codes from the
+// workspace, the fused quantizer writes it there directly.
+void* fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
   DevState* dev = nullptr;
-  FusedPrep f{};
-  if (device_state(&dev) != QURL_OK) return f;
+  if (device_state(&dev) != QURL_OK) return nullptr;
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
-  const WsLayout l = ws_layout(p, ws);
-  f.x16 = l.x16;
-  f.zero = l.counters;
-  f.nzero = l.ncounters;
-  return f;
+  return p.tmem_a ? ws : nullptr;
 }
 
 qurl_status check_fused_out(const void* Wq, const float* sw, int M, int N, int K, int qt, void* Y, int ldy,
@@ -466,11 +430,11 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   if (!gamma_folded || !(eps >= 0.0f) || !std::isfinite(eps)) return QURL_ERR_INVALID_ARG;
   if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedPrep f = fused_prep(M, N, K, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
-                                       f.zero, f.nzero, st));
+  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, x16,
+                                       st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  f.x16 != nullptr, true, true);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const void* Wq, const float* sw, int M,
@@ -480,10 +444,10 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedPrep f = fused_prep(M, N, K, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, f.x16, f.zero, f.nzero, st));
+  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, x16, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  f.x16 != nullptr, true, true);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale, const void* Wq, const float* sw,
@@ -495,11 +459,10 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
   QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedPrep f = fused_prep(M, N, I, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
-                                        f.zero, f.nzero, st));
+  void* x16 = fused_x16(M, N, I, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, x16, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  f.x16 != nullptr, true, true);
+                  x16 != nullptr, true);
 }
 
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,

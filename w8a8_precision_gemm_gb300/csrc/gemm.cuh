@@ -47,7 +47,6 @@ struct Unit {
   int a0, b0;    // first row of the A tile / of the B tile
   int kb0, nkb;  // k-block range
   int split;
-  int tile;      // token tile + tiles_tok * channel tile (the split-K counter index)
 };
 
 template <bool SWAP, int BN>
@@ -62,7 +61,6 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int u) {
   w.kb0 = sp * a.kb_per_split;
   w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
   w.split = sp;
-  w.tile = tok + a.tiles_tok * ch;
   return w;
 }
 
@@ -73,65 +71,6 @@ struct UnitRange {
 
 __device__ __forceinline__ UnitRange unit_range(const GemmArgs& a) {
   return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), a.tiles_tok * a.tiles_ch * a.splits};
-}
-
-// Split-K fixup, run by the 128 epilogue threads (t = 0..127) of a CTA that
-// has just written the partial of its split of a tile to a.part:
-// every thread fences its writes, the CTA's threads meet at a named barrier,
-// one thread counts the split in the tile's counter, and the CTA that brings
-// the counter to a.splits sums all partials of the tile in split order
-// (0, 1, ...) and writes Y (or the raw sum to acc_out).  Partials written by
-// other SMs are read around L1.  Returns after the CTA's share is done.
-template <bool SWAP, int BN, typename T>
-__device__ __forceinline__ void split_fixup(const GemmArgs& a, const Unit& w, int t, int* flag_smem) {
-  __threadfence();
-  named_barrier(1, 128);
-  if (t == 0) {
-    const int old = atomicAdd(a.tile_count + w.tile, 1);
-    *flag_smem = (old == a.splits - 1);
-  }
-  named_barrier(1, 128);
-  if (!*flag_smem) return;
-  __threadfence();
-  const size_t MN = static_cast<size_t>(a.M) * a.N;
-  const T* part = reinterpret_cast<const T*>(a.part);
-  // thread t owns A-tile row t: an output channel (SWAP) or a token
-  const int r = w.a0 + t;
-  if (SWAP) {
-    const int n = r;
-    if (n >= a.N) return;
-    const float swn = a.Y ? __ldg(a.sw + n) : 0.0f;
-    for (int j = 0; j < BN; ++j) {
-      const int m = w.b0 + j;
-      if (m >= a.M) break;
-      const size_t off = static_cast<size_t>(m) * a.N + n;  // a warp covers 32 consecutive channels
-      T acc = __ldcg(part + off);
-      for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
-      if (a.Y) {
-        const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), __ldg(a.sx + m)), swn);
-        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
-      } else {
-        reinterpret_cast<T*>(a.acc_out)[off] = acc;
-      }
-    }
-  } else {
-    const int m = r;
-    if (m >= a.M) return;
-    const float sxm = a.Y ? __ldg(a.sx + m) : 0.0f;
-    for (int j = 0; j < BN; ++j) {
-      const int n = w.b0 + j;
-      if (n >= a.N) break;
-      const size_t off = static_cast<size_t>(m) * a.N + n;
-      T acc = __ldcg(part + off);
-      for (int z = 1; z < a.splits; ++z) acc += __ldcg(part + z * MN + off);
-      if (a.Y) {
-        const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc), sxm), __ldg(a.sw + n));
-        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
-      } else {
-        reinterpret_cast<T*>(a.acc_out)[off] = acc;
-      }
-    }
-  }
 }
 
 template <int QT, bool SWAP, int BN, int STAGES>
@@ -146,7 +85,8 @@ struct GemmCfg {
   static constexpr int B_CONV = BN * 128;
   static constexpr int SMEM_TILES = CSTAGES * (A_CONV + B_CONV) + STAGES * (A_STAGE + B_STAGE);
   static constexpr int SMEM_BYTES = SMEM_TILES + 1024;  // slack for 1024-byte alignment
-  static constexpr int NUM_CONV = 256;                  // INT8 converter threads (warps 6-13)
+  static constexpr int NUM_CONV = 256;                  // INT8 converter threads (warps 6-13), two groups
+  static constexpr int CONV_GROUP = 128;                // threads of one group (alternate k-blocks)
   static constexpr int NUM_THREADS = kInt8 ? 192 + NUM_CONV : 192;
   static constexpr int TMEM_USED = kInt8 ? 3 * BN : 2 * BN;  // two accumulator buffers (+ int32 sum)
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -173,7 +113,6 @@ struct GemmBarriers {
   uint64_t pempty[2];       // epilogue -> MMA (TMEM buffer drained)
   uint64_t done;            // MMA drain on the error path
   uint32_t tmem_base;
-  int last_split;           // split-K: this CTA reduces the tile it just finished
 };
 
 // Wait (bounded, ignoring latched errors) for async copies/MMAs a thread has
@@ -336,11 +275,11 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.empty[s], C::kInt8 ? C::NUM_CONV : 1);
+      mbar_init(&bars.empty[s], C::kInt8 ? C::CONV_GROUP : 1);
     }
 #pragma unroll
     for (int s = 0; s < (C::CSTAGES > 0 ? C::CSTAGES : 1); ++s) {
-      mbar_init(&bars.cfull[s], C::NUM_CONV);
+      mbar_init(&bars.cfull[s], C::CONV_GROUP);
       mbar_init(&bars.cempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -481,7 +420,7 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     const int i = q * 32 + lane;          // row of the A tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t tR = lane_base + 2 * BN;  // INT8: int32 running sum
-    const int emode = args.splits > 1 ? kModeAcc : args.mode;  // a split writes its partial first
+    const int emode = args.mode;
     int cg = 0;
     bool ok = true;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
@@ -530,19 +469,20 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars.pempty[buf]);
       }
-      if (ok && args.splits > 1)
-        split_fixup<SWAP, BN, typename std::conditional<C::kInt8, int, float>::type>(args, w, threadIdx.x - 64,
-                                                                                     &bars.last_split);
     }
   } else {
     // ------------------------------------------------------------ converters (INT8)
+    // Two groups of 128 threads take alternate k-blocks, so two k-blocks are
+    // widened at a time.
     if constexpr (C::kInt8) {
-      const int t = threadIdx.x - 192;
+      const int t = (threadIdx.x - 192) & (C::CONV_GROUP - 1);
+      const int grp = (threadIdx.x - 192) / C::CONV_GROUP;
       int g = 0;
       bool ok = true;
       for (int u = R.u; u < R.end && ok; u += R.stride) {
         const Unit w = unit_of<SWAP, BN>(args, u);
         for (int it = 0; it < w.nkb; ++it, ++g) {
+          if ((g & 1) != grp) continue;
           const int s = g % STAGES;
           if (!warp_wait(&bars.full[s], (g / STAGES) & 1, status)) {
             ok = false;
@@ -553,8 +493,8 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
             ok = false;
             break;
           }
-          convert_tile(stA + s * C::A_STAGE, convA + cs * C::A_CONV, C::BM, t, C::NUM_CONV);
-          convert_tile(stB + s * C::B_STAGE, convB + cs * C::B_CONV, BN, t, C::NUM_CONV);
+          convert_tile(stA + s * C::A_STAGE, convA + cs * C::A_CONV, C::BM, t, C::CONV_GROUP);
+          convert_tile(stB + s * C::B_STAGE, convB + cs * C::B_CONV, BN, t, C::CONV_GROUP);
           fence_proxy_async_smem();
           mbar_arrive(&bars.empty[s]);
           mbar_arrive(&bars.cfull[cs]);
@@ -568,6 +508,48 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Split-K reduction in a fixed order (z = 0, 1, ...), then either the
+// dequantizing epilogue (Y != nullptr) or the raw sum (acc_out).  Every thread
+// takes 4 consecutive outputs (16-byte loads of each partial) when N % 4 == 0.
+template <typename T>
+__global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
+                                     const float* __restrict__ sx, const float* __restrict__ sw,
+                                     __nv_bfloat16* __restrict__ Y, long long ldy, T* __restrict__ acc_out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const size_t total = static_cast<size_t>(M) * N;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const bool vec = (N & 3) == 0;
+  const size_t items = vec ? total / 4 : total;
+  for (size_t it = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
+    const int w = vec ? 4 : 1;
+    const size_t idx = it * w;
+    T s[4] = {};
+    for (int z = 0; z < splits; ++z) {
+      const T* p = part + static_cast<size_t>(z) * total + idx;
+      if (vec) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p));
+        s[0] += *reinterpret_cast<const T*>(&v.x);
+        s[1] += *reinterpret_cast<const T*>(&v.y);
+        s[2] += *reinterpret_cast<const T*>(&v.z);
+        s[3] += *reinterpret_cast<const T*>(&v.w);
+      } else {
+        s[0] += __ldcg(p);
+      }
+    }
+    const int m = static_cast<int>(idx / N);
+    const int n0 = static_cast<int>(idx - static_cast<size_t>(m) * N);
+    for (int e = 0; e < w; ++e) {
+      if (Y != nullptr) {
+        const float y = __fmul_rn(__fmul_rn(static_cast<float>(s[e]), __ldg(sx + m)), __ldg(sw + n0 + e));
+        Y[static_cast<size_t>(m) * ldy + n0 + e] = __float2bfloat16_rn(y);
+      } else {
+        acc_out[idx + e] = s[e];
+      }
+    }
   }
 }
 

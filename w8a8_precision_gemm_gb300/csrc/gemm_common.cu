@@ -11,7 +11,7 @@ namespace qurl {
 // (FP8) or 128 (INT8) channels.  When the tiles do not fill the SMs, K is split
 // so that tiles x splits is close to the SM count, each split at least 4 (FP8)
 // or 8 (INT8) k-blocks deep, as far as the workspace allows.  Workspace
-// layout: [fp16 activation codes (INT8 decode)][split partials][tile counters].
+// layout: [fp16 activation codes (INT8 decode)][split-K partials].
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
@@ -43,16 +43,14 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     const int cap = std::max(1, p.num_kb / min_kb);
     splits = std::max(1, std::min(want, cap));
   }
-  p.num_tiles = static_cast<int>(tiles);
   const size_t per_split = static_cast<size_t>(M) * N * 4;
-  const size_t counters = (static_cast<size_t>(p.num_tiles) * 4 + 255) & ~static_cast<size_t>(255);
-  const size_t avail = ws_avail > p.x16_bytes + counters ? ws_avail - p.x16_bytes - counters : 0;
+  const size_t avail = ws_avail > p.x16_bytes ? ws_avail - p.x16_bytes : 0;
   if (splits > 1 && avail < static_cast<size_t>(splits) * per_split)
     splits = std::max(1, static_cast<int>(std::min<size_t>(avail / per_split, 1 << 20)));
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.part_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
-  p.ws_bytes = p.x16_bytes + (p.splits > 1 ? p.part_bytes + counters : 0);
+  p.ws_bytes = p.x16_bytes + p.part_bytes;
   return p;
 }
 
@@ -69,14 +67,22 @@ int persistent_ctas(const GemmArgs& a) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(units, n)));
 }
 
-__global__ void zero_counters_kernel(int* p, int n) {
-  griddep_launch_dependents();
-  griddep_wait();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
-}
-
-cudaError_t launch_zero_counters(int* p, int n, cudaStream_t st) {
-  return launch_pdl(zero_counters_kernel, dim3(1), dim3(256), 0, st, p, n);
+cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
+                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
+                                 cudaStream_t st) {
+  const size_t total = static_cast<size_t>(M) * N;
+  const size_t items = (N % 4 == 0) ? total / 4 : total;
+  size_t blocks = (items + 255) / 256;
+  blocks = std::min<size_t>(blocks, static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8);
+  blocks = std::max<size_t>(blocks, 1);
+  auto* y = reinterpret_cast<__nv_bfloat16*>(Y);
+  if (qt == kQInt8)
+    return launch_pdl(splitk_reduce_kernel<int>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                      reinterpret_cast<const int*>(part), splits, M, N, sx, sw, y, ldy,
+                      reinterpret_cast<int*>(acc_out));
+  return launch_pdl(splitk_reduce_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                    reinterpret_cast<const float*>(part), splits, M, N, sx, sw, y, ldy,
+                    reinterpret_cast<float*>(acc_out));
 }
 
 }  // namespace qurl

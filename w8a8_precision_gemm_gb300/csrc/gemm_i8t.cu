@@ -53,14 +53,13 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 template <int STAGES, int ASTAGES>
 struct I8tBarriers {
   uint64_t full[STAGES];     // TMA (weights + fp16 activations) landed
-  uint64_t empty[STAGES];    // converters read the weights (256) and the MMA read the activations (1)
+  uint64_t empty[STAGES];    // a converter group read the weights (128) and the MMA read the activations (1)
   uint64_t afull[ASTAGES];   // converters -> MMA: A stage written to TMEM
   uint64_t aempty[ASTAGES];  // MMA -> converters: A stage consumed
   uint64_t pfull[2];
   uint64_t pempty[2];
   uint64_t done;
   uint32_t tmem_base;
-  int last_split;  // split-K: this CTA reduces the tile it just finished
 };
 
 template <int BN, int STAGES, int ASTAGES>
@@ -82,10 +81,10 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.empty[s], 257);  // 256 converter threads + the MMA's commit
+      mbar_init(&bars.empty[s], 129);  // one converter group (128 threads) + the MMA's commit
     }
     for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(&bars.afull[s], 256);
+      mbar_init(&bars.afull[s], 128);
       mbar_init(&bars.aempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -206,7 +205,7 @@ __global__ void __launch_bounds__(448, 1)
     const int i = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t tR = lane_base + 2 * BN;
-    const int emode = args.splits > 1 ? kModeAcc : args.mode;  // a split writes its partial first
+    const int emode = args.mode;
     int cg = 0;
     bool ok = true;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
@@ -247,14 +246,15 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_before();
         mbar_arrive(&bars.pempty[buf]);
       }
-      if (ok && args.splits > 1) split_fixup<true, BN, int>(args, w, threadIdx.x - 64, &bars.last_split);
     }
   } else {
     // ------------------------------------------------------------ converters: weights -> fp16 in TMEM
-    // Two warps per TMEM lane quadrant: warps 6-9 widen codes 0-63 of their
-    // rows (TMEM columns 0-31 of the stage), warps 10-13 codes 64-127.
+    // Two groups of four warps (one per TMEM lane quadrant, one weight row per
+    // lane) take alternate k-blocks, so two k-blocks are widened at a time: a
+    // group's k-block is a serial chain (wait, load, widen, tcgen05.st, wait,
+    // signal) and the groups overlap theirs.
     const int q = warp & 3;
-    const int half = (warp - 6) >> 2;
+    const int grp = (warp - 6) >> 2;
     const int i = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int g = 0;
@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(448, 1)
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<true, BN>(args, u);
       for (int it = 0; it < w.nkb; ++it, ++g) {
+        if ((g & 1) != grp) continue;
         const int s = g % STAGES;
         const int as = g % ASTAGES;
         if (!warp_wait(&bars.full[s], (g / STAGES) & 1, status) ||
@@ -270,17 +271,21 @@ __global__ void __launch_bounds__(448, 1)
           break;
         }
         const uint8_t* wrow = stW + s * C::W_STAGE + (i >> 3) * 1024 + (i & 7) * 128;
-        uint32_t v[32];
+        const uint32_t a_t = lane_base + C::A_BASE + as * C::A_COLS;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = half * 4 + jj;  // 16-byte chunk = k 16j .. 16j+15
-          const uint4 raw = *reinterpret_cast<const uint4*>(wrow + ((j ^ (i & 7)) << 4));
-          uint4 lo, hi;
-          i8x16_to_f16x16(raw, lo, hi);
-          v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
-          v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = half * 4 + jj;  // 16-byte chunk = k 16j .. 16j+15
+            const uint4 raw = *reinterpret_cast<const uint4*>(wrow + ((j ^ (i & 7)) << 4));
+            uint4 lo, hi;
+            i8x16_to_f16x16(raw, lo, hi);
+            v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
+            v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
+          }
+          tmem_st32(a_t + half * 32, v);
         }
-        tmem_st32(lane_base + C::A_BASE + as * C::A_COLS + half * 32, v);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.afull[as]);
@@ -297,14 +302,10 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-// int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense; block 0 also
-// zeroes the following GEMM's split-K tile counters.
-__global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec, int* zero,
-                                 int nzero) {
+// int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense.
+__global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec) {
   griddep_launch_dependents();
   griddep_wait();
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     uint4 lo, hi;
@@ -335,15 +336,14 @@ cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, int* zero, int nzero,
-                             cudaStream_t st) {
+cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st) {
   const size_t nvec = n / 16;
   size_t blocks = (nvec + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec, zero, nzero);
+                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec);
 }
 
 }  // namespace qurl

@@ -38,9 +38,7 @@ struct GemmArgs {
   int* status;       // device status word
   int w_prefetch;    // the previous kernel in the stream does not write Wq: its first
                      // stages may be loaded before waiting for that kernel
-  int* tile_count;     // split K: one counter per output tile (zeroed before the GEMM starts);
-                       // the split that brings it to `splits` reduces the tile's partials
-  void* acc_out;       // raw-accumulator output [M, N] when Y is null
+  void* acc_out;       // raw-accumulator output [M, N] (unused by the kernels; kept with the call)
   int fault;           // test hook: 1 = the producer skips its first k-block, so the consumer's
                        // bounded wait runs out and the kernel latches a timeout
 };
@@ -72,15 +70,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
 // (the operand the INT8 decode GEMM reads), saving it a widening pass.
-// zero / nzero (may be null / 0): also zero the following GEMM's split-K tile
-// counters (after this kernel's own wait for its predecessor).
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, int* zero, int nzero, cudaStream_t st);
+                             void* x16, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* zero, int nzero,
-                                 cudaStream_t st);
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, int* zero, int nzero, cudaStream_t st);
+                                  float* sx, float* h_out, void* x16, cudaStream_t st);
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st);
@@ -100,8 +95,7 @@ struct GemmPlan {
   int num_kb;
   int kb_per_split;
   size_t part_bytes;  // split-K partials (after the fp16 copy)
-  size_t ws_bytes;    // total workspace: fp16 activation copy + split-K partials + tile counters
-  int num_tiles;      // tiles_tok * tiles_ch (one split-K counter each)
+  size_t ws_bytes;    // total workspace: fp16 activation copy + split-K partials
 };
 
 // gemm_plan.cu
@@ -109,7 +103,8 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
 // gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
 // (swap, bn) as a persistent grid.  grid = (token tiles, channel tiles, K
-// splits); with K split, the kernel reduces the partials itself (tile_count).
+// splits); with K split, each split writes its raw partial (mode kModeAcc) and
+// launch_splitk_reduce sums them.
 cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                             dim3 grid, cudaStream_t st);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
@@ -118,8 +113,9 @@ cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUten
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
-cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, int* zero, int nzero,
-                             cudaStream_t st);
-// zero n ints (the split-K tile counters) when no kernel of the call precedes the GEMM
-cudaError_t launch_zero_counters(int* p, int n, cudaStream_t st);
+cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st);
+// split-K reduction in split order: T = int (INT8) or float (FP8)
+cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
+                                 const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
+                                 cudaStream_t st);
 }  // namespace qurl

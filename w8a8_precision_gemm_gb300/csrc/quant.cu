@@ -162,13 +162,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
   }
 }
 
-// Block 0 zeroes the split-K tile counters of the GEMM that follows this
-// kernel (after this kernel's wait for its own predecessor).
-__device__ __forceinline__ void zero_counters(int* zero, int nzero) {
-  if (zero != nullptr && blockIdx.x == 0)
-    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
-}
-
 // Visit the 16-byte vectors idx = threadIdx.x + c * blockDim.x of a row: the
 // first kVPT from the register cache (fully unrolled, so the cache stays in
 // registers), the rest (rows longer than kVPT * blockDim vectors) from memory.
@@ -194,11 +187,9 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 // ------------------------------------------------------------------ activation quant
 
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
-                                 uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16,
-                                 int* zero, int nzero) {
+                                 uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16) {
   griddep_launch_dependents();
   griddep_wait();
-  zero_counters(zero, nzero);
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -230,11 +221,9 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
 
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
-                                     float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16,
-                                     int* zero, int nzero) {
+                                     float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16) {
   griddep_launch_dependents();
   griddep_wait();
-  zero_counters(zero, nzero);
   __shared__ float red[66];
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -301,10 +290,9 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
 
 __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
-                                      float* __restrict__ h_out, uint8_t* __restrict__ x16, int* zero, int nzero) {
+                                      float* __restrict__ h_out, uint8_t* __restrict__ x16) {
   griddep_launch_dependents();
   griddep_wait();
-  zero_counters(zero, nzero);
   __shared__ float red[33];
   const int m = blockIdx.x;
   const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
@@ -451,28 +439,26 @@ int row_threads(int nvec) {
 }  // namespace
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, int* zero, int nzero, cudaStream_t st) {
+                             void* x16, cudaStream_t st) {
   return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                    reinterpret_cast<uint8_t*>(x16), zero, nzero);
+                    reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* zero, int nzero,
-                                 cudaStream_t st) {
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st) {
   return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
-                    sx, ms_out, reinterpret_cast<uint8_t*>(x16), zero, nzero);
+                    sx, ms_out, reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, int* zero, int nzero, cudaStream_t st) {
+                                  float* sx, float* h_out, void* x16, cudaStream_t st) {
   // two vectors (gate, up) are cached per position: use twice the threads
   int t = 32;
   while (t < kRowThreads && t * (kVPT / 2) < I / 8) t *= 2;
   return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
-                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), zero,
-                    nzero);
+                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
