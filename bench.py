@@ -60,6 +60,29 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+DOMINANT_PROFILE = {"int8": "profiles/w8a8_gemm_i8t_kernel_7b_gate_up_m256_int8.md"}
+KERNEL_SOURCES = ["w8a8_precision_gemm_gb300/csrc/gemm.cuh", "w8a8_precision_gemm_gb300/csrc/gemm_i8t.cu",
+                  "w8a8_precision_gemm_gb300/csrc/ptx.cuh", "w8a8_precision_gemm_gb300/csrc/internal.h"]
+
+
+def profiled_traffic(qtype):
+    """DRAM bytes per launch of the dominant kernel from its committed ncu
+    summary -- only while the kernel sources still hash to the captured ones."""
+    import hashlib
+
+    path = DOMINANT_PROFILE.get(qtype)
+    if not path or not os.path.exists(os.path.join(ROOT, path)):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    fields = dict(line.split(": ", 1) for line in open(os.path.join(ROOT, path)).read().splitlines() if ": " in line
+                  and line.split(": ", 1)[0] in ("kernel_sources_sha256_16", "dram_bytes_per_launch"))
+    if fields.get("kernel_sources_sha256_16", "").split()[0:1] != [h.hexdigest()[:16]]:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
 def alg_bytes(M, K, N):
     return N * K + M * K + 2 * M * N + 4 * (M + N)
 
@@ -413,6 +436,24 @@ def run_ours(args):
             per[f"{name}/M{M}"] = {"us": us, "TOPS": ops / (us * 1e-6) / 1e12, "GBps": nb / (us * 1e-6) / 1e9,
                                    "roofline_frac": t_roof / (us * 1e-6),
                                    "launches": nl // R}
+    # ---- each quantizer of the chain on its own (graphs of R calls)
+    per_quant = {}
+    for B in bufs:
+        M = B.M
+        L = layers[0]
+        xq = dense(B.xq, M, HIDDEN)
+        cases = {
+            "rmsnorm_quant/K3584": lambda B=B, xq=xq: q.qurl_rmsnorm_quant(B.x, L.w["qkv"][2], EPS, qt, xq, B.sx),
+            "quant_act/K3584": lambda B=B, xq=xq: q.qurl_quant_act(B.y["qkv"][:, :HIDDEN], S_UAQ, qt, xq, B.sx),
+            "silu_mul_quant/I18944": lambda B=B: q.qurl_silu_mul_quant(B.y["gate_up"], S_UAQ, qt, B.xq, B.sx),
+        }
+        for cname, fn in cases.items():
+            def calls(fn=fn):
+                for _ in range(R):
+                    fn()
+            g, _ = graph_of(calls, q)
+            g.replay()
+            per_quant[f"{cname}/M{M}"] = {"us": time_graph(g, 4, stream) / R * 1e3}
     q.qurl_check_device_status()
 
     ops = step_ops()
@@ -431,7 +472,8 @@ def run_ours(args):
     else:
         roof = {"bound": "hbm", "achieved": d_bytes / (d_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(args.qtype)
+    roof["traffic_source"] = DOMINANT_PROFILE.get(args.qtype) if roof["traffic"] is not None else None
     roof["kernel"] = f"w8a8_gemm_kernel {dname} M={dM} K={dK} N={dN} ({args.qtype})"
     roof["peak_source"] = (f"{pk['source']} " + ("bf16 burst (INT8 runs on the fp16 tensor pipe, same dense rate)"
                                                 if qt == q.INT8 else "bf16 burst x 2 (nominal fp8:bf16 ratio)")
@@ -452,7 +494,7 @@ def run_ours(args):
             "gpu_launches": launches_step * args.steps,
             "launches_per_step": launches_step,
             "clocks": clocks.summary(),
-            "per_gemm": per}
+            "per_gemm": per, "per_quant": per_quant}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -428,11 +428,15 @@ __global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* 
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(count, c);
 }
 
-// Threads per row-CTA: enough that kVPT vectors per thread cover the row, at
+// Threads per row-CTA: enough that `per` vectors per thread cover the row, at
 // most kRowThreads (longer rows stream their tail from L1/L2 in the code pass).
-int row_threads(int nvec) {
+// With few rows (decode batches: fewer rows than ~2 per SM) a row gets about 2
+// vectors per thread instead of kVPT, so each thread's serial chain (loads,
+// divisions, block reductions) is short: such kernels are latency-bound.
+int row_threads(int nvec, int rows, int per = kVPT) {
+  const int want = rows < 304 ? 2 : per;
   int t = 32;
-  while (t < kRowThreads && t * kVPT < nvec) t *= 2;
+  while (t < kRowThreads && t * want < nvec) t *= 2;
   return t;
 }
 
@@ -440,23 +444,22 @@ int row_threads(int nvec) {
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
                              void* x16, cudaStream_t st) {
-  return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
+  return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
                     reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
                                  int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st) {
-  return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8)), 0, st,
+  return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
                     sx, ms_out, reinterpret_cast<uint8_t*>(x16));
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
                                   float* sx, float* h_out, void* x16, cudaStream_t st) {
-  // two vectors (gate, up) are cached per position: use twice the threads
-  int t = 32;
-  while (t < kRowThreads && t * (kVPT / 2) < I / 8) t *= 2;
+  // two vectors (gate, up) are cached per position: half as many per thread
+  const int t = row_threads(I / 8, M, kVPT / 2);
   return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
                     ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
 }
@@ -464,7 +467,7 @@ cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st) {
-  const int t = row_threads(K / 8);
+  const int t = row_threads(K / 8, N);
   cudaError_t e = w_f32 ? launch_pdl(prepare_weights_kernel<true>, dim3(N), dim3(t), 0, st, W, K, ldw, s, qt,
                                      reinterpret_cast<uint8_t*>(Wq), sw, W_scaled)
                         : launch_pdl(prepare_weights_kernel<false>, dim3(N), dim3(t), 0, st, W, K, ldw, s, qt,
