@@ -247,6 +247,57 @@ def test_gemm_int8_chunk_edge_exactness():
     np.testing.assert_array_equal(acc.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("extra", [0, 1])
+def test_gemm_int8_single_pass_limit(extra):
+    """The decode INT8 kernel accumulates a token tile over all of K in one fp32
+    pass when every token has sum_k |x| <= 2^24 / 128 = 131072, else in 1024-deep
+    chunks.  Here sum |x| = 131042 (one pass) or 131073 (chunks), while the
+    partial sums with w = -128 reach -16,773,120 = -(2^24 - 4096) or beyond, and
+    +-1 terms follow that only survive if no low bit is dropped."""
+    K, M, N = 8192, 16, 256
+    xq = np.zeros((M, K), np.int8)
+    xq[:, :8190] = 16
+    xq[:, 8190:] = 1
+    if extra:
+        xq[:, :31] = 17  # sum |x| = 131042 + 31 = 131073: one over the single-pass limit
+    xq[1] = -xq[1]
+    wq = np.full((N, K), -128, np.int8)
+    g = np.random.Generator(np.random.PCG64(5))
+    wq[:, 8190:] = g.choice(np.array([-1, 0, 1], np.int8), size=(N, 2))
+    wq[1::2, :8190] = 127
+    assert int(np.abs(xq.astype(np.int64)).sum(1).max()) == (131073 if extra else 131042)
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
+                     q.workspace(M, N, K, q.INT8))
+    sync_ok()
+    ref = oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT)
+    assert np.abs(ref).max() >= 16_773_120
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("M", [200, 256])
+def test_gemm_int8_mixed_token_tiles(M):
+    """Two 128-token tiles: the first with small activation codes (one fp32 pass
+    over K), the second with uniform codes whose sum |x| needs 1024-deep chunks;
+    through the unfused linear (codes widened by a separate kernel) and the
+    accumulator entry point."""
+    N, K = 384, 4096
+    g = np.random.Generator(np.random.PCG64(M))
+    xq = g.integers(-127, 128, size=(M, K)).astype(np.int8)
+    xq[:128] = g.integers(-20, 21, size=(128, K)).astype(np.int8)
+    wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    xd, wd = to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8)
+    ws = q.workspace(M, N, K, q.INT8)
+    acc = q.gemm_acc(xd, wd, q.INT8, ws)
+    sx = torch.rand(M, device="cuda") * 1e-2 + 1e-3
+    sw = torch.rand(N, device="cuda") * 1e-2 + 1e-3
+    Y = q.linear(xd, sx, wd, sw, q.INT8, ws)
+    sync_ok()
+    ref = oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT)
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+    Yo = oracle.epilogue(ref, f32(sx), f32(sw))
+    np.testing.assert_array_equal(bits(Y), Yo)
+
+
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
 def test_gemm_acc_fp8(M, N, K):
     xq = random_codes(q.FP8_E4M3, (M, K), M * 7 + K)
@@ -400,7 +451,9 @@ def test_split_k_reduction(qt):
         launches = q.qurl_kernel_launches() - n0
         acc = q.gemm_acc(args[0], args[2], qt, ws)
         sync_ok()
-        split = ws is not None and ws.numel() > (((M * K * 2 + 255) // 256) * 256 if qt == q.INT8 else 0)
+        # INT8 decode workspace: fp16 copy of the codes, then per-token sums of |code|
+        act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256 if qt == q.INT8 else 0
+        split = ws is not None and ws.numel() > act
         assert launches == 1 + int(split) + int(qt == q.INT8), (tiles, launches)
         Yo, acco = oracle.w8a8_linear(Xq, sx, Wq, sw, oqt(qt), nthreads=NT)
         if qt == q.INT8:

@@ -192,10 +192,11 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   const bool int8 = (qt == QURL_INT8);
   const bool split = p.splits > 1;
   uint8_t* part = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
+  int* asum = p.tmem_a ? reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off) : nullptr;
   CUtensorMap ta, tb;
   if (p.tmem_a) {
     if (!x16_ready) {
-      QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, static_cast<size_t>(M) * K, dev->num_sms, st));
+      QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, asum, st));
       w_indep = true;  // the widening kernel writes only the workspace
     }
     QURL_TRY(byte_map(Wq, N, K, K, 128, 128, true, &ta));
@@ -222,6 +223,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.part = split ? static_cast<void*>(part) : acc_out;
   a.acc_out = acc_out;
   a.fault = g_inject_timeout.exchange(0);
+  a.asum = asum;
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
   if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
@@ -340,7 +342,7 @@ qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale
   if (!aligned16(Xq)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr,
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr, nullptr,
                                    reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -353,7 +355,7 @@ qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float
   if (!aligned16(Xq) || !aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr,
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr, nullptr,
                                        reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -368,7 +370,7 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
     return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr, nullptr,
                                         reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -404,13 +406,24 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Where the GEMM plan reads an fp16 copy of the INT8 codes from the
-// workspace, the fused quantizer writes it there directly.
-void* fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+// Where the GEMM plan reads an fp16 copy of the INT8 codes (and their
+// per-token sums of |code|) from the workspace, the fused quantizer writes
+// them there directly.
+struct FusedAct {
+  void* x16 = nullptr;
+  int* asum = nullptr;
+};
+
+FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+  FusedAct f;
   DevState* dev = nullptr;
-  if (device_state(&dev) != QURL_OK) return nullptr;
+  if (device_state(&dev) != QURL_OK) return f;
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
-  return p.tmem_a ? ws : nullptr;
+  if (p.tmem_a) {
+    f.x16 = ws;
+    f.asum = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off);
+  }
+  return f;
 }
 
 qurl_status check_fused_out(const void* Wq, const float* sw, int M, int N, int K, int qt, void* Y, int ldy,
@@ -430,11 +443,11 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   if (!gamma_folded || !(eps >= 0.0f) || !std::isfinite(eps)) return QURL_ERR_INVALID_ARG;
   if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, x16,
-                                       st));
+  const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
+                                       f.asum, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr, true);
+                  f.x16 != nullptr, true);
 }
 
 qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const void* Wq, const float* sw, int M,
@@ -444,10 +457,10 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  void* x16 = fused_x16(M, N, K, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, x16, st));
+  const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, f.x16, f.asum, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr, true);
+                  f.x16 != nullptr, true);
 }
 
 qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale, const void* Wq, const float* sw,
@@ -459,10 +472,11 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
   QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  void* x16 = fused_x16(M, N, I, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, x16, st));
+  const FusedAct f = fused_x16(M, N, I, qt, workspace, ws_bytes);
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
+                                        f.asum, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
-                  x16 != nullptr, true);
+                  f.x16 != nullptr, true);
 }
 
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,

@@ -9,9 +9,9 @@ namespace qurl {
 // >= 16 on the N side (<= 256 for FP8, <= 128 for INT8, whose TMEM holds two
 // partial buffers and an int32 running sum).  Prefill: 128-token tiles x 256
 // (FP8) or 128 (INT8) channels.  When the tiles do not fill the SMs, K is split
-// so that tiles x splits is close to the SM count, each split at least 4 (FP8)
-// or 8 (INT8) k-blocks deep, as far as the workspace allows.  Workspace
-// layout: [fp16 activation codes (INT8 decode)][split-K partials].
+// so that tiles x splits is close to the SM count, each split at least 512
+// deep, as far as the workspace allows.  Workspace layout: [fp16 activation
+// codes and per-token sums of |code| (INT8 decode)][split-K partials].
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
@@ -19,9 +19,11 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   // INT8 decode prefers the TMEM-operand kernel, which needs an fp16 copy of
   // the activation codes (2 M K bytes) in the workspace.
   const size_t x16 = (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
-  p.tmem_a = int8 && p.swap && ws_avail >= x16;
-  p.x16_bytes = p.tmem_a ? x16 : 0;
-  p.bk = (int8 && !p.tmem_a) ? 64 : 128;
+  const size_t sums = (static_cast<size_t>(M) * 4 + 255) & ~static_cast<size_t>(255);
+  p.tmem_a = int8 && p.swap && ws_avail >= x16 + sums;
+  p.x16_bytes = p.tmem_a ? x16 + sums : 0;
+  p.asum_off = p.tmem_a ? x16 : 0;
+  p.bk = int8 ? (p.tmem_a ? 256 : 64) : 128;
   p.num_kb = (K + p.bk - 1) / p.bk;
   if (p.swap) {
     const int max_bn = int8 ? 128 : 256;
@@ -38,7 +40,7 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
   int splits = 1;
   if (num_sms > 0 && tiles < num_sms) {
-    const int min_kb = (p.bk == 64) ? 8 : 4;
+    const int min_kb = (p.bk == 64) ? 8 : (p.bk == 256 ? 2 : 4);
     const int want = static_cast<int>(num_sms / tiles);
     const int cap = std::max(1, p.num_kb / min_kb);
     splits = std::max(1, std::min(want, cap));

@@ -1,42 +1,68 @@
 // gemm_i8t.cu -- the INT8 W8A8 GEMM for decode (weights on the MMA M side),
 // with the weight operand widened into TMEM.
 //
-// Per 128-deep k-block a CTA
-//   * TMA-loads its 128 weight rows of int8 codes (16 KB, 128-byte swizzle) and
-//     the tokens' codes already widened to fp16 (BN rows x 256 B, two swizzled
-//     halves) -- the fp16 copy of the activation codes is made once per call,
-//     not once per CTA;
+// Per 256-deep k stage a CTA
+//   * TMA-loads its 128 weight rows of int8 codes (two 128-byte-swizzled
+//     boxes, 32 KB) into a ring of their own, and the tokens' codes already
+//     widened to fp16 (BN rows x 512 B as four swizzled boxes) into a second
+//     ring -- the fp16 copy is made once per call, not once per CTA;
 //   * converter warps (one thread per weight row = TMEM lane) read the row's
-//     128 codes from shared memory, widen them to fp16 (exact) and store them
-//     into a TMEM stage with tcgen05.st: the MMA takes its A operand from TMEM,
-//     so the widened weights never travel through shared memory;
-//   * the MMA warp issues tcgen05.mma kind::f16 [d], [a_tmem], b_desc with fp32
-//     accumulation; every 1024-deep chunk is exact (|partial| < 1024 * 127^2 <
-//     2^24) and the epilogue warps drain it into an int32 running sum in TMEM,
-//     exactly as in the shared-memory INT8 kernel (gemm.cuh).
-// Shared-memory traffic per weight byte: 1 (TMA) + 1 (converter read) + 4
-// (fp16 activations in and out, amortised over the 128 weight rows of the
-// tile at BN = 64) -- half of widening both operands in shared memory.
+//     256 codes into registers, free the weight slot at once, widen the codes
+//     to fp16 (exact) and store them into a TMEM stage with tcgen05.st: the MMA
+//     takes its A operand from TMEM, so the widened weights never travel
+//     through shared memory;
+//   * one thread issues 16 tcgen05.mma kind::f16 [d], [a_tmem], b_desc (fp32
+//     accumulation) after a single barrier wait and frees the TMEM stage and
+//     the activation slot with a single commit.  The issuing thread's fixed
+//     cost per wait/commit is what bounds a 128-deep pipeline at decode sizes,
+//     hence the 256-deep stages.
+//
+// Exactness.  Every product is an integer of magnitude <= 128^2 and the MMA
+// accumulates in fp32, which is exact while every partial sum is an integer of
+// magnitude <= 2^24.  For token t, |partial| <= 128 * S_t with S_t = sum_k
+// |x_tk|, which the kernel that writes the fp16 codes also writes.  A token
+// tile whose tokens all have S_t <= 2^24 / 128 is accumulated over its whole K
+// range in one pass ("fast" tile -- for LLM activations S_t is far below the
+// limit).  Otherwise the tile falls back to 1024-deep chunks (|partial| <=
+// 1024 * 128^2 = 2^24), each drained by the epilogue into an int32 running sum
+// in TMEM.  Both are exact.
+//
+// TMEM: two fp32 accumulators of BN columns (at least 32) -- alternated
+// between fast units; a chunked unit accumulates in the first and keeps its
+// running sum in the second -- then NS stages of 128 columns (256 fp16 per
+// lane) of widened weights.
 #include "gemm.cuh"
 
 namespace qurl {
 
-template <int BN, int STAGES, int ASTAGES>
+// Largest S_t = sum_k |x_tk| for which one fp32 pass over K is exact.
+constexpr int kFastSumMax = (1 << 24) / 128;
+// Saturation of the S_t computed by the activation kernels (> kFastSumMax).
+constexpr int kSumCap = 1 << 24;
+
+template <int BN>
 struct I8tCfg {
   static constexpr int BM = 128;
-  static constexpr int BK = 128;                          // k per k-block
-  static constexpr int W_STAGE = BM * BK;                 // int8 weight tile
-  static constexpr int X_HALF = BN * 128;                 // fp16 [BN][64] swizzled half
-  static constexpr int X_STAGE = 2 * X_HALF;
-  static constexpr int SMEM_BYTES = STAGES * (W_STAGE + X_STAGE) + 1024;
-  static constexpr int NUM_THREADS = 448;  // TMA, MMA, 4 epilogue warps, 8 converter warps
-  static constexpr int A_BASE = ((3 * BN + 63) / 64) * 64;  // TMEM column of the first A stage
-  static constexpr int A_COLS = 64;                       // 128 fp16 per lane per k-block
-  static constexpr int TMEM_USED = A_BASE + ASTAGES * A_COLS;
-  static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int CHUNK_KB = 1024 / BK;
+  static constexpr int BK = 256;                          // k per stage
+  static constexpr int W_BOX = BM * 128;                  // a 128-byte-wide swizzled box of codes
+  static constexpr int W_STAGE = 2 * W_BOX;               // 32 KB
+  static constexpr int X_BOX = BN * 128;                  // BN rows x 64 fp16
+  static constexpr int X_STAGE = 4 * X_BOX;
+  static constexpr int NS = BN >= 128 ? 2 : 3;            // TMEM A stages = activation slots
+  static constexpr int ACC_COLS = BN < 32 ? 32 : BN;      // an epilogue access spans 32 columns
+  static constexpr int A_COLS = BK / 2;                   // 256 fp16 per lane
+  static constexpr int A_BASE = 2 * ACC_COLS;
+  static constexpr int TMEM_USED = A_BASE + NS * A_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int DYN_LIMIT = 227 * 1024 - 1024;     // leaves room for the static barrier block
+  static constexpr int WST_FIT = (DYN_LIMIT - 1024 - NS * X_STAGE) / W_STAGE;
+  static constexpr int WST = WST_FIT < 6 ? WST_FIT : 6;   // weight slots
+  static constexpr int SMEM_BYTES = WST * W_STAGE + NS * X_STAGE + 1024;
+  static constexpr int NUM_THREADS = 512;  // W TMA, MMA, X TMA, mode, 4 epilogue, 8 converter warps
+  static constexpr int CHUNK = 1024 / BK;                 // stages per exact chunk
   static constexpr uint32_t IDESC = umma_idesc_f32acc(0, 0, BM, BN);  // f16 x f16 -> f32
   static_assert(TMEM_USED <= 512, "TMEM has 512 columns");
+  static_assert(WST >= 3, "weight ring depth");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -50,28 +76,56 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
-template <int STAGES, int ASTAGES>
+template <int WST, int NS>
 struct I8tBarriers {
-  uint64_t full[STAGES];     // TMA (weights + fp16 activations) landed
-  uint64_t empty[STAGES];    // a converter group read the weights (128) and the MMA read the activations (1)
-  uint64_t afull[ASTAGES];   // converters -> MMA: A stage written to TMEM
-  uint64_t aempty[ASTAGES];  // MMA -> converters: A stage consumed
-  uint64_t pfull[2];
-  uint64_t pempty[2];
-  uint64_t done;
+  uint64_t wfull[WST];    // TMA -> converters: weight codes landed
+  uint64_t wempty[WST];   // converters (128) -> weight producer: codes are in registers
+  uint64_t xfull[NS];     // TMA -> converters: fp16 activation codes landed
+  uint64_t afull[NS];     // converters (128) -> MMA: A stage in TMEM (and its activation slot landed)
+  uint64_t consumed[NS];  // MMA commit -> converters, activation producer: stage read
+  uint64_t pfull[2];      // MMA commit -> epilogue: accumulator ready
+  uint64_t pempty[2];     // epilogue (128) -> MMA: accumulator drained
+  uint64_t modes;         // mode warp -> MMA, epilogue: fast_mask written
+  uint64_t done;          // MMA drain on the error path
+  uint32_t fast_mask;     // bit t set: token tile t takes one pass over K
   uint32_t tmem_base;
 };
 
-template <int BN, int STAGES, int ASTAGES>
-__global__ void __launch_bounds__(448, 1)
+// Slot index and phase parity of a ring with N slots.
+template <int N>
+struct Ring {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++idx == N) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Sum of |c| over 16 int8 codes (|-128| counts 128).
+__device__ __forceinline__ int abs_sum16(const uint4 v) {
+  unsigned s = 0;
+  s = __dp4a(__vabs4(v.x), 0x01010101u, s);
+  s = __dp4a(__vabs4(v.y), 0x01010101u, s);
+  s = __dp4a(__vabs4(v.z), 0x01010101u, s);
+  s = __dp4a(__vabs4(v.w), 0x01010101u, s);
+  return static_cast<int>(s);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(512, 1)
     w8a8_gemm_i8t_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX16,
                          const GemmArgs args) {
-  using C = I8tCfg<BN, STAGES, ASTAGES>;
-  __shared__ I8tBarriers<STAGES, ASTAGES> bars;
+  using C = I8tCfg<BN>;
+  constexpr int WST = C::WST;
+  constexpr int NS = C::NS;
+  __shared__ I8tBarriers<WST, NS> bars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stW = smem;                           // [STAGES][W_STAGE]
-  uint8_t* stX = stW + STAGES * C::W_STAGE;      // [STAGES][X_STAGE]
+  uint8_t* stW = smem;                       // [WST][W_STAGE]
+  uint8_t* stX = stW + WST * C::W_STAGE;     // [NS][X_STAGE]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -79,18 +133,20 @@ __global__ void __launch_bounds__(448, 1)
   int* status = args.status;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.empty[s], 129);  // one converter group (128 threads) + the MMA's commit
+    for (int s = 0; s < WST; ++s) {
+      mbar_init(&bars.wfull[s], 1);
+      mbar_init(&bars.wempty[s], 128);
     }
-    for (int s = 0; s < ASTAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars.xfull[s], 1);
       mbar_init(&bars.afull[s], 128);
-      mbar_init(&bars.aempty[s], 1);
+      mbar_init(&bars.consumed[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.pfull[b], 1);
       mbar_init(&bars.pempty[b], 128);
     }
+    mbar_init(&bars.modes, 1);
     mbar_init(&bars.done, 1);
     fence_barrier_init();
   }
@@ -109,89 +165,95 @@ __global__ void __launch_bounds__(448, 1)
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
 
+  auto is_fast = [&](uint32_t mask, int u) {
+    const int t = u % args.tiles_tok;
+    return t < 32 && ((mask >> t) & 1u) != 0;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      const uint64_t polW = l2_policy_evict_first();
-      const uint64_t polX = l2_policy_evict_last();
-      // weight tiles of the first stages stream in while the previous kernel
-      // (which, per w_prefetch, does not write Wq) is finishing
+      const uint64_t pol = l2_policy_evict_first();
+      auto load = [&](int slot, const Unit& w, int it) {
+        mbar_arrive_expect_tx(&bars.wfull[slot], C::W_STAGE);
+        const int k0 = (w.kb0 + it) * C::BK;
+        uint8_t* dst = stW + slot * C::W_STAGE;
+        tma_load_2d(dst, &tmW, k0, w.a0, &bars.wfull[slot], pol);
+        tma_load_2d(dst + C::W_BOX, &tmW, k0 + 128, w.a0, &bars.wfull[slot], pol);
+      };
+      // the first slots stream in while the previous kernel (which, per
+      // w_prefetch, does not write Wq) is finishing
       int npre = 0;
       if (args.w_prefetch && !args.fault && R.u < R.end) {
         const Unit w = unit_of<true, BN>(args, R.u);
-        npre = min(STAGES, w.nkb);
-        for (int it = 0; it < npre; ++it) {
-          mbar_arrive_expect_tx(&bars.full[it], C::W_STAGE + C::X_STAGE);
-          tma_load_2d(stW + it * C::W_STAGE, &tmW, (w.kb0 + it) * C::BK, w.a0, &bars.full[it], polW);
-        }
+        npre = min(WST, w.nkb);
+        for (int it = 0; it < npre; ++it) load(it, w, it);
       }
       griddep_wait();
+      Ring<WST> r;
       int g = 0;
       bool ok = true;
       for (int u = R.u; u < R.end && ok; u += R.stride) {
         const Unit w = unit_of<true, BN>(args, u);
-        for (int it = 0; it < w.nkb; ++it, ++g) {
-          const int s = g % STAGES;
-          const int kb = w.kb0 + it;
-          if (args.fault && g == 0) continue;  // injected fault: this stage never fills
-          if (g >= npre) {
-            if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bars.full[s], C::W_STAGE + C::X_STAGE);
-            tma_load_2d(stW + s * C::W_STAGE, &tmW, kb * C::BK, w.a0, &bars.full[s], polW);
+        for (int it = 0; it < w.nkb; ++it, ++g, r.next()) {
+          if (args.fault && g == 0) continue;  // injected fault: this slot never fills
+          if (g < npre) continue;
+          if (!mbar_wait(&bars.wempty[r.idx], r.phase ^ 1u, status)) {
+            ok = false;
+            break;
           }
-          uint8_t* xs = stX + s * C::X_STAGE;
-          tma_load_2d(xs, &tmX16, kb * C::BK * 2, w.b0, &bars.full[s], polX);
-          tma_load_2d(xs + C::X_HALF, &tmX16, kb * C::BK * 2 + 128, w.b0, &bars.full[s], polX);
+          load(r.idx, w, it);
         }
       }
       if (!ok) {
-        for (int it = max(0, g - STAGES); it < g; ++it)
-          mbar_wait_drain(&bars.full[it % STAGES], (it / STAGES) & 1, status);
+        for (int j = max(0, g - WST); j < g; ++j) mbar_wait_drain(&bars.wfull[j % WST], (j / WST) & 1, status);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = true;
-      int g = 0, cg = 0;
+      bool ok = mbar_wait(&bars.modes, 0, status);
+      const uint32_t mask = bars.fast_mask;
+      Ring<NS> r;
+      int nb0 = 0, nb1 = 0;  // accumulator fills issued per buffer
+      int next_fast = 0;
       for (int u = R.u; u < R.end && ok; u += R.stride) {
         const Unit w = unit_of<true, BN>(args, u);
-        for (int it = 0; it < w.nkb; ++it, ++g) {
-          const int kin = it % C::CHUNK_KB;
-          const int buf = cg & 1;
-          if (kin == 0 && cg >= 2) {
-            if (!mbar_wait(&bars.pempty[buf], ((cg >> 1) - 1) & 1, status)) {
+        const bool fast = is_fast(mask, u);
+        int b = 0;
+        uint32_t d = tmem;
+        for (int it = 0; it < w.nkb; ++it, r.next()) {
+          const int kin = fast ? it : it % C::CHUNK;  // stage within the accumulation pass
+          if (kin == 0) {
+            b = fast ? next_fast : 0;
+            const int nb = b ? nb1 : nb0;
+            if (nb > 0 && !mbar_wait(&bars.pempty[b], (nb - 1) & 1, status)) {
               ok = false;
               break;
             }
+            d = tmem + b * C::ACC_COLS;
           }
-          const int s = g % STAGES;
-          const int as = g % ASTAGES;
-          if (!mbar_wait(&bars.full[s], (g / STAGES) & 1, status) ||
-              !mbar_wait(&bars.afull[as], (g / ASTAGES) & 1, status)) {
+          if (!mbar_wait(&bars.afull[r.idx], r.phase, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + buf * BN;
-          const uint32_t a_t = tmem + C::A_BASE + as * C::A_COLS;
-          const uint32_t xs = smem_addr(stX + s * C::X_STAGE);
+          const uint32_t a_t = tmem + C::A_BASE + r.idx * C::A_COLS;
+          const uint32_t xs = smem_addr(stX + r.idx * C::X_STAGE);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t b_addr = xs + (kk >> 2) * C::X_HALF + (kk & 3) * 32;
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint32_t b_addr = xs + (kk >> 2) * C::X_BOX + (kk & 3) * 32;
             umma_f16_tmem_a(d, a_t + kk * 8, umma_desc_sw128(b_addr), C::IDESC, (kin | kk) != 0);
           }
-          umma_commit(&bars.empty[s]);
-          umma_commit(&bars.aempty[as]);
-          if (kin == C::CHUNK_KB - 1 || it == w.nkb - 1) {
-            umma_commit(&bars.pfull[buf]);
-            ++cg;
+          umma_commit(&bars.consumed[r.idx]);
+          const bool pass_end = (it == w.nkb - 1) || (!fast && kin == C::CHUNK - 1);
+          if (pass_end) {
+            umma_commit(&bars.pfull[b]);
+            if (b) ++nb1; else ++nb0;
           }
         }
+        next_fast = fast ? (next_fast ^ 1) : 0;
       }
       if (!ok) {
         umma_commit(&bars.done);
@@ -199,30 +261,79 @@ __global__ void __launch_bounds__(448, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ epilogue (chunk drains)
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ activation producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      Ring<NS> r;
+      int g = 0;
+      bool ok = true;
+      for (int u = R.u; u < R.end && ok; u += R.stride) {
+        const Unit w = unit_of<true, BN>(args, u);
+        for (int it = 0; it < w.nkb; ++it, ++g, r.next()) {
+          if (!mbar_wait(&bars.consumed[r.idx], r.phase ^ 1u, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.xfull[r.idx], C::X_STAGE);
+          uint8_t* xs = stX + r.idx * C::X_STAGE;
+          const int c0 = (w.kb0 + it) * C::BK * 2;  // byte column of the fp16 copy
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(xs + j * C::X_BOX, &tmX16, c0 + j * 128, w.b0, &bars.xfull[r.idx], pol);
+        }
+      }
+      if (!ok) {
+        for (int j = max(0, g - NS); j < g; ++j) mbar_wait_drain(&bars.xfull[j % NS], (j / NS) & 1, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ per-token-tile accumulation mode
+    uint32_t mask = 0;
+    if (args.asum != nullptr) {
+      for (int t = 0; t < args.tiles_tok && t < 32; ++t) {
+        int mx = 0;
+        for (int j = lane; j < BN; j += 32) {
+          const int m = t * BN + j;
+          if (m < args.M) mx = max(mx, __ldg(args.asum + m));
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        if (mx <= kFastSumMax) mask |= 1u << t;
+      }
+    }
+    if (lane == 0) {
+      bars.fast_mask = mask;
+      mbar_arrive(&bars.modes);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int i = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t tR = lane_base + 2 * BN;
+    const uint32_t tR = lane_base + C::ACC_COLS;  // running sum of a chunked unit
     const int emode = args.mode;
-    int cg = 0;
-    bool ok = true;
+    bool ok = warp_wait(&bars.modes, 0, status);
+    const uint32_t mask = bars.fast_mask;
+    int nb0 = 0, nb1 = 0;
+    int next_fast = 0;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<true, BN>(args, u);
-      const int nch = (w.nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
-      for (int c = 0; c < nch; ++c, ++cg) {
-        const int buf = cg & 1;
-        if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) {
+      const bool fast = is_fast(mask, u);
+      const int npass = fast ? 1 : (w.nkb + C::CHUNK - 1) / C::CHUNK;
+      for (int c = 0; c < npass; ++c) {
+        const int b = fast ? next_fast : 0;
+        if (!warp_wait(&bars.pfull[b], (b ? nb1 : nb0) & 1, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool last = (c == nch - 1);
+        const bool last = (c == npass - 1);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t p[32];
-          tmem_ld32(lane_base + buf * BN + c0, p);
+          tmem_ld32(lane_base + b * C::ACC_COLS + c0, p);
           int v[32];
           if (c > 0) {
             uint32_t rs[32];
@@ -244,52 +355,59 @@ __global__ void __launch_bounds__(448, 1)
         }
         if (!last) tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.pempty[buf]);
+        mbar_arrive(&bars.pempty[b]);
+        if (b) ++nb1; else ++nb0;
       }
+      next_fast = fast ? (next_fast ^ 1) : 0;
     }
   } else {
     // ------------------------------------------------------------ converters: weights -> fp16 in TMEM
     // Two groups of four warps (one per TMEM lane quadrant, one weight row per
-    // lane) take alternate k-blocks, so two k-blocks are widened at a time: a
-    // group's k-block is a serial chain (wait, load, widen, tcgen05.st, wait,
-    // signal) and the groups overlap theirs.
+    // lane) take alternate stages.
     const int q = warp & 3;
-    const int grp = (warp - 6) >> 2;
+    const int grp = (warp - 8) >> 2;
     const int i = q * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int row_off = (i >> 3) * 1024 + (i & 7) * 128;
+    Ring<WST> rw;
+    Ring<NS> ra;
     int g = 0;
     bool ok = true;
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<true, BN>(args, u);
-      for (int it = 0; it < w.nkb; ++it, ++g) {
+      for (int it = 0; it < w.nkb; ++it, ++g, rw.next(), ra.next()) {
         if ((g & 1) != grp) continue;
-        const int s = g % STAGES;
-        const int as = g % ASTAGES;
-        if (!warp_wait(&bars.full[s], (g / STAGES) & 1, status) ||
-            !warp_wait(&bars.aempty[as], ((g / ASTAGES) & 1) ^ 1, status)) {
+        if (!warp_wait(&bars.wfull[rw.idx], rw.phase, status)) {
           ok = false;
           break;
         }
-        const uint8_t* wrow = stW + s * C::W_STAGE + (i >> 3) * 1024 + (i & 7) * 128;
-        const uint32_t a_t = lane_base + C::A_BASE + as * C::A_COLS;
+        const uint8_t* wrow = stW + rw.idx * C::W_STAGE + row_off;
+        uint4 raw[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int j = 0; j < 16; ++j)  // 16-byte chunk j = k 16j .. 16j+15, swizzled within its box
+          raw[j] = *reinterpret_cast<const uint4*>(wrow + (j >> 3) * C::W_BOX + (((j & 7) ^ (i & 7)) << 4));
+        mbar_arrive(&bars.wempty[rw.idx]);
+        if (!warp_wait(&bars.xfull[ra.idx], ra.phase, status) ||
+            !warp_wait(&bars.consumed[ra.idx], ra.phase ^ 1u, status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_t = lane_base + C::A_BASE + ra.idx * C::A_COLS;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
           uint32_t v[32];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
-            const int j = half * 4 + jj;  // 16-byte chunk = k 16j .. 16j+15
-            const uint4 raw = *reinterpret_cast<const uint4*>(wrow + ((j ^ (i & 7)) << 4));
             uint4 lo, hi;
-            i8x16_to_f16x16(raw, lo, hi);
+            i8x16_to_f16x16(raw[4 * h + jj], lo, hi);
             v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
             v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
           }
-          tmem_st32(a_t + half * 32, v);
+          tmem_st32(a_t + h * 32, v);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.afull[as]);
-        mbar_arrive(&bars.empty[s]);
+        mbar_arrive(&bars.afull[ra.idx]);
       }
     }
   }
@@ -302,48 +420,61 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-// int8 codes -> fp16 (exact), [M, K] dense -> [M, K] dense.
-__global__ void i8_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec) {
+// One block per row: int8 codes -> fp16 (exact), [M, K] dense -> [M, K]
+// dense, and S_m = sum_k |code| (saturated at kSumCap) for the GEMM's
+// accumulation mode.
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                        int K, int* __restrict__ asum) {
   griddep_launch_dependents();
   griddep_wait();
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+  __shared__ int red[8];
+  const int m = blockIdx.x;
+  const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(m) * K);
+  uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(m) * K * 2);
+  const int nvec = K >> 4;
+  int sum = 0;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 raw = __ldg(s + v);
     uint4 lo, hi;
-    i8x16_to_f16x16(__ldg(src + i), lo, hi);
-    dst[2 * i] = lo;
-    dst[2 * i + 1] = hi;
+    i8x16_to_f16x16(raw, lo, hi);
+    d[2 * v] = lo;
+    d[2 * v + 1] = hi;
+    sum = min(sum + abs_sum16(raw), kSumCap);
+  }
+  sum = min(static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(sum))), kSumCap);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t = min(t + red[w], kSumCap);
+    asum[m] = t;
   }
 }
 
-template <int BN, int STAGES, int ASTAGES>
+template <int BN>
 cudaError_t launch_i8t_inst(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& args, dim3 grid,
                             cudaStream_t stream) {
-  using C = I8tCfg<BN, STAGES, ASTAGES>;
+  using C = I8tCfg<BN>;
   static bool attr_done[64] = {};
-  return launch_persistent(w8a8_gemm_i8t_kernel<BN, STAGES, ASTAGES>, C::NUM_THREADS, C::SMEM_BYTES, tw, tx, args,
-                           grid, stream, attr_done);
+  return launch_persistent(w8a8_gemm_i8t_kernel<BN>, C::NUM_THREADS, C::SMEM_BYTES, tw, tx, args, grid, stream,
+                           attr_done);
 }
 
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_i8t_inst<16, 6, 4>(tw, tx16, a, grid, st);
-    case 32: return launch_i8t_inst<32, 6, 4>(tw, tx16, a, grid, st);
-    case 64: return launch_i8t_inst<64, 5, 4>(tw, tx16, a, grid, st);
-    case 128: return launch_i8t_inst<128, 4, 2>(tw, tx16, a, grid, st);
+    case 16: return launch_i8t_inst<16>(tw, tx16, a, grid, st);
+    case 32: return launch_i8t_inst<32>(tw, tx16, a, grid, st);
+    case 64: return launch_i8t_inst<64>(tw, tx16, a, grid, st);
+    case 128: return launch_i8t_inst<128>(tw, tx16, a, grid, st);
     default: break;
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_i8_to_f16(const void* src, void* dst, size_t n, int num_sms, cudaStream_t st) {
-  const size_t nvec = n / 16;
-  size_t blocks = (nvec + 255) / 256;
-  const size_t cap = static_cast<size_t>(num_sms > 0 ? num_sms : 152) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                    reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), nvec);
+cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, int* asum, cudaStream_t st) {
+  return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, st,
+                    reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), K, asum);
 }
 
 }  // namespace qurl

@@ -67,14 +67,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or kSuspendHintNs
+// pass (then try_wait returns false and the caller polls again), so waiting
+// warps do not take issue slots from the working ones.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -87,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it < 0x7FFFFFFFu; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 3u) == 0) {
       if (*reinterpret_cast<volatile int*>(status) != kDevOk) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
         atomicCAS(status, kDevOk, kDevTimeout);

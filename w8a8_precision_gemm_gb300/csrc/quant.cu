@@ -133,13 +133,19 @@ __device__ __forceinline__ uint2 encode8(const float (&v)[8], float scale, int q
   return make_uint2(lo, hi);
 }
 
+// Saturation of the per-row sums of |code| (any value above 2^24 / 128 means
+// "accumulate in chunks" to the GEMM that reads them).
+constexpr int kAbsSumCap = 1 << 24;
+
 // Store 8 codes (and, for INT8 when x16 is given, the same 8 codes as fp16 --
 // exact, integers of magnitude <= 127 -- for the tensor-core GEMM to read).
-__device__ __forceinline__ void store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
-                                       const float (&v)[8], float scale, int qt) {
+// Returns the sum of |code| of the 8 INT8 codes when x16 is given, else 0.
+__device__ __forceinline__ int store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
+                                      const float (&v)[8], float scale, int qt) {
   const uint2 c = encode8(v, scale, qt);
   reinterpret_cast<uint2*>(q)[idx] = c;
-  if (x16 != nullptr) {
+  if (x16 == nullptr) return 0;
+  {
     uint32_t h[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -150,6 +156,20 @@ __device__ __forceinline__ void store8(uint8_t* __restrict__ q, uint8_t* __restr
       h[e] = *reinterpret_cast<const uint32_t*>(&p);
     }
     reinterpret_cast<uint4*>(x16)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+  return static_cast<int>(__dp4a(__vabs4(c.y), 0x01010101u, __dp4a(__vabs4(c.x), 0x01010101u, 0u)));
+}
+
+// asum[m] = saturated sum over the block of the per-thread sums v (thread 0 stores).
+__device__ __forceinline__ void store_row_sum(int v, int* __restrict__ asum, int m) {
+  __shared__ int ired[32];
+  v = min(static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(min(v, kAbsSumCap)))), kAbsSumCap);
+  if ((threadIdx.x & 31) == 0) ired[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < static_cast<int>((blockDim.x + 31) >> 5); ++w) t = min(t + ired[w], kAbsSumCap);
+    asum[m] = t;
   }
 }
 
@@ -187,7 +207,8 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 // ------------------------------------------------------------------ activation quant
 
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
-                                 uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16) {
+                                 uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16,
+                                 int* __restrict__ asum) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[33];
@@ -208,20 +229,23 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
+  int sabs = 0;
   for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
     float x[8];
     bf16x8_to_f32(u, x);
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
-    store8(out, out16, idx, x, scale, qt);
+    sabs = min(sabs + store8(out, out16, idx, x, scale, qt), kAbsSumCap);
   });
+  if (asum != nullptr) store_row_sum(sabs, asum, m);
 }
 
 // ------------------------------------------------------------------ RMSNorm -> quant
 
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
-                                     float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16) {
+                                     float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16,
+                                     int* __restrict__ asum) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[66];
@@ -268,11 +292,13 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
+  int sabs = 0;
   for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
     float x[8];
     normed(u, idx, x);
-    store8(out, out16, idx, x, scale, qt);
+    sabs = min(sabs + store8(out, out16, idx, x, scale, qt), kAbsSumCap);
   });
+  if (asum != nullptr) store_row_sum(sabs, asum, m);
 }
 
 // ------------------------------------------------------------------ SiLU * up -> quant
@@ -290,7 +316,8 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
 
 __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
-                                      float* __restrict__ h_out, uint8_t* __restrict__ x16) {
+                                      float* __restrict__ h_out, uint8_t* __restrict__ x16,
+                                      int* __restrict__ asum) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[33];
@@ -328,13 +355,15 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * I;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
+  int sabs = 0;
   visit([&](const uint4 g, const uint4 u, int idx) {
     float h[8];
     silu_mul8(g, u, h);
 #pragma unroll
     for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
-    store8(out, out16, idx, h, scale, qt);
+    sabs = min(sabs + store8(out, out16, idx, h, scale, qt), kAbsSumCap);
   });
+  if (asum != nullptr) store_row_sum(sabs, asum, m);
 }
 
 // ------------------------------------------------------------------ weight fold + quant
@@ -443,25 +472,26 @@ int row_threads(int nvec, int rows, int per = kVPT) {
 }  // namespace
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, cudaStream_t st) {
+                             void* x16, int* asum, cudaStream_t st) {
   return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                    reinterpret_cast<uint8_t*>(x16));
+                    reinterpret_cast<uint8_t*>(x16), asum);
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, cudaStream_t st) {
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* asum,
+                                 cudaStream_t st) {
   return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
-                    sx, ms_out, reinterpret_cast<uint8_t*>(x16));
+                    sx, ms_out, reinterpret_cast<uint8_t*>(x16), asum);
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, cudaStream_t st) {
+                                  float* sx, float* h_out, void* x16, int* asum, cudaStream_t st) {
   // two vectors (gate, up) are cached per position: half as many per thread
   const int t = row_threads(I / 8, M, kVPT / 2);
   return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
-                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16));
+                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), asum);
 }
 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
