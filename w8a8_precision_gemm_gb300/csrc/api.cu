@@ -177,6 +177,17 @@ qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int 
     if (_e != cudaSuccess) return cuda_fail(_e); \
   } while (0)
 
+// Where the INT8 decode kernel reads its per-token, per-split sums of |code|.
+qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
+  qurl::CodeSums c{};
+  if (p.tmem_a) {
+    c.asum = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off);
+    c.sum_len = p.kb_per_split * p.bk;
+    c.nsum = p.splits;
+  }
+  return c;
+}
+
 // Run the GEMM; mode bf16 -> Y, otherwise raw accumulators -> acc_out.
 // Workspace layout (see plan_gemm): [fp16 copy of the activation codes (INT8
 // decode)][split-K partials].
@@ -192,11 +203,11 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   const bool int8 = (qt == QURL_INT8);
   const bool split = p.splits > 1;
   uint8_t* part = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
-  int* asum = p.tmem_a ? reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off) : nullptr;
+  const qurl::CodeSums sums = code_sums(p, ws);
   CUtensorMap ta, tb;
   if (p.tmem_a) {
     if (!x16_ready) {
-      QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, asum, st));
+      QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
       w_indep = true;  // the widening kernel writes only the workspace
     }
     QURL_TRY(byte_map(Wq, N, K, K, 128, 128, true, &ta));
@@ -223,7 +234,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.part = split ? static_cast<void*>(part) : acc_out;
   a.acc_out = acc_out;
   a.fault = g_inject_timeout.exchange(0);
-  a.asum = asum;
+  a.asum = sums.asum;
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
   if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
@@ -342,7 +353,7 @@ qurl_status qurl_quant_act(const void* X, int M, int K, int ldx, float pre_scale
   if (!aligned16(Xq)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr, nullptr,
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq, sx, nullptr, qurl::CodeSums{},
                                    reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -355,7 +366,8 @@ qurl_status qurl_rmsnorm_quant(const void* X, int M, int K, int ldx, const float
   if (!aligned16(Xq) || !aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr, nullptr,
+  QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq, sx, ms_out, nullptr,
+                                       qurl::CodeSums{},
                                        reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -370,7 +382,8 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
     return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr, nullptr,
+  QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
+                                        qurl::CodeSums{},
                                         reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -411,7 +424,7 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
 // them there directly.
 struct FusedAct {
   void* x16 = nullptr;
-  int* asum = nullptr;
+  qurl::CodeSums sums{};
 };
 
 FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
@@ -421,7 +434,7 @@ FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
   if (p.tmem_a) {
     f.x16 = ws;
-    f.asum = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off);
+    f.sums = code_sums(p, ws);
   }
   return f;
 }
@@ -445,7 +458,7 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
   QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
-                                       f.asum, st));
+                                       f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
                   f.x16 != nullptr, true);
 }
@@ -458,7 +471,7 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
-  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, f.x16, f.asum, st));
+  QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, f.x16, f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
                   f.x16 != nullptr, true);
 }
@@ -474,7 +487,7 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, I, qt, workspace, ws_bytes);
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
-                                        f.asum, st));
+                                        f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
                   f.x16 != nullptr, true);
 }

@@ -170,60 +170,145 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-// Write 32 accumulator values of one tile row/column.  i = row of the A tile
-// (TMEM lane), columns c0..c0+31 of the B tile.
-template <bool SWAP, int BN, typename T>
-__device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int b0, int split, int i, int c0,
-                                       const T (&v)[32]) {
+// One step of a warp transpose.  Before it each lane holds nb = 2^S
+// consecutive channels (the lane's own number with its low S bits cleared,
+// plus ci) of nt = 32 / nb tokens (its low S bits, plus ti * nb), as
+// x[ci * nt + ti]; lane pairs at distance nb swap the half of their tokens the
+// other one keeps, leaving 2 nb channels of nt / 2 tokens.
+template <int S>
+__device__ __forceinline__ void transpose_step(uint32_t (&x)[32], int lane) {
+  constexpr int nb = 1 << S, nt = 32 >> S, h = nt / 2;
+  const bool bit = ((lane >> S) & 1) != 0;
+  uint32_t y[32];
+#pragma unroll
+  for (int ci = 0; ci < nb; ++ci) {
+#pragma unroll
+    for (int t2 = 0; t2 < h; ++t2) {
+      const uint32_t e = x[ci * nt + 2 * t2], o = x[ci * nt + 2 * t2 + 1];
+      const uint32_t keep = bit ? o : e;
+      const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, bit ? e : o, nb);
+      y[ci * h + t2] = bit ? recv : keep;         // channel ci: this lane's if bit == 0
+      y[(nb + ci) * h + t2] = bit ? keep : recv;  // channel nb + ci: this lane's if bit == 1
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = y[j];
+}
+
+template <typename T>
+__device__ __forceinline__ float acc_to_float(uint32_t bits) {
+  if constexpr (std::is_same<T, int>::value) return static_cast<float>(static_cast<int>(bits));
+  else return __uint_as_float(bits);
+}
+
+// The swap orientation's block of one warp: lane L holds channel a0 + (i & ~31)
+// + L for the tokens b0 + c0 + j, j < 32.  One store per lane and token would
+// write 2 (bf16) or 4 bytes per lane; three transpose steps first leave each
+// lane 8 consecutive channels ((L & ~7) + ci) of 4 tokens ((L & 7) + 8 t), so
+// each store writes 16 contiguous bytes.  sx_lane / sw_lane: lane L's scale of
+// token b0 + c0 + L and of channel a0 + (i & ~31) + L (loaded by the caller
+// ahead of time; used in mode kModeBf16).  Called by all 32 lanes of the warp.
+template <int BN, typename T>
+__device__ __forceinline__ void emit32_swap(const GemmArgs& a, int mode, int a0, int b0, int split, int i, int c0,
+                                            const T (&v)[32], float sx_lane, float sw_lane) {
   const int M = a.M, N = a.N;
+  const int L = threadIdx.x & 31;
+  uint32_t x[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = *reinterpret_cast<const uint32_t*>(&v[j]);
+  transpose_step<0>(x, L);
+  transpose_step<1>(x, L);
+  transpose_step<2>(x, L);
+  const int n0 = a0 + (i & ~31) + (L & ~7);  // the lane's first channel; x[ci * 4 + t]
   if (mode == kModeAcc) {
     T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(split) * M * N;
-    if (SWAP) {
-      const int n = a0 + i;
-      if (n < N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int m = b0 + c0 + j;
-          if (c0 + j < BN && m < M) part[static_cast<size_t>(m) * N + n] = v[j];
-        }
-      }
-    } else {
-      const int m = a0 + i;
-      if (m < M) {
-        T* dst = part + static_cast<size_t>(m) * N + (b0 + c0);
-        const int nvalid = min(32, min(BN - c0, N - (b0 + c0)));
-        if (nvalid == 32 && (N & 3) == 0) {
+    for (int t = 0; t < 4; ++t) {
+      const int jj = (L & 7) + 8 * t;
+      const int m = b0 + c0 + jj;
+      if (c0 + jj >= BN || m >= M) continue;
+      T* dst = part + static_cast<size_t>(m) * N + n0;
+      if (n0 + 8 <= N && (N & 3) == 0) {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(x[t], x[4 + t], x[8 + t], x[12 + t]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(x[16 + t], x[20 + t], x[24 + t], x[28 + t]);
+      } else {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<uint4*>(dst + j) =
-                make_uint4(*reinterpret_cast<const uint32_t*>(&v[j]),
-                           *reinterpret_cast<const uint32_t*>(&v[j + 1]),
-                           *reinterpret_cast<const uint32_t*>(&v[j + 2]),
-                           *reinterpret_cast<const uint32_t*>(&v[j + 3]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nvalid) dst[j] = v[j];
-        }
+        for (int ci = 0; ci < 8; ++ci)
+          if (n0 + ci < N) dst[ci] = *reinterpret_cast<const T*>(&x[ci * 4 + t]);
       }
     }
     return;
   }
   // dequantizing epilogue: y = bf16((fp32(acc) * sx[m]) * sw[n])
-  if (SWAP) {
-    const int n = a0 + i;
-    if (n >= N) return;
-    const float swn = __ldg(a.sw + n);
+  float swv[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int m = b0 + c0 + j;
-      if (c0 + j < BN && m < M) {
-        const float accf = static_cast<float>(v[j]);
-        const float y = __fmul_rn(__fmul_rn(accf, __ldg(a.sx + m)), swn);
-        a.Y[static_cast<size_t>(m) * a.ldy + n] = __float2bfloat16_rn(y);
+  for (int ci = 0; ci < 8; ++ci) swv[ci] = __shfl_sync(0xFFFFFFFFu, sw_lane, (L & ~7) + ci);
+  float sxv[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) sxv[t] = __shfl_sync(0xFFFFFFFFu, sx_lane, (L & 7) + 8 * t);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int jj = (L & 7) + 8 * t;
+    const int m = b0 + c0 + jj;
+    if (c0 + jj >= BN || m >= M) continue;
+    const float sxm = sxv[t];
+    uint32_t packed[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float y0 = __fmul_rn(__fmul_rn(acc_to_float<T>(x[(2 * h) * 4 + t]), sxm), swv[2 * h]);
+      const float y1 = __fmul_rn(__fmul_rn(acc_to_float<T>(x[(2 * h + 1) * 4 + t]), sxm), swv[2 * h + 1]);
+      __nv_bfloat162 p = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+      packed[h] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    __nv_bfloat16* dst = a.Y + static_cast<size_t>(m) * a.ldy + n0;
+    if (n0 + 8 <= N) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    } else {
+#pragma unroll
+      for (int ci = 0; ci < 8; ++ci)
+        if (n0 + ci < N) dst[ci] = reinterpret_cast<const __nv_bfloat16*>(packed)[ci];
+    }
+  }
+}
+
+// Scales the swap epilogue hands to emit32_swap: this lane's token b0 + c0 +
+// lane, and its channel n (0 where out of range or not needed).
+__device__ __forceinline__ float token_scale(const GemmArgs& a, int mode, int m) {
+  return (mode == kModeBf16 && m < a.M) ? __ldg(a.sx + m) : 0.0f;
+}
+__device__ __forceinline__ float channel_scale(const GemmArgs& a, int mode, int n) {
+  return (mode == kModeBf16 && n < a.N) ? __ldg(a.sw + n) : 0.0f;
+}
+
+// Prefill orientation: write 32 accumulator values of one tile row.  i = row
+// of the A tile (TMEM lane = token), columns c0..c0+31 of the B tile.
+template <int BN, typename T>
+__device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int b0, int split, int i, int c0,
+                                       const T (&v)[32]) {
+  const int M = a.M, N = a.N;
+  if (mode == kModeAcc) {
+    T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(split) * M * N;
+    const int m = a0 + i;
+    if (m < M) {
+      T* dst = part + static_cast<size_t>(m) * N + (b0 + c0);
+      const int nvalid = min(32, min(BN - c0, N - (b0 + c0)));
+      if (nvalid == 32 && (N & 3) == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<uint4*>(dst + j) =
+              make_uint4(*reinterpret_cast<const uint32_t*>(&v[j]), *reinterpret_cast<const uint32_t*>(&v[j + 1]),
+                         *reinterpret_cast<const uint32_t*>(&v[j + 2]),
+                         *reinterpret_cast<const uint32_t*>(&v[j + 3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) dst[j] = v[j];
       }
     }
-  } else {
+    return;
+  }
+  // dequantizing epilogue: y = bf16((fp32(acc) * sx[m]) * sw[n])
+  {
     const int m = a0 + i;
     if (m >= M) return;
     const float sxm = __ldg(a.sx + m);
@@ -426,6 +511,10 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     for (int u = R.u; u < R.end && ok; u += R.stride) {
       const Unit w = unit_of<SWAP, BN>(args, u);
       const int nch = (w.nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
+      // swap: scales of this lane's channel and of its token in the first
+      // 32-token block, loaded while the accumulator is being filled
+      const float sw_lane = SWAP ? channel_scale(args, emode, w.a0 + i) : 0.0f;
+      const float sx_first = SWAP ? token_scale(args, emode, w.b0 + lane) : 0.0f;
       for (int c = 0; c < nch; ++c, ++cg) {
         const int buf = cg & 1;
         if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) {
@@ -434,15 +523,21 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
         }
         tc_fence_after();
         const bool last = (c == nch - 1);
+        float sx_lane = sx_first;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
+          // the next block's token scale, in flight while this block is written
+          const float sx_next = (SWAP && last && c0 + 32 < BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
           uint32_t p[32];
           tmem_ld32(lane_base + buf * BN + c0, p);
           if constexpr (!C::kInt8) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
-            emit32<SWAP, BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+            if constexpr (SWAP)
+              emit32_swap<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
+            else
+              emit32<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
           } else {
             int v[32];
             if (c > 0) {
@@ -460,10 +555,13 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) wv[j] = static_cast<uint32_t>(v[j]);
               tmem_st32(tR + c0, wv);
+            } else if constexpr (SWAP) {
+              emit32_swap<BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
             } else {
-              emit32<SWAP, BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+              emit32<BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
             }
           }
+          sx_lane = sx_next;
         }
         if (C::kInt8 && !last) tmem_wait_st();
         tc_fence_before();

@@ -19,10 +19,8 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   // INT8 decode prefers the TMEM-operand kernel, which needs an fp16 copy of
   // the activation codes (2 M K bytes) in the workspace.
   const size_t x16 = (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
-  const size_t sums = (static_cast<size_t>(M) * 4 + 255) & ~static_cast<size_t>(255);
-  p.tmem_a = int8 && p.swap && ws_avail >= x16 + sums;
-  p.x16_bytes = p.tmem_a ? x16 + sums : 0;
-  p.asum_off = p.tmem_a ? x16 : 0;
+  auto sums = [&](int s) { return (static_cast<size_t>(M) * 4 * s + 255) & ~static_cast<size_t>(255); };
+  p.tmem_a = int8 && p.swap && ws_avail >= x16 + sums(1);
   p.bk = int8 ? (p.tmem_a ? 256 : 64) : 128;
   p.num_kb = (K + p.bk - 1) / p.bk;
   if (p.swap) {
@@ -45,12 +43,17 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     const int cap = std::max(1, p.num_kb / min_kb);
     splits = std::max(1, std::min(want, cap));
   }
+  if (p.tmem_a) splits = std::min(splits, kMaxSums);  // one code sum per split and token
   const size_t per_split = static_cast<size_t>(M) * N * 4;
-  const size_t avail = ws_avail > p.x16_bytes ? ws_avail - p.x16_bytes : 0;
-  if (splits > 1 && avail < static_cast<size_t>(splits) * per_split)
-    splits = std::max(1, static_cast<int>(std::min<size_t>(avail / per_split, 1 << 20)));
+  // workspace for s splits: [fp16 codes, code sums (INT8 decode)][s partials if s > 1]
+  auto need = [&](int s) {
+    return (p.tmem_a ? x16 + sums(s) : 0) + (s > 1 ? static_cast<size_t>(s) * per_split : 0);
+  };
+  while (splits > 1 && need(splits) > ws_avail) --splits;
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.x16_bytes = p.tmem_a ? x16 + sums(p.splits) : 0;
+  p.asum_off = p.tmem_a ? x16 : 0;
   p.part_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
   p.ws_bytes = p.x16_bytes + p.part_bytes;
   return p;

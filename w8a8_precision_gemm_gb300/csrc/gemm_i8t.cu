@@ -19,13 +19,13 @@
 //
 // Exactness.  Every product is an integer of magnitude <= 128^2 and the MMA
 // accumulates in fp32, which is exact while every partial sum is an integer of
-// magnitude <= 2^24.  For token t, |partial| <= 128 * S_t with S_t = sum_k
-// |x_tk|, which the kernel that writes the fp16 codes also writes.  A token
-// tile whose tokens all have S_t <= 2^24 / 128 is accumulated over its whole K
-// range in one pass ("fast" tile -- for LLM activations S_t is far below the
-// limit).  Otherwise the tile falls back to 1024-deep chunks (|partial| <=
-// 1024 * 128^2 = 2^24), each drained by the epilogue into an int32 running sum
-// in TMEM.  Both are exact.
+// magnitude <= 2^24.  For token t and the k range of a K split, |partial| <=
+// 128 * S_t with S_t = sum over the range of |x_tk|, which the kernel that
+// writes the fp16 codes also writes.  A unit whose tokens all have S_t <=
+// 2^24 / 128 is accumulated over its k range in one pass ("fast" unit -- for
+// LLM activations S_t is far below the limit).  Otherwise the unit falls back
+// to 1024-deep chunks (|partial| <= 1024 * 128^2 = 2^24), each drained by the
+// epilogue into an int32 running sum in TMEM.  Both are exact.
 //
 // TMEM: two fp32 accumulators of BN columns (at least 32) -- alternated
 // between fast units; a chunked unit accumulates in the first and keeps its
@@ -35,7 +35,7 @@
 
 namespace qurl {
 
-// Largest S_t = sum_k |x_tk| for which one fp32 pass over K is exact.
+// Largest S_t = sum over a k range of |x_tk| for which one fp32 pass is exact.
 constexpr int kFastSumMax = (1 << 24) / 128;
 // Saturation of the S_t computed by the activation kernels (> kFastSumMax).
 constexpr int kSumCap = 1 << 24;
@@ -76,6 +76,8 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+constexpr int kModeWords = 4;  // accumulation modes of a CTA's first 128 units (the rest: chunks)
+
 template <int WST, int NS>
 struct I8tBarriers {
   uint64_t wfull[WST];    // TMA -> converters: weight codes landed
@@ -85,9 +87,9 @@ struct I8tBarriers {
   uint64_t consumed[NS];  // MMA commit -> converters, activation producer: stage read
   uint64_t pfull[2];      // MMA commit -> epilogue: accumulator ready
   uint64_t pempty[2];     // epilogue (128) -> MMA: accumulator drained
-  uint64_t modes;         // mode warp -> MMA, epilogue: fast_mask written
+  uint64_t modes;         // mode warp -> MMA, epilogue: fast_bits written
   uint64_t done;          // MMA drain on the error path
-  uint32_t fast_mask;     // bit t set: token tile t takes one pass over K
+  uint32_t fast_bits[kModeWords];  // bit j set: the CTA's j-th unit takes one pass over its k range
   uint32_t tmem_base;
 };
 
@@ -165,9 +167,9 @@ __global__ void __launch_bounds__(512, 1)
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
 
-  auto is_fast = [&](uint32_t mask, int u) {
-    const int t = u % args.tiles_tok;
-    return t < 32 && ((mask >> t) & 1u) != 0;
+  // j: the unit's position in this CTA's list
+  auto is_fast = [&](int j) {
+    return j < 32 * kModeWords && ((bars.fast_bits[j >> 5] >> (j & 31)) & 1u) != 0;
   };
 
   if (warp == 0) {
@@ -214,13 +216,12 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(&bars.modes, 0, status);
-      const uint32_t mask = bars.fast_mask;
       Ring<NS> r;
       int nb0 = 0, nb1 = 0;  // accumulator fills issued per buffer
       int next_fast = 0;
-      for (int u = R.u; u < R.end && ok; u += R.stride) {
+      for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
         const Unit w = unit_of<true, BN>(args, u);
-        const bool fast = is_fast(mask, u);
+        const bool fast = is_fast(j);
         int b = 0;
         uint32_t d = tmem;
         for (int it = 0; it < w.nkb; ++it, r.next()) {
@@ -289,23 +290,24 @@ __global__ void __launch_bounds__(512, 1)
     }
     __syncwarp();
   } else if (warp == 3) {
-    // ------------------------------------------------------------ per-token-tile accumulation mode
-    uint32_t mask = 0;
+    // ------------------------------------------------------------ accumulation mode of each unit
+    if (lane < kModeWords) bars.fast_bits[lane] = 0;
+    __syncwarp();
     if (args.asum != nullptr) {
-      for (int t = 0; t < args.tiles_tok && t < 32; ++t) {
+      for (int u = R.u, j = 0; u < R.end && j < 32 * kModeWords; u += R.stride, ++j) {
+        const int t = u % args.tiles_tok;
+        const int sp = u / (args.tiles_tok * args.tiles_ch);
         int mx = 0;
-        for (int j = lane; j < BN; j += 32) {
-          const int m = t * BN + j;
-          if (m < args.M) mx = max(mx, __ldg(args.asum + m));
+        for (int c = lane; c < BN; c += 32) {
+          const int m = t * BN + c;
+          if (m < args.M) mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        if (mx <= kFastSumMax) mask |= 1u << t;
+        if (lane == 0 && mx <= kFastSumMax) bars.fast_bits[j >> 5] |= 1u << (j & 31);
       }
     }
-    if (lane == 0) {
-      bars.fast_mask = mask;
-      mbar_arrive(&bars.modes);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.modes);
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ epilogue
@@ -315,13 +317,16 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tR = lane_base + C::ACC_COLS;  // running sum of a chunked unit
     const int emode = args.mode;
     bool ok = warp_wait(&bars.modes, 0, status);
-    const uint32_t mask = bars.fast_mask;
     int nb0 = 0, nb1 = 0;
     int next_fast = 0;
-    for (int u = R.u; u < R.end && ok; u += R.stride) {
+    for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
       const Unit w = unit_of<true, BN>(args, u);
-      const bool fast = is_fast(mask, u);
+      const bool fast = is_fast(j);
       const int npass = fast ? 1 : (w.nkb + C::CHUNK - 1) / C::CHUNK;
+      // scales of this lane's channel and of its token in the first 32-token
+      // block, loaded while the accumulator is being filled
+      const float sw_lane = channel_scale(args, emode, w.a0 + i);
+      const float sx_first = token_scale(args, emode, w.b0 + lane);
       for (int c = 0; c < npass; ++c) {
         const int b = fast ? next_fast : 0;
         if (!warp_wait(&bars.pfull[b], (b ? nb1 : nb0) & 1, status)) {
@@ -330,8 +335,11 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_after();
         const bool last = (c == npass - 1);
+        float sx_lane = sx_first;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
+          // the next block's token scale, in flight while this block is written
+          const float sx_next = (last && c0 + 32 < BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
           uint32_t p[32];
           tmem_ld32(lane_base + b * C::ACC_COLS + c0, p);
           int v[32];
@@ -350,8 +358,9 @@ __global__ void __launch_bounds__(512, 1)
             for (int j = 0; j < 32; ++j) wv[j] = static_cast<uint32_t>(v[j]);
             tmem_st32(tR + c0, wv);
           } else {
-            emit32<true, BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+            emit32_swap<BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
           }
+          sx_lane = sx_next;
         }
         if (!last) tmem_wait_st();
         tc_fence_before();
@@ -421,34 +430,46 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // One block per row: int8 codes -> fp16 (exact), [M, K] dense -> [M, K]
-// dense, and S_m = sum_k |code| (saturated at kSumCap) for the GEMM's
-// accumulation mode.
+// dense, and the row's sums of |code| over the ranges of `sums` (saturated at
+// kSumCap) for the GEMM's accumulation mode.
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                                        int K, int* __restrict__ asum) {
+                                                        int K, const CodeSums sums) {
   griddep_launch_dependents();
   griddep_wait();
-  __shared__ int red[8];
+  __shared__ unsigned long long cnt[kMaxSums];
+  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x) cnt[j] = 0;
+  __syncthreads();
   const int m = blockIdx.x;
   const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(m) * K);
   uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(m) * K * 2);
   const int nvec = K >> 4;
-  int sum = 0;
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    const uint4 raw = __ldg(s + v);
-    uint4 lo, hi;
-    i8x16_to_f16x16(raw, lo, hi);
-    d[2 * v] = lo;
-    d[2 * v + 1] = hi;
-    sum = min(sum + abs_sum16(raw), kSumCap);
+  const int lane = threadIdx.x & 31;
+  // warp-uniform steps over 32 consecutive vectors; ranges are multiples of
+  // 16 vectors, so a step's vectors lie in at most two (r0, r0 + 1)
+  for (int v0 = threadIdx.x & ~31; v0 < nvec; v0 += blockDim.x) {
+    const int v = v0 + lane;
+    unsigned a = 0;
+    if (v < nvec) {
+      const uint4 raw = __ldg(s + v);
+      uint4 lo, hi;
+      i8x16_to_f16x16(raw, lo, hi);
+      d[2 * v] = lo;
+      d[2 * v + 1] = hi;
+      a = static_cast<unsigned>(abs_sum16(raw));
+    }
+    const int r0 = (v0 * 16) / sums.sum_len;
+    const bool first = (v < nvec ? (v * 16) / sums.sum_len : r0) == r0;
+    const unsigned s0 = __reduce_add_sync(0xFFFFFFFFu, first ? a : 0u);
+    const unsigned s1 = __reduce_add_sync(0xFFFFFFFFu, first ? 0u : a);
+    if (lane == 0) {
+      if (s0 != 0) atomicAdd(&cnt[r0], static_cast<unsigned long long>(s0));
+      if (s1 != 0) atomicAdd(&cnt[r0 + 1], static_cast<unsigned long long>(s1));
+    }
   }
-  sum = min(static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(sum))), kSumCap);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t = min(t + red[w], kSumCap);
-    asum[m] = t;
-  }
+  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x)
+    sums.asum[static_cast<size_t>(m) * sums.nsum + j] =
+        static_cast<int>(cnt[j] < static_cast<unsigned long long>(kSumCap) ? cnt[j] : kSumCap);
 }
 
 template <int BN>
@@ -472,9 +493,9 @@ cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, int* asum, cudaStream_t st) {
+cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums sums, cudaStream_t st) {
   return launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, st,
-                    reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), K, asum);
+                    reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), K, sums);
 }
 
 }  // namespace qurl

@@ -41,7 +41,18 @@ struct GemmArgs {
   void* acc_out;       // raw-accumulator output [M, N] (unused by the kernels; kept with the call)
   int fault;           // test hook: 1 = the producer skips its first k-block, so the consumer's
                        // bounded wait runs out and the kernel latches a timeout
-  const int* asum;     // INT8 decode: S_m = sum_k |Xq[m,k]| per token (null: always chunked)
+  const int* asum;     // INT8 decode: [M][splits] sums of |Xq[m,k]| over each split's k range
+                       // (null: every unit accumulates in chunks)
+};
+
+// Per-token sums of |code| over consecutive ranges of sum_len codes (the K
+// splits of the INT8 decode GEMM): asum[m * nsum + j], j < nsum.  Written by
+// the kernel that writes the fp16 copy of the codes; asum null: not wanted.
+constexpr int kMaxSums = 128;
+struct CodeSums {
+  int* asum;
+  int sum_len;  // a multiple of 256
+  int nsum;     // <= kMaxSums
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -70,15 +81,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
-// (the operand the INT8 decode GEMM reads), saving it a widening pass, and
-// then, if asum is not null, asum[m] = sum_k |code| (saturated at 2^24).
+// (the operand the INT8 decode GEMM reads), saving it a widening pass, and,
+// when sums.asum is not null, the code sums the GEMM reads with it.
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, int* asum, cudaStream_t st);
+                             void* x16, CodeSums sums, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* asum,
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, CodeSums sums,
                                  cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, int* asum, cudaStream_t st);
+                                  float* sx, float* h_out, void* x16, CodeSums sums, cudaStream_t st);
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st);
@@ -118,8 +129,8 @@ cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUten
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
-// int8 codes [M, K] -> fp16 [M, K] in dst, and asum[m] = sum_k |code| (saturated).
-cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, int* asum, cudaStream_t st);
+// int8 codes [M, K] -> fp16 [M, K] in dst, and the sums of |code| (saturated at 2^24).
+cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums sums, cudaStream_t st);
 // split-K reduction in split order: T = int (INT8) or float (FP8)
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
                                  const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,

@@ -133,7 +133,7 @@ __device__ __forceinline__ uint2 encode8(const float (&v)[8], float scale, int q
   return make_uint2(lo, hi);
 }
 
-// Saturation of the per-row sums of |code| (any value above 2^24 / 128 means
+// Saturation of the sums of |code| (any value above 2^24 / 128 means
 // "accumulate in chunks" to the GEMM that reads them).
 constexpr int kAbsSumCap = 1 << 24;
 
@@ -160,17 +160,29 @@ __device__ __forceinline__ int store8(uint8_t* __restrict__ q, uint8_t* __restri
   return static_cast<int>(__dp4a(__vabs4(c.y), 0x01010101u, __dp4a(__vabs4(c.x), 0x01010101u, 0u)));
 }
 
-// asum[m] = saturated sum over the block of the per-thread sums v (thread 0 stores).
-__device__ __forceinline__ void store_row_sum(int v, int* __restrict__ asum, int m) {
-  __shared__ int ired[32];
-  v = min(static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(min(v, kAbsSumCap)))), kAbsSumCap);
-  if ((threadIdx.x & 31) == 0) ired[threadIdx.x >> 5] = v;
+// Per-row sums of |code| over the ranges of a CodeSums, in shared-memory
+// counters: one atomic per warp and step (the 32 vectors of 8 codes a warp
+// visits in one step lie in one range, as ranges are multiples of 256 codes).
+// sums_begin zeroes the counters; the block reductions that follow in every
+// kernel order it before the first sums_add_warp.
+__device__ __forceinline__ void sums_begin(unsigned long long* cnt, const CodeSums& cs) {
+  if (cs.asum != nullptr)
+    for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x) cnt[j] = 0;
+}
+
+// Called by all 32 lanes of the warp; idx: this lane's vector; v: its sum (0 if none).
+__device__ __forceinline__ void sums_add_warp(unsigned long long* cnt, const CodeSums& cs, int idx, int v) {
+  if (cs.asum == nullptr) return;
+  const unsigned s = __reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(v));
+  if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(&cnt[(idx * 8) / cs.sum_len], static_cast<unsigned long long>(s));
+}
+
+__device__ __forceinline__ void sums_end(unsigned long long* cnt, const CodeSums& cs, int m) {
+  if (cs.asum == nullptr) return;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int w = 0; w < static_cast<int>((blockDim.x + 31) >> 5); ++w) t = min(t + ired[w], kAbsSumCap);
-    asum[m] = t;
-  }
+  for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x)
+    cs.asum[static_cast<size_t>(m) * cs.nsum + j] =
+        static_cast<int>(cnt[j] < static_cast<unsigned long long>(kAbsSumCap) ? cnt[j] : kAbsSumCap);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
@@ -195,6 +207,23 @@ __device__ __forceinline__ void for_vectors(const uint4* row, int nvec, const ui
   for (int idx = threadIdx.x + NC * blockDim.x; idx < nvec; idx += blockDim.x) f(__ldg(row + idx), idx);
 }
 
+// The same vectors, visited warp-uniformly: every lane calls f(u, idx, valid)
+// in every step of its warp (u is undefined where !valid), so f may use warp
+// collectives.  blockDim.x is a multiple of 32.
+template <int NC, typename F>
+__device__ __forceinline__ void for_vectors_warp(const uint4* row, int nvec, const uint4 (&cache)[NC], F&& f) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    f(cache[c], idx, idx < nvec);
+  }
+  for (int i0 = NC * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += blockDim.x) {
+    const int idx = i0 + (threadIdx.x & 31);
+    const bool valid = idx < nvec;
+    f(valid ? __ldg(row + idx) : make_uint4(0, 0, 0, 0), idx, valid);
+  }
+}
+
 template <int NC>
 __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&cache)[NC]) {
 #pragma unroll
@@ -208,10 +237,12 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
                                  uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16,
-                                 int* __restrict__ asum) {
+                                 const CodeSums sums) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[33];
+  __shared__ unsigned long long cnt[kMaxSums];
+  sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
   const int nvec = K >> 3;
@@ -229,15 +260,18 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
-  int sabs = 0;
-  for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
-    float x[8];
-    bf16x8_to_f32(u, x);
+  for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
+    int v = 0;
+    if (valid) {
+      float x[8];
+      bf16x8_to_f32(u, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
-    sabs = min(sabs + store8(out, out16, idx, x, scale, qt), kAbsSumCap);
+      for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
+      v = store8(out, out16, idx, x, scale, qt);
+    }
+    sums_add_warp(cnt, sums, idx, v);
   });
-  if (asum != nullptr) store_row_sum(sabs, asum, m);
+  sums_end(cnt, sums, m);
 }
 
 // ------------------------------------------------------------------ RMSNorm -> quant
@@ -245,10 +279,12 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
                                      float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16,
-                                     int* __restrict__ asum) {
+                                     const CodeSums sums) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[66];
+  __shared__ unsigned long long cnt[kMaxSums];
+  sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(gamma);
@@ -292,13 +328,16 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
-  int sabs = 0;
-  for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
-    float x[8];
-    normed(u, idx, x);
-    sabs = min(sabs + store8(out, out16, idx, x, scale, qt), kAbsSumCap);
+  for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
+    int v = 0;
+    if (valid) {
+      float x[8];
+      normed(u, idx, x);
+      v = store8(out, out16, idx, x, scale, qt);
+    }
+    sums_add_warp(cnt, sums, idx, v);
   });
-  if (asum != nullptr) store_row_sum(sabs, asum, m);
+  sums_end(cnt, sums, m);
 }
 
 // ------------------------------------------------------------------ SiLU * up -> quant
@@ -317,10 +356,12 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
 __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
                                       float* __restrict__ h_out, uint8_t* __restrict__ x16,
-                                      int* __restrict__ asum) {
+                                      const CodeSums sums) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ float red[33];
+  __shared__ unsigned long long cnt[kMaxSums];
+  sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
   const uint4* urow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu + I);
@@ -337,6 +378,20 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_
     }
     for (int idx = threadIdx.x + (kVPT / 2) * blockDim.x; idx < nvec; idx += blockDim.x)
       f(__ldg(grow + idx), __ldg(urow + idx), idx);
+  };
+  // the same pairs, warp-uniformly (see for_vectors_warp)
+  auto visit_warp = [&](auto&& f) {
+#pragma unroll
+    for (int c = 0; c < kVPT / 2; ++c) {
+      const int idx = threadIdx.x + c * blockDim.x;
+      f(cg[c], cu[c], idx, idx < nvec);
+    }
+    for (int i0 = (kVPT / 2) * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += blockDim.x) {
+      const int idx = i0 + (threadIdx.x & 31);
+      const bool valid = idx < nvec;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      f(valid ? __ldg(grow + idx) : z, valid ? __ldg(urow + idx) : z, idx, valid);
+    }
   };
   float amax = 0.0f;
   visit([&](const uint4 g, const uint4 u, int idx) {
@@ -355,15 +410,18 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_
   if (threadIdx.x == 0) sx[m] = scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * I;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
-  int sabs = 0;
-  visit([&](const uint4 g, const uint4 u, int idx) {
-    float h[8];
-    silu_mul8(g, u, h);
+  visit_warp([&](const uint4 g, const uint4 u, int idx, bool valid) {
+    int v = 0;
+    if (valid) {
+      float h[8];
+      silu_mul8(g, u, h);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
-    sabs = min(sabs + store8(out, out16, idx, h, scale, qt), kAbsSumCap);
+      for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
+      v = store8(out, out16, idx, h, scale, qt);
+    }
+    sums_add_warp(cnt, sums, idx, v);
   });
-  if (asum != nullptr) store_row_sum(sabs, asum, m);
+  sums_end(cnt, sums, m);
 }
 
 // ------------------------------------------------------------------ weight fold + quant
@@ -472,26 +530,29 @@ int row_threads(int nvec, int rows, int per = kVPT) {
 }  // namespace
 
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
-                             void* x16, int* asum, cudaStream_t st) {
+                             void* x16, CodeSums sums, cudaStream_t st) {
+  if (x16 == nullptr) sums.asum = nullptr;
   return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                    reinterpret_cast<uint8_t*>(x16), asum);
+                    reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
-                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, int* asum,
+                                 int qt, void* Xq, float* sx, float* ms_out, void* x16, CodeSums sums,
                                  cudaStream_t st) {
+  if (x16 == nullptr) sums.asum = nullptr;
   return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
-                    sx, ms_out, reinterpret_cast<uint8_t*>(x16), asum);
+                    sx, ms_out, reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, int* asum, cudaStream_t st) {
+                                  float* sx, float* h_out, void* x16, CodeSums sums, cudaStream_t st) {
+  if (x16 == nullptr) sums.asum = nullptr;
   // two vectors (gate, up) are cached per position: half as many per thread
   const int t = row_threads(I / 8, M, kVPT / 2);
   return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
-                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), asum);
+                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
