@@ -12,10 +12,10 @@
 //     takes its A operand from TMEM, so the widened weights never travel
 //     through shared memory;
 //   * one thread issues 16 tcgen05.mma kind::f16 [d], [a_tmem], b_desc (fp32
-//     accumulation) after a single barrier wait and frees the TMEM stage and
-//     the activation slot with a single commit.  The issuing thread's fixed
-//     cost per wait/commit is what bounds a 128-deep pipeline at decode sizes,
-//     hence the 256-deep stages.
+//     accumulation) once the activation slot and the TMEM stage are full, and
+//     frees both with a single commit.  The issuing thread's fixed cost per
+//     wait/commit is what bounds a 128-deep pipeline at decode sizes, hence
+//     the 256-deep stages.
 //
 // Exactness.  Every product is an integer of magnitude <= 128^2 and the MMA
 // accumulates in fp32, which is exact while every partial sum is an integer of
@@ -82,8 +82,8 @@ template <int WST, int NS>
 struct I8tBarriers {
   uint64_t wfull[WST];    // TMA -> converters: weight codes landed
   uint64_t wempty[WST];   // converters (128) -> weight producer: codes are in registers
-  uint64_t xfull[NS];     // TMA -> converters: fp16 activation codes landed
-  uint64_t afull[NS];     // converters (128) -> MMA: A stage in TMEM (and its activation slot landed)
+  uint64_t xfull[NS];     // TMA -> MMA: fp16 activation codes landed
+  uint64_t afull[NS];     // converters (128) -> MMA: A stage in TMEM
   uint64_t consumed[NS];  // MMA commit -> converters, activation producer: stage read
   uint64_t pfull[2];      // MMA commit -> epilogue: accumulator ready
   uint64_t pempty[2];     // epilogue (128) -> MMA: accumulator drained
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             d = tmem + b * C::ACC_COLS;
           }
-          if (!mbar_wait(&bars.afull[r.idx], r.phase, status)) {
+          if (!mbar_wait(&bars.xfull[r.idx], r.phase, status) || !mbar_wait(&bars.afull[r.idx], r.phase, status)) {
             ok = false;
             break;
           }
@@ -396,8 +396,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int j = 0; j < 16; ++j)  // 16-byte chunk j = k 16j .. 16j+15, swizzled within its box
           raw[j] = *reinterpret_cast<const uint4*>(wrow + (j >> 3) * C::W_BOX + (((j & 7) ^ (i & 7)) << 4));
         mbar_arrive(&bars.wempty[rw.idx]);
-        if (!warp_wait(&bars.xfull[ra.idx], ra.phase, status) ||
-            !warp_wait(&bars.consumed[ra.idx], ra.phase ^ 1u, status)) {
+        if (!warp_wait(&bars.consumed[ra.idx], ra.phase ^ 1u, status)) {
           ok = false;
           break;
         }
