@@ -92,6 +92,35 @@ def test_quant_act_strided_rows(qt):
     np.testing.assert_array_equal(f32(sx), so)
 
 
+def test_quant_act_int8_half_integer_quotients():
+    """INT8 codes round v / scale to the nearest integer, ties to even.  With
+    absmax 127 (scale exactly 1) or 190.5 at pre-scale 1.5 (scale exactly 1.5)
+    the quotients land exactly on half-integers, and one bf16 ulp either side of
+    them: the kernel's reciprocal shortcut must hand every such code to the
+    exact division."""
+    K = 256
+    row = np.zeros(K, np.float32)
+    row[0] = 127.0
+    halves = np.array([0.5, 1.5, 2.5, 3.5, 4.5, 10.5, 63.5, 64.5, 100.5, 126.5], np.float32)
+    row[1:11] = halves
+    row[11:21] = -halves
+    b = torch.from_numpy(halves).to(torch.bfloat16)
+    up = (b.view(torch.int16) + 1).view(torch.bfloat16).float().numpy()  # next bf16 above
+    dn = (b.view(torch.int16) - 1).view(torch.bfloat16).float().numpy()  # next bf16 below
+    row[21:31], row[31:41], row[41:51] = up, dn, -up
+    g = np.random.Generator(np.random.PCG64(3))
+    row[51:] = np.round(g.uniform(-126, 126, K - 51) * 2) / 2  # more halves and integers
+    X = torch.from_numpy(np.stack([row, row * np.float32(0.75)])).to(torch.bfloat16)
+    for pre in (1.0, 1.5):
+        Xq, sx = q.quant_act(X.cuda(), q.INT8, pre_scale=pre)
+        sync_ok()
+        qo, so = oracle.quant_act(bits(X), oracle.INT8, pre_scale=pre)
+        np.testing.assert_array_equal(codes(Xq), qo)
+        np.testing.assert_array_equal(f32(sx), so)
+    c = codes(Xq)[0].view(np.int8)
+    assert list(c[1:6]) == [0, 2, 2, 4, 4]  # 0.5 -> 0, 1.5 -> 2, 2.5 -> 2, 3.5 -> 4, 4.5 -> 4 (ties to even)
+
+
 @pytest.mark.parametrize("qt", QTS)
 @pytest.mark.parametrize("M,K", [(16, 256), (33, 3584), (7, 5120), (4, 70000)])
 def test_rmsnorm_quant(qt, M, K):

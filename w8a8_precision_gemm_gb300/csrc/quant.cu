@@ -113,23 +113,44 @@ __device__ __forceinline__ float row_scale(float amax, int qt) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, qt == kQInt8 ? 127.0f : 448.0f);
 }
 
-__device__ __forceinline__ uint8_t encode(float v, float scale, int qt) {
-  const float r = __fdiv_rn(v, scale);
-  if (qt == kQInt8) {
-    int q = __float2int_rn(r);
+// A row's quantization step: the scale and, for INT8, its reciprocal.
+struct Enc {
+  float scale;
+  float inv;
+  int qt;
+};
+
+__device__ __forceinline__ Enc make_enc(float amax, int qt) {
+  const float scale = row_scale(amax, qt);
+  return {scale, __frcp_rn(scale), qt};
+}
+
+// Code of v / scale.  INT8: the IEEE quotient fl(v / scale) rounded to the
+// nearest integer, ties to even, clamped to +-127.  For |v / scale| < 256 the
+// product r = v * fl(1 / scale) lies within 5e-5 of fl(v / scale) (three
+// roundings of relative size 2^-24 each), so wherever r is more than 1e-4 away
+// from a half-integer both round to the same integer and r is used; otherwise
+// (one code in ~5000, and NaN or out-of-range inputs) the quotient itself is
+// computed.  The codes are therefore those of the plain division.
+__device__ __forceinline__ uint8_t encode(float v, const Enc& e) {
+  if (e.qt == kQInt8) {
+    const float r = __fmul_rn(v, e.inv);
+    const float f = r - floorf(r);
+    const bool fast = fabsf(r) < 256.0f && fabsf(f - 0.5f) > 1e-4f;
+    int q = __float2int_rn(fast ? r : __fdiv_rn(v, e.scale));
     q = max(-127, min(127, q));
     return static_cast<uint8_t>(static_cast<int8_t>(q));
   }
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, e.scale), __NV_SATFINITE, __NV_E4M3));
 }
 
 // 8 values -> 8 code bytes packed in a uint2 (little-endian byte order = k order).
-__device__ __forceinline__ uint2 encode8(const float (&v)[8], float scale, int qt) {
+__device__ __forceinline__ uint2 encode8(const float (&v)[8], const Enc& en) {
   uint32_t lo = 0, hi = 0;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) lo |= static_cast<uint32_t>(encode(v[e], scale, qt)) << (8 * e);
+  for (int e = 0; e < 4; ++e) lo |= static_cast<uint32_t>(encode(v[e], en)) << (8 * e);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) hi |= static_cast<uint32_t>(encode(v[4 + e], scale, qt)) << (8 * e);
+  for (int e = 0; e < 4; ++e) hi |= static_cast<uint32_t>(encode(v[4 + e], en)) << (8 * e);
   return make_uint2(lo, hi);
 }
 
@@ -141,8 +162,8 @@ constexpr int kAbsSumCap = 1 << 24;
 // exact, integers of magnitude <= 127 -- for the tensor-core GEMM to read).
 // Returns the sum of |code| of the 8 INT8 codes when x16 is given, else 0.
 __device__ __forceinline__ int store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
-                                      const float (&v)[8], float scale, int qt) {
-  const uint2 c = encode8(v, scale, qt);
+                                      const float (&v)[8], const Enc& en) {
+  const uint2 c = encode8(v, en);
   reinterpret_cast<uint2*>(q)[idx] = c;
   if (x16 == nullptr) return 0;
   {
@@ -256,8 +277,8 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
     for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(x[e], pre)));
   });
   amax = block_reduce<true>(amax, red);
-  const float scale = row_scale(amax, qt);
-  if (threadIdx.x == 0) sx[m] = scale;
+  const Enc en = make_enc(amax, qt);
+  if (threadIdx.x == 0) sx[m] = en.scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
@@ -267,7 +288,7 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
       bf16x8_to_f32(u, x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
-      v = store8(out, out16, idx, x, scale, qt);
+      v = store8(out, out16, idx, x, en);
     }
     sums_add_warp(cnt, sums, idx, v);
   });
@@ -324,8 +345,8 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
     for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
   });
   amax = block_reduce<true>(amax, red);
-  const float scale = row_scale(amax, qt);
-  if (threadIdx.x == 0) sx[m] = scale;
+  const Enc en = make_enc(amax, qt);
+  if (threadIdx.x == 0) sx[m] = en.scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
@@ -333,7 +354,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
     if (valid) {
       float x[8];
       normed(u, idx, x);
-      v = store8(out, out16, idx, x, scale, qt);
+      v = store8(out, out16, idx, x, en);
     }
     sums_add_warp(cnt, sums, idx, v);
   });
@@ -369,34 +390,10 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_
   uint4 cg[kVPT / 2], cu[kVPT / 2];
   fill_cache(grow, nvec, cg);
   fill_cache(urow, nvec, cu);
-  // visit (gate, up) vector pairs: cached ones unrolled, the rest from memory
-  auto visit = [&](auto&& f) {
-#pragma unroll
-    for (int c = 0; c < kVPT / 2; ++c) {
-      const int idx = threadIdx.x + c * blockDim.x;
-      if (idx < nvec) f(cg[c], cu[c], idx);
-    }
-    for (int idx = threadIdx.x + (kVPT / 2) * blockDim.x; idx < nvec; idx += blockDim.x)
-      f(__ldg(grow + idx), __ldg(urow + idx), idx);
-  };
-  // the same pairs, warp-uniformly (see for_vectors_warp)
-  auto visit_warp = [&](auto&& f) {
-#pragma unroll
-    for (int c = 0; c < kVPT / 2; ++c) {
-      const int idx = threadIdx.x + c * blockDim.x;
-      f(cg[c], cu[c], idx, idx < nvec);
-    }
-    for (int i0 = (kVPT / 2) * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += blockDim.x) {
-      const int idx = i0 + (threadIdx.x & 31);
-      const bool valid = idx < nvec;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      f(valid ? __ldg(grow + idx) : z, valid ? __ldg(urow + idx) : z, idx, valid);
-    }
-  };
+  // pass 1: h = silu(g) * u, kept in registers for the cached positions
+  float hc[kVPT / 2][8];
   float amax = 0.0f;
-  visit([&](const uint4 g, const uint4 u, int idx) {
-    float h[8];
-    silu_mul8(g, u, h);
+  auto take = [&](const float (&h)[8], int idx) {
     if (h_out) {
       float4* ho = reinterpret_cast<float4*>(h_out + static_cast<size_t>(m) * I) + 2 * idx;
       ho[0] = make_float4(h[0], h[1], h[2], h[3]);
@@ -404,23 +401,46 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(h[e], pre)));
-  });
+  };
+#pragma unroll
+  for (int c = 0; c < kVPT / 2; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    if (idx < nvec) {
+      silu_mul8(cg[c], cu[c], hc[c]);
+      take(hc[c], idx);
+    }
+  }
+  for (int idx = threadIdx.x + (kVPT / 2) * blockDim.x; idx < nvec; idx += blockDim.x) {
+    float h[8];
+    silu_mul8(__ldg(grow + idx), __ldg(urow + idx), h);
+    take(h, idx);
+  }
   amax = block_reduce<true>(amax, red);
-  const float scale = row_scale(amax, qt);
-  if (threadIdx.x == 0) sx[m] = scale;
+  const Enc en = make_enc(amax, qt);
+  if (threadIdx.x == 0) sx[m] = en.scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * I;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
-  visit_warp([&](const uint4 g, const uint4 u, int idx, bool valid) {
+  // pass 2: codes (warp-uniform steps, see for_vectors_warp)
+  auto put = [&](float (&h)[8], int idx, bool valid) {
     int v = 0;
     if (valid) {
-      float h[8];
-      silu_mul8(g, u, h);
 #pragma unroll
       for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
-      v = store8(out, out16, idx, h, scale, qt);
+      v = store8(out, out16, idx, h, en);
     }
     sums_add_warp(cnt, sums, idx, v);
-  });
+  };
+#pragma unroll
+  for (int c = 0; c < kVPT / 2; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    put(hc[c], idx, idx < nvec);
+  }
+  for (int i0 = (kVPT / 2) * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += blockDim.x) {
+    const int idx = i0 + (threadIdx.x & 31);
+    float h[8] = {};
+    if (idx < nvec) silu_mul8(__ldg(grow + idx), __ldg(urow + idx), h);
+    put(h, idx, idx < nvec);
+  }
   sums_end(cnt, sums, m);
 }
 
@@ -457,8 +477,8 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
     for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fdiv_rn(w[e], s)));
   }
   amax = block_reduce<true>(amax, red);
-  const float scale = row_scale(amax, qt);
-  if (threadIdx.x == 0) sw[n] = scale;
+  const Enc en = make_enc(amax, qt);
+  if (threadIdx.x == 0) sw[n] = en.scale;
   // pass 2: codes; W' is written here, after the row has been read (each
   // thread rewrites only the vectors it has just read, so W_scaled may alias W)
   uint2* out = reinterpret_cast<uint2*>(Wq + static_cast<size_t>(n) * K);
@@ -472,7 +492,7 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
       o[0] = make_float4(w[0], w[1], w[2], w[3]);
       o[1] = make_float4(w[4], w[5], w[6], w[7]);
     }
-    out[idx] = encode8(w, scale, qt);
+    out[idx] = encode8(w, en);
   }
 }
 
