@@ -374,7 +374,10 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
   }
 }
 
-__global__ void __launch_bounds__(kRowThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
+// MINB = 2: two blocks per SM (at most 64 registers a thread) when there are
+// more rows than SMs, so a batch of up to two rows per SM runs as one wave.
+template <int MINB>
+__global__ void __launch_bounds__(kRowThreads, MINB) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ GU, int I, long long ldgu, float pre,
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
                                       float* __restrict__ h_out, uint8_t* __restrict__ x16,
                                       const CodeSums sums) {
@@ -571,8 +574,12 @@ cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, 
   if (x16 == nullptr) sums.asum = nullptr;
   // two vectors (gate, up) are cached per position: half as many per thread
   const int t = row_threads(I / 8, M, kVPT / 2);
-  return launch_pdl(silu_mul_quant_kernel, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I,
-                    ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), sums);
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  auto* kern = (sms > 0 && M > sms) ? silu_mul_quant_kernel<2> : silu_mul_quant_kernel<1>;
+  return launch_pdl(kern, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt,
+                    reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
