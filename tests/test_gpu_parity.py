@@ -303,6 +303,45 @@ def test_gemm_int8_single_pass_limit(extra):
     np.testing.assert_array_equal(acc.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("M", [8, 24, 48, 100, 128, 256])
+@pytest.mark.parametrize("K", [1040, 3600])
+@pytest.mark.parametrize("small", [True, False])
+def test_gemm_int8_decode_tiles(M, K, small):
+    """The decode kernel at every token-tile width (16 .. 128), K ragged against
+    the 256-deep stage (1040 = 4 stages + 16, 3600 = 14 stages + 16) and split
+    across CTAs, with small activation codes (one fp32 pass per split) and
+    uniform ones (1024-deep chunks)."""
+    N = 1160  # 9 channel tiles + 8 rows: few tiles, so K is split
+    g = np.random.Generator(np.random.PCG64(M * 131 + K + small))
+    lim = 10 if small else 127
+    xq = g.integers(-lim, lim + 1, size=(M, K)).astype(np.int8)
+    wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
+                     q.workspace(M, N, K, q.INT8))
+    sync_ok()
+    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT))
+
+
+@pytest.mark.parametrize("M", [16, 64, 256])
+@pytest.mark.parametrize("small", [True, False])
+def test_gemm_int8_decode_unsplit_long_k(M, small):
+    """A workspace with room for the fp16 codes and their sums but not for split
+    partials makes every unit run over all of K = 4352 (17 stages): uniform codes
+    take five 1024-deep chunks drained into the int32 running sum (the last one
+    ragged), small codes one fp32 pass."""
+    N, K = 392, 4352
+    g = np.random.Generator(np.random.PCG64(M + 7 * small))
+    lim = 10 if small else 127
+    xq = g.integers(-lim, lim + 1, size=(M, K)).astype(np.int8)
+    wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256
+    assert q.qurl_workspace_size(M, N, K, q.INT8) > act  # the full-size plan would split K
+    ws = torch.empty(act, dtype=torch.uint8, device="cuda")
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8, ws)
+    sync_ok()
+    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_i8(xq.view(np.uint8), wq.view(np.uint8), nthreads=NT))
+
+
 @pytest.mark.parametrize("M", [200, 256])
 def test_gemm_int8_mixed_token_tiles(M):
     """Two 128-token tiles: the first with small activation codes (one fp32 pass
