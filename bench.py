@@ -372,11 +372,30 @@ def run_ours(args):
         for B, L in zip(bufs, layers):
             chain(q, qt, L, B)
 
+    copy_stream = torch.cuda.Stream()
+
     def step_e2e():
-        for B, L in zip(bufs, layers):
-            B.x.copy_(X_host[B.M], non_blocking=True)
+        """Both batches' inputs go host -> device on a copy stream while the
+        first batch computes; each batch's output goes device -> host on the
+        copy stream as soon as its chain ends, overlapping the next chain."""
+        main = torch.cuda.current_stream()
+        copy_stream.wait_stream(main)
+        landed = []
+        with torch.cuda.stream(copy_stream):
+            for B in bufs:
+                B.x.copy_(X_host[B.M], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                landed.append(ev)
+        for B, L, ev in zip(bufs, layers, landed):
+            main.wait_event(ev)
             chain(q, qt, L, B)
-            Y_host[B.M].copy_(B.y["down"], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(main)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                Y_host[B.M].copy_(B.y["down"], non_blocking=True)
+        main.wait_stream(copy_stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
