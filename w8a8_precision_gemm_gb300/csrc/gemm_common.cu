@@ -5,22 +5,25 @@
 
 namespace qurl {
 
-// Decode (M <= 256): weights on the MMA M side, tokens padded to a power of two
-// >= 16 on the N side (<= 256 for FP8, <= 128 for INT8, whose TMEM holds two
-// partial buffers and an int32 running sum).  Prefill: 128-token tiles x 256
-// (FP8) or 128 (INT8) channels.  When the tiles do not fill the SMs, K is split
+// Decode (M <= 256, and INT8 at any M given the workspace): weights on the MMA
+// M side, tokens padded to a power of two >= 16 on the N side (<= 256 for FP8,
+// <= 128 for INT8, whose TMEM also holds the widened weights).  FP8 prefill and
+// INT8 prefill without workspace: 128-token tiles x 256 (FP8) or 128 (INT8)
+// channels.  When the tiles do not fill the SMs, K is split
 // so that tiles x splits is close to the SM count, each split at least 512
 // deep, as far as the workspace allows.  Workspace layout: [fp16 activation
 // codes and per-token sums of |code| (INT8 decode)][split-K partials].
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
-  p.swap = (M <= 256);
-  // INT8 decode prefers the TMEM-operand kernel, which needs an fp16 copy of
-  // the activation codes (2 M K bytes) in the workspace.
+  // INT8 prefers the TMEM-operand kernel (weights on the MMA M side at every
+  // M), which needs an fp16 copy of the activation codes (2 M K bytes) and
+  // their sums in the workspace; without it, INT8 widens both operands in
+  // shared memory.
   const size_t x16 = (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
   auto sums = [&](int s) { return (static_cast<size_t>(M) * 4 * s + 255) & ~static_cast<size_t>(255); };
-  p.tmem_a = int8 && p.swap && ws_avail >= x16 + sums(1);
+  p.tmem_a = int8 && ws_avail >= x16 + sums(1);
+  p.swap = p.tmem_a || M <= 256;
   p.bk = int8 ? (p.tmem_a ? 256 : 64) : 128;
   p.num_kb = (K + p.bk - 1) / p.bk;
   if (p.swap) {

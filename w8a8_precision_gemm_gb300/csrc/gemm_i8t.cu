@@ -87,9 +87,9 @@ struct I8tBarriers {
   uint64_t consumed[NS];  // MMA commit -> converters, activation producer: stage read
   uint64_t pfull[2];      // MMA commit -> epilogue: accumulator ready
   uint64_t pempty[2];     // epilogue (128) -> MMA: accumulator drained
-  uint64_t modes;         // mode warp -> MMA, epilogue: fast_bits written
   uint64_t done;          // MMA drain on the error path
   uint32_t fast_bits[kModeWords];  // bit j set: the CTA's j-th unit takes one pass over its k range
+  uint32_t mode_count;    // mode warp -> MMA, epilogue: bits of units < mode_count are written
   uint32_t tmem_base;
 };
 
@@ -105,6 +105,33 @@ struct Ring {
     }
   }
 };
+
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+// Bounded wait until *count > j (a counter another warp of the CTA raises).
+__device__ __forceinline__ bool wait_count(const uint32_t* count, uint32_t j, int* status) {
+  if (ld_acquire_cta(count) > j) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_cta(count) > j) return true;
+    if ((it & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(status) != kDevOk) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(status, kDevOk, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
 
 // Sum of |c| over 16 int8 codes (|-128| counts 128).
 __device__ __forceinline__ int abs_sum16(const uint4 v) {
@@ -148,7 +175,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&bars.pfull[b], 1);
       mbar_init(&bars.pempty[b], 128);
     }
-    mbar_init(&bars.modes, 1);
+    bars.mode_count = 0;
     mbar_init(&bars.done, 1);
     fence_barrier_init();
   }
@@ -167,10 +194,11 @@ __global__ void __launch_bounds__(512, 1)
   griddep_launch_dependents();
   if (warp != 0) griddep_wait();
 
-  // j: the unit's position in this CTA's list
+  // j: the unit's position in this CTA's list (call after wait_count(.., j, ..))
   auto is_fast = [&](int j) {
     return j < 32 * kModeWords && ((bars.fast_bits[j >> 5] >> (j & 31)) & 1u) != 0;
   };
+  constexpr int kModeUnits = 32 * kModeWords;
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer
@@ -215,12 +243,16 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(&bars.modes, 0, status);
+      bool ok = true;
       Ring<NS> r;
       int nb0 = 0, nb1 = 0;  // accumulator fills issued per buffer
       int next_fast = 0;
       for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
         const Unit w = unit_of<true, BN>(args, u);
+        if (j < kModeUnits && !wait_count(&bars.mode_count, j, status)) {
+          ok = false;
+          break;
+        }
         const bool fast = is_fast(j);
         int b = 0;
         uint32_t d = tmem;
@@ -291,10 +323,12 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ accumulation mode of each unit
+    // Published unit by unit (mode_count), so the MMA starts on the first
+    // unit while the modes of later ones are still being read.
     if (lane < kModeWords) bars.fast_bits[lane] = 0;
     __syncwarp();
     if (args.asum != nullptr) {
-      for (int u = R.u, j = 0; u < R.end && j < 32 * kModeWords; u += R.stride, ++j) {
+      for (int u = R.u, j = 0; u < R.end && j < kModeUnits; u += R.stride, ++j) {
         const int t = u % args.tiles_tok;
         const int sp = u / (args.tiles_tok * args.tiles_ch);
         int mx = 0;
@@ -303,11 +337,14 @@ __global__ void __launch_bounds__(512, 1)
           if (m < args.M) mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        if (lane == 0 && mx <= kFastSumMax) bars.fast_bits[j >> 5] |= 1u << (j & 31);
+        if (lane == 0) {
+          if (mx <= kFastSumMax) bars.fast_bits[j >> 5] |= 1u << (j & 31);
+          st_release_cta(&bars.mode_count, static_cast<uint32_t>(j + 1));
+        }
+        __syncwarp();
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars.modes);
+    if (lane == 0) st_release_cta(&bars.mode_count, 0xFFFFFFFFu);  // all published (the rest: chunks)
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ epilogue
@@ -316,11 +353,15 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t tR = lane_base + C::ACC_COLS;  // running sum of a chunked unit
     const int emode = args.mode;
-    bool ok = warp_wait(&bars.modes, 0, status);
+    bool ok = true;
     int nb0 = 0, nb1 = 0;
     int next_fast = 0;
     for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
       const Unit w = unit_of<true, BN>(args, u);
+      if (j < kModeUnits && !__all_sync(0xFFFFFFFFu, wait_count(&bars.mode_count, j, status))) {
+        ok = false;
+        break;
+      }
       const bool fast = is_fast(j);
       const int npass = fast ? 1 : (w.nkb + C::CHUNK - 1) / C::CHUNK;
       // scales of this lane's channel and of its token in the first 32-token
@@ -395,11 +436,11 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j)  // 16-byte chunk j = k 16j .. 16j+15, swizzled within its box
           raw[j] = *reinterpret_cast<const uint4*>(wrow + (j >> 3) * C::W_BOX + (((j & 7) ^ (i & 7)) << 4));
-        mbar_arrive(&bars.wempty[rw.idx]);
         if (!warp_wait(&bars.consumed[ra.idx], ra.phase ^ 1u, status)) {
           ok = false;
           break;
         }
+        tc_fence_after();  // the stores below come after the MMAs that read this stage
         const uint32_t a_t = lane_base + C::A_BASE + ra.idx * C::A_COLS;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -413,6 +454,9 @@ __global__ void __launch_bounds__(512, 1)
           }
           tmem_st32(a_t + h * 32, v);
         }
+        // the weight slot is released only once every code read from it has
+        // been used (widened into the stores above)
+        mbar_arrive(&bars.wempty[rw.idx]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.afull[ra.idx]);
