@@ -7,10 +7,10 @@
 //     widened to fp16 (BN rows x 512 B as four swizzled boxes) into a second
 //     ring -- the fp16 copy is made once per call, not once per CTA;
 //   * converter warps (one thread per weight row = TMEM lane) read the row's
-//     256 codes into registers, free the weight slot at once, widen the codes
-//     to fp16 (exact) and store them into a TMEM stage with tcgen05.st: the MMA
-//     takes its A operand from TMEM, so the widened weights never travel
-//     through shared memory;
+//     256 codes into registers, widen them to fp16 (exact) and store them into
+//     a TMEM stage with tcgen05.st, then free the weight slot: the MMA takes
+//     its A operand from TMEM, so the widened weights never travel through
+//     shared memory;
 //   * one thread issues 16 tcgen05.mma kind::f16 [d], [a_tmem], b_desc (fp32
 //     accumulation) once the activation slot and the TMEM stage are full, and
 //     frees both with a single commit.  The issuing thread's fixed cost per
