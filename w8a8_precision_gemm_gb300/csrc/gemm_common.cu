@@ -39,14 +39,39 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     p.tiles_ch = (N + p.bn - 1) / p.bn;
   }
   const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
+  const int min_kb = (p.bk == 64) ? 8 : (p.bk == 256 ? 2 : 4);
+  const int cap = std::max(1, std::min(p.num_kb / min_kb, p.tmem_a ? kMaxSums : 1 << 20));
   int splits = 1;
-  if (num_sms > 0 && tiles < num_sms) {
-    const int min_kb = (p.bk == 64) ? 8 : (p.bk == 256 ? 2 : 4);
-    const int want = static_cast<int>(num_sms / tiles);
-    const int cap = std::max(1, p.num_kb / min_kb);
-    splits = std::max(1, std::min(want, cap));
+  if (num_sms > 0 && tiles < num_sms) splits = std::max(1, std::min(static_cast<int>(num_sms / tiles), cap));
+  if (num_sms > 0) {
+    // Rough time of s splits: rounds of units over the SMs x (k-blocks per
+    // unit + a fixed pipeline fill and drain), plus the reduction kernel
+    // (launch, reading s partials, writing the output).  A split count is
+    // taken over the rule above only when it is predicted 10% faster: this
+    // fixes shapes whose tiles leave a wave mostly empty (e.g. 320 tiles on
+    // 152 SMs), and leaves the rest alone.
+    const double stage_us = p.tmem_a ? (p.bn >= 128 ? 0.95 : 0.8) : (p.swap ? 0.36 : 0.45);
+    const double fill = p.tmem_a ? 3.0 : 5.0;
+    auto est = [&](int s) {
+      const int kps = (p.num_kb + s - 1) / s;
+      const int ns = (p.num_kb + kps - 1) / kps;
+      const double rounds = static_cast<double>((tiles * ns + num_sms - 1) / num_sms);
+      double t = rounds * (kps + fill) * stage_us;
+      if (ns > 1) t += 3.0 + (static_cast<double>(ns) * M * N * 4 + static_cast<double>(M) * N * 2) / 4e6;
+      return t;
+    };
+    const double t_rule = est(splits);
+    int best = splits;
+    double t_best = t_rule;
+    for (int s = 1; s <= std::min(cap, 64); ++s) {
+      const double t = est(s);
+      if (t < t_best) {
+        t_best = t;
+        best = s;
+      }
+    }
+    if (t_best < 0.9 * t_rule) splits = best;
   }
-  if (p.tmem_a) splits = std::min(splits, kMaxSums);  // one code sum per split and token
   const size_t per_split = static_cast<size_t>(M) * N * 4;
   // workspace for s splits: [fp16 codes, code sums (INT8 decode)][s partials if s > 1]
   auto need = [&](int s) {
