@@ -60,6 +60,8 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# prefill shapes timed beside the decode step (tensor-bound; 7B and 32B layer classes)
+PREFILL = [("7b", "gate_up", 4096), ("32b", "down", 1024)]
 DOMINANT_PROFILE = {"int8": "profiles/w8a8_gemm_i8t_kernel_7b_gate_up_m256_int8.md"}
 KERNEL_SOURCES = ["w8a8_precision_gemm_gb300/csrc/gemm.cuh", "w8a8_precision_gemm_gb300/csrc/gemm_i8t.cu",
                   "w8a8_precision_gemm_gb300/csrc/ptx.cuh", "w8a8_precision_gemm_gb300/csrc/internal.h"]
@@ -473,6 +475,32 @@ def run_ours(args):
             g, _ = graph_of(calls, q)
             g.replay()
             per_quant[f"{cname}/M{M}"] = {"us": time_graph(g, 4, stream) / R * 1e3}
+    # ---- prefill shapes of the same layer classes (context beside the decode step)
+    prefill = {}
+    R2 = 4
+    for model, pname, M in PREFILL:
+        K, N = (synth.SHAPES_7B if model == "7b" else synth.SHAPES_32B)[pname]
+        Wm = synth.weights(f"bench/prefill/{model}/{pname}/W", N, K).cuda()
+        Wq, sw, _, _ = q.prepare_weights(Wm, qt, s=S_UAQ, keep_scaled=False)
+        del Wm
+        Xq, sx = q.quant_act(synth.activations(f"bench/prefill/{model}/{pname}/X", M, K).cuda(), qt)
+        wsp = q.workspace(M, N, K, qt)
+        Yp = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+        def pcalls(Xq=Xq, sx=sx, Wq=Wq, sw=sw, wsp=wsp, Yp=Yp):
+            for _ in range(R2):
+                q.qurl_w8a8_linear(Xq, sx, Wq, sw, qt, Yp, wsp)
+
+        g, nl = graph_of(pcalls, q)
+        g.replay()
+        us = time_graph(g, 3, stream) / R2 * 1e3
+        ops_p = 2 * M * N * K
+        nb = alg_bytes(M, K, N)
+        t_roof = max(ops_p / (pk["bf16_tflops"] * (2 if qt == q.FP8_E4M3 else 1) * 1e12), nb / (pk["hbm_gbs"] * 1e9))
+        prefill[f"{model}_{pname}_M{M}"] = {"M": M, "K": K, "N": N, "us": us, "TOPS": ops_p / (us * 1e-6) / 1e12,
+                                            "roofline_frac": t_roof / (us * 1e-6), "launches": nl // R2}
+        del g, Wq, sw, Xq, sx, wsp, Yp
+        torch.cuda.empty_cache()
     q.qurl_check_device_status()
 
     ops = step_ops()
@@ -493,7 +521,8 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(args.qtype)
     roof["traffic_source"] = DOMINANT_PROFILE.get(args.qtype) if roof["traffic"] is not None else None
-    roof["kernel"] = f"w8a8_gemm_kernel {dname} M={dM} K={dK} N={dN} ({args.qtype})"
+    kname = "w8a8_gemm_i8t_kernel" if qt == q.INT8 else "w8a8_gemm_kernel"
+    roof["kernel"] = f"{kname} {dname} M={dM} K={dK} N={dN} ({args.qtype})"
     roof["peak_source"] = (f"{pk['source']} " + ("bf16 burst (INT8 runs on the fp16 tensor pipe, same dense rate)"
                                                 if qt == q.INT8 else "bf16 burst x 2 (nominal fp8:bf16 ratio)")
                            if roof["bound"] == "tensor" else f"{pk['source']} HBM copy")
@@ -513,7 +542,7 @@ def run_ours(args):
             "gpu_launches": launches_step * args.steps,
             "launches_per_step": launches_step,
             "clocks": clocks.summary(),
-            "per_gemm": per, "per_quant": per_quant}
+            "per_gemm": per, "per_quant": per_quant, "prefill": prefill}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -562,6 +562,8 @@ FULL = [
     ("7b", "gate_up", 256, q.FP8_E4M3), ("7b", "down", 64, q.FP8_E4M3), ("7b", "qkv", 4096, q.FP8_E4M3),
     ("32b", "gate_up", 1024, q.INT8), ("32b", "down", 256, q.FP8_E4M3), ("32b", "o_proj", 8192, q.FP8_E4M3),
     ("32b", "qkv", 8192, q.INT8),
+    # shapes whose K is split to fill the last wave (320 and 160 tiles on 152 SMs; 80 tiles)
+    ("32b", "down", 1024, q.INT8), ("32b", "down", 1024, q.FP8_E4M3), ("32b", "down", 256, q.INT8),
 ]
 
 
