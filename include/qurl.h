@@ -134,10 +134,11 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
 /*
  * Bytes of workspace the linear entry points (qurl_w8a8_linear,
  * qurl_w8a8_gemm_acc and the fused *_linear entries) use for this shape at
- * full speed: split-K partial sums and, for INT8 with M <= 256, an fp16 copy
- * of the activation codes.  A smaller workspace (or none) is accepted: the
- * kernels then split K into fewer parts and INT8 widens the codes in shared
- * memory instead (slower, same result).
+ * full speed: split-K partial sums and, for INT8, an fp16 copy of the
+ * activation codes (2 M K bytes) with per-token sums of |code| over each K
+ * split.  A smaller workspace (or none) is accepted: the kernels then split K
+ * into fewer parts and INT8, without room for the fp16 copy, widens both
+ * operands in shared memory instead (slower, same result).
  */
 size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
 
@@ -147,10 +148,12 @@ size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
  *   Y[m,n]   = bf16_RNE( (fp32(acc) * sx[m]) * sw[n] )
  * Xq [M, K], Wq [N, K] codes; sx [M], sw [N] fp32; Y [M, N] bf16, row stride
  * ldy.  workspace: device scratch of ws_bytes (may be NULL / 0).
- * INT8 runs on the fp16 tensor path: the codes are widened to fp16 (exact),
- * each 1024-deep chunk of k is accumulated in fp32 (exact: every partial sum
- * is an integer below 1024 * 127^2 < 2^24) and the chunks are added in int32,
- * so the int32 accumulator and the bf16 Y are exact.
+ * INT8 runs on the fp16 tensor path: the codes are widened to fp16 (exact)
+ * and accumulated in fp32, which is exact while every partial sum is an
+ * integer of magnitude <= 2^24: a token tile whose tokens have sum |x| <=
+ * 2^24 / 128 over the k range is accumulated in one pass, any other in
+ * 1024-deep chunks (1024 * 128^2 = 2^24) added in int32.  The int32
+ * accumulator and the bf16 Y are therefore exact for any codes.
  */
 qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N,
                              int K, qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
