@@ -17,9 +17,9 @@
 // INT8: this toolchain has no tcgen05 kind::i8 for sm_103a, so the int8 codes
 // are widened to fp16 (every integer of magnitude <= 2048 is exact in fp16)
 // and multiplied with kind::f16 into fp32 TMEM accumulators.  Each product is
-// an integer of magnitude <= 127^2 and every partial sum over a chunk of 1024
-// k stays below 1024 * 127^2 = 16,516,096 < 2^24, so the fp32 accumulation
-// of one chunk is exact; the epilogue warps drain each chunk from TMEM,
+// an integer of magnitude <= 128^2 and every partial sum over a chunk of 1024
+// k stays within 1024 * 128^2 = 2^24, so the fp32 accumulation of one chunk
+// is exact; the epilogue warps drain each chunk from TMEM,
 // convert it to int32 and add it to an int32 running sum that also lives in
 // TMEM.  Two TMEM partial buffers let the MMA fill one chunk while the other
 // is drained.  The int32 result is therefore exact.
@@ -27,7 +27,8 @@
 // Orientation: with SWAP the weight tile is the MMA's M side (128 output
 // channels per CTA) and the tokens are its N side (BN <= 256) -- the layout for
 // small-M decode, where every weight byte is read once.  Without SWAP the
-// tokens are the M side (prefill).
+// tokens are the M side (FP8 prefill; INT8 prefill without a workspace -- with
+// one, INT8 at every M runs the TMEM-operand kernel of gemm_i8t.cu).
 #pragma once
 
 #include <cuda_bf16.h>
