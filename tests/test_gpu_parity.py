@@ -363,6 +363,26 @@ def test_gemm_int8_prefill_repeatable():
     np.testing.assert_array_equal(runs[0].cpu().numpy()[np.ix_(rows, cols)], ref)
 
 
+def test_gemm_int8_more_units_than_mode_slots():
+    """160 x 124 tiles: every CTA walks 131 units, beyond the 128 whose
+    accumulation mode the kernel records, so the last ones take the chunked
+    path without a recorded mode."""
+    M, N, K = 128 * 160, 128 * 124, 512
+    g = np.random.Generator(np.random.PCG64(23))
+    xq = g.integers(-20, 21, size=(M, K)).astype(np.int8)
+    wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
+                     q.workspace(M, N, K, q.INT8))
+    sync_ok()
+    rows = np.sort(g.choice(M, size=96, replace=False))
+    rows[-1] = M - 1  # a token of the last tile (the last units of their CTAs)
+    cols = np.sort(g.choice(N, size=128, replace=False))
+    ref = oracle.gemm_i8(xq[rows].view(np.uint8), wq[cols].view(np.uint8), nthreads=NT)
+    got = acc[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    del acc
+    np.testing.assert_array_equal(got, ref)
+
+
 @pytest.mark.parametrize("M", [200, 256])
 def test_gemm_int8_mixed_token_tiles(M):
     """Two 128-token tiles: the first with small activation codes (one fp32 pass
