@@ -422,6 +422,46 @@ def test_gemm_acc_fp8(M, N, K):
     assert float((err / (absref + 1e-30)).max()) < 1e-4
 
 
+def _random_shapes(n, seed):
+    """Seeded shapes across the decode and prefill ranges: any M and N, K a
+    multiple of 16 (the row-stride rule of the codes), some with code
+    magnitudes that force chunked INT8 accumulation."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for _ in range(n):
+        M = int(g.choice([g.integers(1, 65), g.integers(65, 300), g.integers(300, 1200)]))
+        N = int(g.choice([g.integers(1, 200), g.integers(200, 3000)]))
+        K = 16 * int(g.integers(1, 400))
+        out.append((M, N, K, bool(g.integers(0, 2)), bool(g.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,with_ws,big", _random_shapes(24, 2026))
+@pytest.mark.parametrize("qt", QTS)
+def test_gemm_random_shapes(qt, M, N, K, with_ws, big):
+    """Accumulators of seeded random shapes, with the full workspace (split K,
+    INT8 through the TMEM-operand kernel) or none (INT8 widened in shared
+    memory): INT8 exact, FP8 within the fp32 accumulation bound."""
+    g = np.random.Generator(np.random.PCG64(M * 1009 + N * 31 + K))
+    if qt == q.INT8:
+        lim = 127 if big else 12
+        xq = g.integers(-lim, lim + 1, size=(M, K)).astype(np.int8).view(np.uint8)
+        wq = g.integers(-127, 128, size=(N, K)).astype(np.int8).view(np.uint8)
+    else:
+        xq = random_codes(qt, (M, K), M * 7 + K + 1)
+        wq = random_codes(qt, (N, K), N * 13 + K + 1)
+    ws = q.workspace(M, N, K, qt) if with_ws else None
+    acc = q.gemm_acc(to_dev(xq, qt), to_dev(wq, qt), qt, ws)
+    sync_ok()
+    if qt == q.INT8:
+        np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_i8(xq, wq, nthreads=NT))
+    else:
+        ref = oracle.gemm_fp8(xq, wq, nthreads=NT)
+        absref = oracle.gemm_fp8(xq & np.uint8(0x7F), wq & np.uint8(0x7F), nthreads=NT)
+        err = np.abs(acc.cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= absref * (K * 2.0 ** -23) + 1e-30)
+
+
 def _layer(qt, M, N, K, tag, s=1.0):
     """Oracle-quantized inputs of one projection (oracle computes every input)."""
     X = synth.activations(f"{tag}/X", M, K)
