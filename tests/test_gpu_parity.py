@@ -612,6 +612,27 @@ def test_split_k_reduction(qt):
             assert max_abs_rel(oracle.bf16_decode(bits(Y)), oracle.bf16_decode(Yo)) <= 1e-2
 
 
+def test_split_workspace_reused_across_calls():
+    """One workspace serves consecutive split-K calls of different shapes and
+    kinds (linear, raw accumulators): nothing a call leaves behind -- fp16
+    codes, code sums, partials of another shape -- changes the next result."""
+    M, K = 64, 3584
+    ws = q.workspace(M, 4608, K, q.INT8)
+    for N, tag in ((4608, "a"), (3584, "b"), (4608, "a")):
+        assert q.qurl_workspace_size(M, N, K, q.INT8) <= ws.numel()
+        Xq, sx, Wq, sw = _layer(q.INT8, M, N, K, f"gpu/splitreuse/{tag}")
+        args = (to_dev(Xq, q.INT8), torch.from_numpy(sx).cuda(), to_dev(Wq, q.INT8), torch.from_numpy(sw).cuda(),
+                q.INT8)
+        Y1 = q.linear(*args, ws)
+        acc = q.gemm_acc(args[0], args[2], q.INT8, ws)
+        Y2 = q.linear(*args, ws)
+        sync_ok()
+        Yo, acco = oracle.w8a8_linear(Xq, sx, Wq, sw, oracle.INT8, nthreads=NT)
+        np.testing.assert_array_equal(bits(Y1), Yo)
+        np.testing.assert_array_equal(bits(Y2), Yo)
+        np.testing.assert_array_equal(acc.cpu().numpy(), acco)
+
+
 # ------------------------------------------------------------------ full-size projections (sampled)
 
 FULL = [
