@@ -258,7 +258,7 @@ __device__ __forceinline__ void emit32_swap(const GemmArgs& a, int mode, int a0,
     for (int h = 0; h < 4; ++h) {
       const float y0 = __fmul_rn(__fmul_rn(acc_to_float<T>(x[(2 * h) * 4 + t]), sxm), swv[2 * h]);
       const float y1 = __fmul_rn(__fmul_rn(acc_to_float<T>(x[(2 * h + 1) * 4 + t]), sxm), swv[2 * h + 1]);
-      __nv_bfloat162 p = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+      __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);  // one paired RNE conversion
       packed[h] = *reinterpret_cast<uint32_t*>(&p);
     }
     __nv_bfloat16* dst = a.Y + static_cast<size_t>(m) * a.ldy + n0;
@@ -321,7 +321,7 @@ __device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int 
       for (int j = 0; j < 32; j += 2) {
         const float y0 = __fmul_rn(__fmul_rn(static_cast<float>(v[j]), sxm), __ldg(a.sw + b0 + c0 + j));
         const float y1 = __fmul_rn(__fmul_rn(static_cast<float>(v[j + 1]), sxm), __ldg(a.sw + b0 + c0 + j + 1));
-        __nv_bfloat162 p = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+        __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);  // one paired RNE conversion
         packed[j / 2] = *reinterpret_cast<uint32_t*>(&p);
       }
 #pragma unroll

@@ -383,6 +383,17 @@ __global__ void __launch_bounds__(512, 1)
           const float sx_next = (last && c0 + 32 < BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
           uint32_t p[32];
           tmem_ld32(lane_base + b * C::ACC_COLS + c0, p);
+          if (c == 0 && last && emode == kModeBf16) {
+            // a single pass: the fp32 accumulator already holds the exact
+            // integer, so it is scaled as it is (no int32 round trip, whose
+            // two conversions per element bound this epilogue)
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(p[j]);
+            emit32_swap<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, f, sx_lane, sw_lane);
+            sx_lane = sx_next;
+            continue;
+          }
           int v[32];
           if (c > 0) {
             uint32_t rs[32];
