@@ -216,7 +216,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
     const long long a_rows = p.swap ? N : M;
     const long long b_rows = p.swap ? M : N;
     QURL_TRY(byte_map(p.swap ? Wq : Xq, a_rows, K, K, p.bk, 128, !int8, &ta));
-    QURL_TRY(byte_map(p.swap ? Xq : Wq, b_rows, K, K, p.bk, p.bn, !int8, &tb));
+    QURL_TRY(byte_map(p.swap ? Xq : Wq, b_rows, K, K, p.bk, p.pair ? p.bn / 2 : p.bn, !int8, &tb));
   }
   qurl::GemmArgs a{};
   a.M = M;
@@ -238,6 +238,8 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
   if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
+  else if (p.pair)
+    QURL_CUDA(qurl::launch_gemm_fp8_pair(ta, tb, a, grid, st));
   else
     QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
                    : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));

@@ -35,15 +35,19 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     p.tiles_ch = (N + 127) / 128;
   } else {
     p.bn = int8 ? 128 : 256;
-    p.tiles_tok = (M + 127) / 128;
+    // FP8 prefill runs on CTA pairs: 256 tokens x 256 channels per pair
+    p.pair = !int8;
+    p.tiles_tok = (M + (p.pair ? 255 : 127)) / (p.pair ? 256 : 128);
     p.tiles_ch = (N + p.bn - 1) / p.bn;
   }
   const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
+  // units run one per SM, or one per SM pair
+  const int slots = p.pair ? num_sms / 2 : num_sms;
   const int min_kb = (p.bk == 64) ? 8 : (p.bk == 256 ? 2 : 4);
   const int cap = std::max(1, std::min(p.num_kb / min_kb, p.tmem_a ? kMaxSums : 1 << 20));
   int splits = 1;
-  if (num_sms > 0 && tiles < num_sms) splits = std::max(1, std::min(static_cast<int>(num_sms / tiles), cap));
-  if (num_sms > 0) {
+  if (slots > 0 && tiles < slots) splits = std::max(1, std::min(static_cast<int>(slots / tiles), cap));
+  if (slots > 0) {
     // Rough time of s splits: rounds of units over the SMs x (k-blocks per
     // unit + a fixed pipeline fill and drain), plus the reduction kernel
     // (launch, reading s partials, writing the output).  A split count is
@@ -55,7 +59,7 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     auto est = [&](int s) {
       const int kps = (p.num_kb + s - 1) / s;
       const int ns = (p.num_kb + kps - 1) / kps;
-      const double rounds = static_cast<double>((tiles * ns + num_sms - 1) / num_sms);
+      const double rounds = static_cast<double>((tiles * ns + slots - 1) / slots);
       double t = rounds * (kps + fill) * stage_us;
       if (ns > 1) t += 3.0 + (static_cast<double>(ns) * M * N * 4 + static_cast<double>(M) * N * 2) / 4e6;
       return t;

@@ -80,6 +80,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// launch_pdl for a kernel whose CTAs work in clusters of two (grid.x even).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // quant.cu.  x16 (may be null): also write the INT8 codes as fp16 [M, K]
 // (the operand the INT8 decode GEMM reads), saving it a widening pass, and,
 // when sums.asum is not null, the code sums the GEMM reads with it.
@@ -100,6 +122,8 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
 struct GemmPlan {
   bool swap;         // weights on the MMA M side (decode)
   bool tmem_a;       // INT8 decode: weights widened into TMEM, fp16 activation copy in the workspace
+  bool pair;         // FP8 prefill on CTA pairs: token tiles of 256 (grid.x), channel tiles of 256,
+                     // B staged 128 channel rows per CTA
   size_t x16_bytes;  // bytes at the start of the workspace for that fp16 copy and, after it
                      // (at asum_off), the per-token sums of |code| (256-aligned pieces)
   size_t asum_off;
@@ -125,6 +149,9 @@ cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUte
                             dim3 grid, cudaStream_t st);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                            dim3 grid, cudaStream_t st);
+// gemm_fp8p.cu: FP8 prefill on CTA pairs (grid = pair token tiles, channel tiles, K splits).
+cudaError_t launch_gemm_fp8_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, dim3 grid,
+                                 cudaStream_t st);
 // gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
