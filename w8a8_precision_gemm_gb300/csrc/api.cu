@@ -239,7 +239,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
   else if (p.pair)
-    QURL_CUDA(qurl::launch_gemm_fp8_pair(ta, tb, a, grid, st));
+    QURL_CUDA(qurl::launch_gemm_fp8_pair(p.swap, p.bn, ta, tb, a, grid, st));
   else
     QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
                    : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));

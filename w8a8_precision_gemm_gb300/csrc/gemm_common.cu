@@ -31,8 +31,14 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
     int bn = 16;
     while (bn < M && bn < max_bn) bn *= 2;
     p.bn = bn;
+    // FP8 decode runs on CTA pairs (256 channels per pair) when it has 128 or
+    // more tokens and enough work: at least 1024 k-blocks of pair tiles (7B
+    // gate_up and down at M = 256; measured slower on the small qkv / o_proj,
+    // where half as many tiles need more K splits)
     p.tiles_tok = (M + bn - 1) / bn;
-    p.tiles_ch = (N + 127) / 128;
+    p.pair = !int8 && bn >= 128 &&
+             static_cast<long long>(p.tiles_tok) * ((N + 255) / 256) * ((K + p.bk - 1) / p.bk) >= 1024;
+    p.tiles_ch = p.pair ? (N + 255) / 256 : (N + 127) / 128;
   } else {
     p.bn = int8 ? 128 : 256;
     // FP8 prefill runs on CTA pairs: 256 tokens x 256 channels per pair

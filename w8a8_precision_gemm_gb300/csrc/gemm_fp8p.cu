@@ -1,13 +1,15 @@
-// gemm_fp8p.cu -- the FP8-E4M3 W8A8 GEMM for prefill on CTA pairs.
+// gemm_fp8p.cu -- the FP8-E4M3 W8A8 GEMM on CTA pairs.
 //
 // The two CTAs of a cluster share every MMA (tcgen05.mma.cta_group::2
-// kind::f8f6f4, M = 256 tokens, N = 256 channels, K = 32): each CTA stages
-// 128 token rows (A) and 128 channel rows (B) of a k-block, the pair's MMA
-// reads both CTAs' tiles, and each CTA's TMEM receives its 128 token rows x
-// 256 channels of the accumulator.  Per k-block an SM therefore takes in
-// 32 KB for 128 x 256 x 128 multiply-adds instead of 48 KB (128 token rows +
-// 256 channel rows on one SM): the operand bytes a CTA keeps in flight over
-// the load latency are what bounds the single-CTA kernel.
+// kind::f8f6f4, M = 256, N = BN, K = 32): each CTA stages 128 rows of the A
+// operand and BN / 2 rows of the B operand of a k-block, the pair's MMA reads
+// both CTAs' tiles, and each CTA's TMEM receives its 128 A rows x BN columns
+// of the accumulator.  Prefill: A = 128 token rows, B = 256 channels (per
+// k-block an SM takes in 32 KB for 128 x 256 x 128 multiply-adds instead of
+// 48 KB).  Decode (SWAP): A = 128 weight rows, B = the BN tokens (the weight
+// stream per SM is unchanged, the token bytes halve, and more weight stages
+// fit in shared memory).  The operand bytes a CTA keeps in flight over the
+// load latency are what bounds the single-CTA kernels.
 //
 // Synchronisation without thread-level traffic between the CTAs on the
 // k-block path: both CTAs' TMA loads complete on rank 0's "full" barrier
@@ -20,22 +22,24 @@
 
 namespace qurl {
 
-template <int STAGES>
+template <int BN_, int STAGES>
 struct Fp8PairCfg {
-  static constexpr int BM = 128;             // token rows per CTA (MMA M = 256 per pair)
-  static constexpr int BN = 256;             // channels per pair MMA
-  static constexpr int BNH = 128;            // channel rows this CTA stages
+  static constexpr int BM = 128;             // A rows per CTA (MMA M = 256 per pair)
+  static constexpr int BN = BN_;             // MMA N (B rows of the pair)
+  static constexpr int BNH = BN / 2;         // B rows this CTA stages
   static constexpr int BK = 128;             // k (bytes of e4m3 codes) per k-block
   static constexpr int A_STAGE = BM * BK;    // 16 KB
-  static constexpr int B_STAGE = BNH * BK;   // 16 KB
+  static constexpr int B_STAGE = BNH * BK;
   static constexpr int PAIR_TX = 2 * (A_STAGE + B_STAGE);  // bytes rank 0's barrier counts per stage
   static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024;
   static constexpr int NUM_THREADS = 192;    // producer, MMA, 4 epilogue warps
-  static constexpr int TMEM_COLS = 512;      // two 256-column fp32 accumulators
+  static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN;  // two BN-column fp32 accumulators
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_KB = BK / MMA_K_BYTES;
   static constexpr uint32_t IDESC = umma_idesc_f32acc(0, 0, 2 * BM, BN);  // e4m3 x e4m3 -> f32
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "pair MMA N");
+  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation: a power of two");
 };
 
 template <int STAGES>
@@ -48,32 +52,34 @@ struct Fp8PairBarriers {
   uint32_t tmem_base;
 };
 
-// This CTA's part of unit u: token rows a0 .. a0 + 127 (rank r takes the
-// r-th half of the pair's 256), channels b0 .. b0 + 255 of the output, and
-// channel rows b0 + 128 r .. of B to stage.
+// This CTA's part of unit u: A rows a0 .. a0 + 127 (rank r takes the r-th
+// half of the pair's 256), B columns b0 .. b0 + BN - 1 of the output, of which
+// it stages rows b0 + r BN / 2 ...  Prefill: A = tokens, B = channels;
+// SWAP: A = channels, B = tokens.  Units are numbered token tile fastest.
 struct PairUnit {
   int a0, b0, kb0, nkb, split;
 };
 
+template <bool SWAP, int BN>
 __device__ __forceinline__ PairUnit pair_unit(const GemmArgs& a, int u, uint32_t rank) {
   const int tok = u % a.tiles_tok;
   const int rest = u / a.tiles_tok;
   const int ch = rest % a.tiles_ch;
   const int sp = rest / a.tiles_ch;
   PairUnit w;
-  w.a0 = tok * 256 + static_cast<int>(rank) * 128;
-  w.b0 = ch * 256;
+  w.a0 = (SWAP ? ch : tok) * 256 + static_cast<int>(rank) * 128;
+  w.b0 = (SWAP ? tok : ch) * BN;
   w.kb0 = sp * a.kb_per_split;
   w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
   w.split = sp;
   return w;
 }
 
-template <int STAGES>
+template <bool SWAP, int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     w8a8_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const GemmArgs args) {
-  using C = Fp8PairCfg<STAGES>;
+  using C = Fp8PairCfg<BN, STAGES>;
   __shared__ Fp8PairBarriers<STAGES> bars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -119,13 +125,14 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint64_t polA = l2_policy_evict_last();
-      const uint64_t polB = l2_policy_evict_normal();
+      // the operand read once (weights, decode) streams through L2 first
+      const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
       const uint32_t full0 = cluster_map(&bars.full[0], 0);
       int g = 0;
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; u += u_stride) {
-        const PairUnit w = pair_unit(args, u, rank);
+        const PairUnit w = pair_unit<SWAP, BN>(args, u, rank);
         for (int it = 0; it < w.nkb; ++it, ++g) {
           const int s = g % STAGES;
           if (args.fault && g == 0) continue;  // injected fault: this stage never fills
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
       int g = 0;   // k-blocks consumed
       int cg = 0;  // accumulators filled (buffer cg & 1)
       for (int u = u_begin; u < u_end && ok; u += u_stride) {
-        const PairUnit w = pair_unit(args, u, rank);
+        const PairUnit w = pair_unit<SWAP, BN>(args, u, rank);
         const int buf = cg & 1;
         // the epilogues of both CTAs must have drained this buffer's previous tile
         if (cg >= 2 && !mbar_wait_cluster(&bars.pempty[buf], ((cg >> 1) - 1) & 1, status)) {
@@ -197,18 +204,28 @@ __global__ void __launch_bounds__(192, 1)
     const int emode = args.mode;
     int cg = 0;
     for (int u = u_begin; u < u_end; u += u_stride, ++cg) {
-      const PairUnit w = pair_unit(args, u, rank);
+      const PairUnit w = pair_unit<SWAP, BN>(args, u, rank);
       const int buf = cg & 1;
+      // swap: scales of this lane's channel and of its token in the first
+      // 32-token block, loaded while the accumulator is being filled
+      const float sw_lane = SWAP ? channel_scale(args, emode, w.a0 + i) : 0.0f;
+      const float sx_first = SWAP ? token_scale(args, emode, w.b0 + lane) : 0.0f;
       if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) break;
       tc_fence_after();
+      float sx_lane = sx_first;
 #pragma unroll 1
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
+        const float sx_next = (SWAP && c0 + 32 < C::BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
         uint32_t p[32];
         tmem_ld32(lane_base + buf * C::BN + c0, p);
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
-        emit32<256, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+        if constexpr (SWAP)
+          emit32_swap<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
+        else
+          emit32<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+        sx_lane = sx_next;
       }
       tc_fence_before();
       __syncwarp();
@@ -227,11 +244,11 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-cudaError_t launch_gemm_fp8_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args_in, dim3 grid,
-                                 cudaStream_t stream) {
-  constexpr int STAGES = 6;
-  using C = Fp8PairCfg<STAGES>;
-  auto kern = w8a8_gemm_fp8_pair_kernel<STAGES>;
+template <bool SWAP, int BN, int STAGES>
+cudaError_t launch_pair_inst(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args_in, dim3 grid,
+                             cudaStream_t stream) {
+  using C = Fp8PairCfg<BN, STAGES>;
+  auto kern = w8a8_gemm_fp8_pair_kernel<SWAP, BN, STAGES>;
   static bool attr_done[64] = {};
   static int max_pairs[64] = {};
   int dev = 0;
@@ -270,6 +287,19 @@ cudaError_t launch_gemm_fp8_pair(const CUtensorMap& ta, const CUtensorMap& tb, c
   const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(units, max_pairs[dev])));
   return launch_pdl_pair(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(C::NUM_THREADS), C::SMEM_BYTES, stream,
                          ta, tb, args);
+}
+
+// Stage counts fill ~192-200 KB of shared memory: (128 + BN / 2) x 128 B per stage.
+cudaError_t launch_gemm_fp8_pair(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                                 dim3 grid, cudaStream_t st) {
+  if (!swap) return bn == 256 ? launch_pair_inst<false, 256, 6>(ta, tb, a, grid, st) : cudaErrorInvalidValue;
+  switch (bn) {
+    case 64: return launch_pair_inst<true, 64, 9>(ta, tb, a, grid, st);
+    case 128: return launch_pair_inst<true, 128, 8>(ta, tb, a, grid, st);
+    case 256: return launch_pair_inst<true, 256, 6>(ta, tb, a, grid, st);
+    default: break;
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qurl

@@ -122,8 +122,8 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
 struct GemmPlan {
   bool swap;         // weights on the MMA M side (decode)
   bool tmem_a;       // INT8 decode: weights widened into TMEM, fp16 activation copy in the workspace
-  bool pair;         // FP8 prefill on CTA pairs: token tiles of 256 (grid.x), channel tiles of 256,
-                     // B staged 128 channel rows per CTA
+  bool pair;         // FP8 on CTA pairs: 256-row A tiles per pair (prefill: tokens, swap: channels),
+                     // each CTA staging half of the bn B rows
   size_t x16_bytes;  // bytes at the start of the workspace for that fp16 copy and, after it
                      // (at asum_off), the per-token sums of |code| (256-aligned pieces)
   size_t asum_off;
@@ -149,9 +149,10 @@ cudaError_t launch_gemm_fp8(bool swap, int bn, const CUtensorMap& ta, const CUte
                             dim3 grid, cudaStream_t st);
 cudaError_t launch_gemm_i8(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                            dim3 grid, cudaStream_t st);
-// gemm_fp8p.cu: FP8 prefill on CTA pairs (grid = pair token tiles, channel tiles, K splits).
-cudaError_t launch_gemm_fp8_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, dim3 grid,
-                                 cudaStream_t st);
+// gemm_fp8p.cu: FP8 on CTA pairs, 256-row A tiles per pair (grid = token tiles, channel tiles,
+// K splits; prefill: 256 tokens x 256 channels, swap: 256 channels x bn tokens, bn in {64, 128, 256}).
+cudaError_t launch_gemm_fp8_pair(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                                 dim3 grid, cudaStream_t st);
 // gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
