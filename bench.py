@@ -62,9 +62,13 @@ def peaks():
 
 # prefill shapes timed beside the decode step (tensor-bound; 7B and 32B layer classes)
 PREFILL = [("7b", "gate_up", 4096), ("32b", "down", 1024)]
-DOMINANT_PROFILE = {"int8": "profiles/w8a8_gemm_i8t_kernel_7b_gate_up_m256_int8.md"}
-KERNEL_SOURCES = ["w8a8_precision_gemm_gb300/csrc/gemm.cuh", "w8a8_precision_gemm_gb300/csrc/gemm_i8t.cu",
-                  "w8a8_precision_gemm_gb300/csrc/ptx.cuh", "w8a8_precision_gemm_gb300/csrc/internal.h"]
+DOMINANT_PROFILE = {"int8": "profiles/w8a8_gemm_i8t_kernel_7b_gate_up_m256_int8.md",
+                    "fp8": "profiles/w8a8_gemm_fp8_pair_kernel_7b_gate_up_m256_fp8.md"}
+_CSRC = "w8a8_precision_gemm_gb300/csrc/"
+KERNEL_SOURCES = {"int8": [_CSRC + f for f in ("gemm.cuh", "gemm_i8t.cu", "ptx.cuh", "internal.h")],
+                  "fp8": [_CSRC + f for f in ("gemm.cuh", "gemm_fp8p.cu", "ptx.cuh", "internal.h")]}
+# the kernel each qtype's dominant GEMM (gate_up, M = 256) runs
+DOMINANT_KERNEL = {"int8": "w8a8_gemm_i8t_kernel", "fp8": "w8a8_gemm_fp8_pair_kernel"}
 
 
 def profiled_traffic(qtype):
@@ -76,7 +80,7 @@ def profiled_traffic(qtype):
     if not path or not os.path.exists(os.path.join(ROOT, path)):
         return None
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[qtype]:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     fields = dict(line.split(": ", 1) for line in open(os.path.join(ROOT, path)).read().splitlines() if ": " in line
                   and line.split(": ", 1)[0] in ("kernel_sources_sha256_16", "dram_bytes_per_launch"))
@@ -521,7 +525,7 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(args.qtype)
     roof["traffic_source"] = DOMINANT_PROFILE.get(args.qtype) if roof["traffic"] is not None else None
-    kname = "w8a8_gemm_i8t_kernel" if qt == q.INT8 else "w8a8_gemm_kernel"
+    kname = DOMINANT_KERNEL[args.qtype]
     roof["kernel"] = f"{kname} {dname} M={dM} K={dK} N={dN} ({args.qtype})"
     roof["peak_source"] = (f"{pk['source']} " + ("bf16 burst (INT8 runs on the fp16 tensor pipe, same dense rate)"
                                                 if qt == q.INT8 else "bf16 burst x 2 (nominal fp8:bf16 ratio)")
