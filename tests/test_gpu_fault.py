@@ -13,11 +13,15 @@ from w8a8_precision_gemm_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("qt", [q.INT8, q.FP8_E4M3])
-def test_bounded_wait_times_out_and_context_survives(qt):
-    M, N, K = 16, 512, 256
-    X = synth.activations("fault/X", M, K).cuda()
-    W = synth.weights("fault/W", N, K).cuda()
+@pytest.mark.parametrize("qt,M,N,K", [
+    (q.INT8, 16, 512, 256),
+    (q.FP8_E4M3, 16, 512, 256),
+    (q.FP8_E4M3, 300, 512, 256),     # prefill: the CTA-pair kernel
+    (q.FP8_E4M3, 256, 8192, 4096),   # decode shape that runs on CTA pairs
+])
+def test_bounded_wait_times_out_and_context_survives(qt, M, N, K):
+    X = synth.activations(f"fault/X/{M}/{K}", M, K).cuda()
+    W = synth.weights(f"fault/W/{N}/{K}", N, K).cuda()
     Wq, sw, _, _ = q.prepare_weights(W, qt, s=1.5, keep_scaled=False)
     Xq, sx = q.quant_act(X, qt)
     ws = q.workspace(M, N, K, qt)
