@@ -364,10 +364,10 @@ def test_gemm_int8_prefill_repeatable():
 
 
 def test_gemm_int8_more_units_than_mode_slots():
-    """160 x 124 tiles: every CTA walks 131 units, beyond the 128 whose
-    accumulation mode the kernel records, so the last ones take the chunked
-    path without a recorded mode."""
-    M, N, K = 128 * 160, 128 * 124, 512
+    """102 x 98 tiles of 256 x 256 on the CTA pairs: every pair walks ~131
+    units, beyond the 128 whose accumulation mode the kernel records, so the
+    last ones take the chunked path (two half passes) without a recorded mode."""
+    M, N, K = 256 * 102, 256 * 98, 512
     g = np.random.Generator(np.random.PCG64(23))
     xq = g.integers(-20, 21, size=(M, K)).astype(np.int8)
     wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)

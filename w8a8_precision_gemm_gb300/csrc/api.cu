@@ -211,7 +211,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
       w_indep = true;  // the widening kernel writes only the workspace
     }
     QURL_TRY(byte_map(Wq, N, K, K, 128, 128, true, &ta));
-    QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, p.bn, true, &tb));
+    QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, p.pair ? 64 : p.bn, true, &tb));
   } else {
     const long long a_rows = p.swap ? N : M;
     const long long b_rows = p.swap ? M : N;
@@ -236,7 +236,9 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.fault = g_inject_timeout.exchange(0);
   a.asum = sums.asum;
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
-  if (p.tmem_a)
+  if (p.tmem_a && p.pair)
+    QURL_CUDA(qurl::launch_gemm_i8p(ta, tb, a, grid, st));
+  else if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
   else if (p.pair)
     QURL_CUDA(qurl::launch_gemm_fp8_pair(p.swap, p.bn, ta, tb, a, grid, st));

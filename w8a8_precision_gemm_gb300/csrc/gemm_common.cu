@@ -27,17 +27,35 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   p.bk = int8 ? (p.tmem_a ? 256 : 64) : 128;
   p.num_kb = (K + p.bk - 1) / p.bk;
   if (p.swap) {
-    const int max_bn = int8 ? 128 : 256;
+    const int max_bn = (int8 && !p.tmem_a) ? 128 : 256;
     int bn = 16;
     while (bn < M && bn < max_bn) bn *= 2;
+    // CTA pairs (256 channels per pair) when there is enough work, at least
+    // 1024 stages of pair tiles (stages of 128 bytes of K for FP8, 256 for
+    // INT8; measured slower on the small qkv / o_proj, where half as many
+    // tiles need more K splits): FP8 beyond 64 tokens (7B gate_up and down
+    // at M = 256), INT8 beyond 256 tokens with 256-token tiles (prefill; in
+    // the decode chain at M = 256 the single-CTA kernel, whose accumulator is
+    // double-buffered and which overlaps the quantizer before it, measured
+    // as fast)
+    const long long pair_work = static_cast<long long>((M + (p.tmem_a ? 255 : bn - 1)) / (p.tmem_a ? 256 : bn)) *
+                                ((N + 255) / 256) * p.num_kb;
+    // INT8 pairs also need to fill their waves: a round of 256 x 256 units on
+    // the SM pairs takes ~1.8 rounds of 128 x 128 units on the SMs (measured on
+    // 7B gate_up, M = 4096), so the pairs are taken only when they need fewer
+    // rounds by that factor (e.g. not for 32B qkv at M = 1024: 112 pair units
+    // fill two rounds of 76 pairs half-way, 448 single units three rounds)
+    bool pair_waves = true;
+    if (p.tmem_a && bn == 256 && num_sms >= 2) {
+      const long long up = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+      const long long us = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
+      const long long rp = (up + num_sms / 2 - 1) / (num_sms / 2), rs = (us + num_sms - 1) / num_sms;
+      pair_waves = 18 * rp <= 10 * rs;
+    }
+    if (p.tmem_a && bn == 256 && (pair_work < 1024 || M <= 256 || !pair_waves)) bn = 128;  // single-CTA tiles
     p.bn = bn;
-    // FP8 decode runs on CTA pairs (256 channels per pair) when it has 128 or
-    // more tokens and enough work: at least 1024 k-blocks of pair tiles (7B
-    // gate_up and down at M = 256; measured slower on the small qkv / o_proj,
-    // where half as many tiles need more K splits)
     p.tiles_tok = (M + bn - 1) / bn;
-    p.pair = !int8 && bn >= 128 &&
-             static_cast<long long>(p.tiles_tok) * ((N + 255) / 256) * ((K + p.bk - 1) / p.bk) >= 1024;
+    p.pair = pair_work >= 1024 && ((p.tmem_a && bn == 256) || (!int8 && bn >= 128));
     p.tiles_ch = p.pair ? (N + 255) / 256 : (N + 127) / 128;
   } else {
     p.bn = int8 ? 128 : 256;

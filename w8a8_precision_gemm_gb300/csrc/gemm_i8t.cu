@@ -483,6 +483,479 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA pairs, 256 x 256 tiles
+//
+// Token tiles above 128 run on CTA pairs: the two CTAs of a cluster share
+// every MMA (tcgen05.mma.cta_group::2 kind::f16, M = 256 channels -- 128
+// widened weight rows in each CTA's TMEM -- by N = 256 tokens), so one
+// issued MMA does twice the work of the single-CTA kernel's and one stage of
+// 16 MMAs lasts ~1 us: the on-chip refill loop of the widened weights (MMA
+// done -> both CTAs widen the next rows -> rank 0 learns of it) has that long
+// to close, and the bytes staged per SM buy twice the MMA work.  Each CTA
+// stages 128 of the 256 tokens as two 64-row groups (tokens 64 r .. and
+// 128 + 64 r .., r = cluster rank); the pair MMA maps CTA r's rows to
+// accumulator columns 128 r .., and the epilogue maps the columns back.
+//
+// TMEM: one 256-column fp32 accumulator (no second buffer: the epilogue of a
+// tile and the first MMAs of the next do not overlap) and two 128-column A
+// stages.  A unit that needs chunked accumulation runs as two N = 128
+// half-passes (one 64-row group of each CTA per half), each in 1024-deep
+// chunks drained into an int32 running sum kept in the accumulator's upper
+// 128 columns.  Both CTAs' activation loads complete on rank 0's barrier,
+// rank 1's converter warps arrive on rank 0's A-stage barrier, and one
+// multicast commit releases a stage in both CTAs.
+struct I8pCfg {
+  static constexpr int BM = 128;                     // weight rows per CTA
+  static constexpr int BN = 256;                     // tokens per unit (MMA N of a full pass)
+  static constexpr int BK = 256;                     // k per stage
+  static constexpr int W_BOX = BM * 128;
+  static constexpr int W_STAGE = 2 * W_BOX;          // 32 KB
+  static constexpr int XG = 64;                      // token rows of one group
+  static constexpr int X_BOX = 2 * XG * 128;         // one 128-byte k column of both groups: 16 KB
+  static constexpr int X_STAGE = 4 * X_BOX;          // 64 KB
+  static constexpr int NS = 2;                       // activation slots = TMEM A stages
+  static constexpr int ACC_COLS = 256;
+  static constexpr int A_COLS = BK / 2;
+  static constexpr int A_BASE = ACC_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int WST = 3;
+  static constexpr int SMEM_BYTES = WST * W_STAGE + NS * X_STAGE + 1024;
+  static constexpr int NUM_THREADS = 512;
+  static constexpr int CHUNK = 1024 / BK;
+  static constexpr uint32_t IDESC_FULL = umma_idesc_f32acc(0, 0, 2 * BM, BN);
+  static constexpr uint32_t IDESC_HALF = umma_idesc_f32acc(0, 0, 2 * BM, BN / 2);
+  static constexpr int AFULL_ARRIVALS = 128 + 4;     // rank 0's converters, and rank 1's four warps
+  static_assert(A_BASE + NS * A_COLS <= TMEM_COLS, "TMEM has 512 columns");
+  static_assert(SMEM_BYTES <= 227 * 1024 - 1024, "shared memory per CTA");
+};
+
+struct I8pBarriers {
+  uint64_t wfull[I8pCfg::WST];
+  uint64_t wempty[I8pCfg::WST];
+  uint64_t xfull[I8pCfg::NS];     // rank 0: both CTAs' activation bytes of a stage
+  uint64_t afull[I8pCfg::NS];     // rank 0: both CTAs' converters
+  uint64_t consumed[I8pCfg::NS];  // MMA commit (multicast): stage read
+  uint64_t pfull;                 // MMA commit (multicast): accumulator (or chunk) ready
+  uint64_t pempty;                // rank 0: epilogue warps of both CTAs (8): accumulator drained
+  uint64_t done;
+  uint32_t fast_bits[kModeWords];
+  uint32_t mode_count;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void umma_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Unit u of the pair grid: a0 = this CTA's 128 weight rows, b0 = the first of
+// the unit's 256 tokens.
+__device__ __forceinline__ Unit unit_i8p(const GemmArgs& a, int u, uint32_t rank) {
+  const int tok = u % a.tiles_tok;
+  const int rest = u / a.tiles_tok;
+  const int ch = rest % a.tiles_ch;
+  const int sp = rest / a.tiles_ch;
+  Unit w;
+  w.a0 = ch * 256 + static_cast<int>(rank) * 128;
+  w.b0 = tok * 256;
+  w.kb0 = sp * a.kb_per_split;
+  w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
+  w.split = sp;
+  return w;
+}
+
+// First token of accumulator columns c0 .. c0 + 31 (c0 a multiple of 32):
+// full pass -- column c comes from CTA c / 128, row c % 128 of its two
+// 64-token groups; half pass h -- column c from CTA c / 64, row c % 64 of
+// its group h.
+__device__ __forceinline__ int i8p_token(int b0, int c0, int h, bool full) {
+  if (full) {
+    const int r = c0 >> 7, j = c0 & 127;
+    return b0 + 64 * r + (j & 63) + ((j >> 6) << 7);
+  }
+  return b0 + 128 * h + 64 * (c0 >> 6) + (c0 & 63);
+}
+
+__global__ void __launch_bounds__(512, 1)
+    w8a8_gemm_i8p_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX16,
+                         const GemmArgs args) {
+  using C = I8pCfg;
+  constexpr int WST = C::WST;
+  constexpr int NS = C::NS;
+  __shared__ I8pBarriers bars;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stW = smem;                       // [WST][W_STAGE]
+  uint8_t* stX = stW + WST * C::W_STAGE;     // [NS][X_STAGE]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const UnitRange R{static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1),
+                    args.tiles_tok * args.tiles_ch * args.splits};
+  int* status = args.status;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WST; ++s) {
+      mbar_init(&bars.wfull[s], 1);
+      mbar_init(&bars.wempty[s], 128);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars.xfull[s], 1);
+      mbar_init(&bars.afull[s], C::AFULL_ARRIVALS);
+      mbar_init(&bars.consumed[s], 1);
+    }
+    mbar_init(&bars.pfull, 1);
+    mbar_init(&bars.pempty, 8);
+    bars.mode_count = 0;
+    mbar_init(&bars.done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmX16);
+  }
+  if (warp == 1) {
+    tmem_alloc<2>(&bars.tmem_base, C::TMEM_COLS);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any signal reaches them
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  griddep_launch_dependents();
+  if (warp != 0) griddep_wait();
+
+  constexpr int kModeUnits = 32 * kModeWords;
+  auto is_fast = [&](int j) {
+    return j < kModeUnits && ((bars.fast_bits[j >> 5] >> (j & 31)) & 1u) != 0;
+  };
+  // passes over the unit's k range: one (fast) or two halves (chunked)
+  auto passes_of = [&](int j, bool& ok) {
+    if (j < kModeUnits && !wait_count(&bars.mode_count, j, status)) ok = false;
+    return is_fast(j) ? 1 : 2;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ weight producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      auto load = [&](int slot, const Unit& w, int it) {
+        mbar_arrive_expect_tx(&bars.wfull[slot], C::W_STAGE);
+        const int k0 = (w.kb0 + it) * C::BK;
+        uint8_t* dst = stW + slot * C::W_STAGE;
+        tma_load_2d(dst, &tmW, k0, w.a0, &bars.wfull[slot], pol);
+        tma_load_2d(dst + C::W_BOX, &tmW, k0 + 128, w.a0, &bars.wfull[slot], pol);
+      };
+      // the first pass's first stages are the same in either mode
+      int npre = 0;
+      if (args.w_prefetch && !args.fault && R.u < R.end) {
+        const Unit w = unit_i8p(args, R.u, rank);
+        npre = min(WST, w.nkb);
+        for (int it = 0; it < npre; ++it) load(it, w, it);
+      }
+      griddep_wait();
+      Ring<WST> r;
+      int g = 0;
+      bool ok = true;
+      for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
+        const Unit w = unit_i8p(args, u, rank);
+        const int np = passes_of(j, ok);
+        for (int h = 0; h < np && ok; ++h)
+          for (int it = 0; it < w.nkb; ++it, ++g, r.next()) {
+            if (args.fault && g == 0) continue;  // injected fault: this slot never fills
+            if (g < npre) continue;
+            if (!mbar_wait(&bars.wempty[r.idx], r.phase ^ 1u, status)) {
+              ok = false;
+              break;
+            }
+            load(r.idx, w, it);
+          }
+      }
+      if (!ok) {
+        for (int jj = max(0, g - WST); jj < g; ++jj) mbar_wait_drain(&bars.wfull[jj % WST], (jj / WST) & 1, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (rank == 0 && lane == 0) {
+      bool ok = true;
+      Ring<NS> r;
+      int nd = 0;  // accumulator fills committed (epilogue drains to wait for)
+      for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
+        const Unit w = unit_i8p(args, u, rank);
+        const int np = passes_of(j, ok);
+        const bool full = (np == 1);
+        for (int h = 0; h < np && ok; ++h) {
+          for (int it = 0; it < w.nkb; ++it, r.next()) {
+            const int kin = full ? it : it % C::CHUNK;  // stage within the accumulation pass
+            if (kin == 0 && nd > 0 && !mbar_wait_cluster(&bars.pempty, (nd - 1) & 1, status)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&bars.xfull[r.idx], r.phase, status) ||
+                !mbar_wait_cluster(&bars.afull[r.idx], r.phase, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_t = tmem + C::A_BASE + r.idx * C::A_COLS;
+            // half pass h: each CTA's 64-row group h
+            const uint32_t xs = smem_addr(stX + r.idx * C::X_STAGE) + (full ? 0u : static_cast<uint32_t>(h * C::XG * 128));
+            const uint32_t idesc = full ? C::IDESC_FULL : C::IDESC_HALF;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint32_t b_addr = xs + (kk >> 2) * C::X_BOX + (kk & 3) * 32;
+              umma_f16_tmem_a_pair(tmem, a_t + kk * 8, umma_desc_sw128(b_addr), idesc, (kin | kk) != 0);
+            }
+            umma_commit_pair(&bars.consumed[r.idx], 0x3);
+            if (it == w.nkb - 1 || (!full && kin == C::CHUNK - 1)) {
+              umma_commit_pair(&bars.pfull, 0x3);
+              ++nd;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        umma_commit_pair(&bars.done, 0x1);
+        mbar_wait_drain(&bars.done, 0, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ activation producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      const uint32_t xfull0 = cluster_map(&bars.xfull[0], 0);
+      Ring<NS> r;
+      int g = 0;
+      bool ok = true;
+      for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
+        const Unit w = unit_i8p(args, u, rank);
+        const int np = passes_of(j, ok);
+        for (int h = 0; h < np && ok; ++h)
+          for (int it = 0; it < w.nkb; ++it, ++g, r.next()) {
+            if (!mbar_wait(&bars.consumed[r.idx], r.phase ^ 1u, status)) {
+              ok = false;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(&bars.xfull[r.idx], 2 * C::X_STAGE);
+            uint8_t* xs = stX + r.idx * C::X_STAGE;
+            const int c0 = (w.kb0 + it) * C::BK * 2;  // byte column of the fp16 copy
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc)
+#pragma unroll
+              for (int grp = 0; grp < 2; ++grp)
+                tma_load_2d_pair(xs + kc * C::X_BOX + grp * C::XG * 128, &tmX16, c0 + kc * 128,
+                                 w.b0 + grp * 128 + static_cast<int>(rank) * C::XG, xfull0 + r.idx * 8, pol);
+          }
+      }
+      if (!ok && rank == 0) {
+        // rank 0's barriers count both CTAs' bytes; rank 1 leaves only after
+        // the closing cluster barrier, which rank 0 reaches after this
+        for (int jj = max(0, g - NS); jj < g; ++jj) mbar_wait_drain(&bars.xfull[jj % NS], (jj / NS) & 1, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ accumulation mode of each unit
+    if (lane < kModeWords) bars.fast_bits[lane] = 0;
+    __syncwarp();
+    if (args.asum != nullptr) {
+      for (int u = R.u, j = 0; u < R.end && j < kModeUnits; u += R.stride, ++j) {
+        const int t = u % args.tiles_tok;
+        const int sp = u / (args.tiles_tok * args.tiles_ch);
+        int mx = 0;
+        for (int c = lane; c < C::BN; c += 32) {
+          const int m = t * C::BN + c;
+          if (m < args.M) mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        if (lane == 0) {
+          if (mx <= kFastSumMax) bars.fast_bits[j >> 5] |= 1u << (j & 31);
+          st_release_cta(&bars.mode_count, static_cast<uint32_t>(j + 1));
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) st_release_cta(&bars.mode_count, 0xFFFFFFFFu);
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int i = q * 32 + lane;  // weight row of this CTA's tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t tR = lane_base + 128;  // running sum of a chunked half pass
+    const uint32_t pempty0 = cluster_map(&bars.pempty, 0);
+    const int emode = args.mode;
+    bool ok = true;
+    int nd = 0;
+    auto drained = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(pempty0);  // rank 0's next MMA writes both CTAs' TMEM
+      ++nd;
+    };
+    for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
+      const Unit w = unit_i8p(args, u, rank);
+      if (j < kModeUnits && !__all_sync(0xFFFFFFFFu, wait_count(&bars.mode_count, j, status))) {
+        ok = false;
+        break;
+      }
+      const bool full = is_fast(j);
+      const float sw_lane = channel_scale(args, emode, w.a0 + i);
+      if (full) {
+        float sx_lane = token_scale(args, emode, i8p_token(w.b0, 0, 0, true) + lane);
+        if (!warp_wait(&bars.pfull, nd & 1, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          const int tb = i8p_token(w.b0, c0, 0, true);
+          const float sx_next =
+              c0 + 32 < C::BN ? token_scale(args, emode, i8p_token(w.b0, c0 + 32, 0, true) + lane) : 0.0f;
+          uint32_t p[32];
+          tmem_ld32(lane_base + c0, p);
+          if (emode == kModeBf16) {
+            float f[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(p[jj]);
+            emit32_swap<C::BN, float>(args, emode, w.a0, tb - c0, w.split, i, c0, f, sx_lane, sw_lane);
+          } else {
+            int v[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) v[jj] = __float2int_rn(__uint_as_float(p[jj]));
+            emit32_swap<C::BN, int>(args, emode, w.a0, tb - c0, w.split, i, c0, v, sx_lane, sw_lane);
+          }
+          sx_lane = sx_next;
+        }
+        drained();
+      } else {
+        const int npass = (w.nkb + C::CHUNK - 1) / C::CHUNK;
+        for (int h = 0; h < 2 && ok; ++h) {
+          for (int c = 0; c < npass; ++c) {
+            if (!warp_wait(&bars.pfull, nd & 1, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const bool last = (c == npass - 1);
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::BN / 2; c0 += 32) {
+              const int tb = i8p_token(w.b0, c0, h, false);
+              const float sx_lane = last ? token_scale(args, emode, tb + lane) : 0.0f;
+              uint32_t p[32];
+              tmem_ld32(lane_base + c0, p);
+              int v[32];
+              if (c > 0) {
+                uint32_t rs[32];
+                tmem_ld32(tR + c0, rs);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) v[jj] = static_cast<int>(rs[jj]) + __float2int_rn(__uint_as_float(p[jj]));
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) v[jj] = __float2int_rn(__uint_as_float(p[jj]));
+              }
+              if (!last) {
+                uint32_t wv[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) wv[jj] = static_cast<uint32_t>(v[jj]);
+                tmem_st32(tR + c0, wv);
+              } else {
+                emit32_swap<C::BN, int>(args, emode, w.a0, tb - c0, w.split, i, c0, v, sx_lane, sw_lane);
+              }
+            }
+            if (!last) tmem_wait_st();
+            drained();
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ converters (both CTAs)
+    const int q = warp & 3;
+    const int grp = (warp - 8) >> 2;
+    const int i = q * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int row_off = (i >> 3) * 1024 + (i & 7) * 128;
+    const uint32_t afull0 = cluster_map(&bars.afull[0], 0);
+    Ring<WST> rw;
+    Ring<NS> ra;
+    int g = 0;
+    bool ok = true;
+    for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
+      const Unit w = unit_i8p(args, u, rank);
+      bool mok = true;
+      const int np = __all_sync(0xFFFFFFFFu, j >= kModeUnits || wait_count(&bars.mode_count, j, status))
+                         ? (is_fast(j) ? 1 : 2)
+                         : (mok = false, 2);
+      if (!mok) {
+        ok = false;
+        break;
+      }
+      for (int h = 0; h < np && ok; ++h)
+        for (int it = 0; it < w.nkb; ++it, ++g, rw.next(), ra.next()) {
+          if ((g & 1) != grp) continue;
+          if (!warp_wait(&bars.wfull[rw.idx], rw.phase, status)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* wrow = stW + rw.idx * C::W_STAGE + row_off;
+          uint4 raw[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            raw[jj] = *reinterpret_cast<const uint4*>(wrow + (jj >> 3) * C::W_BOX + (((jj & 7) ^ (i & 7)) << 4));
+          if (!warp_wait(&bars.consumed[ra.idx], ra.phase ^ 1u, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_t = lane_base + C::A_BASE + ra.idx * C::A_COLS;
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            uint32_t v[32];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              uint4 lo, hi;
+              i8x16_to_f16x16(raw[4 * hh + jj], lo, hi);
+              v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
+              v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
+            }
+            tmem_st32(a_t + hh * 32, v);
+          }
+          mbar_arrive(&bars.wempty[rw.idx]);
+          tmem_wait_st();
+          tc_fence_before();
+          if (rank == 0) {
+            mbar_arrive(&bars.afull[ra.idx]);
+          } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(afull0 + ra.idx * 8);
+          }
+        }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // neither CTA frees its TMEM or exits while rank 0's MMAs, commits or the
+  // peer's copies and arrivals may still reach it
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<2>(tmem, C::TMEM_COLS);
+  }
+}
+
 // One block per row: int8 codes -> fp16 (exact), [M, K] dense -> [M, K]
 // dense, and the row's sums of |code| over the ranges of `sums` (saturated at
 // kSumCap) for the GEMM's accumulation mode.
@@ -545,6 +1018,50 @@ cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx
     default: break;
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_i8p(const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& args_in, dim3 grid,
+                            cudaStream_t stream) {
+  using C = I8pCfg;
+  auto kern = w8a8_gemm_i8p_kernel;
+  static bool attr_done[64] = {};
+  static int max_pairs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  if (max_pairs[dev] <= 0) {
+    // one cluster of two CTAs per pair of SMs, as many as can be resident
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(C::NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorLaunchOutOfResources;
+    max_pairs[dev] = n;
+  }
+  GemmArgs args = args_in;
+  args.tiles_tok = grid.x;
+  args.tiles_ch = grid.y;
+  args.splits = grid.z;
+  const long long units = static_cast<long long>(args.tiles_tok) * args.tiles_ch * args.splits;
+  const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(units, max_pairs[dev])));
+  return launch_pdl_pair(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(C::NUM_THREADS), C::SMEM_BYTES, stream,
+                         tw, tx16, args);
 }
 
 cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums sums, cudaStream_t st) {

@@ -122,8 +122,8 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
 struct GemmPlan {
   bool swap;         // weights on the MMA M side (decode)
   bool tmem_a;       // INT8 decode: weights widened into TMEM, fp16 activation copy in the workspace
-  bool pair;         // FP8 on CTA pairs: 256-row A tiles per pair (prefill: tokens, swap: channels),
-                     // each CTA staging half of the bn B rows
+  bool pair;         // CTA pairs: 256-row A tiles per pair (FP8 prefill: tokens; FP8 swap and the INT8
+                     // TMEM-operand kernel: channels), each CTA staging half of the bn B rows
   size_t x16_bytes;  // bytes at the start of the workspace for that fp16 copy and, after it
                      // (at asum_off), the per-token sums of |code| (256-aligned pieces)
   size_t asum_off;
@@ -156,6 +156,10 @@ cudaError_t launch_gemm_fp8_pair(bool swap, int bn, const CUtensorMap& ta, const
 // gemm_i8t.cu: the INT8 decode GEMM with the weight operand in TMEM, and the
 // int8 -> fp16 widening of the activation codes it reads.
 cudaError_t launch_gemm_i8t(int bn, const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
+                            cudaStream_t st);
+// gemm_i8t.cu: the same on CTA pairs, 256 channels x 256 tokens per pair (grid = 256-token tiles,
+// 256-channel tiles, K splits; the fp16 codes' tensor map has 64-row boxes).
+cudaError_t launch_gemm_i8p(const CUtensorMap& tw, const CUtensorMap& tx16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
 // int8 codes [M, K] -> fp16 [M, K] in dst, and the sums of |code| (saturated at 2^24).
 cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums sums, cudaStream_t st);
