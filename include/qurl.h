@@ -246,6 +246,18 @@ qurl_status qurl_check_device_status(qurl_stream_t stream);
  * clears the word, and later calls run normally.  One-shot; always QURL_OK. */
 qurl_status qurl_debug_inject_timeout(void);
 
+/* The GEMM plan the library takes for an M x N x K product of `qt` codes on a
+ * GPU with `num_sms` SMs and `ws_bytes` of workspace (SIZE_MAX: as much as
+ * qurl_workspace_size asks for).  Host-side only; no device is needed.  Not
+ * a computation of the method: a window on the tiling, for tests and tuning.
+ * out[0..7]: kernel (0 = operands staged in shared memory, INT8 widened
+ * there; 1 = INT8 with the widened weights in TMEM; 2 = the same on CTA
+ * pairs, 256 x 256 tiles; 3 = FP8 on CTA pairs), weights on the MMA M side
+ * (1) or tokens (0), token tile width, token tiles, channel tiles, K splits,
+ * k-blocks per split, workspace bytes the plan uses.  QURL_ERR_INVALID_ARG
+ * for a null `out`, a non-positive size or SM count, or an unknown qt. */
+qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, long long* out);
+
 /* Static, human-readable name of a status code. */
 const char* qurl_status_string(qurl_status s);
 

@@ -42,7 +42,7 @@ def test_status_strings_and_version(L):
     assert L.qurl_status_string(0) == b"QURL_OK"
     assert L.qurl_status_string(6) == b"QURL_ERR_TIMEOUT"
     assert L.qurl_status_string(99) == b"QURL_ERR_UNKNOWN"
-    assert L.qurl_version() == 100
+    assert L.qurl_version() == 101
 
 
 FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced: calls fail validation first
@@ -101,3 +101,56 @@ def test_workspace_size_without_gpu(L):
     ws = L.qurl_workspace_size(64, 4608, 3584, 1)  # FP8 decode: split-K partials only
     assert ws > 0 and ws % (64 * 4608 * 4) == 0
     assert L.qurl_workspace_size(8192, 55296, 5120, 1) == 0  # prefill fills the GPU without splitting K
+
+
+def _tile_widths(p):
+    """(token tile width, channel tile width) of a plan."""
+    pair = p["kernel"] in (2, 3)
+    if p["swap"]:
+        return p["bn"], (256 if pair else 128)
+    return (256 if pair else 128), p["bn"]
+
+
+@pytest.mark.parametrize("M,N,K,qt,kernel", [
+    # INT8 with its workspace: the TMEM-operand kernel; CTA pairs only for prefill
+    # sizes whose 256 x 256 units fill their waves
+    (64, 37888, 3584, 0, 1), (256, 37888, 3584, 0, 1), (256, 4608, 3584, 0, 1),
+    (4096, 37888, 3584, 0, 2), (4096, 3584, 18944, 0, 2), (8192, 7168, 5120, 0, 2),
+    (1024, 7168, 5120, 0, 1), (1024, 5120, 27648, 0, 1),
+    # FP8: pairs for prefill and for the larger decode shapes
+    (64, 37888, 3584, 1, 0), (256, 4608, 3584, 1, 0), (256, 37888, 3584, 1, 3),
+    (256, 3584, 18944, 1, 3), (4096, 37888, 3584, 1, 3), (300, 520, 2048, 1, 3),
+])
+def test_plan_routing_and_coverage(M, N, K, qt, kernel):
+    """The kernel each shape is routed to (the choices the measurements made) and
+    that every plan's tiles and K splits cover the problem exactly once."""
+    import w8a8_precision_gemm_gb300 as q
+
+    p = q.plan(M, N, K, qt, 152)
+    assert p["kernel"] == kernel, p
+    tw, cw = _tile_widths(p)
+    assert (p["tiles_tok"] - 1) * tw < M <= p["tiles_tok"] * tw
+    assert (p["tiles_ch"] - 1) * cw < N <= p["tiles_ch"] * cw
+    bk = 256 if p["kernel"] in (1, 2) else (64 if qt == 0 else 128)
+    num_kb = -(-K // bk)
+    assert (p["splits"] - 1) * p["kb_per_split"] < num_kb <= p["splits"] * p["kb_per_split"]
+
+
+def test_plan_workspace_and_fallbacks(L):
+    import ctypes
+    import w8a8_precision_gemm_gb300 as q
+
+    # the plan's workspace is what qurl_workspace_size reports (160 SMs without a device)
+    for M, N, K, qt in ((64, 4608, 3584, 0), (256, 37888, 3584, 0), (64, 3584, 18944, 1), (4096, 3584, 3584, 0)):
+        assert q.plan(M, N, K, qt, 160)["ws_bytes"] == L.qurl_workspace_size(M, N, K, qt)
+    # no workspace: INT8 widens both operands in shared memory and K is not split
+    p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=0)
+    assert p["kernel"] == 0 and p["splits"] == 1 and p["ws_bytes"] == 0
+    # a workspace too small for split partials keeps the TMEM kernel unsplit
+    act = 64 * 3584 * 2 + 256
+    p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=act)
+    assert p["kernel"] == 1 and p["splits"] == 1 and p["ws_bytes"] <= act
+    out = (ctypes.c_longlong * 8)()
+    assert L.qurl_debug_plan(64, 4608, 3584, 0, 0, 0, out) == 1
+    assert L.qurl_debug_plan(64, 4608, 3584, 7, 152, 0, out) == 1
+    assert L.qurl_debug_plan(64, 4608, 3584, 0, 152, 0, None) == 1

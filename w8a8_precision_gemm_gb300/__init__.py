@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
             "qurl_count_diff": [P, P, z, P, P],
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
+            "qurl_debug_plan": [i, i, i, i, i, z, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -233,6 +234,15 @@ def qurl_count_diff(a, b, count, stream=None):
 
 def qurl_check_device_status(stream=None):
     _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
+
+
+def plan(M, N, K, qt, num_sms, ws_bytes=None):
+    """The GEMM plan for a shape (host-side; see qurl_debug_plan)."""
+    out = (ctypes.c_longlong * 8)()
+    ws = ctypes.c_size_t(-1).value if ws_bytes is None else ws_bytes
+    _ok(load().qurl_debug_plan(M, N, K, qt, num_sms, ws, out), "qurl_debug_plan")
+    keys = ("kernel", "swap", "bn", "tiles_tok", "tiles_ch", "splits", "kb_per_split", "ws_bytes")
+    return dict(zip(keys, list(out)))
 
 
 def qurl_debug_inject_timeout():

@@ -318,7 +318,7 @@ const char* qurl_status_string(qurl_status s) {
   return "QURL_ERR_UNKNOWN";
 }
 
-int qurl_version(void) { return 100; }
+int qurl_version(void) { return 101; }
 
 unsigned long long qurl_kernel_launches(void) { return qurl::g_kernel_launches.load(); }
 
@@ -389,6 +389,21 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
                                         qurl::CodeSums{},
                                         reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, long long* out) {
+  if (!out || !valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt) || num_sms <= 0)
+    return QURL_ERR_INVALID_ARG;
+  const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, num_sms, ws_bytes);
+  out[0] = p.tmem_a ? (p.pair ? 2 : 1) : (p.pair ? 3 : 0);
+  out[1] = p.swap ? 1 : 0;
+  out[2] = p.bn;
+  out[3] = p.tiles_tok;
+  out[4] = p.tiles_ch;
+  out[5] = p.splits;
+  out[6] = p.kb_per_split;
+  out[7] = static_cast<long long>(p.ws_bytes);
   return QURL_OK;
 }
 
