@@ -343,10 +343,11 @@ def test_gemm_int8_decode_unsplit_long_k(M, small):
 
 
 def test_gemm_int8_prefill_repeatable():
-    """A prefill shape where every CTA walks ~20 units, so each shared-memory
-    slot and TMEM stage is reused hundreds of times: three runs must agree bit
-    for bit (a slot released before its reads had landed once corrupted ~1% of
-    the outputs, differently on every run), and a sample matches the oracle."""
+    """A prefill shape (on the CTA pairs) where every pair walks ~4 units of
+    14 stages, so each shared-memory slot and TMEM stage is reused hundreds of
+    times: three runs must agree bit for bit (a slot released before its reads
+    had landed once corrupted ~1% of the outputs, differently on every run),
+    and a sample matches the oracle."""
     M, N, K = 4096, 4608, 3584
     X = synth.activations("gpu/repeat/X", M, K)
     W = synth.weights("gpu/repeat/W", N, K)
@@ -361,6 +362,53 @@ def test_gemm_int8_prefill_repeatable():
     cols = np.sort(g.choice(N, size=256, replace=False))
     ref = oracle.gemm_i8(codes(Xq)[rows], codes(Wq)[cols], nthreads=NT)
     np.testing.assert_array_equal(runs[0].cpu().numpy()[np.ix_(rows, cols)], ref)
+
+
+@pytest.mark.parametrize("M,N", [(2048, 4096), (2000, 4000)])
+def test_gemm_int8_pair_modes(M, N):
+    """Prefill shapes on the 256 x 256 CTA pairs (ragged in the second case):
+    token tiles alternate between small codes (one fp32 pass, N = 256 MMAs) and
+    full-range codes (chunked: two N = 128 half passes, each in 1024-deep chunks
+    with the int32 running sum in the accumulator's upper half); exact int32
+    against the oracle on rows from every tile edge."""
+    K = 4096
+    g = np.random.Generator(np.random.PCG64(M + N))
+    xq = g.integers(-10, 11, size=(M, K)).astype(np.int8)
+    big = (np.arange(M) // 256) % 2 == 1
+    xq[big] = g.integers(-127, 128, size=(int(big.sum()), K)).astype(np.int8)
+    wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    assert q.plan(M, N, K, q.INT8, torch.cuda.get_device_properties(0).multi_processor_count)["kernel"] == 2
+    acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
+                     q.workspace(M, N, K, q.INT8))
+    sync_ok()
+    edges = [r for t0 in range(0, M, 64) for r in (t0, t0 + 31, t0 + 63) if r < M] + [M - 1]
+    rows = np.unique(np.array(edges))
+    cols = np.unique(np.concatenate([np.sort(g.choice(N, size=96, replace=False)), [0, 127, 128, 255, N - 1]]))
+    ref = oracle.gemm_i8(xq[rows].view(np.uint8), wq[cols].view(np.uint8), nthreads=NT)
+    got = acc[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_fp8_pair_prefill_repeatable():
+    """FP8 prefill on the CTA pairs: three runs of the fp32 accumulators agree
+    bit for bit, and a sample lies within the fp32 accumulation bound of the
+    oracle's exact sums."""
+    M, N, K = 4096, 4608, 3584
+    assert q.plan(M, N, K, q.FP8_E4M3, torch.cuda.get_device_properties(0).multi_processor_count)["kernel"] == 3
+    xq = random_codes(q.FP8_E4M3, (M, K), 41)
+    wq = random_codes(q.FP8_E4M3, (N, K), 43)
+    Xd, Wd = to_dev(xq, q.FP8_E4M3), to_dev(wq, q.FP8_E4M3)
+    ws = q.workspace(M, N, K, q.FP8_E4M3)
+    runs = [q.gemm_acc(Xd, Wd, q.FP8_E4M3, ws) for _ in range(3)]
+    sync_ok()
+    assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
+    g = np.random.Generator(np.random.PCG64(19))
+    rows = np.unique(np.concatenate([np.sort(g.choice(M, size=48, replace=False)), [0, 255, 256, M - 1]]))
+    cols = np.unique(np.concatenate([np.sort(g.choice(N, size=96, replace=False)), [0, 127, 128, 255, N - 1]]))
+    ref = oracle.gemm_fp8(xq[rows], wq[cols], nthreads=NT)
+    absref = oracle.gemm_fp8(xq[rows] & np.uint8(0x7F), wq[cols] & np.uint8(0x7F), nthreads=NT)
+    got = runs[0].cpu().numpy()[np.ix_(rows, cols)].astype(np.float64)
+    assert np.all(np.abs(got - ref) <= absref * (K * 2.0 ** -23) + 1e-30)
 
 
 def test_gemm_int8_more_units_than_mode_slots():
