@@ -364,14 +364,14 @@ def test_gemm_int8_prefill_repeatable():
     np.testing.assert_array_equal(runs[0].cpu().numpy()[np.ix_(rows, cols)], ref)
 
 
-@pytest.mark.parametrize("M,N", [(2048, 4096), (2000, 4000)])
-def test_gemm_int8_pair_modes(M, N):
-    """Prefill shapes on the 256 x 256 CTA pairs (ragged in the second case):
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 4096), (2000, 4000, 4000)])
+def test_gemm_int8_pair_modes(M, N, K):
+    """Prefill shapes on the 256 x 256 CTA pairs (ragged in M, N and K in the
+    second case: the last 256-deep stage reads 160 codes and zero fill):
     token tiles alternate between small codes (one fp32 pass, N = 256 MMAs) and
     full-range codes (chunked: two N = 128 half passes, each in 1024-deep chunks
     with the int32 running sum in the accumulator's upper half); exact int32
     against the oracle on rows from every tile edge."""
-    K = 4096
     g = np.random.Generator(np.random.PCG64(M + N))
     xq = g.integers(-10, 11, size=(M, K)).astype(np.int8)
     big = (np.arange(M) // 256) % 2 == 1
