@@ -50,6 +50,7 @@ S_UAQ = 1.5
 EPS = 1e-6
 PROJ = [("qkv", 3584, 4608), ("o_proj", 3584, 3584), ("gate_up", 3584, 37888), ("down", 18944, 3584)]
 DOMINANT = ("gate_up", 256)
+CLOCK_LEAD = 0.5  # s of untimed step replays right before the timed region
 
 
 def peaks():
@@ -132,11 +133,13 @@ REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_pow
 
 
 class ClockSampler:
-    """nvidia-smi every 100 ms while the timed region runs."""
+    """nvidia-smi every 100 ms while the timed region runs.  Each sample carries
+    the host time it arrived, so the summary can keep those taken in and next to
+    the timed region."""
 
     def __init__(self, index):
         self.index = index
-        self.samples = []
+        self.samples = []  # (host time, sm MHz, max sm MHz, event-reason mask)
         self.proc = None
 
     def __enter__(self):
@@ -149,6 +152,9 @@ class ClockSampler:
             self.thread.start()
         except OSError:
             self.proc = None
+        deadline = time.perf_counter() + 3.0  # nvidia-smi's first sample, before any timing starts
+        while self.proc and not self.samples and time.perf_counter() < deadline and self.proc.poll() is None:
+            time.sleep(0.02)
         return self
 
     def _read(self):
@@ -156,7 +162,7 @@ class ClockSampler:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 3:
                 try:
-                    self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+                    self.samples.append((time.perf_counter(), float(parts[0]), float(parts[1]), int(parts[2], 16)))
                 except ValueError:
                     pass
 
@@ -169,16 +175,21 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0, t1, lead):
+        """Clocks over [t0 - lead, t1 + 0.15 s]: the timed region [t0, t1] and
+        the same step replayed for `lead` seconds right before it."""
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [s[0] for s in self.samples]
+        sel = [x for x in self.samples if t0 - lead <= x[0] <= t1 + 0.15] or self.samples
+        sm = [x[1] for x in sel]
         mask = 0
-        for s in self.samples:
-            mask |= s[2]
+        for x in sel:
+            mask |= x[3]
         reasons = [name for bit, name in REASON_BITS.items() if mask & bit and name != "gpu_idle"]
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
-                "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(x[2] for x in sel), "reasons": reasons,
+                "samples": len(sel), "samples_in_timed_region": sum(t0 <= x[0] <= t1 + 0.15 for x in sel),
+                "window": f"the timed region ({(t1 - t0) * 1e3:.0f} ms) and {lead:.1f} s of the same step "
+                          "replayed just before it"}
 
 
 # ------------------------------------------------------------------ the layer
@@ -418,15 +429,23 @@ def run_ours(args):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        # untimed lead-in: the same step replayed for CLOCK_LEAD s, so that clock samples next to a
+        # short timed region see the GPU under this load
+        t_lead = time.perf_counter()
+        while time.perf_counter() - t_lead < CLOCK_LEAD:
+            for _ in range(16):
+                g_step.replay()
+            torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter()
+        t0_wall = time.perf_counter()
         start.record(stream)
         for _ in range(args.steps):
             g_step.replay()
         end.record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+        t1_wall = time.perf_counter()
+        t_wall = t1_wall - t0_wall
         barrier(world)
     q.qurl_check_device_status()
     _, ms_step = job_throughput(step_ops(), start.elapsed_time(end) / args.steps, world)
@@ -545,7 +564,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_step * args.steps,
             "launches_per_step": launches_step,
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(t0_wall, t1_wall, CLOCK_LEAD),
             "per_gemm": per, "per_quant": per_quant, "prefill": prefill}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
