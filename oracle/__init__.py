@@ -9,11 +9,14 @@ What each function computes, and which passage of the source pages it restates,
 is written in ``qurl_oracle.c``.  Pages: Paper-Notes ICLR2026, "QuRL: Efficient
 Reinforcement Learning with Quantized Rollout" -- sections "更新感知量化 (UAQ)"
 (invariant scaling), "损失函数 / 训练策略" (per-channel / per-token INT8 or FP8,
-s = 1.5) and "系统集成与工程实现" (one-time UAQ preprocessing, INT8/FP8 matmul).
+s = 1.5; the GRPO/DAPO decoupled objective), "系统集成与工程实现" (one-time UAQ
+preprocessing, INT8/FP8 matmul) and "自适应裁剪范围 (ACR)" (the token objective
+of the quantized rollout).
 
 Parity pinning: every function here is pinned by tests under ``tests/`` that
 check it against library routines (torch CPU casts and rounding, numpy integer
-and fp64 matmul), closed forms and invariants -- see test_oracle_pins.py.
+and fp64 matmul), closed forms and invariants -- see test_oracle_pins.py and
+test_oracle_acr.py.
 """
 from __future__ import annotations
 
@@ -77,8 +80,10 @@ def lib():
             L.orc_epilogue_f64.argtypes = [P, P, P, i, i, P, i]
             L.orc_count_diff.restype = ctypes.c_uint64
             L.orc_count_diff.argtypes = [P, P, z]
+            L.orc_acr_objective.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_double, ctypes.c_double, i,
+                                            P, P, P]
             for name in ("orc_quant_rows_f32", "orc_quant_act", "orc_prepare_weights", "orc_rmsnorm_quant",
-                         "orc_silu_mul_quant", "orc_gemm_i8", "orc_gemm_fp8"):
+                         "orc_silu_mul_quant", "orc_gemm_i8", "orc_gemm_fp8", "orc_acr_objective"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -251,3 +256,26 @@ def count_diff(a, b) -> int:
     b = _c(b, np.uint8)
     assert a.size == b.size
     return int(lib().orc_count_diff(_p(a), _p(b), a.size))
+
+
+# ---------------------------------------------------------------- ACR objective
+
+ACR_NSTATS = 6
+ACR_STATS = ("objective", "n_valid", "clipped_frac", "mean_tis_weight", "capped_frac", "kl_behav_prox")
+
+
+def acr_objective(logp, logp_prox, logp_behav, adv, mask, eps=0.2, C=2.0, adaptive=True):
+    """The decoupled-PPO token objective with truncated importance weights and
+    ACR's clipping range (qurl_oracle.c, orc_acr_objective).  Inputs: [T]
+    float32 log-probabilities and advantages, [T] uint8 mask.  Returns
+    (stats float64 [6] in ACR_STATS order, term float64 [T], dterm float64 [T])."""
+    lp, lpp, lpb, a = (_c(x, np.float32) for x in (logp, logp_prox, logp_behav, adv))
+    m = _c(mask, np.uint8)
+    T = lp.size
+    assert lpp.size == lpb.size == a.size == m.size == T
+    term = np.empty(T, np.float64)
+    dterm = np.empty(T, np.float64)
+    stats = np.empty(ACR_NSTATS, np.float64)
+    _check(lib().orc_acr_objective(_p(lp), _p(lpp), _p(lpb), _p(a), _p(m), T, float(eps), float(C),
+                                   1 if adaptive else 0, _p(term), _p(dterm), _p(stats)), "acr_objective")
+    return stats, term, dterm

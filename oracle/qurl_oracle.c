@@ -19,6 +19,11 @@
  *                   preprocessing; the rollout runs INT8/FP8 matmul kernels.
  *     [NOTES/FRAME] section "方法详解 > 整体框架": step (1) quantizes theta_old
  *                   for every rollout.
+ *     [NOTES/ACR]   section "方法详解 > 关键设计 > 自适应裁剪范围 (ACR)": the
+ *                   decoupled-PPO objective of the quantized rollout, with the
+ *                   truncated importance weight min(pi_prox / pi_behav, C) and
+ *                   the clipping range [1 - eps, (1 + eps) / r]; section
+ *                   "损失函数 / 训练策略": the GRPO/DAPO decoupled variant.
  *
  * Readings where the pages are silent (symmetric absmax scaling, round to
  * nearest even, IEEE division, saturating clamp, zero rows, RMSNorm epsilon,
@@ -464,4 +469,80 @@ uint64_t orc_count_diff(const uint8_t* a, const uint8_t* b, size_t n) {
     uint64_t c = 0;
     for (size_t i = 0; i < n; ++i) c += (a[i] != b[i]);
     return c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* ACR token objective [NOTES/ACR]                                           */
+/* ------------------------------------------------------------------------ */
+
+#define ORC_ACR_NSTATS 6
+
+/* The decoupled-PPO objective of a quantized rollout over T token slots.
+ *
+ * Per valid token (mask != 0), with the three log-probabilities of the token
+ * the rollout sampled -- logp (the policy being trained, pi_theta), logp_prox
+ * (the full-precision old actor, the proximal policy pi_prox) and logp_behav
+ * (the quantized old actor that generated it, the behaviour policy) -- and its
+ * advantage A:
+ *   w     = min(pi_prox / pi_behav, C)       truncated importance weight (TIS);
+ *                                            it is the scaling factor r of ACR
+ *   R     = pi_theta / pi_prox               the clipping ratio
+ *   upper = (1 + eps) / w   (adaptive)  or  1 + eps  (plain TIS)
+ *   c     = clip(R, 1 - eps, upper) = min(max(R, 1 - eps), upper)
+ *   term  = w * min(R A, c A)
+ * and the objective is the token-level mean of term over the valid tokens
+ * (the GRPO/DAPO decoupled variant averages over all tokens of the batch).
+ *
+ * dterm = d term / d logp: w A R where the unclipped product R A is the
+ * minimum (dR / dlogp = R), 0 where the clipped constant c A is; the gradient
+ * of the objective is dterm / n.  Masked slots: term = dterm = 0.
+ *
+ * stats[0] objective (0 when n = 0)      stats[3] mean w
+ * stats[1] n, the number of valid tokens stats[4] fraction with pi_prox / pi_behav > C
+ * stats[2] fraction clipped (R A > c A)  stats[5] mean of logp_behav - logp_prox
+ * (the sample estimate of KL(pi_behav || pi_prox), tokens drawn from pi_behav).
+ * Everything in fp64 from the fp32 inputs; sums in token order.
+ * term, dterm: [T] or NULL. */
+int orc_acr_objective(const float* logp, const float* logp_prox, const float* logp_behav, const float* adv,
+                      const uint8_t* mask, int64_t T, double eps, double C, int adaptive, double* term,
+                      double* dterm, double* stats) {
+    if (T < 0 || !(eps > 0.0 && eps < 1.0) || !(C > 0.0) || !stats) return ORC_ERR_ARG;
+    double sum_term = 0.0, sum_w = 0.0, sum_kl = 0.0;
+    int64_t n = 0, clipped = 0, capped = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        double tt = 0.0, dt = 0.0;
+        if (mask[t]) {
+            const double ratio_pb = exp((double)logp_prox[t] - (double)logp_behav[t]);
+            const double w = ratio_pb < C ? ratio_pb : C;
+            const double R = exp((double)logp[t] - (double)logp_prox[t]);
+            const double lower = 1.0 - eps;
+            const double upper = adaptive ? (1.0 + eps) / w : 1.0 + eps;
+            double c = R > lower ? R : lower;
+            if (c > upper) c = upper;
+            const double A = (double)adv[t];
+            const double u = R * A, v = c * A;
+            if (u <= v) {
+                tt = w * u;
+                dt = w * A * R;
+            } else {
+                tt = w * v;
+                ++clipped;
+            }
+            ++n;
+            sum_term += tt;
+            sum_w += w;
+            capped += ratio_pb > C;
+            sum_kl += (double)logp_behav[t] - (double)logp_prox[t];
+        }
+        if (term) term[t] = tt;
+        if (dterm) dterm[t] = dt;
+    }
+    const double dn = (double)n;
+    stats[0] = n ? sum_term / dn : 0.0;
+    stats[1] = dn;
+    stats[2] = n ? (double)clipped / dn : 0.0;
+    stats[3] = n ? sum_w / dn : 0.0;
+    stats[4] = n ? (double)capped / dn : 0.0;
+    stats[5] = n ? sum_kl / dn : 0.0;
+    return ORC_OK;
 }

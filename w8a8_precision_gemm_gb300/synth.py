@@ -11,7 +11,8 @@ Distributions (the workloads of the QuRL rollout actor's projections):
   * weights W ~ N(0, 0.02) in fp32 (the training master copy);
   * RMSNorm gain gamma ~ 1 + N(0, 0.1) in fp32;
   * weight update dW ~ N(0, 1e-7) in fp32 (the size of one RL update: lr ~1e-6
-    times gradients ~0.1-1).
+    times gradients ~0.1-1);
+  * rollout token log-probabilities for the ACR objective (``rollout``).
 Standard deviations, not variances.  Generator: numpy PCG64 seeded per tensor
 from a stable name, so every run and every machine draws the same numbers.
 """
@@ -85,3 +86,31 @@ SHAPES_32B = {
     "gate_up": (5120, 55296),
     "down": (27648, 5120),
 }
+
+
+def rollout(name: str, n_seq: int, max_len: int, kl: float = 0.025, step_std: float = 0.1,
+            mean_nll: float = 0.3) -> dict:
+    """One mini-batch of quantized rollouts, token slots flattened response by
+    response ([n_seq * max_len]; slots past a response's length are padding):
+      * logp_prox:  the full-precision old actor's log-probability of each
+        sampled token, -Exponential(mean_nll) (mostly confident tokens, a tail);
+      * logp_behav: the quantized actor that sampled the tokens, logp_prox +
+        N(kl, sqrt(2 kl)) -- for a small perturbation the log-ratio of the
+        sampled token has mean KL(behav || prox) and variance 2 KL; kl = 0.025
+        is the late-training divergence the pages report (0.002 early);
+      * logp:       the policy being trained, a few updates on, logp_prox +
+        N(0, step_std);
+      * adv:        one N(0, 1) advantage per response (group-normalised
+        rewards), repeated over its tokens;
+      * mask:       1 on the first len_i slots of response i, len_i uniform in
+        [max_len / 8, max_len].
+    float32 arrays and a uint8 mask, on the CPU."""
+    g = rng(name)
+    T = n_seq * max_len
+    lpp = -g.exponential(mean_nll, size=T).astype(np.float32)
+    lpb = (lpp + g.normal(kl, np.sqrt(2.0 * kl), size=T)).astype(np.float32)
+    lp = (lpp + g.normal(0.0, step_std, size=T)).astype(np.float32)
+    adv = np.repeat(g.standard_normal(n_seq).astype(np.float32), max_len)
+    lens = g.integers(max(1, max_len // 8), max_len + 1, size=n_seq)
+    mask = (np.arange(max_len)[None, :] < lens[:, None]).astype(np.uint8).reshape(T)
+    return {"logp": lp, "logp_prox": lpp, "logp_behav": lpb, "adv": adv, "mask": mask}
