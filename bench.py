@@ -51,6 +51,11 @@ EPS = 1e-6
 PROJ = [("qkv", 3584, 4608), ("o_proj", 3584, 3584), ("gate_up", 3584, 37888), ("down", 18944, 3584)]
 DOMINANT = ("gate_up", 256)
 CLOCK_LEAD = 0.5  # s of untimed step replays right before the timed region
+# the ACR token objective timed beside the step: one mini-batch of 512 responses x 8192 token slots
+ACR_SEQ, ACR_LEN, ACR_EPS, ACR_C = 512, 8192, 0.2, 2.0
+ACR_KEYS = ("logp", "logp_prox", "logp_behav", "adv", "mask")
+ACR_PROFILE = "profiles/acr_objective_kernel_512x8192.md"
+ACR_SOURCES = ["w8a8_precision_gemm_gb300/csrc/objective.cu", "w8a8_precision_gemm_gb300/csrc/objective.h"]
 
 
 def peaks():
@@ -75,13 +80,16 @@ DOMINANT_KERNEL = {"int8": "w8a8_gemm_i8t_kernel", "fp8": "w8a8_gemm_fp8_pair_ke
 def profiled_traffic(qtype):
     """DRAM bytes per launch of the dominant kernel from its committed ncu
     summary -- only while the kernel sources still hash to the captured ones."""
+    return traffic_from_profile(DOMINANT_PROFILE.get(qtype), KERNEL_SOURCES.get(qtype, []))
+
+
+def traffic_from_profile(path, sources):
     import hashlib
 
-    path = DOMINANT_PROFILE.get(qtype)
     if not path or not os.path.exists(os.path.join(ROOT, path)):
         return None
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[qtype]:
+    for f in sources:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     fields = dict(line.split(": ", 1) for line in open(os.path.join(ROOT, path)).read().splitlines() if ": " in line
                   and line.split(": ", 1)[0] in ("kernel_sources_sha256_16", "dram_bytes_per_launch"))
@@ -367,6 +375,69 @@ def time_graph(g, reps, stream):
     return a.elapsed_time(b) / reps
 
 
+def acr_bytes(T):
+    """Algorithmic bytes of one ACR objective call per token slot: the four fp32
+    inputs and the mask byte in, the fp32 derivative out (the per-CTA partials
+    and the statistics are a few KB)."""
+    return T * (4 * 4 + 1 + 4)
+
+
+def acr_inputs(q, synth, j):
+    T = ACR_SEQ * ACR_LEN
+    r = synth.rollout(f"bench/acr/{j}", ACR_SEQ, ACR_LEN)
+    d = {k: torch.from_numpy(r[k]).cuda() for k in ACR_KEYS}
+    d["dterm"] = torch.empty(T, dtype=torch.float32, device="cuda")
+    d["stats"] = torch.empty(q.ACR_NSTATS, dtype=torch.float64, device="cuda")
+    return r, d
+
+
+def acr_call(q, d, ws):
+    q.qurl_acr_objective(d["logp"], d["logp_prox"], d["logp_behav"], d["adv"], d["mask"], ACR_EPS, ACR_C, True,
+                         None, d["dterm"], d["stats"], ws)
+
+
+def time_acr(q, synth, stream, pk, cpu_baseline):
+    """The ACR token objective on the mini-batch: a graph of R calls rotating
+    over three input sets, 88 MB each (71 MB in, 17 MB of derivatives out), so
+    the two sets touched since a set's last call (176 MB) exceed the 129 MB L2."""
+    T = ACR_SEQ * ACR_LEN
+    host, sets = zip(*(acr_inputs(q, synth, j) for j in range(3)))
+    ws = q.acr_workspace()
+    R = 21
+
+    def calls():
+        for i in range(R):
+            acr_call(q, sets[i % 3], ws)
+
+    g, nl = graph_of(calls, q)
+    g.replay()
+    us = time_graph(g, 5, stream) / R * 1e3
+    q.qurl_check_device_status()
+    gbs = acr_bytes(T) / (us * 1e-6) / 1e9
+    stats = sets[0]["stats"].cpu().tolist()
+    out = {"workload": f"{ACR_SEQ} responses x {ACR_LEN} token slots (lengths uniform in [{ACR_LEN // 8}, {ACR_LEN}]), "
+                       f"ACR, eps={ACR_EPS}, C={ACR_C}; dterm written, term not",
+           "tokens": T, "valid_tokens": int(stats[1]), "us_per_call": us, "launches_per_call": nl // R,
+           "tokens_per_s": T / (us * 1e-6),
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": traffic_from_profile(ACR_PROFILE, ACR_SOURCES),
+                        "peak_source": f"{pk['source']} HBM copy",
+                        "timing": f"CUDA events around a graph of {R} calls (one kernel a call) rotating over "
+                                  "three input sets (264 MB > L2); bytes = 21 per token slot"},
+           "stats": dict(zip(q.ACR_STATS, stats))}
+    if cpu_baseline:
+        import oracle
+
+        oracle.build()
+        r = host[0]
+        t0 = time.perf_counter()
+        oracle.acr_objective(*(r[k] for k in ACR_KEYS), eps=ACR_EPS, C=ACR_C, adaptive=True)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": T / dt, "unit": "token slots/s", "cores": 1, "kind": "oracle",
+                               "sample": f"the whole mini-batch ({T} slots) once, single-threaded C, {dt:.2f} s"}
+    return out
+
+
 def run_ours(args):
     rank, world = dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -525,6 +596,8 @@ def run_ours(args):
         del g, Wq, sw, Xq, sx, wsp, Yp
         torch.cuda.empty_cache()
     q.qurl_check_device_status()
+    # ---- the ACR token objective of the same RL step (beside the rollout's linear layers)
+    acr = time_acr(q, synth, stream, pk, rank == 0 and world == 1 and not args.no_cpu_baseline)
 
     ops = step_ops()
     nbytes = step_bytes()
@@ -565,7 +638,7 @@ def run_ours(args):
             "gpu_launches": launches_step * args.steps,
             "launches_per_step": launches_step,
             "clocks": clocks.summary(t0_wall, t1_wall, CLOCK_LEAD),
-            "per_gemm": per, "per_quant": per_quant, "prefill": prefill}
+            "per_gemm": per, "per_quant": per_quant, "prefill": prefill, "acr_objective": acr}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -587,6 +660,15 @@ def run_single(args):
     import w8a8_precision_gemm_gb300 as q
     from w8a8_precision_gemm_gb300 import synth
 
+    if args.single == "acr":
+        _, d = acr_inputs(q, synth, 0)
+        ws = q.acr_workspace()
+        for _ in range(args.single_reps):
+            acr_call(q, d, ws)
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+        print(json.dumps({"single": "acr", "tokens": ACR_SEQ * ACR_LEN, "reps": args.single_reps}))
+        return 0
     model, proj = args.single.split(":")
     K, N = (synth.SHAPES_7B if model == "7b" else synth.SHAPES_32B)[proj]
     M = args.single_m
@@ -616,7 +698,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=32, help="tokens per oracle step (reference arm / sample)")
     ap.add_argument("--cpu-full-step", action="store_true", default=True,
                     help="time the oracle on one whole step (both batches) for cpu_baseline")
-    ap.add_argument("--single", default=None, help="model:proj, e.g. 7b:gate_up -- run one linear for profiling")
+    ap.add_argument("--single", default=None,
+                    help="model:proj, e.g. 7b:gate_up -- run one linear for profiling; 'acr': the ACR objective")
     ap.add_argument("--single-m", type=int, default=256)
     ap.add_argument("--single-reps", type=int, default=3)
     args = ap.parse_args()

@@ -14,6 +14,11 @@
  *           the weights; the rollout runs INT8/FP8 matrix-multiply kernels.
  *   [FRAME] section "方法详解 > 整体框架": every RL step quantizes the current
  *           weights theta_old for the rollout.
+ *   [ACR]   section "方法详解 > 关键设计 > 自适应裁剪范围 (ACR)": the decoupled
+ *           PPO objective with the truncated weight min(pi_prox / pi_behav, C)
+ *           and the clipping range [1 - eps, (1 + eps) / r].
+ *   [OBJ]   section "损失函数 / 训练策略": the GRPO/DAPO decoupled variant, a
+ *           token-level mean.
  *
  * Conventions (all entry points):
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
@@ -231,6 +236,52 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
  */
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,
                             qurl_stream_t stream);
+
+/*
+ * ACR token objective of a quantized rollout ([ACR], [OBJ]): the decoupled-PPO
+ * objective with the truncated importance weight of TIS and ACR's adaptive
+ * clipping range, over T token slots (the responses of a mini-batch, padded
+ * slots masked out).  Per valid slot t (mask[t] != 0):
+ *   w     = min(exp(logp_prox - logp_behav), C)    truncated weight pi_prox / pi_behav (= r)
+ *   R     = exp(logp - logp_prox)                  pi_theta / pi_prox
+ *   upper = (1 + eps) / w  if adaptive,  1 + eps otherwise (plain TIS)
+ *   c     = min(max(R, 1 - eps), upper)            (the upper bound wins when below the lower)
+ *   term  = w * min(R adv, c adv)
+ *   dterm = d term / d logp = w adv R where R adv <= c adv, else 0 (clipped)
+ * fp32 arithmetic, expf, no fused multiply-adds; padded slots give 0 and their
+ * values (even NaN) are never used.  The objective is the mean term over the
+ * valid slots, so its gradient with respect to logp[t] is dterm[t] / n.
+ *
+ *   logp, logp_prox, logp_behav  [T] fp32 log-probabilities of the sampled
+ *       tokens under the policy being trained, the full-precision old actor and
+ *       the quantized actor that generated them; finite, with |differences|
+ *       below 80 (fp32 exp range).
+ *   adv   [T] fp32 advantages (a response's advantage repeated over its tokens).
+ *   mask  [T] bytes, nonzero = valid token.
+ *   eps in (0, 1); C > 0; adaptive 1 (ACR) or 0 (plain TIS clipping).
+ *   term, dterm  [T] fp32 (out) or NULL.
+ *   stats  [QURL_ACR_NSTATS] fp64 device array (out): [0] objective (0 when no
+ *       slot is valid), [1] n valid, [2] clipped fraction (R adv > c adv),
+ *       [3] mean w, [4] fraction with pi_prox / pi_behav > C, [5] mean of
+ *       logp_behav - logp_prox (the sample estimate of KL(pi_behav || pi_prox)).
+ *       Sums: fp32 per thread, fp64 across threads in a fixed order, so the
+ *       results are identical run to run.
+ *   workspace  qurl_acr_workspace_size() bytes of device scratch, 16-byte
+ *       aligned, ZERO-FILLED before its first use: its last 256 bytes hold a
+ *       counter the call's CTAs take tickets from; the last CTA resets it, so
+ *       every call leaves the workspace ready for the next one.  Calls that may
+ *       run at the same time need separate workspaces.
+ * Every pointer 16-byte aligned except stats (8).  T = 0 is valid (all stats 0;
+ * the token pointers may then be NULL).  Errors: QURL_ERR_INVALID_ARG (NULL
+ * pointer, T < 0 or >= 2^40, eps or C out of range, adaptive not 0/1),
+ * QURL_ERR_WORKSPACE (ws_bytes too small), QURL_ERR_ALIGNMENT.
+ * One kernel launch on `stream`.
+ */
+#define QURL_ACR_NSTATS 6
+size_t qurl_acr_workspace_size(void);
+qurl_status qurl_acr_objective(const float* logp, const float* logp_prox, const float* logp_behav, const float* adv,
+                               const uint8_t* mask, long long T, float eps, float C, int adaptive, float* term,
+                               float* dterm, double* stats, void* workspace, size_t ws_bytes, qurl_stream_t stream);
 
 /* Synchronise `stream`, then return and clear the device status word of the
  * current device (QURL_OK, or QURL_ERR_TIMEOUT from a kernel's bounded wait),

@@ -20,7 +20,8 @@ def test_header_declares_the_boundary():
     names = q.exported_names()
     for required in ("qurl_prepare_weights", "qurl_quant_act", "qurl_w8a8_linear", "qurl_rmsnorm_quant_linear",
                      "qurl_rmsnorm_quant", "qurl_silu_mul_quant", "qurl_w8a8_gemm_acc", "qurl_count_diff",
-                     "qurl_workspace_size", "qurl_check_device_status", "qurl_status_string", "qurl_version"):
+                     "qurl_workspace_size", "qurl_check_device_status", "qurl_status_string", "qurl_version",
+                     "qurl_acr_objective", "qurl_acr_workspace_size"):
         assert required in names
 
 
@@ -42,7 +43,7 @@ def test_status_strings_and_version(L):
     assert L.qurl_status_string(0) == b"QURL_OK"
     assert L.qurl_status_string(6) == b"QURL_ERR_TIMEOUT"
     assert L.qurl_status_string(99) == b"QURL_ERR_UNKNOWN"
-    assert L.qurl_version() == 101
+    assert L.qurl_version() == 102
 
 
 FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced: calls fail validation first
@@ -93,6 +94,26 @@ def test_other_validation(L):
     assert L.qurl_count_diff(FAKE_ODD, FAKE, 16, FAKE, None) == 3
     assert L.qurl_rmsnorm_quant_linear(FAKE, 256, FAKE, 1e-6, FAKE, FAKE, 4, 8, 256, 0, FAKE, 8, FAKE, None,
                                        None, 0, None) == 1
+
+
+def test_acr_objective_validation(L):
+    ws = L.qurl_acr_workspace_size()
+    assert ws >= 1024 * 64
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    acr = L.qurl_acr_objective
+    assert acr(*ok, 100, 0.2, 2.0, 1, None, FAKE, None, FAKE, ws, None) == 1      # stats NULL
+    assert acr(*ok, 100, 0.2, 2.0, 1, None, FAKE, FAKE, None, ws, None) == 1      # workspace NULL
+    assert acr(None, *ok[1:], 100, 0.2, 2.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 1  # logp NULL, T > 0
+    assert acr(*ok, -1, 0.2, 2.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 1       # T < 0
+    assert acr(*ok, 100, 0.0, 2.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 1      # eps out of (0, 1)
+    assert acr(*ok, 100, 1.0, 2.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 1
+    assert acr(*ok, 100, 0.2, 0.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 1      # C <= 0
+    assert acr(*ok, 100, 0.2, float("nan"), 1, None, FAKE, FAKE, FAKE, ws, None) == 1
+    assert acr(*ok, 100, 0.2, 2.0, 2, None, FAKE, FAKE, FAKE, ws, None) == 1      # adaptive not 0 / 1
+    assert acr(*ok, 100, 0.2, 2.0, 1, None, FAKE, FAKE, FAKE, ws - 1, None) == 4  # workspace too small
+    assert acr(FAKE_ODD, *ok[1:], 100, 0.2, 2.0, 1, None, FAKE, FAKE, FAKE, ws, None) == 3
+    assert acr(*ok, 100, 0.2, 2.0, 1, FAKE_ODD, FAKE, FAKE, FAKE, ws, None) == 3  # term misaligned
+    assert acr(*ok, 100, 0.2, 2.0, 1, None, FAKE, ctypes.c_void_p(0x10004), FAKE, ws, None) == 3  # stats % 8
 
 
 def test_workspace_size_without_gpu(L):

@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
+            "qurl_acr_objective": [P, P, P, P, P, ctypes.c_longlong, f, f, i, P, P, P, P, z, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.qurl_workspace_size.argtypes = [i, i, i, i]
         L.qurl_workspace_size.restype = ctypes.c_size_t
+        L.qurl_acr_workspace_size.argtypes = []
+        L.qurl_acr_workspace_size.restype = ctypes.c_size_t
         L.qurl_status_string.argtypes = [ctypes.c_int]
         L.qurl_status_string.restype = ctypes.c_char_p
         L.qurl_version.argtypes = []
@@ -232,6 +235,24 @@ def qurl_count_diff(a, b, count, stream=None):
     _ok(load().qurl_count_diff(_ptr(a), _ptr(b), n, _ptr(count), _stream(stream)), "qurl_count_diff")
 
 
+def qurl_acr_objective(logp, logp_prox, logp_behav, adv, mask, eps, C, adaptive, term, dterm, stats, workspace,
+                       stream=None):
+    ins = (logp, logp_prox, logp_behav, adv)
+    _dense(*ins, mask, term, dterm, stats, workspace)
+    T = logp.numel()
+    for t in ins + tuple(x for x in (term, dterm) if x is not None):
+        if t.dtype != torch.float32 or t.numel() != T:
+            raise ValueError("log-probabilities, advantages, term and dterm are fp32 [T]")
+    if mask.dtype not in (torch.uint8, torch.bool) or mask.numel() != T:
+        raise ValueError("mask is uint8 / bool [T]")
+    if stats.dtype != torch.float64 or stats.numel() < ACR_NSTATS:
+        raise ValueError("stats is fp64 [6]")
+    _ok(load().qurl_acr_objective(*(_ptr(t) for t in ins), _ptr(mask), T, float(eps), float(C), 1 if adaptive else 0,
+                                  _ptr(term), _ptr(dterm), _ptr(stats), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+        "qurl_acr_objective")
+
+
 def qurl_check_device_status(stream=None):
     _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
 
@@ -329,3 +350,29 @@ def count_diff(a, b, stream=None) -> torch.Tensor:
     c = torch.empty(1, dtype=torch.int64, device=a.device)
     qurl_count_diff(a, b, c, stream)
     return c
+
+
+# ---------------------------------------------------------------- ACR objective
+
+ACR_NSTATS = 6
+ACR_STATS = ("objective", "n_valid", "clipped_frac", "mean_tis_weight", "capped_frac", "kl_behav_prox")
+
+
+def acr_workspace(device="cuda") -> torch.Tensor:
+    """Scratch for qurl_acr_objective: zero-filled once (its ticket counter),
+    left ready for reuse by every call."""
+    return torch.zeros(int(load().qurl_acr_workspace_size()), dtype=torch.uint8, device=device)
+
+
+def acr_objective(logp, logp_prox, logp_behav, adv, mask, eps=0.2, C=2.0, adaptive=True, want_term=False,
+                  want_dterm=True, workspace=None, stream=None):
+    """The ACR token objective (qurl_acr_objective).  Returns (stats fp64 [6] in
+    ACR_STATS order, dterm fp32 [T] or None, term fp32 [T] or None)."""
+    dev = logp.device
+    T = logp.numel()
+    stats = torch.empty(ACR_NSTATS, dtype=torch.float64, device=dev)
+    dterm = torch.empty(T, dtype=torch.float32, device=dev) if want_dterm else None
+    term = torch.empty(T, dtype=torch.float32, device=dev) if want_term else None
+    ws = acr_workspace(dev) if workspace is None else workspace
+    qurl_acr_objective(logp, logp_prox, logp_behav, adv, mask, eps, C, adaptive, term, dterm, stats, ws, stream)
+    return stats, dterm, term

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "objective.h"
 #include "qurl.h"
 
 namespace qurl {
@@ -318,7 +319,7 @@ const char* qurl_status_string(qurl_status s) {
   return "QURL_ERR_UNKNOWN";
 }
 
-int qurl_version(void) { return 101; }
+int qurl_version(void) { return 102; }
 
 unsigned long long qurl_kernel_launches(void) { return qurl::g_kernel_launches.load(); }
 
@@ -518,6 +519,27 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_count_diff(a, b, n, count, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+size_t qurl_acr_workspace_size(void) { return qurl::kAcrWorkspaceBytes; }
+
+qurl_status qurl_acr_objective(const float* logp, const float* logp_prox, const float* logp_behav, const float* adv,
+                               const uint8_t* mask, long long T, float eps, float C, int adaptive, float* term,
+                               float* dterm, double* stats, void* workspace, size_t ws_bytes, qurl_stream_t stream) {
+  if (!stats || !workspace || T < 0 || T >= (1LL << 40)) return QURL_ERR_INVALID_ARG;
+  if (T > 0 && (!logp || !logp_prox || !logp_behav || !adv || !mask)) return QURL_ERR_INVALID_ARG;
+  if (!(eps > 0.f && eps < 1.f) || !(C > 0.f && C <= 3.0e38f) || (adaptive != 0 && adaptive != 1))
+    return QURL_ERR_INVALID_ARG;
+  if (ws_bytes < qurl::kAcrWorkspaceBytes) return QURL_ERR_WORKSPACE;
+  if (!aligned16(logp) || !aligned16(logp_prox) || !aligned16(logp_behav) || !aligned16(adv) || !aligned16(mask) ||
+      (term && !aligned16(term)) || (dterm && !aligned16(dterm)) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(stats) & 7u) != 0)
+    return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_acr_objective(logp, logp_prox, logp_behav, adv, mask, T, eps, C, adaptive, term, dterm, stats,
+                                       workspace, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
 
