@@ -2,7 +2,9 @@
 public header declares, and rejects bad arguments on the host before any launch
 (no compute call is made here)."""
 import ctypes
+import os
 import re
+import subprocess
 
 import pytest
 
@@ -29,6 +31,28 @@ def test_every_declared_symbol_is_exported(L):
     for name in q.exported_names():
         assert hasattr(L, name), name
         assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_plain_c_client_compiles_links_and_calls(L, tmp_path):
+    """The header is strict C99 and a C program links libqurl and calls the
+    entry points that need no device (version, sizes, status strings, and an
+    argument error returned before any launch)."""
+    src = tmp_path / "client.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "qurl.h"\n'
+        "int main(void) {\n"
+        "  const int v = qurl_version();\n"
+        "  const size_t ws = qurl_acr_workspace_size();\n"
+        "  const qurl_status e = qurl_quant_act(0, 4, 256, 256, 1.0f, QURL_INT8, 0, 0, 0);\n"
+        '  printf("%d %zu %s %d\\n", v, ws, qurl_status_string(e), (int)e);\n'
+        "  return (v > 0 && ws > 0 && e == QURL_ERR_INVALID_ARG) ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_build.LIB)
+    subprocess.run(["cc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(q.HEADER),
+                    str(src), "-L", libdir, "-lqurl", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out == [str(L.qurl_version()), str(L.qurl_acr_workspace_size()), "QURL_ERR_INVALID_ARG", "1"]
 
 
 def test_header_entry_points_are_extern_c():
