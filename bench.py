@@ -644,7 +644,7 @@ def run_ours(args):
         import oracle
 
         oracle.build()
-        counts = list(M_LIST) if args.cpu_full_step else [args.ref_tokens]
+        counts = [args.ref_tokens] if args.cpu_sample else list(M_LIST)
         ops_s, dt, cores = cpu_oracle_time(synth, oracle, W, gammas, counts)
         line["cpu_baseline"] = {"value": ops_s / dt / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
                                 "sample": f"oracle chain (all four projections, full N and K) on batches of "
@@ -696,8 +696,8 @@ def main():
     ap.add_argument("--qtype", choices=["int8", "fp8"], default="int8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=32, help="tokens per oracle step (reference arm / sample)")
-    ap.add_argument("--cpu-full-step", action="store_true", default=True,
-                    help="time the oracle on one whole step (both batches) for cpu_baseline")
+    ap.add_argument("--cpu-sample", action="store_true",
+                    help="time the oracle for cpu_baseline on --ref-tokens tokens instead of one whole step")
     ap.add_argument("--single", default=None,
                     help="model:proj, e.g. 7b:gate_up -- run one linear for profiling; 'acr': the ACR objective")
     ap.add_argument("--single-m", type=int, default=256)
