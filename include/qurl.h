@@ -64,7 +64,8 @@ typedef enum {
     QURL_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, unknown enum, bad stride */
     QURL_ERR_UNSUPPORTED = 2, /* shape the kernels do not cover (e.g. K % 16 != 0) */
     QURL_ERR_ALIGNMENT = 3,   /* pointer or row stride not 16-byte aligned */
-    QURL_ERR_WORKSPACE = 4,   /* the shape needs more scratch than qurl_w8a8_linear_static_scratch holds */
+    QURL_ERR_WORKSPACE = 4,   /* scratch too small: the workspace given to qurl_acr_objective, or the
+                                 buffer built into qurl_w8a8_linear_static_scratch for this shape */
     QURL_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed */
     QURL_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out */
 } qurl_status;
@@ -180,10 +181,17 @@ qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, co
  *   - Limit: a shape whose qurl_workspace_size exceeds 32 MiB (33,554,432
  *     bytes) returns QURL_ERR_WORKSPACE and launches nothing (every 7B / 32B
  *     decode projection up to M = 256 fits).
- *   - The buffer is held by every GPU on which this entry point is used, until
- *     the process exits.  Its device address is looked up (cudaGetSymbolAddress)
- *     on the first call made with that device current, so make that first call
- *     before any stream capture.
+ *   - The buffer lives in a CUDA module of its own.  Under the CUDA runtime's
+ *     default lazy module loading, a device commits its 32 MiB on the first
+ *     call of this entry point made with that device current (the call looks
+ *     the buffer's device address up with cudaGetSymbolAddress, which loads
+ *     the module) and holds them until the process exits; devices on which
+ *     only other entry points are called do not hold it.  Under
+ *     CUDA_MODULE_LOADING=EAGER the module is loaded, on every device the
+ *     library is used on, when the library's first call binds that device's
+ *     context.  A caller that reserves the rest of HBM for its own pools
+ *     should therefore make one call of this entry point on each device
+ *     before reserving, and make that first call before any stream capture.
  *   - All calls on a device share the buffer, and it keeps what the last call
  *     left there (nothing in it needs to start at zero).  Calls whose kernels
  *     overlap on the GPU -- e.g. issued on two streams without ordering between

@@ -193,8 +193,11 @@ qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
 // Workspace layout (see plan_gemm): [fp16 copy of the activation codes (INT8
 // decode)][split-K partials].
 //   x16_ready: the fp16 copy is already there (a fused quantizer wrote it);
-//   w_indep:   the kernel launched just before the GEMM does not write Wq, so
-//              the GEMM may load weights before that kernel ends.
+//   w_indep:   the kernel launched just before the GEMM is one of this
+//              library's quantizers (or the widening kernel): it does not write
+//              Wq and lets the GEMM launch only after its own wait, so every
+//              earlier kernel has completed and the GEMM may load weights
+//              before that kernel ends.
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
                      bool x16_ready = false, bool w_indep = false) {
@@ -252,59 +255,9 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   return QURL_OK;
 }
 
-// ------------------------------------------------------------------ library-owned scratch
-
-// Scratch memory of qurl_w8a8_linear_static_scratch.  It is part of the
-// library's device image: every GPU on which the library is used holds these
-// bytes until the process exits, and every call of that entry point on a
-// device shares them.  On the host, g_static_scratch only names the variable;
-// its device address is looked up per device with cudaGetSymbolAddress.
-constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
-static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
-void* g_static_scratch_dev[kMaxDevices] = {};
-
-// Device address of the static scratch on the current device, looked up on the
-// first call made with that device current.
-qurl_status static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return QURL_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_static_scratch_dev[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || p == nullptr) return cuda_fail(e);
-    g_static_scratch_dev[dev] = p;
-  }
-  *out = g_static_scratch_dev[dev];
-  return QURL_OK;
-}
-
 }  // namespace
 
 extern "C" {
-
-qurl_status qurl_w8a8_linear_static_scratch(const void* Xq, const float* sx, const void* Wq, const float* sw,
-                                            int M, int N, int K, qurl_qtype qt, void* Y, int ldy,
-                                            qurl_stream_t stream) {
-  QURL_TRY(check_gemm(Xq, Wq, M, N, K, qt, nullptr, 0));
-  if (!sx || !sw || !Y || ldy < N) return QURL_ERR_INVALID_ARG;
-  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
-  DevState* dev = nullptr;
-  QURL_TRY(device_state(&dev));
-  // the scratch this shape uses at full speed must fit the static buffer
-  const size_t need = qurl::plan_gemm(M, N, K, qt, dev->num_sms, static_cast<size_t>(-1)).ws_bytes;
-  if (need > kStaticScratchBytes) return QURL_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  QURL_TRY(static_scratch(&scratch));
-  // nothing in the scratch has to start at zero: every byte the kernels read
-  // there (fp16 activation codes, split-K partial sums) is written earlier in
-  // the same call
-  return run_gemm(Xq, sx, Wq, sw, M, N, K, qt, Y, ldy, nullptr, scratch, kStaticScratchBytes,
-                  reinterpret_cast<cudaStream_t>(stream));
-}
-
 
 const char* qurl_status_string(qurl_status s) {
   switch (s) {

@@ -617,8 +617,8 @@ template <typename T>
 __global__ void splitk_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
                                      const float* __restrict__ sx, const float* __restrict__ sw,
                                      __nv_bfloat16* __restrict__ Y, long long ldy, T* __restrict__ acc_out) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const size_t total = static_cast<size_t>(M) * N;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   const bool vec = (N & 3) == 0;

@@ -961,8 +961,8 @@ __global__ void __launch_bounds__(512, 1)
 // kSumCap) for the GEMM's accumulation mode.
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                                         int K, const CodeSums sums) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ unsigned long long cnt[kMaxSums];
   for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x) cnt[j] = 0;
   __syncthreads();

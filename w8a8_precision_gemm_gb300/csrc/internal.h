@@ -36,8 +36,9 @@ struct GemmArgs {
   long long ldy;
   void* part;        // [splits][M][N] int32 (INT8) or fp32 (FP8), mode kModeAcc
   int* status;       // device status word
-  int w_prefetch;    // the previous kernel in the stream does not write Wq: its first
-                     // stages may be loaded before waiting for that kernel
+  int w_prefetch;    // the previous kernel in the stream does not write Wq and triggers
+                     // its dependents only after its own wait (so every earlier kernel has
+                     // completed): the first stages may be loaded before waiting for it
   void* acc_out;       // raw-accumulator output [M, N] (unused by the kernels; kept with the call)
   int fault;           // test hook: 1 = the producer skips its first k-block, so the consumer's
                        // bounded wait runs out and the kernel latches a timeout
@@ -63,6 +64,15 @@ extern std::atomic<unsigned long long> g_kernel_launches;
 // calls griddepcontrol.wait before it reads anything the previous kernel may
 // have written (weights excepted where the caller says they are not written
 // there, see GemmArgs::w_prefetch).
+//
+// Who may start early.  The GEMMs allow their dependents to launch right after
+// their prologue.  Every other kernel (quantizers, widening, reductions, weight
+// preparation, the objective) allows it only after its own griddepcontrol.wait
+// has returned, i.e. once the kernel before it has completed.  A GEMM that
+// loads weight tiles before its own wait (w_prefetch) follows one of those
+// kernels, so its launch implies that every kernel two or more places earlier
+// in the stream -- e.g. a qurl_prepare_weights that rewrote Wq -- has completed
+// and its writes are visible.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {

@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(kObjThreads, kObjCtasPerSm)
                          const float* __restrict__ adv, const uint8_t* __restrict__ mask, long long T, float eps,
                          float C, int adaptive, float* __restrict__ term_out, float* __restrict__ dterm_out,
                          double* __restrict__ partials, unsigned int* __restrict__ ticket, double* __restrict__ stats) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const bool ad = adaptive != 0;
   const int tid = threadIdx.x;
   ObjAcc acc;

@@ -259,8 +259,8 @@ __device__ __forceinline__ void fill_cache(const uint4* row, int nvec, uint4 (&c
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
                                  uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16,
                                  const CodeSums sums) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[33];
   __shared__ unsigned long long cnt[kMaxSums];
   sums_begin(cnt, sums);
@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
                                      float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16,
                                      const CodeSums sums) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[66];
   __shared__ unsigned long long cnt[kMaxSums];
   sums_begin(cnt, sums);
@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kRowThreads, MINB) silu_mul_quant_kernel(const
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
                                       float* __restrict__ h_out, uint8_t* __restrict__ x16,
                                       const CodeSums sums) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[33];
   __shared__ unsigned long long cnt[kMaxSums];
   sums_begin(cnt, sums);
@@ -465,8 +465,8 @@ __device__ __forceinline__ void load_w8(const void* row, int idx, float (&w)[8])
 template <bool kF32>
 __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void* __restrict__ W, int K, long long ldw, float s, int qt,
                                        uint8_t* __restrict__ Wq, float* __restrict__ sw, float* W_scaled) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[33];
   const int n = blockIdx.x;
   const char* row = reinterpret_cast<const char*>(W) + static_cast<size_t>(n) * ldw * (kF32 ? 4 : 2);
@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
 }
 
 __global__ void fold_gamma_kernel(const float* __restrict__ gamma, int K, float s, float* __restrict__ out) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k < K) out[k] = __fmul_rn(gamma[k], s);
 }
@@ -517,8 +517,8 @@ __device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
 
 __global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b, size_t n,
                                   unsigned long long* __restrict__ count) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const size_t nv = n >> 4;
   const uint4* a4 = reinterpret_cast<const uint4*>(a);
   const uint4* b4 = reinterpret_cast<const uint4*>(b);
