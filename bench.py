@@ -70,13 +70,13 @@ ACR_SOURCES = [_CSRC + "objective.cu", _CSRC + "objective.h"]
 # committed ncu summaries of the GEMM kernels, keyed by the kernel's name; a summary's DRAM traffic is
 # used only while the kernel's sources hash to the ones it was captured from
 GEMM_PROFILES = {
-    "w8a8_gemm_i8p_kernel": ("profiles/w8a8_gemm_i8p_kernel_32b_gate_up_int8.md",
-                             [_CSRC + f for f in ("gemm.cuh", "gemm_i8t.cu", "ptx.cuh", "internal.h")]),
+    "w8a8_gemm_i8w_kernel": ("profiles/w8a8_gemm_i8w_kernel_32b_gate_up_int8.md",
+                             [_CSRC + f for f in ("gemm.cuh", "gemm_i8w.cu", "ptx.cuh", "internal.h")]),
     "w8a8_gemm_fp8_pair_kernel": ("profiles/w8a8_gemm_fp8_pair_kernel_32b_gate_up_fp8.md",
                                   [_CSRC + f for f in ("gemm.cuh", "gemm_fp8p.cu", "ptx.cuh", "internal.h")]),
 }
 KERNEL_NAMES = {0: "w8a8_gemm_kernel", 1: "w8a8_gemm_i8t_kernel", 2: "w8a8_gemm_i8p_kernel",
-                3: "w8a8_gemm_fp8_pair_kernel"}
+                3: "w8a8_gemm_fp8_pair_kernel", 4: "w8a8_gemm_i8w_kernel"}
 
 
 def peaks():
@@ -587,6 +587,72 @@ def time_acr(q, stream, pk, cpu_baseline):
     return out
 
 
+def time_kv_cache(q, stream, pk, l2):
+    """FP8 key/value cache quantization of the 32B-class qkv output at M = 8192
+    tokens (8 KV heads of 128) into a paged cache through a shuffled slot
+    mapping; a graph of calls rotating over enough qkv outputs that the key and
+    value columns read exceed 2 x L2.  Bytes per token: the keys and values in
+    (bf16), their codes and fp32 scales out, the slot index."""
+    model, M = "32b", 8192
+    hid = MODELS[model]["hidden"]
+    kvh, hd = 8, 128
+    N = MODELS[model]["shapes"]["qkv"][1]
+    per_token = 2 * kvh * hd * 2 + 2 * kvh * hd + 2 * kvh * 4 + 8
+    k = min(n_sets(M * 2 * kvh * hd * 2, l2), 16)
+    base = synth.activations("bench/kv/qkv", M, N).cuda()
+    ins = [torch.roll(base, i * 13, 0).contiguous() for i in range(k)]
+    S = 2 * M
+    slots = torch.from_numpy(np.random.Generator(np.random.PCG64(5)).permutation(S)[:M].astype(np.int64)).cuda()
+    caches = q.kv_cache(S, kvh, hd)
+    R = max(k, 8)
+
+    def calls():
+        for r in range(R):
+            q.qurl_kv_cache_quant(ins[r % k], hid, kvh, hd, slots, *caches)
+
+    g, nl = graph_of(calls, q)
+    g.replay()
+    us = time_graph(g, 5, stream) / R * 1e3
+    q.qurl_check_device_status()
+    nb = per_token * M
+    return {"workload": f"32B-class qkv output, M = {M} tokens, {kvh} KV heads of {hd}, per-token-per-head FP8 "
+                        "scales, paged cache through a shuffled slot mapping",
+            "us_per_call": us, "tokens_per_s": M / (us * 1e-6), "launches_per_call": nl // R,
+            "roofline": {"bound": "hbm", "achieved": nb / (us * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": nb / (pk["hbm_gbs"] * 1e9) / (us * 1e-6),
+                         "timing": f"CUDA events around a graph of {R} calls rotating over {k} inputs"}}
+
+
+def time_tensor_routes(q, stream, pk):
+    """The rate of each tensor route an 8-bit product can take on this GPU, from
+    the library's probe kernels (fixed instruction counts on zero operands),
+    timed with CUDA events: which route INT8 should take, and what its roofline
+    divides by."""
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    routes = {0: ("mma.sync.m16n8k32 s8*s8->s32 (warp MMA)", 4 * nsm, 20000),
+              1: ("tcgen05.mma kind::f16 fp16*fp16->fp32, M128 N256 K16, operands in shared memory", nsm, 20000),
+              2: ("tcgen05.mma kind::f16, A in tensor memory", nsm, 20000),
+              3: ("tcgen05.mma kind::f8f6f4 e4m3*e4m3->fp32, M128 N256 K32", nsm, 20000)}
+    out = {}
+    for r, (name, ctas, iters) in routes.items():
+        q.qurl_debug_mma_probe(r, ctas, 100, stream)  # warm (module load, TMEM)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ops = q.qurl_debug_mma_probe(r, ctas, iters, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        out[f"route{r}"] = {"instruction": name, "ctas": ctas, "TOPS": ops / (ms * 1e-3) / 1e12,
+                            "frac_of_bf16_peak": ops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+    q.qurl_check_device_status()
+    best = max(("route0", "route1", "route2"), key=lambda k: out[k]["TOPS"])
+    out["int8_best"] = best
+    out["note"] = ("INT8 codes are exact in fp16, so route 1/2 multiply them exactly; the INT8 roofline divides by "
+                   "the measured bf16 (= fp16) dense rate")
+    return out
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 
 def oracle_chain(oracle, oq, prepared, hid, X_bits, nthreads):
@@ -835,6 +901,8 @@ def run_ours(args):
 
     # ---- the ACR token objective of the same RL step (beside the rollout's linear layers)
     acr = time_acr(q, stream, pk, rank == 0 and world == 1 and not args.no_cpu_baseline)
+    routes = time_tensor_routes(q, stream, pk)
+    kv = time_kv_cache(q, stream, pk, l2)
 
     value = ops * world / (ms_step * 1e-3) / 1e12
     step_bytes = sum(alg_bytes(M, K, N) for qtype, M in passes for _, K, N in chain_shapes(model))
@@ -856,7 +924,7 @@ def run_ours(args):
             "clocks": clocks.summary(t0_wall, t1_wall, CLOCK_LEAD),
             "per_gemm": per_gemm, "per_quant": per_quant,
             "decode_7b": decode_7b, "chain_7b": chain_7b, "weight_requant": requant,
-            "acr_objective": acr}
+            "acr_objective": acr, "tensor_routes": routes, "kv_cache_fp8": kv}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

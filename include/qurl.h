@@ -19,6 +19,9 @@
  *           and the clipping range [1 - eps, (1 + eps) / r].
  *   [OBJ]   section "损失函数 / 训练策略": the GRPO/DAPO decoupled variant, a
  *           token-level mean.
+ *   [LIMITS] section "局限与展望": FP8 KV-cache quantization is not yet
+ *           optimized in the rollout engine (page 5's FP8-RL entry quantizes
+ *           the KV cache to FP8).
  *
  * Conventions (all entry points):
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
@@ -179,8 +182,9 @@ qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, co
  * callers that have no handle on the application's allocator.
  *
  *   - Limit: a shape whose qurl_workspace_size exceeds 32 MiB (33,554,432
- *     bytes) returns QURL_ERR_WORKSPACE and launches nothing (every 7B / 32B
- *     decode projection up to M = 256 fits).
+ *     bytes) returns QURL_ERR_WORKSPACE and launches nothing.  Every 7B-class
+ *     decode projection up to M = 256 fits, and every 32B-class one but the
+ *     INT8 down projection (K = 27648) at M = 256.
  *   - The buffer lives in a CUDA module of its own.  Under the CUDA runtime's
  *     default lazy module loading, a device commits its 32 MiB on the first
  *     call of this entry point made with that device current (the call looks
@@ -246,6 +250,40 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
                             qurl_stream_t stream);
 
 /*
+ * FP8 key/value cache quantization ([LIMITS]: section "局限与展望" names FP8
+ * KV-cache quantization as not yet optimized in the rollout engine; page 5's
+ * FP8-RL entry quantizes the KV cache to FP8 beside its W8A8 layers).  The
+ * granularity is this library's reading: the per-token rule applied to each
+ * attention head.  For token m and KV head h of the fused qkv output
+ *   key   = qkv[m, q_dim + h hd .. + hd),   value = qkv[m, q_dim + kv hd + h hd .. + hd)
+ * (hd = head_dim, kv = kv_heads), each vector is quantized as one row:
+ *   scale = max|x| / 448 (1 for an all-zero vector), code = e4m3_RNE_satfinite(x / scale)
+ * and stored in slot s = slot_mapping[m] of the caches:
+ *   k_cache[s][h][0 .. hd) bytes, k_scale[s][h] fp32 (likewise v_cache, v_scale).
+ * Slots are the flattened (block, offset) positions of a paged cache, so the
+ * caches are [num_slots, kv_heads, head_dim] bytes and [num_slots, kv_heads]
+ * fp32.  A negative slot (a padding token) writes nothing.  Slots are read on
+ * the device: one >= num_slots writes nothing and latches QURL_ERR_INVALID_ARG
+ * in the device status word (qurl_check_device_status).
+ *   qkv [M, ldq] bf16 (ldq >= q_dim + 2 kv hd, a multiple of 8); slot_mapping
+ *   [M] int64; head_dim a multiple of 16, at most 256; q_dim a multiple of 8.
+ * M = 0 is valid (nothing launched).  One kernel launch.
+ */
+qurl_status qurl_kv_cache_quant(const void* qkv, int M, int ldq, int q_dim, int kv_heads, int head_dim,
+                                const int64_t* slot_mapping, long long num_slots, void* k_cache, float* k_scale,
+                                void* v_cache, float* v_scale, qurl_stream_t stream);
+
+/*
+ * Read-back of an FP8 cache (the values an attention kernel consumes):
+ *   out[i][h hd + d] = bf16_RNE(fp32(e4m3 value of cache[slots[i]][h][d]) * scale[slots[i]][h])
+ * out [n, kv_heads * head_dim] bf16.  A slot outside [0, num_slots) writes
+ * nothing for that row and latches QURL_ERR_INVALID_ARG in the device status
+ * word.  n = 0 is valid.
+ */
+qurl_status qurl_kv_cache_dequant(const void* cache, const float* scale, const int64_t* slots, int n, int kv_heads,
+                                  int head_dim, long long num_slots, void* out, qurl_stream_t stream);
+
+/*
  * ACR token objective of a quantized rollout ([ACR], [OBJ]): the decoupled-PPO
  * objective with the truncated importance weight of TIS and ACR's adaptive
  * clipping range, over T token slots (the responses of a mini-batch, padded
@@ -295,8 +333,9 @@ qurl_status qurl_acr_objective(const float* logp, const float* logp_prox, const 
                                float* dterm, double* stats, void* workspace, size_t ws_bytes, qurl_stream_t stream);
 
 /* Synchronise `stream`, then return and clear the device status word of the
- * current device (QURL_OK, or QURL_ERR_TIMEOUT from a kernel's bounded wait),
- * or QURL_ERR_CUDA if the synchronisation itself failed. */
+ * current device (QURL_OK, QURL_ERR_TIMEOUT from a kernel's bounded wait, or
+ * QURL_ERR_INVALID_ARG from an index a kernel found out of range), or
+ * QURL_ERR_CUDA if the synchronisation itself failed. */
 qurl_status qurl_check_device_status(qurl_stream_t stream);
 
 /* Fault injection, for testing the failure path: the next GEMM this process
@@ -319,6 +358,23 @@ qurl_status qurl_debug_inject_timeout(void);
  * k-blocks per split, workspace bytes the plan uses.  QURL_ERR_INVALID_ARG
  * for a null `out`, a non-positive size or SM count, or an unknown qt. */
 qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, long long* out);
+
+/* Tensor-rate probe (not a computation of the method: it measures the
+ * denominators of the roofline).  Launches, asynchronously on `stream`, a
+ * kernel that issues `iters` multiply-accumulate instructions of one kind on
+ * zero operands and nothing else; *ops receives the operations (2 x
+ * multiply-adds) the launch performs, so that timing the launch with CUDA
+ * events gives the instruction's rate on this GPU.
+ *   route 0: mma.sync.m16n8k32 s8 x s8 -> s32 (warp-level integer MMA), 8 warps
+ *            per CTA, four independent accumulator chains per warp;
+ *   route 1: tcgen05.mma kind::f16 (fp16 x fp16 -> fp32, M 128, N 256, K 16),
+ *            operands in shared memory -- the INT8 GEMMs' route, codes widened
+ *            to fp16;
+ *   route 2: the same with the A operand in tensor memory;
+ *   route 3: tcgen05.mma kind::f8f6f4 (e4m3 x e4m3 -> fp32, M 128, N 256, K 32).
+ * ctas in [1, 4096] (routes 1-3: at most the SM count, one CTA per SM), iters
+ * in [1, 2^24].  QURL_ERR_INVALID_ARG otherwise. */
+qurl_status qurl_debug_mma_probe(int route, int ctas, int iters, double* ops, qurl_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* qurl_status_string(qurl_status s);

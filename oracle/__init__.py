@@ -82,8 +82,11 @@ def lib():
             L.orc_count_diff.argtypes = [P, P, z]
             L.orc_acr_objective.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_double, ctypes.c_double, i,
                                             P, P, P]
+            L.orc_kv_cache_quant.argtypes = [P, i, i, i, i, i, P, P, P, P, P]
+            L.orc_kv_cache_dequant.argtypes = [P, P, P, i, i, i, P]
             for name in ("orc_quant_rows_f32", "orc_quant_act", "orc_prepare_weights", "orc_rmsnorm_quant",
-                         "orc_silu_mul_quant", "orc_gemm_i8", "orc_gemm_fp8", "orc_acr_objective"):
+                         "orc_silu_mul_quant", "orc_gemm_i8", "orc_gemm_fp8", "orc_acr_objective",
+                         "orc_kv_cache_quant", "orc_kv_cache_dequant"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -205,6 +208,31 @@ def silu_mul_quant(GU_bits, qtype, pre_scale=1.0, h_given=None):
     _check(lib().orc_silu_mul_quant(_p(GU), M, I, I2, float(pre_scale), _p(hg), qtype, _p(q), _p(s), _p(h)),
            "silu_mul_quant")
     return q, s, h
+
+
+def kv_cache_quant(QKV_bits, q_dim, kv_heads, head_dim, slot_mapping, caches):
+    """FP8 quantization of the keys and values of the qkv output QKV (uint16
+    bf16 bits [M, >= q_dim + 2 kv_heads head_dim]) per token and head, into
+    slot slot_mapping[m] of the caches (kc u8 [S, kv_heads, head_dim], ks f32
+    [S, kv_heads], vc, vs), which are updated in place; negative slots skip."""
+    X = _c(QKV_bits, np.uint16)
+    M, ldq = X.shape
+    slots = _c(slot_mapping, np.int64)
+    kc, ks, vc, vs = caches
+    for a in caches:
+        assert a.flags["C_CONTIGUOUS"]
+    _check(lib().orc_kv_cache_quant(_p(X), M, ldq, q_dim, kv_heads, head_dim, _p(slots), _p(kc), _p(ks), _p(vc),
+                                    _p(vs)), "kv_cache_quant")
+    return caches
+
+
+def kv_cache_dequant(cache, scale, slots, kv_heads, head_dim):
+    """bf16 bits [n, kv_heads * head_dim] of the cached values of the given slots."""
+    s = _c(slots, np.int64)
+    out = np.empty((s.size, kv_heads * head_dim), np.uint16)
+    _check(lib().orc_kv_cache_dequant(_p(_c(cache, np.uint8)), _p(_c(scale, np.float32)), _p(s), s.size, kv_heads,
+                                      head_dim, _p(out)), "kv_cache_dequant")
+    return out
 
 
 def gemm_i8(Xq, Wq, nthreads=1):

@@ -19,6 +19,9 @@
  *                   preprocessing; the rollout runs INT8/FP8 matmul kernels.
  *     [NOTES/FRAME] section "方法详解 > 整体框架": step (1) quantizes theta_old
  *                   for every rollout.
+ *     [NOTES/LIMITS] section "局限与展望": FP8 KV-cache quantization is named
+ *                   as not yet optimized in the rollout engine (with page 5's
+ *                   FP8-RL entry, which quantizes the KV cache to FP8).
  *     [NOTES/ACR]   section "方法详解 > 关键设计 > 自适应裁剪范围 (ACR)": the
  *                   decoupled-PPO objective of the quantized rollout, with the
  *                   truncated importance weight min(pi_prox / pi_behav, C) and
@@ -338,6 +341,73 @@ int orc_silu_mul_quant(const uint16_t* GU, int M, int I, int ldgu, float pre_sca
         quant_row(v, I, qtype, Xq + (size_t)m * I, sx + m);
     }
     free(v);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 key/value cache quantization [NOTES/LIMITS]                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [NOTES/LIMITS] section "局限与展望" names FP8 quantization of the KV cache
+ * as what the rollout engine does not yet do well, and the FP8-RL entry of the
+ * related-work list (page 5) quantizes the KV cache to FP8 beside its W8A8
+ * layers.  Neither fixes the granularity; the reading taken here is the
+ * method's per-token rule applied to each attention head.
+ *
+ * QKV[M, ldq] bf16 holds, per token, the query (q_dim columns), then the keys
+ * and then the values of kv_heads heads of head_dim columns each (the fused
+ * qkv projection's output).  For token m and head h, the key vector
+ * k = QKV[m, q_dim + h hd .. + hd) is quantized as one row (quant_row, FP8:
+ * scale = max|k| / 448, codes e4m3_RNE_satfinite(k / scale)); likewise the
+ * value vector at q_dim + kv_heads hd + h hd.  The codes of token m go to slot
+ * s = slot_mapping[m] of the caches: kc[s][h][0 .. hd), ks[s][h] (and vc, vs);
+ * a negative slot (a padding token) writes nothing.  Slots are the flattened
+ * (block, offset) positions of a paged cache.
+ */
+int orc_kv_cache_quant(const uint16_t* QKV, int M, int ldq, int q_dim, int kv_heads, int head_dim,
+                       const int64_t* slot_mapping, uint8_t* kc, float* ks, uint8_t* vc, float* vs) {
+    if (!QKV || !slot_mapping || !kc || !ks || !vc || !vs || M < 0 || q_dim < 0 || kv_heads <= 0 ||
+        head_dim <= 0 || ldq < q_dim + 2 * kv_heads * head_dim)
+        return ORC_ERR_ARG;
+    float* v = (float*)malloc(sizeof(float) * (size_t)head_dim);
+    if (!v) return ORC_ERR_ARG;
+    for (int m = 0; m < M; ++m) {
+        const int64_t slot = slot_mapping[m];
+        if (slot < 0) continue;
+        for (int part = 0; part < 2; ++part) {
+            uint8_t* codes = part == 0 ? kc : vc;
+            float* scales = part == 0 ? ks : vs;
+            for (int h = 0; h < kv_heads; ++h) {
+                const size_t col = (size_t)q_dim + (size_t)part * kv_heads * head_dim + (size_t)h * head_dim;
+                for (int d = 0; d < head_dim; ++d) v[d] = orc_bf16_decode(QKV[(size_t)m * ldq + col + d]);
+                const size_t at = (size_t)slot * kv_heads + h;
+                quant_row(v, head_dim, ORC_FP8_E4M3, codes + at * head_dim, scales + at);
+            }
+        }
+    }
+    free(v);
+    return ORC_OK;
+}
+
+/*
+ * The values a cache holds, for the slots a reader gathers: out[n][h hd + d] =
+ * bf16_RNE(fp32(e4m3 value of code) * scale) of slot slots[n], head h (the
+ * e4m3 value is exact in fp32, so one fp32 rounding and one bf16 rounding).
+ */
+int orc_kv_cache_dequant(const uint8_t* cache, const float* scale, const int64_t* slots, int n, int kv_heads,
+                         int head_dim, uint16_t* out) {
+    if (!cache || !scale || !slots || !out || n < 0 || kv_heads <= 0 || head_dim <= 0) return ORC_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (slots[i] < 0) return ORC_ERR_ARG;
+        for (int h = 0; h < kv_heads; ++h) {
+            const size_t at = (size_t)slots[i] * kv_heads + h;
+            for (int d = 0; d < head_dim; ++d) {
+                const float x = (float)orc_e4m3_decode(cache[at * head_dim + d]) * scale[at];
+                out[((size_t)i * kv_heads + h) * head_dim + d] = orc_bf16_encode(x);
+            }
+        }
+    }
     return ORC_OK;
 }
 

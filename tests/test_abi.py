@@ -150,17 +150,19 @@ def test_workspace_size_without_gpu(L):
 
 def _tile_widths(p):
     """(token tile width, channel tile width) of a plan."""
-    pair = p["kernel"] in (2, 3)
+    pair = p["kernel"] in (2, 3, 4)
     if p["swap"]:
         return p["bn"], (256 if pair else 128)
     return (256 if pair else 128), p["bn"]
 
 
 @pytest.mark.parametrize("M,N,K,qt,kernel", [
-    # INT8 with its workspace: the TMEM-operand kernel; CTA pairs only for prefill
-    # sizes whose 256 x 256 units fill their waves
+    # INT8 with its workspace: the TMEM-operand kernel; from 2048 tokens on, and
+    # where 256 x 256 pair units would fill their waves, CTA pairs with both
+    # operands widened in the workspace
     (64, 37888, 3584, 0, 1), (256, 37888, 3584, 0, 1), (256, 4608, 3584, 0, 1),
-    (4096, 37888, 3584, 0, 2), (4096, 3584, 18944, 0, 2), (8192, 7168, 5120, 0, 2),
+    (1536, 8192, 4096, 0, 4), (2000, 4000, 4000, 0, 4),
+    (4096, 37888, 3584, 0, 4), (4096, 3584, 18944, 0, 4), (8192, 7168, 5120, 0, 4), (2048, 256, 16384, 0, 4),
     (1024, 7168, 5120, 0, 1), (1024, 5120, 27648, 0, 1),
     # FP8: pairs for prefill and for the larger decode shapes
     (64, 37888, 3584, 1, 0), (256, 4608, 3584, 1, 0), (256, 37888, 3584, 1, 3),
@@ -177,6 +179,8 @@ def test_plan_routing_and_coverage(M, N, K, qt, kernel):
     assert (p["tiles_tok"] - 1) * tw < M <= p["tiles_tok"] * tw
     assert (p["tiles_ch"] - 1) * cw < N <= p["tiles_ch"] * cw
     bk = 256 if p["kernel"] in (1, 2) else (64 if qt == 0 else 128)
+    if p["kernel"] == 4:
+        assert p["kb_per_split"] % 4 == 0 or p["splits"] == 1  # split ranges hold whole 256-code sum ranges
     num_kb = -(-K // bk)
     assert (p["splits"] - 1) * p["kb_per_split"] < num_kb <= p["splits"] * p["kb_per_split"]
 
@@ -191,10 +195,17 @@ def test_plan_workspace_and_fallbacks(L):
     # no workspace: INT8 widens both operands in shared memory and K is not split
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=0)
     assert p["kernel"] == 0 and p["splits"] == 1 and p["ws_bytes"] == 0
-    # a workspace too small for split partials keeps the TMEM kernel unsplit
-    act = 64 * 3584 * 2 + 256
+    # a workspace too small for split partials keeps the TMEM kernel unsplit (fp16 codes, their
+    # sums, and one 128 x 128 int32 running-sum region per SM)
+    act = 64 * 3584 * 2 + 256 + 152 * 128 * 128 * 4
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=act)
     assert p["kernel"] == 1 and p["splits"] == 1 and p["ws_bytes"] <= act
+    # without room for the running sums: both operands widened in shared memory
+    assert q.plan(64, 4608, 3584, 0, 152, ws_bytes=act - 1024)["kernel"] == 0
+    # a workspace too small to widen the weights keeps the CTA-pair kernel with the weights in TMEM
+    wide = q.plan(1536, 8192, 4096, 0, 152)
+    assert wide["kernel"] == 4
+    assert q.plan(1536, 8192, 4096, 0, 152, ws_bytes=wide["ws_bytes"] - 1)["kernel"] == 2
     out = (ctypes.c_longlong * 8)()
     assert L.qurl_debug_plan(64, 4608, 3584, 0, 0, 0, out) == 1
     assert L.qurl_debug_plan(64, 4608, 3584, 7, 152, 0, out) == 1

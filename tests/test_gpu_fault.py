@@ -18,6 +18,8 @@ pytestmark = pytest.mark.gpu
     (q.FP8_E4M3, 16, 512, 256),
     (q.FP8_E4M3, 300, 512, 256),     # prefill: the CTA-pair kernel
     (q.FP8_E4M3, 256, 8192, 4096),   # decode shape that runs on CTA pairs
+    (q.INT8, 1536, 8192, 4096),      # INT8 on CTA pairs, widened weights in TMEM
+    (q.INT8, 2048, 512, 256),        # INT8 on CTA pairs, both operands widened in the workspace
 ])
 def test_bounded_wait_times_out_and_context_survives(qt, M, N, K):
     X = synth.activations(f"fault/X/{M}/{K}", M, K).cuda()
@@ -25,6 +27,9 @@ def test_bounded_wait_times_out_and_context_survives(qt, M, N, K):
     Wq, sw, _, _ = q.prepare_weights(W, qt, s=1.5, keep_scaled=False)
     Xq, sx = q.quant_act(X, qt)
     ws = q.workspace(M, N, K, qt)
+    if qt == q.INT8 and (M, N, K) == (1536, 8192, 4096):  # keep the CTA-pair kernel with weights in TMEM
+        wide = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)["ws_bytes"]
+        ws = torch.empty(wide - 1, dtype=torch.uint8, device="cuda")
     ref = q.linear(Xq, sx, Wq, sw, qt, ws)
     q.qurl_check_device_status()
     q.qurl_debug_inject_timeout()

@@ -80,6 +80,35 @@ def test_quant_act_exact(qt, M, K):
         np.testing.assert_array_equal(f32(sx), so)
 
 
+def test_quant_act_fp8_midpoint_quotients():
+    """FP8 codes round v / scale to the nearest e4m3 value, ties to even, with
+    saturation.  With absmax 448 (scale exactly 1) or 672 at pre-scale 1.5
+    (scale exactly 1.5) the quotients are every e4m3 rounding midpoint -- normal
+    ones from 2^-6 to 448 and the subnormal ones below 2^-6 -- and one bf16 ulp
+    either side of them: the kernel's reciprocal shortcut, which lands within a
+    few fp32 ulps of the quotient, must hand each such code to the exact
+    division."""
+    mids = [(1 + (2 * k + 1) / 16) * 2.0 ** e for e in range(-6, 9) for k in range(8)]
+    mids = [m for m in mids if m < 448] + [(j + 0.5) * 2.0 ** -9 for j in range(8)]
+    b = torch.tensor(mids, dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(b.float(), torch.tensor(mids))  # every midpoint is a bf16 value
+    up = (b.view(torch.int16) + 1).view(torch.bfloat16).float()
+    dn = (b.view(torch.int16) - 1).view(torch.bfloat16).float()
+    vals = torch.cat([b.float(), up, dn])
+    row = torch.cat([torch.tensor([448.0]), vals, -vals])
+    K = ((row.numel() + 15) // 16) * 16
+    X = torch.zeros((1, K), dtype=torch.float32)
+    X[0, : row.numel()] = row
+    X = X.to(torch.bfloat16)
+    for pre in (1.0, 1.5):
+        Xq, sx = q.quant_act(X.cuda(), q.FP8_E4M3, pre_scale=pre)
+        sync_ok()
+        qo, so = oracle.quant_act(bits(X), oracle.FP8_E4M3, pre_scale=pre)
+        np.testing.assert_array_equal(codes(Xq), qo)
+        np.testing.assert_array_equal(f32(sx), so)
+    assert mids[48] == 1.0625 and codes(Xq)[0, 1 + 48] == 0x38  # 1.0625 (between 1 and 1.125) -> 1.0 (even)
+
+
 @pytest.mark.parametrize("qt", QTS)
 def test_quant_act_strided_rows(qt):
     """The o_proj input is a column slice of the qkv output (row stride 4608)."""
@@ -325,16 +354,19 @@ def test_gemm_int8_decode_tiles(M, K, small):
 @pytest.mark.parametrize("M", [16, 64, 256])
 @pytest.mark.parametrize("small", [True, False])
 def test_gemm_int8_decode_unsplit_long_k(M, small):
-    """A workspace with room for the fp16 codes and their sums but not for split
-    partials makes every unit run over all of K = 4352 (17 stages): uniform codes
-    take five 1024-deep chunks drained into the int32 running sum (the last one
+    """A workspace with room for the fp16 codes, their sums and the running sums
+    of chunked units but not for split partials makes every unit run over all of
+    K = 4352 (17 stages): uniform codes take five 1024-deep chunks (alternating
+    the two accumulators) added into the int32 running sum (the last one
     ragged), small codes one fp32 pass."""
     N, K = 392, 4352
     g = np.random.Generator(np.random.PCG64(M + 7 * small))
     lim = 10 if small else 127
     xq = g.integers(-lim, lim + 1, size=(M, K)).astype(np.int8)
     wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
-    act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # fp16 codes, their sums, and the per-CTA running sums of chunked units (128 x 128 int32 each)
+    act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256 + sms * 128 * 128 * 4
     assert q.qurl_workspace_size(M, N, K, q.INT8) > act  # the full-size plan would split K
     ws = torch.empty(act, dtype=torch.uint8, device="cuda")
     acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8, ws)
@@ -364,7 +396,18 @@ def test_gemm_int8_prefill_repeatable():
     np.testing.assert_array_equal(runs[0].cpu().numpy()[np.ix_(rows, cols)], ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 4096, 4096), (2000, 4000, 4000)])
+def pair_tmem_workspace(M, N, K):
+    """A workspace one byte short of what the kernel with widened weights needs:
+    the plan falls back to the CTA-pair kernel with the widened weights in TMEM."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wide = q.plan(M, N, K, q.INT8, sms)
+    assert wide["kernel"] == 4
+    p = q.plan(M, N, K, q.INT8, sms, ws_bytes=wide["ws_bytes"] - 1)
+    assert p["kernel"] == 2
+    return torch.empty(p["ws_bytes"], dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("M,N,K", [(1536, 8192, 4096), (2000, 4000, 4000)])
 def test_gemm_int8_pair_modes(M, N, K):
     """Prefill shapes on the 256 x 256 CTA pairs (ragged in M, N and K in the
     second case: the last 256-deep stage reads 160 codes and zero fill):
@@ -377,9 +420,8 @@ def test_gemm_int8_pair_modes(M, N, K):
     big = (np.arange(M) // 256) % 2 == 1
     xq[big] = g.integers(-127, 128, size=(int(big.sum()), K)).astype(np.int8)
     wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
-    assert q.plan(M, N, K, q.INT8, torch.cuda.get_device_properties(0).multi_processor_count)["kernel"] == 2
     acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
-                     q.workspace(M, N, K, q.INT8))
+                     pair_tmem_workspace(M, N, K))
     sync_ok()
     edges = [r for t0 in range(0, M, 64) for r in (t0, t0 + 31, t0 + 63) if r < M] + [M - 1]
     rows = np.unique(np.array(edges))
@@ -412,15 +454,17 @@ def test_fp8_pair_prefill_repeatable():
 
 
 def test_gemm_int8_more_units_than_mode_slots():
-    """102 x 98 tiles of 256 x 256 on the CTA pairs: every pair walks ~131
-    units, beyond the 128 whose accumulation mode the kernel records, so the
-    last ones take the chunked path (two half passes) without a recorded mode."""
-    M, N, K = 256 * 102, 256 * 98, 512
+    """7 x 1400 tiles of 256 x 256 on the CTA pairs with the widened weights in
+    TMEM (the workspace leaves no room to widen the weights in it): every pair
+    walks ~129 units, beyond the 128 whose accumulation mode the kernel records,
+    so the last ones take the chunked path (two half passes) without a recorded
+    mode."""
+    M, N, K = 256 * 7, 256 * 1400, 256
     g = np.random.Generator(np.random.PCG64(23))
     xq = g.integers(-20, 21, size=(M, K)).astype(np.int8)
     wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
     acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8,
-                     q.workspace(M, N, K, q.INT8))
+                     pair_tmem_workspace(M, N, K))
     sync_ok()
     rows = np.sort(g.choice(M, size=96, replace=False))
     rows[-1] = M - 1  # a token of the last tile (the last units of their CTAs)

@@ -82,7 +82,10 @@ def load() -> ctypes.CDLL:
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
+            "qurl_debug_mma_probe": [i, i, i, P, P],
             "qurl_acr_objective": [P, P, P, P, P, ctypes.c_longlong, f, f, i, P, P, P, P, z, P],
+            "qurl_kv_cache_quant": [P, i, i, i, i, i, P, ctypes.c_longlong, P, P, P, P, P],
+            "qurl_kv_cache_dequant": [P, P, P, i, i, i, ctypes.c_longlong, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -253,6 +256,32 @@ def qurl_acr_objective(logp, logp_prox, logp_behav, adv, mask, eps, C, adaptive,
         "qurl_acr_objective")
 
 
+def qurl_kv_cache_quant(qkv, q_dim, kv_heads, head_dim, slot_mapping, k_cache, k_scale, v_cache, v_scale,
+                        stream=None):
+    _dense(slot_mapping, k_cache, k_scale, v_cache, v_scale)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping is int64")
+    M = qkv.shape[0]
+    _ok(load().qurl_kv_cache_quant(_ptr(qkv), M, _ld(qkv), q_dim, kv_heads, head_dim, _ptr(slot_mapping),
+                                   k_cache.shape[0], _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+                                   _stream(stream)), "qurl_kv_cache_quant")
+
+
+def qurl_kv_cache_dequant(cache, scale, slots, out, stream=None):
+    _dense(cache, scale, slots, out)
+    num_slots, kv_heads, head_dim = cache.shape
+    _ok(load().qurl_kv_cache_dequant(_ptr(cache), _ptr(scale), _ptr(slots), slots.numel(), kv_heads, head_dim,
+                                     num_slots, _ptr(out), _stream(stream)), "qurl_kv_cache_dequant")
+
+
+def kv_cache(num_slots, kv_heads, head_dim, device="cuda"):
+    """Empty FP8 key and value caches with their scales: (k_cache, k_scale, v_cache, v_scale)."""
+    return (torch.empty((num_slots, kv_heads, head_dim), dtype=torch.float8_e4m3fn, device=device),
+            torch.empty((num_slots, kv_heads), dtype=torch.float32, device=device),
+            torch.empty((num_slots, kv_heads, head_dim), dtype=torch.float8_e4m3fn, device=device),
+            torch.empty((num_slots, kv_heads), dtype=torch.float32, device=device))
+
+
 def qurl_check_device_status(stream=None):
     _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
 
@@ -264,6 +293,13 @@ def plan(M, N, K, qt, num_sms, ws_bytes=None):
     _ok(load().qurl_debug_plan(M, N, K, qt, num_sms, ws, out), "qurl_debug_plan")
     keys = ("kernel", "swap", "bn", "tiles_tok", "tiles_ch", "splits", "kb_per_split", "ws_bytes")
     return dict(zip(keys, list(out)))
+
+
+def qurl_debug_mma_probe(route, ctas, iters, stream=None) -> float:
+    """Launch a tensor-rate probe (see include/qurl.h); returns the operations it performs."""
+    ops = ctypes.c_double(0.0)
+    _ok(load().qurl_debug_mma_probe(route, ctas, iters, ctypes.byref(ops), _stream(stream)), "qurl_debug_mma_probe")
+    return ops.value
 
 
 def qurl_debug_inject_timeout():

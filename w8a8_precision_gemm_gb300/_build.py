@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libqurl.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_common.cu", "gemm_fp8.cu", "gemm_fp8p.cu", "gemm_i8.cu", "gemm_i8t.cu", "objective.cu",
-           "static_scratch.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_common.cu", "gemm_fp8.cu", "gemm_fp8p.cu", "gemm_i8.cu", "gemm_i8t.cu", "gemm_i8w.cu", "objective.cu",
+           "static_scratch.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

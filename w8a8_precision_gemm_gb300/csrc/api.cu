@@ -178,13 +178,16 @@ qurl_status check_gemm(const void* Xq, const void* Wq, int M, int N, int K, int 
     if (_e != cudaSuccess) return cuda_fail(_e); \
   } while (0)
 
-// Where the INT8 decode kernel reads its per-token, per-split sums of |code|.
+// Where the INT8 kernels that read an fp16 copy of the activation codes find
+// its per-token, per-split sums of |code| (and, for the kernel with widened
+// weights, of code^2).
 qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
   qurl::CodeSums c{};
-  if (p.tmem_a) {
+  if (p.tmem_a || p.wide) {
     c.asum = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + p.asum_off);
     c.sum_len = p.kb_per_split * p.bk;
     c.nsum = p.splits;
+    if (p.wide) c.qsum = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(ws) + p.qsum_off);
   }
   return c;
 }
@@ -209,7 +212,15 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   uint8_t* part = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
   const qurl::CodeSums sums = code_sums(p, ws);
   CUtensorMap ta, tb;
-  if (p.tmem_a) {
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  if (p.wide) {
+    if (!x16_ready) QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
+    QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, wsb + p.w16_off, reinterpret_cast<unsigned*>(wsb + p.qn_off),
+                                         dev->num_sms, st));
+    w_indep = false;  // the GEMM reads the widened weights the kernel before it writes
+    QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, 128, true, &ta));
+    QURL_TRY(byte_map(wsb + p.w16_off, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
+  } else if (p.tmem_a) {
     if (!x16_ready) {
       QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
       w_indep = true;  // the widening kernel writes only the workspace
@@ -239,8 +250,13 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.acc_out = acc_out;
   a.fault = g_inject_timeout.exchange(0);
   a.asum = sums.asum;
+  a.qsum = sums.qsum;
+  a.qn = p.wide ? reinterpret_cast<const unsigned*>(wsb + p.qn_off) : nullptr;
+  a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
-  if (p.tmem_a && p.pair)
+  if (p.wide)
+    QURL_CUDA(qurl::launch_gemm_i8w(ta, tb, a, grid, st));
+  else if (p.tmem_a && p.pair)
     QURL_CUDA(qurl::launch_gemm_i8p(ta, tb, a, grid, st));
   else if (p.tmem_a)
     QURL_CUDA(qurl::launch_gemm_i8t(p.bn, ta, tb, a, grid, st));
@@ -346,11 +362,22 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
   return QURL_OK;
 }
 
+qurl_status qurl_debug_mma_probe(int route, int ctas, int iters, double* ops, qurl_stream_t stream) {
+  if (route < 0 || route > 3 || ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 24) || !ops)
+    return QURL_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  if (route > 0 && ctas > dev->num_sms) return QURL_ERR_INVALID_ARG;  // one CTA per SM
+  QURL_CUDA(qurl::launch_probe(route, ctas, iters, dev->status, reinterpret_cast<cudaStream_t>(stream)));
+  *ops = qurl::probe_ops(route, ctas, iters);
+  return QURL_OK;
+}
+
 qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, long long* out) {
   if (!out || !valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt) || num_sms <= 0)
     return QURL_ERR_INVALID_ARG;
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, num_sms, ws_bytes);
-  out[0] = p.tmem_a ? (p.pair ? 2 : 1) : (p.pair ? 3 : 0);
+  out[0] = p.wide ? 4 : p.tmem_a ? (p.pair ? 2 : 1) : (p.pair ? 3 : 0);
   out[1] = p.swap ? 1 : 0;
   out[2] = p.bn;
   out[3] = p.tiles_tok;
@@ -405,7 +432,7 @@ FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
   DevState* dev = nullptr;
   if (device_state(&dev) != QURL_OK) return f;
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
-  if (p.tmem_a) {
+  if (p.tmem_a || p.wide) {
     f.x16 = ws;
     f.sums = code_sums(p, ws);
   }
@@ -475,6 +502,44 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
   return QURL_OK;
 }
 
+qurl_status qurl_kv_cache_quant(const void* qkv, int M, int ldq, int q_dim, int kv_heads, int head_dim,
+                                const int64_t* slot_mapping, long long num_slots, void* k_cache, float* k_scale,
+                                void* v_cache, float* v_scale, qurl_stream_t stream) {
+  if (M < 0 || q_dim < 0 || kv_heads <= 0 || head_dim <= 0 || num_slots < 0) return QURL_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0 || head_dim > 256 || q_dim % 8 != 0) return QURL_ERR_UNSUPPORTED;
+  if (static_cast<long long>(ldq) < static_cast<long long>(q_dim) + 2LL * kv_heads * head_dim)
+    return QURL_ERR_INVALID_ARG;
+  if (M == 0) return QURL_OK;
+  if (!qkv || !slot_mapping || !k_cache || !k_scale || !v_cache || !v_scale) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || (static_cast<long long>(ldq) * 2) % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0 || (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
+    return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_kv_cache_quant(qkv, M, ldq, q_dim, kv_heads, head_dim,
+                                        reinterpret_cast<const long long*>(slot_mapping), num_slots, k_cache, k_scale,
+                                        v_cache, v_scale, dev->status, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_kv_cache_dequant(const void* cache, const float* scale, const int64_t* slots, int n, int kv_heads,
+                                  int head_dim, long long num_slots, void* out, qurl_stream_t stream) {
+  if (n < 0 || kv_heads <= 0 || head_dim <= 0 || num_slots < 0) return QURL_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0 || head_dim > 256) return QURL_ERR_UNSUPPORTED;
+  if (n == 0) return QURL_OK;
+  if (!cache || !scale || !slots || !out) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(slots) & 7u) != 0 ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+    return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_kv_cache_dequant(cache, scale, reinterpret_cast<const long long*>(slots), n, kv_heads,
+                                          head_dim, num_slots, out, dev->status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
 size_t qurl_acr_workspace_size(void) { return qurl::kAcrWorkspaceBytes; }
 
 qurl_status qurl_acr_objective(const float* logp, const float* logp_prox, const float* logp_behav, const float* adv,
@@ -505,7 +570,7 @@ qurl_status qurl_check_device_status(qurl_stream_t stream) {
   if (v != 0) {
     const int zero = 0;
     QURL_CUDA(cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
-    return v == qurl::kDevTimeout ? QURL_ERR_TIMEOUT : QURL_ERR_CUDA;
+    return v == qurl::kDevTimeout ? QURL_ERR_TIMEOUT : v == qurl::kDevBadIndex ? QURL_ERR_INVALID_ARG : QURL_ERR_CUDA;
   }
   return QURL_OK;
 }

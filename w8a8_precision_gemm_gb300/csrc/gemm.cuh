@@ -134,6 +134,33 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
   return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+// Bounded wait until *count > j (a counter another warp of the CTA raises).
+__device__ __forceinline__ bool wait_count(const uint32_t* count, uint32_t j, int* status) {
+  if (ld_acquire_cta(count) > j) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_cta(count) > j) return true;
+    if ((it & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(status) != kDevOk) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(status, kDevOk, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // 16 int8 codes -> 16 fp16 values, exactly: with u = c + 128 in [0, 255], the
 // fp16 with bits 0x6400 | u is 1024 + u; subtracting 1152 leaves c.
 __device__ __forceinline__ void i8x16_to_f16x16(const uint4 v, uint4& lo, uint4& hi) {

@@ -13,7 +13,69 @@ namespace qurl {
 // so that tiles x splits is close to the SM count, each split at least 512
 // deep, as far as the workspace allows.  Workspace layout: [fp16 activation
 // codes and per-token sums of |code| (INT8 decode)][split-K partials].
+// INT8 prefill from this many tokens on: CTA pairs with both operands widened
+// to fp16 in the workspace (the weights' widening, 3 N K bytes of HBM traffic,
+// costs ~425 / M of the GEMM's tensor time).  Below it the TMEM-operand
+// kernels are faster (measured on the 32B-class shapes at M = 512 and 1024),
+// except their CTA-pair form, whose chunked accumulation runs two half passes
+// over the weights: where the planner would pick that form, the widened kernel
+// takes its place (gate_up at M = 1024: 447-453 us against 399 us with small
+// activation codes and 780 us with normed ones).
+constexpr int kWideMinM = 2048;
+
+// The INT8 plan on CTA pairs with widened operands, when the workspace holds it.
+bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  p = GemmPlan{};
+  p.wide = true;
+  p.pair = true;
+  p.swap = false;
+  p.bn = 256;
+  p.bk = 64;
+  p.num_kb = (K + 63) / 64;
+  p.tiles_tok = (M + 255) / 256;
+  p.tiles_ch = (N + 255) / 256;
+  const long long tiles = static_cast<long long>(p.tiles_tok) * p.tiles_ch;
+  const int slots = std::max(1, num_sms / 2);
+  // K splits (ranges of a multiple of 4 k-blocks, 256 codes: the code sums' granularity) only when the
+  // pair tiles leave the pairs mostly idle
+  int splits = 1;
+  if (tiles < slots) splits = std::max(1, std::min(static_cast<int>(slots / tiles), std::min(p.num_kb / 16, kMaxSums)));
+  int kps = (p.num_kb + splits - 1) / splits;
+  kps = (kps + 3) & ~3;
+  splits = (p.num_kb + kps - 1) / kps;
+  const size_t x16 = al(static_cast<size_t>(M) * K * 2);
+  const size_t sums = al(static_cast<size_t>(M) * 4 * splits);
+  const size_t w16 = al(static_cast<size_t>(N) * K * 2);
+  const size_t qn = al(static_cast<size_t>(N) * 4);
+  const size_t scratch = static_cast<size_t>(i8w_max_ctas(num_sms)) * 256 * 128 * 4;
+  const size_t part = splits > 1 ? static_cast<size_t>(splits) * M * N * 4 : 0;
+  p.kb_per_split = kps;
+  p.splits = splits;
+  p.asum_off = x16;
+  p.qsum_off = x16 + sums;
+  p.w16_off = p.qsum_off + sums;
+  p.qn_off = p.w16_off + w16;
+  p.scratch_off = p.qn_off + qn;
+  p.x16_bytes = p.scratch_off + scratch;  // everything before the split-K partials
+  p.part_bytes = part;
+  p.ws_bytes = p.x16_bytes + part;
+  return p.ws_bytes <= ws_avail;
+}
+
+GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
+
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
+  GemmPlan w{};
+  if (qt == kQInt8 && M >= kWideMinM && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
+  const GemmPlan p = plan_narrow(M, N, K, qt, num_sms, ws_avail);
+  if (p.tmem_a && p.pair && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
+  return p;
+}
+
+// The plans without widened weights: TMEM-operand INT8 kernels, FP8, and the
+// shared-memory INT8 kernel.
+GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan p{};
   const bool int8 = (qt == kQInt8);
   // INT8 prefers the TMEM-operand kernel (weights on the MMA M side at every
@@ -22,7 +84,9 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   // shared memory.
   const size_t x16 = (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
   auto sums = [&](int s) { return (static_cast<size_t>(M) * 4 * s + 255) & ~static_cast<size_t>(255); };
-  p.tmem_a = int8 && ws_avail >= x16 + sums(1);
+  // the running sums of chunked units, one 128 x 128 int32 region per CTA
+  const size_t scratch = static_cast<size_t>(std::max(num_sms, 1)) * 128 * 128 * 4;
+  p.tmem_a = int8 && ws_avail >= x16 + sums(1) + scratch;
   p.swap = p.tmem_a || M <= 256;
   p.bk = int8 ? (p.tmem_a ? 256 : 64) : 128;
   p.num_kb = (K + p.bk - 1) / p.bk;
@@ -103,13 +167,14 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   const size_t per_split = static_cast<size_t>(M) * N * 4;
   // workspace for s splits: [fp16 codes, code sums (INT8 decode)][s partials if s > 1]
   auto need = [&](int s) {
-    return (p.tmem_a ? x16 + sums(s) : 0) + (s > 1 ? static_cast<size_t>(s) * per_split : 0);
+    return (p.tmem_a ? x16 + sums(s) + scratch : 0) + (s > 1 ? static_cast<size_t>(s) * per_split : 0);
   };
   while (splits > 1 && need(splits) > ws_avail) --splits;
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
-  p.x16_bytes = p.tmem_a ? x16 + sums(p.splits) : 0;
+  p.x16_bytes = p.tmem_a ? x16 + sums(p.splits) + scratch : 0;
   p.asum_off = p.tmem_a ? x16 : 0;
+  p.scratch_off = p.tmem_a ? x16 + sums(p.splits) : 0;
   p.part_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * per_split : 0;
   p.ws_bytes = p.x16_bytes + p.part_bytes;
   return p;

@@ -27,16 +27,20 @@
 // to 1024-deep chunks (|partial| <= 1024 * 128^2 = 2^24), each drained by the
 // epilogue into an int32 running sum in TMEM.  Both are exact.
 //
-// TMEM: two fp32 accumulators of BN columns (at least 32) -- alternated
-// between fast units; a chunked unit accumulates in the first and keeps its
-// running sum in the second -- then NS stages of 128 columns (256 fp16 per
-// lane) of widened weights.
+// TMEM: two fp32 accumulators of BN columns (at least 32), alternated between
+// accumulation passes -- a fast unit is one pass, a chunked unit one pass per
+// 1024-deep chunk, so the MMA fills one buffer while the epilogue drains the
+// other and adds a chunk into the unit's int32 running sum (kept in a scratch
+// region of the workspace, one per CTA) -- then NS stages of 128 columns (256
+// fp16 per lane) of widened weights.
 #include "gemm.cuh"
 
 namespace qurl {
 
 // Largest S_t = sum over a k range of |x_tk| for which one fp32 pass is exact.
 constexpr int kFastSumMax = (1 << 24) / 128;
+// A CTA's scratch for the running sum of a chunked unit: 128 columns x 128 rows.
+constexpr int kI8tScratchInts = 128 * 128;
 // Saturation of the S_t computed by the activation kernels (> kFastSumMax).
 constexpr int kSumCap = 1 << 24;
 
@@ -106,33 +110,6 @@ struct Ring {
   }
 };
 
-__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-
-// Bounded wait until *count > j (a counter another warp of the CTA raises).
-__device__ __forceinline__ bool wait_count(const uint32_t* count, uint32_t j, int* status) {
-  if (ld_acquire_cta(count) > j) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(64);
-    if (ld_acquire_cta(count) > j) return true;
-    if ((it & 15u) == 0) {
-      if (*reinterpret_cast<volatile int*>(status) != kDevOk) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        atomicCAS(status, kDevOk, kDevTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 // Sum of |c| over 16 int8 codes (|-128| counts 128).
 __device__ __forceinline__ int abs_sum16(const uint4 v) {
   unsigned s = 0;
@@ -141,6 +118,16 @@ __device__ __forceinline__ int abs_sum16(const uint4 v) {
   s = __dp4a(__vabs4(v.z), 0x01010101u, s);
   s = __dp4a(__vabs4(v.w), 0x01010101u, s);
   return static_cast<int>(s);
+}
+
+// Sum of c^2 over 16 int8 codes (at most 16 x 128^2).
+__device__ __forceinline__ unsigned sq_sum16(const uint4 v) {
+  int s = 0;
+  s = __dp4a(static_cast<int>(v.x), static_cast<int>(v.x), s);
+  s = __dp4a(static_cast<int>(v.y), static_cast<int>(v.y), s);
+  s = __dp4a(static_cast<int>(v.z), static_cast<int>(v.z), s);
+  s = __dp4a(static_cast<int>(v.w), static_cast<int>(v.w), s);
+  return static_cast<unsigned>(s);
 }
 
 template <int BN>
@@ -245,8 +232,8 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       bool ok = true;
       Ring<NS> r;
-      int nb0 = 0, nb1 = 0;  // accumulator fills issued per buffer
-      int next_fast = 0;
+      int nb[2] = {0, 0};  // accumulator fills committed per buffer
+      int nextbuf = 0;     // passes (a fast unit, or one chunk of a chunked unit) alternate the buffers
       for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
         const Unit w = unit_of<true, BN>(args, u);
         if (j < kModeUnits && !wait_count(&bars.mode_count, j, status)) {
@@ -259,9 +246,9 @@ __global__ void __launch_bounds__(512, 1)
         for (int it = 0; it < w.nkb; ++it, r.next()) {
           const int kin = fast ? it : it % C::CHUNK;  // stage within the accumulation pass
           if (kin == 0) {
-            b = fast ? next_fast : 0;
-            const int nb = b ? nb1 : nb0;
-            if (nb > 0 && !mbar_wait(&bars.pempty[b], (nb - 1) & 1, status)) {
+            b = nextbuf;
+            nextbuf ^= 1;
+            if (nb[b] > 0 && !mbar_wait(&bars.pempty[b], (nb[b] - 1) & 1, status)) {
               ok = false;
               break;
             }
@@ -283,10 +270,9 @@ __global__ void __launch_bounds__(512, 1)
           const bool pass_end = (it == w.nkb - 1) || (!fast && kin == C::CHUNK - 1);
           if (pass_end) {
             umma_commit(&bars.pfull[b]);
-            if (b) ++nb1; else ++nb0;
+            ++nb[b];
           }
         }
-        next_fast = fast ? (next_fast ^ 1) : 0;
       }
       if (!ok) {
         umma_commit(&bars.done);
@@ -351,11 +337,12 @@ __global__ void __launch_bounds__(512, 1)
     const int q = warp & 3;
     const int i = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t tR = lane_base + C::ACC_COLS;  // running sum of a chunked unit
+    // the int32 running sum of a chunked unit: this CTA's scratch region, [column][row]
+    int* scr = args.scratch + static_cast<size_t>(blockIdx.x) * kI8tScratchInts + i;
     const int emode = args.mode;
     bool ok = true;
-    int nb0 = 0, nb1 = 0;
-    int next_fast = 0;
+    int nb[2] = {0, 0};
+    int nextbuf = 0;
     for (int u = R.u, j = 0; u < R.end && ok; u += R.stride, ++j) {
       const Unit w = unit_of<true, BN>(args, u);
       if (j < kModeUnits && !__all_sync(0xFFFFFFFFu, wait_count(&bars.mode_count, j, status))) {
@@ -369,8 +356,9 @@ __global__ void __launch_bounds__(512, 1)
       const float sw_lane = channel_scale(args, emode, w.a0 + i);
       const float sx_first = token_scale(args, emode, w.b0 + lane);
       for (int c = 0; c < npass; ++c) {
-        const int b = fast ? next_fast : 0;
-        if (!warp_wait(&bars.pfull[b], (b ? nb1 : nb0) & 1, status)) {
+        const int b = nextbuf;
+        nextbuf ^= 1;
+        if (!warp_wait(&bars.pfull[b], nb[b] & 1, status)) {
           ok = false;
           break;
         }
@@ -381,9 +369,16 @@ __global__ void __launch_bounds__(512, 1)
         for (int c0 = 0; c0 < BN; c0 += 32) {
           // the next block's token scale, in flight while this block is written
           const float sx_next = (last && c0 + 32 < BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
+          int* sc = scr + static_cast<size_t>(c0) * 128;
+          // the running sum is loaded before the accumulator, so both reads are in flight together
+          int prev[32];
+          if (c > 0) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) prev[jj] = __ldcg(sc + jj * 128);
+          }
           uint32_t p[32];
           tmem_ld32(lane_base + b * C::ACC_COLS + c0, p);
-          if (c == 0 && last && emode == kModeBf16) {
+          if (npass == 1 && emode == kModeBf16) {
             // a single pass: the fp32 accumulator already holds the exact
             // integer, so it is scaled as it is (no int32 round trip, whose
             // two conversions per element bound this epilogue)
@@ -395,31 +390,24 @@ __global__ void __launch_bounds__(512, 1)
             continue;
           }
           int v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
           if (c > 0) {
-            uint32_t rs[32];
-            tmem_ld32(tR + c0, rs);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = static_cast<int>(rs[j]) + __float2int_rn(__uint_as_float(p[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float2int_rn(__uint_as_float(p[j]));
+            for (int j = 0; j < 32; ++j) v[j] += prev[j];
           }
           if (!last) {
-            uint32_t wv[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) wv[j] = static_cast<uint32_t>(v[j]);
-            tmem_st32(tR + c0, wv);
+            for (int j = 0; j < 32; ++j) __stcg(sc + j * 128, v[j]);
           } else {
             emit32_swap<BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
           }
           sx_lane = sx_next;
         }
-        if (!last) tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.pempty[b]);
-        if (b) ++nb1; else ++nb0;
+        ++nb[b];
       }
-      next_fast = fast ? (next_fast ^ 1) : 0;
     }
   } else {
     // ------------------------------------------------------------ converters: weights -> fp16 in TMEM
@@ -957,14 +945,14 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // One block per row: int8 codes -> fp16 (exact), [M, K] dense -> [M, K]
-// dense, and the row's sums of |code| over the ranges of `sums` (saturated at
-// kSumCap) for the GEMM's accumulation mode.
+// dense, and the row's sums of |code| (saturated at kSumCap) and, when wanted,
+// of code^2 over the ranges of `sums`, for the GEMM's accumulation mode.
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                                         int K, const CodeSums sums) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ unsigned long long cnt[kMaxSums];
-  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x) cnt[j] = 0;
+  __shared__ unsigned long long cnt[2 * kMaxSums];
+  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x) cnt[j] = cnt[kMaxSums + j] = 0;
   __syncthreads();
   const int m = blockIdx.x;
   const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(m) * K);
@@ -975,7 +963,7 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restric
   // 16 vectors, so a step's vectors lie in at most two (r0, r0 + 1)
   for (int v0 = threadIdx.x & ~31; v0 < nvec; v0 += blockDim.x) {
     const int v = v0 + lane;
-    unsigned a = 0;
+    unsigned a = 0, q = 0;
     if (v < nvec) {
       const uint4 raw = __ldg(s + v);
       uint4 lo, hi;
@@ -983,20 +971,29 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const uint8_t* __restric
       d[2 * v] = lo;
       d[2 * v + 1] = hi;
       a = static_cast<unsigned>(abs_sum16(raw));
+      q = sq_sum16(raw);
     }
     const int r0 = (v0 * 16) / sums.sum_len;
     const bool first = (v < nvec ? (v * 16) / sums.sum_len : r0) == r0;
     const unsigned s0 = __reduce_add_sync(0xFFFFFFFFu, first ? a : 0u);
     const unsigned s1 = __reduce_add_sync(0xFFFFFFFFu, first ? 0u : a);
+    const unsigned q0 = __reduce_add_sync(0xFFFFFFFFu, first ? q : 0u);
+    const unsigned q1 = __reduce_add_sync(0xFFFFFFFFu, first ? 0u : q);
     if (lane == 0) {
       if (s0 != 0) atomicAdd(&cnt[r0], static_cast<unsigned long long>(s0));
       if (s1 != 0) atomicAdd(&cnt[r0 + 1], static_cast<unsigned long long>(s1));
+      if (q0 != 0) atomicAdd(&cnt[kMaxSums + r0], static_cast<unsigned long long>(q0));
+      if (q1 != 0) atomicAdd(&cnt[kMaxSums + r0 + 1], static_cast<unsigned long long>(q1));
     }
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x)
+  for (int j = threadIdx.x; j < sums.nsum; j += blockDim.x) {
     sums.asum[static_cast<size_t>(m) * sums.nsum + j] =
         static_cast<int>(cnt[j] < static_cast<unsigned long long>(kSumCap) ? cnt[j] : kSumCap);
+    if (sums.qsum)
+      sums.qsum[static_cast<size_t>(m) * sums.nsum + j] =
+          static_cast<unsigned>(cnt[kMaxSums + j] < 0xFFFFFFFFull ? cnt[kMaxSums + j] : 0xFFFFFFFFull);
+  }
 }
 
 template <int BN>

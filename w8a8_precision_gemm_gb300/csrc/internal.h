@@ -15,6 +15,7 @@ namespace qurl {
 // Status codes written by kernels into the per-device status word.
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 6;  // QURL_ERR_TIMEOUT
+constexpr int kDevBadIndex = 1;  // QURL_ERR_INVALID_ARG: an index read on the device was out of range
 
 constexpr int kQInt8 = 0;  // QURL_INT8
 constexpr int kQFp8 = 1;   // QURL_FP8_E4M3
@@ -44,6 +45,11 @@ struct GemmArgs {
                        // bounded wait runs out and the kernel latches a timeout
   const int* asum;     // INT8 decode: [M][splits] sums of |Xq[m,k]| over each split's k range
                        // (null: every unit accumulates in chunks)
+  const unsigned* qsum;  // INT8 on pairs with widened weights: [M][splits] sums of Xq[m,k]^2 over
+                         // each split's k range, and
+  const unsigned* qn;    // [N] sums of Wq[n,k]^2 over all of K (null: not available)
+  int* scratch;          // INT8 on pairs with widened weights: per CTA, the int32 running sum of a
+                         // unit accumulated in chunks ([gridDim.x][256 columns][128 rows])
 };
 
 // Per-token sums of |code| over consecutive ranges of sum_len codes (the K
@@ -52,8 +58,9 @@ struct GemmArgs {
 constexpr int kMaxSums = 128;
 struct CodeSums {
   int* asum;
-  int sum_len;  // a multiple of 256
-  int nsum;     // <= kMaxSums
+  int sum_len;     // a multiple of 256
+  int nsum;        // <= kMaxSums
+  unsigned* qsum;  // the sums of code^2 over the same ranges (saturated at 2^32 - 1), or null
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -127,6 +134,13 @@ cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long
                                    cudaStream_t st);
 cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned long long* count, int num_sms,
                               cudaStream_t st);
+// quant.cu: FP8 key/value cache quantization into slots, and its read-back (status: the device status word)
+cudaError_t launch_kv_cache_quant(const void* QKV, int M, long long ldq, int q_dim, int kv_heads, int head_dim,
+                                  const long long* slots, long long num_slots, void* kc, float* ks, void* vc,
+                                  float* vs, int* status, cudaStream_t st);
+cudaError_t launch_kv_cache_dequant(const void* cache, const float* scale, const long long* slots, int n,
+                                    int kv_heads, int head_dim, long long num_slots, void* out, int* status,
+                                    cudaStream_t st);
 
 // How one GEMM call is cut into CTAs.
 struct GemmPlan {
@@ -146,6 +160,12 @@ struct GemmPlan {
   int kb_per_split;
   size_t part_bytes;  // split-K partials (after the fp16 copy)
   size_t ws_bytes;    // total workspace: fp16 activation copy + split-K partials
+  // INT8 on CTA pairs with both operands widened to fp16 in the workspace (prefill):
+  bool wide;
+  size_t qsum_off;     // per-token sums of code^2 (after the sums of |code|)
+  size_t w16_off;      // fp16 copy of the weight codes [N, K]
+  size_t qn_off;       // per-channel sums of code^2 [N]
+  size_t scratch_off;  // running sums of chunked units, one region per CTA
 };
 
 // gemm_plan.cu
@@ -173,8 +193,20 @@ cudaError_t launch_gemm_i8p(const CUtensorMap& tw, const CUtensorMap& tx16, cons
                             cudaStream_t st);
 // int8 codes [M, K] -> fp16 [M, K] in dst, and the sums of |code| (saturated at 2^24).
 cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums sums, cudaStream_t st);
+// gemm_i8w.cu: the INT8 GEMM on CTA pairs with both operands widened to fp16 (grid = 256-token tiles,
+// 256-channel tiles, K splits), and the widening of the weight codes with their sums of code^2.
+cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, const GemmArgs& a, dim3 grid,
+                            cudaStream_t st);
+cudaError_t launch_widen_weights(const void* Wq, int N, int K, void* w16, unsigned* qn, int num_sms,
+                                 cudaStream_t st);
+// the CTAs an i8w launch of this plan runs (one per SM of the resident pairs), for sizing its scratch
+int i8w_max_ctas(int num_sms);
 // split-K reduction in split order: T = int (INT8) or float (FP8)
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
                                  const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
                                  cudaStream_t st);
+// probe.cu: tensor-rate probes (route 0: mma.sync s8; 1: tcgen05 kind::f16 from shared memory; 2: the
+// same with A in TMEM; 3: tcgen05 kind::f8f6f4), and the multiply-add operations x 2 of a launch.
+cudaError_t launch_probe(int route, int ctas, int iters, int* status, cudaStream_t st);
+double probe_ops(int route, int ctas, int iters);
 }  // namespace qurl

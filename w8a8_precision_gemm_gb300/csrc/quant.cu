@@ -73,8 +73,11 @@ __device__ __forceinline__ void two_sum_acc(float& s, float& c, float y) {
   c = __fadd_rn(c, err);
 }
 
-// Block-wide sum of (s, c) pairs, compensated; every thread gets the result.
-__device__ __forceinline__ void block_reduce_pair(float& s, float& c, float* red) {
+// The row's mean of squares ms = (s + c) / K (the compensated block sum of
+// x^2, divided in fp64 and rounded to fp32) and r = 1 / sqrt(ms + eps)
+// (correctly rounded fp32 square root and division), computed by one thread
+// and handed to every thread of the block.
+__device__ __forceinline__ void block_mean_sq(float s, float c, float* red, int K, float eps, float& ms, float& r) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -99,13 +102,14 @@ __device__ __forceinline__ void block_reduce_pair(float& s, float& c, float* red
       tc = __fadd_rn(tc, oc);
     }
     if (lane == 0) {
-      red[64] = ts;
-      red[65] = tc;
+      const float m = static_cast<float>((static_cast<double>(ts) + static_cast<double>(tc)) / static_cast<double>(K));
+      red[64] = m;
+      red[65] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(m, eps)));
     }
   }
   __syncthreads();
-  s = red[64];
-  c = red[65];
+  ms = red[64];
+  r = red[65];
   __syncthreads();
 }
 
@@ -125,23 +129,34 @@ __device__ __forceinline__ Enc make_enc(float amax, int qt) {
   return {scale, __frcp_rn(scale), qt};
 }
 
-// Code of v / scale.  INT8: the IEEE quotient fl(v / scale) rounded to the
-// nearest integer, ties to even, clamped to +-127.  For |v / scale| < 256 the
-// product r = v * fl(1 / scale) lies within 5e-5 of fl(v / scale) (three
-// roundings of relative size 2^-24 each), so wherever r is more than 1e-4 away
-// from a half-integer both round to the same integer and r is used; otherwise
-// (one code in ~5000, and NaN or out-of-range inputs) the quotient itself is
-// computed.  The codes are therefore those of the plain division.
+// Code of v / scale.  Both types are decided on the IEEE quotient fl(v /
+// scale), but most codes come from the product r = v * fl(1 / scale) instead:
+// r carries two roundings of relative size 2^-24 on top of the exact quotient,
+// so it lies within 2.5 units in the last place of fl(v / scale).
+//  * INT8: fl(v / scale) rounded to the nearest integer, ties to even, clamped
+//    to +-127.  For |r| < 256 r is within 5e-5 of the quotient, so wherever r
+//    is more than 1e-4 away from a half-integer both round to the same integer
+//    and r is used; otherwise (one code in ~5000, and NaN or out-of-range
+//    inputs) the quotient itself is computed.
+//  * FP8-E4M3: round to nearest even with saturation to +-448.  For magnitudes
+//    of at least 2^-6 (e4m3's normal range) the code keeps 3 of fp32's 23
+//    fraction bits, so r and the quotient give the same code unless the 20
+//    dropped bits of r lie within 8 units of the halfway pattern 0x80000; then,
+//    and below 2^-6 (e4m3 subnormals round at another bit) or for non-finite
+//    r, the quotient itself is computed.
+// The codes are therefore those of the plain division.
 __device__ __forceinline__ uint8_t encode(float v, const Enc& e) {
+  const float r = __fmul_rn(v, e.inv);
   if (e.qt == kQInt8) {
-    const float r = __fmul_rn(v, e.inv);
     const float f = r - floorf(r);
     const bool fast = fabsf(r) < 256.0f && fabsf(f - 0.5f) > 1e-4f;
     int q = __float2int_rn(fast ? r : __fdiv_rn(v, e.scale));
     q = max(-127, min(127, q));
     return static_cast<uint8_t>(static_cast<int8_t>(q));
   }
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, e.scale), __NV_SATFINITE, __NV_E4M3));
+  const uint32_t b = __float_as_uint(r) & 0x7FFFFFFFu;
+  const bool fast = b >= 0x3C800000u && b < 0x7F800000u && ((b & 0xFFFFFu) - 0x7FFF8u) > 16u;
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(fast ? r : __fdiv_rn(v, e.scale), __NV_SATFINITE, __NV_E4M3));
 }
 
 // 8 values -> 8 code bytes packed in a uint2 (little-endian byte order = k order).
@@ -160,50 +175,66 @@ constexpr int kAbsSumCap = 1 << 24;
 
 // Store 8 codes (and, for INT8 when x16 is given, the same 8 codes as fp16 --
 // exact, integers of magnitude <= 127 -- for the tensor-core GEMM to read).
-// Returns the sum of |code| of the 8 INT8 codes when x16 is given, else 0.
-__device__ __forceinline__ int store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
-                                      const float (&v)[8], const Enc& en) {
+// Returns the sum of |code| and the sum of code^2 of the 8 INT8 codes when x16
+// is given, else zeros.
+__device__ __forceinline__ int2 store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
+                                       const float (&v)[8], const Enc& en) {
   const uint2 c = encode8(v, en);
   reinterpret_cast<uint2*>(q)[idx] = c;
-  if (x16 == nullptr) return 0;
+  if (x16 == nullptr) return make_int2(0, 0);
   {
+    // the same 8 codes as fp16, exactly: with u = c + 128 in [0, 255], the
+    // fp16 with bits 0x6400 | u is 1024 + u, and subtracting 1152 leaves c
+    const uint32_t w[2] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
     uint32_t h[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t w = e < 2 ? c.x : c.y;
-      const int lo = static_cast<int8_t>((w >> (16 * (e & 1))) & 0xFF);
-      const int hi = static_cast<int8_t>((w >> (16 * (e & 1) + 8)) & 0xFF);
-      const __half2 p = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
-      h[e] = *reinterpret_cast<const uint32_t*>(&p);
+      const uint32_t p = __byte_perm(w[e >> 1], 0x64646464u, (e & 1) ? 0x4342 : 0x4140);
+      const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&p), bias);
+      h[e] = *reinterpret_cast<const uint32_t*>(&d);
     }
     reinterpret_cast<uint4*>(x16)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
   }
-  return static_cast<int>(__dp4a(__vabs4(c.y), 0x01010101u, __dp4a(__vabs4(c.x), 0x01010101u, 0u)));
+  const int a = static_cast<int>(__dp4a(__vabs4(c.y), 0x01010101u, __dp4a(__vabs4(c.x), 0x01010101u, 0u)));
+  const int sq = __dp4a(static_cast<int>(c.y), static_cast<int>(c.y), __dp4a(static_cast<int>(c.x),
+                                                                              static_cast<int>(c.x), 0));
+  return make_int2(a, sq);
 }
 
-// Per-row sums of |code| over the ranges of a CodeSums, in shared-memory
-// counters: one atomic per warp and step (the 32 vectors of 8 codes a warp
-// visits in one step lie in one range, as ranges are multiples of 256 codes).
+// Per-row sums of |code| (and of code^2) over the ranges of a CodeSums, in
+// shared-memory counters cnt[0, kMaxSums) and cnt[kMaxSums, 2 kMaxSums): one
+// atomic per warp, step and sum (the 32 vectors of 8 codes a warp visits in
+// one step lie in one range, as ranges are multiples of 256 codes).
 // sums_begin zeroes the counters; the block reductions that follow in every
 // kernel order it before the first sums_add_warp.
 __device__ __forceinline__ void sums_begin(unsigned long long* cnt, const CodeSums& cs) {
   if (cs.asum != nullptr)
-    for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x) cnt[j] = 0;
+    for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x) cnt[j] = cnt[kMaxSums + j] = 0;
 }
 
-// Called by all 32 lanes of the warp; idx: this lane's vector; v: its sum (0 if none).
-__device__ __forceinline__ void sums_add_warp(unsigned long long* cnt, const CodeSums& cs, int idx, int v) {
+// Called by all 32 lanes of the warp; idx: this lane's vector; v: its sums (0 if none).
+__device__ __forceinline__ void sums_add_warp(unsigned long long* cnt, const CodeSums& cs, int idx, int2 v) {
   if (cs.asum == nullptr) return;
-  const unsigned s = __reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(v));
-  if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(&cnt[(idx * 8) / cs.sum_len], static_cast<unsigned long long>(s));
+  const unsigned s = __reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(v.x));
+  const unsigned q = cs.qsum ? __reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(v.y)) : 0u;
+  if ((threadIdx.x & 31) == 0) {
+    const int r = (idx * 8) / cs.sum_len;
+    if (s != 0) atomicAdd(&cnt[r], static_cast<unsigned long long>(s));
+    if (q != 0) atomicAdd(&cnt[kMaxSums + r], static_cast<unsigned long long>(q));
+  }
 }
 
 __device__ __forceinline__ void sums_end(unsigned long long* cnt, const CodeSums& cs, int m) {
   if (cs.asum == nullptr) return;
   __syncthreads();
-  for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x)
+  for (int j = threadIdx.x; j < cs.nsum; j += blockDim.x) {
     cs.asum[static_cast<size_t>(m) * cs.nsum + j] =
         static_cast<int>(cnt[j] < static_cast<unsigned long long>(kAbsSumCap) ? cnt[j] : kAbsSumCap);
+    if (cs.qsum)
+      cs.qsum[static_cast<size_t>(m) * cs.nsum + j] =
+          static_cast<unsigned>(cnt[kMaxSums + j] < 0xFFFFFFFFull ? cnt[kMaxSums + j] : 0xFFFFFFFFull);
+  }
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
@@ -262,7 +293,7 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
   griddep_wait();
   griddep_launch_dependents();
   __shared__ float red[33];
-  __shared__ unsigned long long cnt[kMaxSums];
+  __shared__ unsigned long long cnt[2 * kMaxSums];
   sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -282,7 +313,7 @@ __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloa
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
-    int v = 0;
+    int2 v = make_int2(0, 0);
     if (valid) {
       float x[8];
       bf16x8_to_f32(u, x);
@@ -304,7 +335,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
   griddep_wait();
   griddep_launch_dependents();
   __shared__ float red[66];
-  __shared__ unsigned long long cnt[kMaxSums];
+  __shared__ unsigned long long cnt[2 * kMaxSums];
   sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * ldx);
@@ -325,9 +356,14 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
 #pragma unroll
     for (int e = 0; e < 8; ++e) two_sum_acc(ss, sc, __fmul_rn(x[e], x[e]));
   });
-  block_reduce_pair(ss, sc, red);
-  const float ms = static_cast<float>((static_cast<double>(ss) + static_cast<double>(sc)) / static_cast<double>(K));
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  // the gain of the vectors this thread normalises is read while the sums are reduced
+#pragma unroll
+  for (int c = 0; c < kVPT; ++c) {
+    const int idx = threadIdx.x + c * blockDim.x;
+    if (idx < nvec) asm volatile("prefetch.global.L1 [%0];" ::"l"(g4 + 2 * idx));
+  }
+  float ms, r;
+  block_mean_sq(ss, sc, red, K, eps, ms, r);
   if (threadIdx.x == 0 && ms_out) ms_out[m] = ms;
   // v = (x * r) * gamma'
   auto normed = [&](const uint4 u, int idx, float (&x)[8]) {
@@ -350,7 +386,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
-    int v = 0;
+    int2 v = make_int2(0, 0);
     if (valid) {
       float x[8];
       normed(u, idx, x);
@@ -369,8 +405,12 @@ __device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float 
   bf16x8_to_f32(uu, u);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
+    // g / (1 + exp(-g)) to within ~2 units in the last place (h is held to a
+    // relative 2e-6 of the exact value; the codes are decided on this h).  A
+    // denominator beyond 2^126 (g < -87.3) makes |h| < 2e-36: 0.
     const float den = __fadd_rn(1.0f, expf(-g[e]));
-    h[e] = __fmul_rn(__fdiv_rn(g[e], den), u[e]);
+    const float sg = den < 0x1p126f ? __fdividef(g[e], den) : 0.0f;
+    h[e] = __fmul_rn(sg, u[e]);
   }
 }
 
@@ -384,7 +424,7 @@ __global__ void __launch_bounds__(kRowThreads, MINB) silu_mul_quant_kernel(const
   griddep_wait();
   griddep_launch_dependents();
   __shared__ float red[33];
-  __shared__ unsigned long long cnt[kMaxSums];
+  __shared__ unsigned long long cnt[2 * kMaxSums];
   sums_begin(cnt, sums);
   const int m = blockIdx.x;
   const uint4* grow = reinterpret_cast<const uint4*>(GU + static_cast<size_t>(m) * ldgu);
@@ -425,7 +465,7 @@ __global__ void __launch_bounds__(kRowThreads, MINB) silu_mul_quant_kernel(const
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
   // pass 2: codes (warp-uniform steps, see for_vectors_warp)
   auto put = [&](float (&h)[8], int idx, bool valid) {
-    int v = 0;
+    int2 v = make_int2(0, 0);
     if (valid) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
@@ -538,6 +578,86 @@ __global__ void count_diff_kernel(const uint8_t* __restrict__ a, const uint8_t* 
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(count, c);
 }
 
+// ------------------------------------------------------------------ FP8 key/value cache
+
+// One warp per (token, KV head, key or value): the head's head_dim values
+// (16-byte vectors of 8 bf16, one per lane; head_dim <= 256) are quantized as
+// one row with the FP8 rule -- the per-token rule applied to each attention
+// head -- and the codes and the scale are written to the token's cache slot.
+// A negative slot (padding) writes nothing; a slot >= num_slots writes
+// nothing and latches kDevBadIndex.
+__global__ void __launch_bounds__(256) kv_cache_quant_kernel(const __nv_bfloat16* __restrict__ QKV, int M,
+                                                             long long ldq, int q_dim, int kv_heads, int head_dim,
+                                                             const long long* __restrict__ slots,
+                                                             long long num_slots, uint8_t* __restrict__ kc,
+                                                             float* __restrict__ ks, uint8_t* __restrict__ vc,
+                                                             float* __restrict__ vs, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= static_cast<long long>(M) * kv_heads * 2) return;
+  const int part = static_cast<int>(item & 1);  // 0: key, 1: value
+  const long long th = item >> 1;
+  const int h = static_cast<int>(th % kv_heads);
+  const long long m = th / kv_heads;
+  const long long slot = __ldg(slots + m);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) atomicCAS(status, kDevOk, kDevBadIndex);
+    return;
+  }
+  const int nvec = head_dim >> 3;
+  const uint4* src = reinterpret_cast<const uint4*>(QKV + m * ldq + q_dim + static_cast<long long>(part) * kv_heads * head_dim +
+                                                    static_cast<long long>(h) * head_dim);
+  float x[8] = {};
+  if (lane < nvec) bf16x8_to_f32(__ldg(src + lane), x);
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  amax = warp_max(amax);
+  const Enc en = make_enc(amax, kQFp8);
+  const long long at = slot * kv_heads + h;
+  uint8_t* dst = (part ? vc : kc) + at * head_dim;
+  if (lane < nvec) reinterpret_cast<uint2*>(dst)[lane] = encode8(x, en);
+  if (lane == 0) (part ? vs : ks)[at] = en.scale;
+}
+
+// The values a cache holds for the slots a reader gathers: out[n][h hd + d] =
+// bf16_RNE(fp32(e4m3 value) * scale); one thread per 8 values.
+__global__ void __launch_bounds__(256) kv_cache_dequant_kernel(const uint8_t* __restrict__ cache,
+                                                               const float* __restrict__ scale,
+                                                               const long long* __restrict__ slots, int n,
+                                                               int kv_heads, int head_dim, long long num_slots,
+                                                               __nv_bfloat16* __restrict__ out, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int per_row = kv_heads * head_dim / 8;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(n) * per_row) return;
+  const long long i = idx / per_row;
+  const int j = static_cast<int>(idx - i * per_row);
+  const long long slot = __ldg(slots + i);
+  if (slot < 0 || slot >= num_slots) {
+    atomicCAS(status, kDevOk, kDevBadIndex);
+    return;
+  }
+  const int h = (j * 8) / head_dim;
+  const float sc = __ldg(scale + slot * kv_heads + h);
+  const uint2 c = __ldg(reinterpret_cast<const uint2*>(cache + slot * kv_heads * head_dim) + j);
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t w = e < 2 ? c.x : c.y;
+    const int sh = 16 * (e & 1);
+    const __nv_fp8_e4m3 a = *reinterpret_cast<const __nv_fp8_e4m3*>(reinterpret_cast<const uint8_t*>(&w) + sh / 8);
+    const __nv_fp8_e4m3 b = *reinterpret_cast<const __nv_fp8_e4m3*>(reinterpret_cast<const uint8_t*>(&w) + sh / 8 + 1);
+    const __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(static_cast<float>(a), sc), __fmul_rn(static_cast<float>(b), sc));
+    o[e] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  reinterpret_cast<uint4*>(out + i * kv_heads * head_dim)[j] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Threads per row-CTA: enough that `per` vectors per thread cover the row, at
 // most kRowThreads (longer rows stream their tail from L1/L2 in the code pass).
 // With few rows (decode batches: fewer rows than ~2 per SM) a row gets about 2
@@ -606,6 +726,25 @@ cudaError_t launch_count_diff(const void* a, const void* b, size_t n, unsigned l
   if (blocks < 1) blocks = 1;
   return launch_pdl(count_diff_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
                     reinterpret_cast<const uint8_t*>(a), reinterpret_cast<const uint8_t*>(b), n, count);
+}
+
+cudaError_t launch_kv_cache_quant(const void* QKV, int M, long long ldq, int q_dim, int kv_heads, int head_dim,
+                                  const long long* slots, long long num_slots, void* kc, float* ks, void* vc,
+                                  float* vs, int* status, cudaStream_t st) {
+  const long long items = static_cast<long long>(M) * kv_heads * 2;
+  const unsigned blocks = static_cast<unsigned>((items + 7) / 8);
+  return launch_pdl(kv_cache_quant_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const __nv_bfloat16*>(QKV),
+                    M, ldq, q_dim, kv_heads, head_dim, slots, num_slots, reinterpret_cast<uint8_t*>(kc), ks,
+                    reinterpret_cast<uint8_t*>(vc), vs, status);
+}
+
+cudaError_t launch_kv_cache_dequant(const void* cache, const float* scale, const long long* slots, int n,
+                                    int kv_heads, int head_dim, long long num_slots, void* out, int* status,
+                                    cudaStream_t st) {
+  const long long items = static_cast<long long>(n) * kv_heads * head_dim / 8;
+  const unsigned blocks = static_cast<unsigned>((items + 255) / 256);
+  return launch_pdl(kv_cache_dequant_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint8_t*>(cache),
+                    scale, slots, n, kv_heads, head_dim, num_slots, reinterpret_cast<__nv_bfloat16*>(out), status);
 }
 
 }  // namespace qurl
