@@ -290,7 +290,7 @@ class Buffers:
         self.sx = torch.empty(M, dtype=torch.float32, device=dev)
         self.y = {name: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for name, _, N in chain_shapes(model)}
         nws = max(q.qurl_workspace_size(M, N, K, qt) for _, K, N in chain_shapes(model))
-        self.ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(nws, 16), dtype=torch.uint8, device=dev)  # its last bytes: handoff counters
 
 
 def dense(buf, M, K):

@@ -145,9 +145,16 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
  * qurl_w8a8_gemm_acc and the fused *_linear entries) use for this shape at
  * full speed: split-K partial sums and, for INT8, an fp16 copy of the
  * activation codes (2 M K bytes) with per-token sums of |code| over each K
- * split.  A smaller workspace (or none) is accepted: the kernels then split K
- * into fewer parts and INT8, without room for the fp16 copy, widens both
- * operands in shared memory instead (slower, same result).
+ * split, the int32 running sums of units accumulated in chunks (one region
+ * per SM), and from 2048 tokens on an fp16 copy of the weight codes (2 N K
+ * bytes) with their per-channel sums of squares.  The last 256 bytes of any
+ * workspace hold two counters through which the CTAs of a fused decode call
+ * hand over (see the fused entries): they must be zero before the
+ * workspace's first use by a fused entry, and every call leaves them zero.
+ * A smaller workspace (or none) is accepted: the kernels then split K into
+ * fewer parts and INT8, without room for the fp16 copies, keeps the weights
+ * in TMEM or widens both operands in shared memory instead (slower, same
+ * result); a fused entry then runs its quantizer as a separate kernel.
  */
 size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
 
@@ -218,6 +225,18 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
  * ([UAQ]: s lives in gamma', so Y = W (RMSNorm_gamma(X)) up to quantization).
  * Xq_scratch [M, K] codes and sx_scratch [M] fp32 are caller-provided
  * intermediate buffers (they hold the quantized activation afterwards).
+ *
+ * The fused entries (this one and the two below) compute exactly what their
+ * quantizer followed by qurl_w8a8_linear computes.  For decode batches (M <=
+ * 256) with a full workspace they are ONE kernel (plus the split-K reduction
+ * where K is split): the GEMM's CTAs first quantize the input rows between
+ * them, hand over through the two counters in the workspace's last 256 bytes
+ * (zero before the first use, left zero by every call), then run the product.
+ * Calls sharing a workspace must not overlap on the GPU.  If that handoff
+ * times out (qurl_check_device_status returns QURL_ERR_TIMEOUT) the counters
+ * are left set: zero the workspace's last 256 bytes before its next use.
+ * Otherwise (prefill, or a smaller workspace) the quantizer is a separate
+ * kernel launched before the GEMM.
  */
 qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma_folded, float eps,
                                       const void* Wq, const float* sw, int M, int N, int K, qurl_qtype qt,
@@ -340,11 +359,13 @@ qurl_status qurl_check_device_status(qurl_stream_t stream);
 
 /* Fault injection, for testing the failure path: the next GEMM this process
  * launches (any linear / gemm_acc entry) skips the first k-block load of each
- * CTA, so a shared-memory stage is never filled; the waits on it run out
- * after ~1 s, the kernel latches QURL_ERR_TIMEOUT in the device status word,
- * lets its own copies land, frees its tensor memory and exits.  Its outputs
- * are then undefined; qurl_check_device_status() returns QURL_ERR_TIMEOUT and
- * clears the word, and later calls run normally.  One-shot; always QURL_OK. */
+ * CTA, so a shared-memory stage is never filled -- or, in a fused decode call,
+ * its first CTA does not arrive at the handoff; the waits run out after ~1 s,
+ * the kernel latches QURL_ERR_TIMEOUT in the device status word, lets its own
+ * copies land, frees its tensor memory and exits.  Its outputs are then
+ * undefined; qurl_check_device_status() returns QURL_ERR_TIMEOUT and clears
+ * the word, and later calls run normally (after a fused call, once the
+ * workspace's last 256 bytes are zeroed again).  One-shot; always QURL_OK. */
 qurl_status qurl_debug_inject_timeout(void);
 
 /* The GEMM plan the library takes for an M x N x K product of `qt` codes on a

@@ -143,9 +143,9 @@ def test_acr_objective_validation(L):
 def test_workspace_size_without_gpu(L):
     # sized for the SM count of the device (or the largest target when none is visible)
     assert L.qurl_workspace_size(0, 8, 256, 0) == 0
-    ws = L.qurl_workspace_size(64, 4608, 3584, 1)  # FP8 decode: split-K partials only
-    assert ws > 0 and ws % (64 * 4608 * 4) == 0
-    assert L.qurl_workspace_size(8192, 55296, 5120, 1) == 0  # prefill fills the GPU without splitting K
+    ws = L.qurl_workspace_size(64, 4608, 3584, 1)  # FP8 decode: split-K partials and the handoff counters
+    assert ws > 256 and (ws - 256) % (64 * 4608 * 4) == 0
+    assert L.qurl_workspace_size(8192, 55296, 5120, 1) == 256  # prefill fills the GPU without splitting K
 
 
 def _tile_widths(p):
@@ -194,10 +194,10 @@ def test_plan_workspace_and_fallbacks(L):
         assert q.plan(M, N, K, qt, 160)["ws_bytes"] == L.qurl_workspace_size(M, N, K, qt)
     # no workspace: INT8 widens both operands in shared memory and K is not split
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=0)
-    assert p["kernel"] == 0 and p["splits"] == 1 and p["ws_bytes"] == 0
+    assert p["kernel"] == 0 and p["splits"] == 1 and p["ws_bytes"] == 256  # (a fused call wants the counters)
     # a workspace too small for split partials keeps the TMEM kernel unsplit (fp16 codes, their
     # sums, and one 128 x 128 int32 running-sum region per SM)
-    act = 64 * 3584 * 2 + 256 + 152 * 128 * 128 * 4
+    act = 64 * 3584 * 2 + 256 + 152 * 128 * 128 * 4 + 256  # ... and the handoff counters
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=act)
     assert p["kernel"] == 1 and p["splits"] == 1 and p["ws_bytes"] <= act
     # without room for the running sums: both operands widened in shared memory

@@ -365,8 +365,9 @@ def test_gemm_int8_decode_unsplit_long_k(M, small):
     xq = g.integers(-lim, lim + 1, size=(M, K)).astype(np.int8)
     wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # fp16 codes, their sums, and the per-CTA running sums of chunked units (128 x 128 int32 each)
-    act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256 + sms * 128 * 128 * 4
+    # fp16 codes, their sums, the per-CTA running sums of chunked units (128 x 128 int32 each) and
+    # the fused entries' handoff counters
+    act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256 + sms * 128 * 128 * 4 + 256
     assert q.qurl_workspace_size(M, N, K, q.INT8) > act  # the full-size plan would split K
     ws = torch.empty(act, dtype=torch.uint8, device="cuda")
     acc = q.gemm_acc(to_dev(xq.view(np.uint8), q.INT8), to_dev(wq.view(np.uint8), q.INT8), q.INT8, ws)
@@ -692,9 +693,7 @@ def test_split_k_reduction(qt):
         launches = q.qurl_kernel_launches() - n0
         acc = q.gemm_acc(args[0], args[2], qt, ws)
         sync_ok()
-        # INT8 decode workspace: fp16 copy of the codes, then per-token sums of |code|
-        act = ((M * K * 2 + 255) // 256) * 256 + ((M * 4 + 255) // 256) * 256 if qt == q.INT8 else 0
-        split = ws is not None and ws.numel() > act
+        split = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)["splits"] > 1
         assert launches == 1 + int(split) + int(qt == q.INT8), (tiles, launches)
         Yo, acco = oracle.w8a8_linear(Xq, sx, Wq, sw, oqt(qt), nthreads=NT)
         if qt == q.INT8:

@@ -364,8 +364,11 @@ def silu_mul_quant(GU, qt, pre_scale=1.0, want_h=False, stream=None):
 
 
 def workspace(M, N, K, qt, device="cuda"):
+    """Workspace for a linear call of this shape, zero-filled: its last 256 bytes
+    hold the fused entry points' handoff counters, which must start at zero (and
+    which every call leaves at zero)."""
     nbytes = qurl_workspace_size(M, N, K, qt)
-    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
+    return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
 
 
 def linear(Xq, sx, Wq, sw, qt, ws=None, stream=None):

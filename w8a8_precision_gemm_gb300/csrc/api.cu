@@ -201,9 +201,12 @@ qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
 //              Wq and lets the GEMM launch only after its own wait, so every
 //              earlier kernel has completed and the GEMM may load weights
 //              before that kernel ends.
+//   fq:        a fused entry's quantizer for the decode GEMM to run first (null:
+//              the activation codes are an input), writing its code sums to fsums.
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                     bool x16_ready = false, bool w_indep = false) {
+                     bool x16_ready = false, bool w_indep = false, const qurl::FusedQuant* fq = nullptr,
+                     qurl::CodeSums fsums = qurl::CodeSums{}) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
@@ -253,6 +256,11 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.qsum = sums.qsum;
   a.qn = p.wide ? reinterpret_cast<const unsigned*>(wsb + p.qn_off) : nullptr;
   a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
+  if (fq) {
+    a.fq = *fq;
+    a.fsums = fsums;
+    a.w_prefetch = 0;  // the kernel before this one may write Wq; the fused kernel loads weights after its wait
+  }
   const dim3 grid(p.tiles_tok, p.tiles_ch, p.splits);
   if (p.wide)
     QURL_CUDA(qurl::launch_gemm_i8w(ta, tb, a, grid, st));
@@ -425,6 +433,8 @@ qurl_status qurl_w8a8_gemm_acc(const void* Xq, const void* Wq, int M, int N, int
 struct FusedAct {
   void* x16 = nullptr;
   qurl::CodeSums sums{};
+  bool in_gemm = false;      // the GEMM kernel runs the quantizer itself
+  unsigned* sync = nullptr;  // its handoff counters (the workspace's last bytes)
 };
 
 FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
@@ -436,7 +446,33 @@ FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
     f.x16 = ws;
     f.sums = code_sums(p, ws);
   }
+  // decode plans whose GEMM kernel runs the quantizer itself: the INT8 kernel
+  // with the widened weights in TMEM (single CTA) and the FP8 decode kernels
+  f.in_gemm = ws != nullptr && ws_bytes >= p.ws_bytes && M <= 256 && p.swap && !p.wide &&
+              (qt == QURL_INT8 ? (p.tmem_a && !p.pair) : true);
+  if (f.in_gemm)
+    f.sync = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(ws) +
+                                         ((ws_bytes - qurl::kSyncBytes) & ~static_cast<size_t>(15)));
   return f;
+}
+
+// A fused entry as one GEMM kernel that quantizes its input rows first (plus
+// the split-K reduction where K is split).
+qurl_status run_fused(const FusedAct& f, int kind, const void* X, int ldx, const float* gamma, float eps, float pre,
+                      const void* Wq, const float* sw, int M, int N, int K, int qt, void* Y, int ldy, void* Xq,
+                      float* sx, void* ws, size_t ws_bytes, cudaStream_t st) {
+  qurl::FusedQuant fq{};
+  fq.kind = kind;
+  fq.X = X;
+  fq.ldx = ldx;
+  fq.gamma = gamma;
+  fq.eps = eps;
+  fq.pre = pre;
+  fq.Xq = Xq;
+  fq.sx = sx;
+  fq.x16 = f.x16;
+  fq.sync = f.sync;
+  return run_gemm(Xq, sx, Wq, sw, M, N, K, qt, Y, ldy, nullptr, ws, ws_bytes, st, true, false, &fq, f.sums);
 }
 
 qurl_status check_fused_out(const void* Wq, const float* sw, int M, int N, int K, int qt, void* Y, int ldy,
@@ -457,6 +493,9 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  if (f.in_gemm)
+    return run_fused(f, qurl::kFuseRmsNorm, X, ldx, gamma_folded, eps, 1.0f, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
+                     sx_scratch, workspace, ws_bytes, st);
   QURL_CUDA(qurl::launch_rmsnorm_quant(X, M, K, ldx, gamma_folded, eps, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
                                        f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
@@ -471,6 +510,9 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  if (f.in_gemm)
+    return run_fused(f, qurl::kFuseQuant, X, ldx, nullptr, 0.0f, pre_scale, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
+                     sx_scratch, workspace, ws_bytes, st);
   QURL_CUDA(qurl::launch_quant_act(X, M, K, ldx, pre_scale, qt, Xq_scratch, sx_scratch, f.x16, f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, K, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
                   f.x16 != nullptr, true);
@@ -486,6 +528,9 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const FusedAct f = fused_x16(M, N, I, qt, workspace, ws_bytes);
+  if (f.in_gemm)
+    return run_fused(f, qurl::kFuseSiluMul, GU, ldgu, nullptr, 0.0f, pre_scale, Wq, sw, M, N, I, qt, Y, ldy,
+                     Xq_scratch, sx_scratch, workspace, ws_bytes, st);
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
                                         f.sums, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,

@@ -36,6 +36,7 @@
 
 #include <type_traits>
 
+#include "fused_quant.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -301,8 +302,9 @@ __device__ __forceinline__ void emit32_swap(const GemmArgs& a, int mode, int a0,
 
 // Scales the swap epilogue hands to emit32_swap: this lane's token b0 + c0 +
 // lane, and its channel n (0 where out of range or not needed).
+// (coherent loads: in a fused call this grid itself wrote sx)
 __device__ __forceinline__ float token_scale(const GemmArgs& a, int mode, int m) {
-  return (mode == kModeBf16 && m < a.M) ? __ldg(a.sx + m) : 0.0f;
+  return (mode == kModeBf16 && m < a.M) ? __ldcg(a.sx + m) : 0.0f;
 }
 __device__ __forceinline__ float channel_scale(const GemmArgs& a, int mode, int n) {
   return (mode == kModeBf16 && n < a.N) ? __ldg(a.sw + n) : 0.0f;
@@ -415,29 +417,45 @@ __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
-  if (warp != 0) griddep_wait();
+  // a fused call quantizes its input rows first (decode orientation; FP8)
+  const bool fused = SWAP && !C::kInt8 && args.fq.kind != kFuseNone;
+  if (warp != 0 || fused) griddep_wait();
 
-  if (warp == 0) {
+  const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
+  const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
+  // Weight tiles of the first stages may stream in while the previous kernel
+  // (which, per w_prefetch, does not write Wq) is finishing, or, in a fused
+  // call, while this kernel quantizes its input rows.
+  int npre = 0;  // meaningful in the producer thread
+  if (warp == 0 && lane == 0 && (args.w_prefetch || fused) && !args.fault && R.u < R.end) {
+    const Unit w = unit_of<SWAP, BN>(args, R.u);
+    npre = min(STAGES, w.nkb);
+    for (int it = 0; it < npre; ++it) {
+      mbar_arrive_expect_tx(&bars.full[it], C::A_STAGE + C::B_STAGE);
+      const int kc = (w.kb0 + it) * C::BK;
+      if (SWAP)
+        tma_load_2d(stA + it * C::A_STAGE, &tmA, kc, w.a0, &bars.full[it], polA);
+      else
+        tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, w.b0, &bars.full[it], polB);
+    }
+  }
+  bool run = true;
+  if constexpr (SWAP && !C::kInt8) {
+    if (fused)  // the token stages are free until the handoff: they hold the rows' reduction scratch
+      run = fused_quant_prologue<4>(args.fq, args.fsums, args.M, args.K, QT,
+                                    *reinterpret_cast<rq::RowScratch*>(stB), args.status, args.fault);
+  }
+
+  if (!run) {
+    // the handoff ran out (the timeout is latched): no role runs; the weight
+    // copies already issued land before the CTA leaves (their barriers also
+    // count the token halves never issued: bounded waits)
+    if (warp == 0 && lane == 0)
+      for (int j = 0; j < npre; ++j) mbar_wait_drain(&bars.full[j], 0, args.status);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
-      const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
-      // Weight tiles of the first stages may stream in while the previous
-      // kernel (which, per w_prefetch, does not write Wq) is finishing.
-      int npre = 0;
-      if (args.w_prefetch && !args.fault && R.u < R.end) {
-        const Unit w = unit_of<SWAP, BN>(args, R.u);
-        npre = min(STAGES, w.nkb);
-        for (int it = 0; it < npre; ++it) {
-          mbar_arrive_expect_tx(&bars.full[it], C::A_STAGE + C::B_STAGE);
-          const int kc = (w.kb0 + it) * C::BK;
-          if (SWAP)
-            tma_load_2d(stA + it * C::A_STAGE, &tmA, kc, w.a0, &bars.full[it], polA);
-          else
-            tma_load_2d(stB + it * C::B_STAGE, &tmB, kc, w.b0, &bars.full[it], polB);
-        }
-      }
-      griddep_wait();
+      if (!fused) griddep_wait();
       int g = 0;  // k-blocks issued by this CTA (ring position)
       bool ok = true;
       for (int u = R.u; u < R.end && ok; u += R.stride) {

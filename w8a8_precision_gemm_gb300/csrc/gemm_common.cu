@@ -65,11 +65,19 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
 
 GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
-GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
+GemmPlan plan_data(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan w{};
   if (qt == kQInt8 && M >= kWideMinM && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
   const GemmPlan p = plan_narrow(M, N, K, qt, num_sms, ws_avail);
   if (p.tmem_a && p.pair && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
+  return p;
+}
+
+// The last kSyncBytes of every workspace are reserved for the handoff counters
+// of the fused entry points; the plan's regions fit before them.
+GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
+  GemmPlan p = plan_data(M, N, K, qt, num_sms, ws_avail >= kSyncBytes ? ws_avail - kSyncBytes : 0);
+  p.ws_bytes += kSyncBytes;
   return p;
 }
 

@@ -18,6 +18,7 @@
 // rank 0's MMA thread releases each stage in both CTAs with one multicast
 // commit.  Only the epilogue's "accumulator drained" signal crosses CTAs by
 // thread arrivals (once per tile).
+#include "fused_quant.cuh"
 #include "gemm.cuh"
 
 namespace qurl {
@@ -122,13 +123,41 @@ __global__ void __launch_bounds__(192, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  if (warp == 0) {
+  // the operand read once (weights, decode) streams through L2 first
+  const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
+  const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
+  const uint32_t full0 = cluster_map(&bars.full[0], 0);
+  // A fused call (decode) quantizes its input rows first; meanwhile the weight
+  // halves of the first stages stream in (their barriers on rank 0 are armed
+  // with both CTAs' full stage bytes, the token halves follow the handoff).
+  const bool fused = SWAP && args.fq.kind != kFuseNone;
+  int npre = 0;  // meaningful in the producer thread
+  if (fused && warp == 0 && lane == 0 && !args.fault && u_begin < u_end) {
+    const PairUnit w = pair_unit<SWAP, BN>(args, u_begin, rank);
+    npre = min(STAGES, w.nkb);
+    for (int it = 0; it < npre; ++it) {
+      if (rank == 0) mbar_arrive_expect_tx(&bars.full[it], C::PAIR_TX);
+      tma_load_2d_pair(stA + it * C::A_STAGE, &tmA, (w.kb0 + it) * C::BK, w.a0, full0 + it * 8, polA);
+    }
+  }
+  bool run = true;
+  if constexpr (SWAP) {
+    if (fused)  // the token stages are free until the handoff: they hold the rows' reduction scratch
+      run = fused_quant_prologue<4>(args.fq, args.fsums, args.M, args.K, kQFp8,
+                                    *reinterpret_cast<rq::RowScratch*>(stB), status, args.fault);
+  }
+
+  if (!run) {
+    // the handoff ran out (the timeout is latched): no role runs.  Rank 0's
+    // barriers of the stages issued count both CTAs' weight halves (and the
+    // token halves never issued: bounded waits), so once they are done no copy
+    // of either CTA is in flight; rank 1 leaves after the closing cluster
+    // barrier, which rank 0 reaches after this.
+    if (warp == 0 && lane == 0 && rank == 0)
+      for (int j = 0; j < npre; ++j) mbar_wait_drain(&bars.full[j], 0, status);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      // the operand read once (weights, decode) streams through L2 first
-      const uint64_t polA = SWAP ? l2_policy_evict_first() : l2_policy_evict_last();
-      const uint64_t polB = SWAP ? l2_policy_evict_last() : l2_policy_evict_normal();
-      const uint32_t full0 = cluster_map(&bars.full[0], 0);
       int g = 0;
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; u += u_stride) {
@@ -136,6 +165,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int it = 0; it < w.nkb; ++it, ++g) {
           const int s = g % STAGES;
           if (args.fault && g == 0) continue;  // injected fault: this stage never fills
+          if (g < npre) {  // the weight half is in flight; add the token half
+            tma_load_2d_pair(stB + s * C::B_STAGE, &tmB, (w.kb0 + it) * C::BK, w.b0 + static_cast<int>(rank) * C::BNH,
+                             full0 + s * 8, polB);
+            continue;
+          }
           if (!mbar_wait(&bars.empty[s], ((g / STAGES) & 1) ^ 1, status)) {
             ok = false;
             break;

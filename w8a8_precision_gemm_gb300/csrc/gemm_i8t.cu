@@ -33,6 +33,7 @@
 // other and adds a chunk into the unit's int32 running sum (kept in a scratch
 // region of the workspace, one per CTA) -- then NS stages of 128 columns (256
 // fp16 per lane) of widened weights.
+#include "fused_quant.cuh"
 #include "gemm.cuh"
 
 namespace qurl {
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   griddep_launch_dependents();
-  if (warp != 0) griddep_wait();
+  const bool fused = args.fq.kind != kFuseNone;
+  if (warp != 0 || fused) griddep_wait();
 
   // j: the unit's position in this CTA's list (call after wait_count(.., j, ..))
   auto is_fast = [&](int j) {
@@ -187,26 +189,37 @@ __global__ void __launch_bounds__(512, 1)
   };
   constexpr int kModeUnits = 32 * kModeWords;
 
-  if (warp == 0) {
+  const uint64_t wpol = l2_policy_evict_first();
+  auto wload = [&](int slot, const Unit& w, int it) {
+    mbar_arrive_expect_tx(&bars.wfull[slot], C::W_STAGE);
+    const int k0 = (w.kb0 + it) * C::BK;
+    uint8_t* dst = stW + slot * C::W_STAGE;
+    tma_load_2d(dst, &tmW, k0, w.a0, &bars.wfull[slot], wpol);
+    tma_load_2d(dst + C::W_BOX, &tmW, k0 + 128, w.a0, &bars.wfull[slot], wpol);
+  };
+  // The first weight slots stream in while the previous kernel (which, per
+  // w_prefetch, does not write Wq) is finishing, or, in a fused call, while
+  // this kernel quantizes its input rows (after its own grid-dependency wait).
+  int npre = 0;  // meaningful in the producer thread
+  if (warp == 0 && lane == 0 && (args.w_prefetch || fused) && !args.fault && R.u < R.end) {
+    const Unit w = unit_of<true, BN>(args, R.u);
+    npre = min(WST, w.nkb);
+    for (int it = 0; it < npre; ++it) wload(it, w, it);
+  }
+  bool run = true;
+  if (fused)  // the activation ring is free until the handoff: it holds the rows' reduction scratch
+    run = fused_quant_prologue<1>(args.fq, args.fsums, args.M, args.K, kQInt8,
+                                  *reinterpret_cast<rq::RowScratch*>(stX), status, args.fault);
+
+  if (!run) {
+    // the handoff ran out (the timeout is latched): no role runs; the weight
+    // copies already issued land before the CTA leaves
+    if (warp == 0 && lane == 0)
+      for (int j = 0; j < npre; ++j) mbar_wait_drain(&bars.wfull[j], 0, status);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      auto load = [&](int slot, const Unit& w, int it) {
-        mbar_arrive_expect_tx(&bars.wfull[slot], C::W_STAGE);
-        const int k0 = (w.kb0 + it) * C::BK;
-        uint8_t* dst = stW + slot * C::W_STAGE;
-        tma_load_2d(dst, &tmW, k0, w.a0, &bars.wfull[slot], pol);
-        tma_load_2d(dst + C::W_BOX, &tmW, k0 + 128, w.a0, &bars.wfull[slot], pol);
-      };
-      // the first slots stream in while the previous kernel (which, per
-      // w_prefetch, does not write Wq) is finishing
-      int npre = 0;
-      if (args.w_prefetch && !args.fault && R.u < R.end) {
-        const Unit w = unit_of<true, BN>(args, R.u);
-        npre = min(WST, w.nkb);
-        for (int it = 0; it < npre; ++it) load(it, w, it);
-      }
-      griddep_wait();
+      if (!fused) griddep_wait();
       Ring<WST> r;
       int g = 0;
       bool ok = true;
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(512, 1)
             ok = false;
             break;
           }
-          load(r.idx, w, it);
+          wload(r.idx, w, it);
         }
       }
       if (!ok) {
@@ -320,7 +333,7 @@ __global__ void __launch_bounds__(512, 1)
         int mx = 0;
         for (int c = lane; c < BN; c += 32) {
           const int m = t * BN + c;
-          if (m < args.M) mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
+          if (m < args.M) mx = max(mx, __ldcg(args.asum + static_cast<size_t>(m) * args.splits + sp));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
         if (lane == 0) {

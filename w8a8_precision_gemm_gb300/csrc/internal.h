@@ -23,6 +23,37 @@ constexpr int kQFp8 = 1;   // QURL_FP8_E4M3
 constexpr int kModeBf16 = 0;  // GEMM epilogue dequantizes and writes Y
 constexpr int kModeAcc = 1;   // GEMM writes the raw accumulator of its split to part
 
+// Per-token sums of |code| over consecutive ranges of sum_len codes (the K
+// splits of the INT8 decode GEMM): asum[m * nsum + j], j < nsum.  Written by
+// the kernel that writes the fp16 copy of the codes; asum null: not wanted.
+constexpr int kMaxSums = 128;
+struct CodeSums {
+  int* asum;
+  int sum_len;     // a multiple of 256
+  int nsum;        // <= kMaxSums
+  unsigned* qsum;  // the sums of code^2 over the same ranges (saturated at 2^32 - 1), or null
+};
+
+// The quantizer of a fused entry point, run by the decode GEMM kernel itself
+// before its main loop (kind 0: none -- the activation codes are an input).
+// Every CTA quantizes rows blockIdx.x, blockIdx.x + gridDim.x, ... < M and the
+// CTAs then hand over through two counters in the caller's workspace.
+constexpr int kFuseNone = 0;
+constexpr int kFuseRmsNorm = 1;  // RMSNorm with the folded gain -> quant
+constexpr int kFuseQuant = 2;    // quant with the UAQ pre-scale
+constexpr int kFuseSiluMul = 3;  // SiLU(gate) * up -> quant (pre-scale)
+struct FusedQuant {
+  int kind;
+  const void* X;       // bf16 [M, ldx] (kFuseSiluMul: [M, 2K], gate | up)
+  long long ldx;
+  const float* gamma;  // kFuseRmsNorm: folded gain [K]
+  float eps, pre;
+  void* Xq;            // codes [M, K]
+  float* sx;           // scales [M]
+  void* x16;           // INT8 decode: the fp16 copy of the codes (and `sums`), else null
+  unsigned* sync;      // two handoff counters, zero between calls
+};
+
 struct GemmArgs {
   int M, N, K;       // tokens, output channels, depth
   int num_kb;        // k-blocks covering K
@@ -48,19 +79,9 @@ struct GemmArgs {
   const unsigned* qsum;  // INT8 on pairs with widened weights: [M][splits] sums of Xq[m,k]^2 over
                          // each split's k range, and
   const unsigned* qn;    // [N] sums of Wq[n,k]^2 over all of K (null: not available)
-  int* scratch;          // INT8 on pairs with widened weights: per CTA, the int32 running sum of a
-                         // unit accumulated in chunks ([gridDim.x][256 columns][128 rows])
-};
-
-// Per-token sums of |code| over consecutive ranges of sum_len codes (the K
-// splits of the INT8 decode GEMM): asum[m * nsum + j], j < nsum.  Written by
-// the kernel that writes the fp16 copy of the codes; asum null: not wanted.
-constexpr int kMaxSums = 128;
-struct CodeSums {
-  int* asum;
-  int sum_len;     // a multiple of 256
-  int nsum;        // <= kMaxSums
-  unsigned* qsum;  // the sums of code^2 over the same ranges (saturated at 2^32 - 1), or null
+  int* scratch;          // INT8: per CTA, the int32 running sum of a unit accumulated in chunks
+  FusedQuant fq;         // decode fused entries: the quantizer this kernel runs first
+  CodeSums fsums;        // ... and where it writes the code sums (INT8 decode)
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -168,7 +189,10 @@ struct GemmPlan {
   size_t scratch_off;  // running sums of chunked units, one region per CTA
 };
 
-// gemm_plan.cu
+// gemm_common.cu.  ws_bytes of a plan includes kSyncBytes at the end of the
+// workspace: the two handoff counters of the fused entry points live in the
+// last kSyncBytes of the caller's workspace.
+constexpr size_t kSyncBytes = 256;
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
 // gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
