@@ -958,9 +958,27 @@ def run_single(args):
         print(json.dumps({"single": "acr", "tokens": ACR_SEQ * ACR_LEN, "reps": args.single_reps}))
         return 0
     model, proj = args.single.split(":")
-    K, N = MODELS[model]["shapes"][proj]
     M = args.single_m
     qt = qt_of(q, args.qtype)
+    if proj in ("rmsnorm_quant", "quant_act", "silu_mul_quant"):
+        K = MODELS[model]["inter"] if proj == "silu_mul_quant" else MODELS[model]["hidden"]
+        cols = 2 * K if proj == "silu_mul_quant" else K
+        X = synth.activations(f"single/{model}/{proj}/X", M, cols).cuda()
+        Xq = torch.empty((M, K), dtype=q.code_dtype(qt), device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        gf = (synth.gamma(f"single/{model}/g", K) * S_UAQ).cuda()
+        for _ in range(args.single_reps):
+            if proj == "rmsnorm_quant":
+                q.qurl_rmsnorm_quant(X, gf, EPS, qt, Xq, sx)
+            elif proj == "quant_act":
+                q.qurl_quant_act(X, S_UAQ, qt, Xq, sx)
+            else:
+                q.qurl_silu_mul_quant(X, S_UAQ, qt, Xq, sx)
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+        print(json.dumps({"single": args.single, "M": M, "K": K, "qtype": args.qtype, "reps": args.single_reps}))
+        return 0
+    K, N = MODELS[model]["shapes"][proj]
     W = synth.weights(f"single/{model}/{proj}/W", N, K).cuda()
     Wq, sw, _, _ = q.prepare_weights(W, qt, s=S_UAQ, keep_scaled=False)
     del W
@@ -985,7 +1003,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=32,
                     help="tokens per 8-bit type in one oracle step (reference arm and cpu_baseline)")
     ap.add_argument("--single", default=None,
-                    help="model:proj, e.g. 32b:gate_up -- run one linear for profiling; 'acr': the ACR objective")
+                    help="model:proj, e.g. 32b:gate_up -- run one linear for profiling (or one quantizer: "
+                         "32b:rmsnorm_quant, 32b:quant_act, 32b:silu_mul_quant); 'acr': the ACR objective")
     ap.add_argument("--qtype", choices=list(QTYPES), default="int8", help="qtype of --single")
     ap.add_argument("--single-m", type=int, default=256)
     ap.add_argument("--single-reps", type=int, default=3)

@@ -368,6 +368,23 @@ qurl_status qurl_check_device_status(qurl_stream_t stream);
  * workspace's last 256 bytes are zeroed again).  One-shot; always QURL_OK. */
 qurl_status qurl_debug_inject_timeout(void);
 
+/* Where a fused quantize -> linear entry (qurl_rmsnorm_quant_linear,
+ * qurl_quant_act_linear, qurl_silu_mul_quant_linear) runs its quantizer for a
+ * decode batch (M <= 256, on the plans whose GEMM kernel can take it): inside
+ * the GEMM kernel (one launch: the GEMM's CTAs quantize the rows between them,
+ * then meet at a grid-wide handoff) or as its own kernel just before the GEMM
+ * (two launches: the GEMM starts early under programmatic dependent launch and
+ * reads its weights while the quantizer runs).
+ *   on = 0: always its own kernel;
+ *   on = 1 (the default): inside the GEMM where that measured faster on GB300
+ *     -- RMSNorm rows for INT8, and for FP8 at M <= 64; per-token rows for
+ *     INT8 at M <= 64; never SiLU * up rows;
+ *   on = 2: inside the GEMM wherever the plan allows.
+ * All three give bit-identical outputs.  Process-wide, for calls made after it
+ * returns; the previous setting goes to *previous when that is not NULL.
+ * QURL_ERR_INVALID_ARG unless on is 0, 1 or 2. */
+qurl_status qurl_set_fused_decode(int on, int* previous);
+
 /* The GEMM plan the library takes for an M x N x K product of `qt` codes on a
  * GPU with `num_sms` SMs and `ws_bytes` of workspace (SIZE_MAX: as much as
  * qurl_workspace_size asks for).  Host-side only; no device is needed.  Not

@@ -26,6 +26,15 @@ S = 1.5
 SHAPES = [(64, 4608, 3584), (16, 512, 256), (200, 3584, 3584), (256, 37888, 3584), (256, 3584, 18944)]
 
 
+@pytest.fixture(autouse=True)
+def fused_decode_on():
+    """These tests exercise the in-kernel quantizer wherever a plan allows it
+    (mode 2), then restore the previous mode."""
+    prev = q.qurl_set_fused_decode(2)
+    yield
+    q.qurl_set_fused_decode(prev)
+
+
 def _bits(t):
     return t.contiguous().view(torch.int16).clone()
 
@@ -133,3 +142,61 @@ def test_fused_handoff_timeout_is_reported(qt, M, N, K):
     torch.cuda.synchronize()
     q.qurl_check_device_status()
     assert torch.equal(_bits(Y), _bits(Y0))
+
+
+@pytest.mark.parametrize("qt", [q.INT8, q.FP8_E4M3])
+@pytest.mark.parametrize("kind", ["rms", "act", "silu"])
+@pytest.mark.parametrize("M,N,K", [(64, 4608, 3584), (256, 3584, 18944)])
+def test_fused_entry_switch_gives_identical_results(qt, kind, M, N, K):
+    """The same fused entry with the quantizer inside the GEMM kernel and as
+    its own kernel before it: one launch fewer in the first case, and codes,
+    scales and bf16 outputs bit-identical."""
+    X, Wq, sw, gf = _setup(qt, kind, M, N, K, f"switch/{kind}/{M}")
+    ws = q.workspace(M, N, K, qt)
+    res = {}
+    for on in (True, False):
+        q.qurl_set_fused_decode(2 if on else 0)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        Xq = torch.empty((M, K), dtype=q.code_dtype(qt), device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        n0 = q.qurl_kernel_launches()
+        _fused(kind, X, gf, Wq, sw, qt, Y, Xq, sx, ws)
+        res[on] = (q.qurl_kernel_launches() - n0, Xq.view(torch.uint8).clone(), sx.clone(), _bits(Y))
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+    assert res[False][0] == res[True][0] + 1
+    for a, b in zip(res[True][1:], res[False][1:]):
+        assert torch.equal(a, b)
+
+
+def test_fused_decode_switch_rejects_other_values():
+    lib = q.load()
+    assert lib.qurl_set_fused_decode(3, None) == 1  # QURL_ERR_INVALID_ARG
+    assert lib.qurl_set_fused_decode(-1, None) == 1
+
+
+@pytest.mark.parametrize("qt", [q.INT8, q.FP8_E4M3])
+@pytest.mark.parametrize("kind,M", [("rms", 64), ("rms", 256), ("act", 64), ("act", 256), ("silu", 64)])
+def test_fused_decode_default_routing(qt, kind, M):
+    """Mode 1 (the default) quantizes inside the GEMM only where that measured
+    faster: RMSNorm rows for INT8 and for FP8 at M <= 64, per-token rows for
+    INT8 at M <= 64, SiLU * up rows never.  Same outputs as mode 0."""
+    N, K = 4608, 3584
+    X, Wq, sw, gf = _setup(qt, kind, M, N, K, f"route/{kind}/{M}")
+    ws = q.workspace(M, N, K, qt)
+    plan = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)
+    expect = {"rms": qt == q.INT8 or M <= 64, "act": qt == q.INT8 and M <= 64, "silu": False}[kind]
+    got = {}
+    for mode in (2, 1, 0):
+        q.qurl_set_fused_decode(mode)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        Xq = torch.empty((M, K), dtype=q.code_dtype(qt), device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        n0 = q.qurl_kernel_launches()
+        _fused(kind, X, gf, Wq, sw, qt, Y, Xq, sx, ws)
+        got[mode] = (q.qurl_kernel_launches() - n0, _bits(Y))
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+    assert got[2][0] == got[0][0] - 1, plan  # the plan can take the quantizer
+    assert got[1][0] == (got[2][0] if expect else got[0][0]), (plan, got)
+    assert torch.equal(got[1][1], got[0][1]) and torch.equal(got[2][1], got[0][1])

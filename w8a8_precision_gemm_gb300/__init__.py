@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
             "qurl_count_diff": [P, P, z, P, P],
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
+            "qurl_set_fused_decode": [i, P],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
             "qurl_debug_mma_probe": [i, i, i, P, P],
             "qurl_acr_objective": [P, P, P, P, P, ctypes.c_longlong, f, f, i, P, P, P, P, z, P],
@@ -305,6 +306,15 @@ def qurl_debug_mma_probe(route, ctas, iters, stream=None) -> float:
 def qurl_debug_inject_timeout():
     """Test hook: the next GEMM launch stalls on purpose and times out (~1 s)."""
     _ok(load().qurl_debug_inject_timeout(), "qurl_debug_inject_timeout")
+
+
+def qurl_set_fused_decode(mode: int) -> int:
+    """Where the fused entries quantize a decode batch: 0 its own kernel, 1 inside
+    the GEMM kernel where that is faster (default), 2 inside it wherever possible.
+    Returns the previous mode."""
+    prev = ctypes.c_int(0)
+    _ok(load().qurl_set_fused_decode(int(mode), ctypes.byref(prev)), "qurl_set_fused_decode")
+    return prev.value
 
 
 def qurl_status_string(s: int) -> str:

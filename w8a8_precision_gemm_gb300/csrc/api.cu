@@ -19,6 +19,7 @@ std::atomic<unsigned long long> g_kernel_launches{0};
 
 namespace {
 std::atomic<int> g_inject_timeout{0};  // one-shot test hook, see qurl_debug_inject_timeout
+std::atomic<int> g_fused_decode{1};    // 0 never, 1 where it pays, 2 always: see qurl_set_fused_decode
 }  // namespace
 
 namespace {
@@ -305,6 +306,13 @@ qurl_status qurl_debug_inject_timeout(void) {
   return QURL_OK;
 }
 
+qurl_status qurl_set_fused_decode(int on, int* previous) {
+  if (on < 0 || on > 2) return QURL_ERR_INVALID_ARG;
+  const int old = g_fused_decode.exchange(on);
+  if (previous) *previous = old;
+  return QURL_OK;
+}
+
 qurl_status qurl_prepare_weights(const void* W, qurl_ftype w_type, int N, int K, int ldw, const float* gamma,
                                  float s, qurl_qtype qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                  qurl_stream_t stream) {
@@ -437,7 +445,20 @@ struct FusedAct {
   unsigned* sync = nullptr;  // its handoff counters (the workspace's last bytes)
 };
 
-FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+// Whether the GEMM kernel's own CTAs quantize a decode batch faster than a
+// quantizer kernel launched before the GEMM (which overlaps the GEMM's weight
+// prefetch).  Measured on GB300 for the 7B- and 32B-class chains at M = 64 and
+// 256: RMSNorm rows pay for INT8 at both sizes and for FP8 at M = 64 (1-5 us
+// per call); per-token rows pay for INT8 at M = 64; SiLU * up rows, whose
+// intermediate-size rows leave one CTA per row with 19-28 k values to
+// transform, never do (up to 2.3x slower at M = 256).
+bool in_gemm_pays(int kind, int qt, int M) {
+  if (kind == qurl::kFuseRmsNorm) return qt == QURL_INT8 || M <= 64;
+  if (kind == qurl::kFuseQuant) return qt == QURL_INT8 && M <= 64;
+  return false;
+}
+
+FusedAct fused_x16(int kind, int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
   FusedAct f;
   DevState* dev = nullptr;
   if (device_state(&dev) != QURL_OK) return f;
@@ -446,10 +467,12 @@ FusedAct fused_x16(int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
     f.x16 = ws;
     f.sums = code_sums(p, ws);
   }
-  // decode plans whose GEMM kernel runs the quantizer itself: the INT8 kernel
-  // with the widened weights in TMEM (single CTA) and the FP8 decode kernels
-  f.in_gemm = ws != nullptr && ws_bytes >= p.ws_bytes && M <= 256 && p.swap && !p.wide &&
-              (qt == QURL_INT8 ? (p.tmem_a && !p.pair) : true);
+  // decode plans whose GEMM kernel can run the quantizer itself: the INT8
+  // kernel with the widened weights in TMEM (single CTA) and the FP8 decode
+  // kernels
+  const int mode = g_fused_decode.load(std::memory_order_relaxed);
+  f.in_gemm = mode != 0 && (mode == 2 || in_gemm_pays(kind, qt, M)) && ws != nullptr && ws_bytes >= p.ws_bytes &&
+              M <= 256 && p.swap && !p.wide && (qt == QURL_INT8 ? (p.tmem_a && !p.pair) : true);
   if (f.in_gemm)
     f.sync = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(ws) +
                                          ((ws_bytes - qurl::kSyncBytes) & ~static_cast<size_t>(15)));
@@ -492,7 +515,7 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   if (!gamma_folded || !(eps >= 0.0f) || !std::isfinite(eps)) return QURL_ERR_INVALID_ARG;
   if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseRmsNorm, M, N, K, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseRmsNorm, X, ldx, gamma_folded, eps, 1.0f, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
                      sx_scratch, workspace, ws_bytes, st);
@@ -509,7 +532,7 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(M, N, K, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseQuant, M, N, K, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseQuant, X, ldx, nullptr, 0.0f, pre_scale, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
                      sx_scratch, workspace, ws_bytes, st);
@@ -527,7 +550,7 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
   QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(M, N, I, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseSiluMul, M, N, I, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseSiluMul, GU, ldgu, nullptr, 0.0f, pre_scale, Wq, sw, M, N, I, qt, Y, ldy,
                      Xq_scratch, sx_scratch, workspace, ws_bytes, st);

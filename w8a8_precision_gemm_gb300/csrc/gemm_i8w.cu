@@ -72,20 +72,40 @@ struct I8wBarriers {
   uint32_t tmem_base;
 };
 
+// Token tiles per group of the unit order below.
+constexpr int kI8wTokGroup = 16;
+
+// Tile coordinates of unit u.  Units run K split slowest, then groups of
+// kI8wTokGroup token tiles, then channel tiles, token tile fastest: the pairs
+// running together cover a few channel tiles of one token group, so a
+// channel tile's weights are read from HBM once per token group and the
+// group's activations (16 x 256 rows) stay in L2 while its channel tiles go by.
+struct UnitCoords {
+  int tok, ch, sp;
+};
+__device__ __forceinline__ UnitCoords i8w_coords(const GemmArgs& a, int u) {
+  const int per_split = a.tiles_tok * a.tiles_ch;
+  UnitCoords c;
+  c.sp = u / per_split;
+  const int v = u - c.sp * per_split;
+  const int gi = v / (kI8wTokGroup * a.tiles_ch);  // only the last group can be short
+  const int gs = min(kI8wTokGroup, a.tiles_tok - gi * kI8wTokGroup);
+  const int r = v - gi * kI8wTokGroup * a.tiles_ch;
+  c.ch = r / gs;
+  c.tok = gi * kI8wTokGroup + (r - c.ch * gs);
+  return c;
+}
+
 // This CTA's part of unit u: token rows a0 .. a0 + 127, output channels
-// b0 .. b0 + 255 of which it stages b0 + 128 rank ..; units are numbered token
-// tile fastest, so the pairs running together share channel tiles through L2.
+// b0 .. b0 + 255 of which it stages b0 + 128 rank ...
 __device__ __forceinline__ Unit i8w_unit(const GemmArgs& a, int u, uint32_t rank) {
-  const int tok = u % a.tiles_tok;
-  const int rest = u / a.tiles_tok;
-  const int ch = rest % a.tiles_ch;
-  const int sp = rest / a.tiles_ch;
+  const UnitCoords c = i8w_coords(a, u);
   Unit w;
-  w.a0 = tok * 256 + static_cast<int>(rank) * 128;
-  w.b0 = ch * 256;
-  w.kb0 = sp * a.kb_per_split;
+  w.a0 = c.tok * 256 + static_cast<int>(rank) * 128;
+  w.b0 = c.ch * 256;
+  w.kb0 = c.sp * a.kb_per_split;
   w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
-  w.split = sp;
+  w.split = c.sp;
   return w;
 }
 
@@ -234,9 +254,8 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
     __syncwarp();
     if (args.asum != nullptr) {
       for (int u = u_begin, j = 0; u < u_end && j < kI8wModeUnits; u += u_stride, ++j) {
-        const int t = u % args.tiles_tok;
-        const int ch = (u / args.tiles_tok) % args.tiles_ch;
-        const int sp = u / (args.tiles_tok * args.tiles_ch);
+        const UnitCoords uc = i8w_coords(args, u);
+        const int t = uc.tok, ch = uc.ch, sp = uc.sp;
         int smax = 0;
         unsigned qmax = 0, nmax = 0;
         for (int c = lane; c < 256; c += 32) {
