@@ -70,6 +70,16 @@ __device__ __forceinline__ void two_sum_acc(float& s, float& c, float y) {
   c = __fadd_rn(c, err);
 }
 
+// The same for two independent accumulator pairs at once (lanes x and y).
+__device__ __forceinline__ void two_sum_acc2(float2& s, float2& c, float2 y) {
+  const float2 t = __fadd2_rn(s, y);
+  const float2 bp = __fadd2_rn(t, make_float2(-s.x, -s.y));
+  const float2 tb = __fadd2_rn(t, make_float2(-bp.x, -bp.y));
+  const float2 err = __fadd2_rn(__fadd2_rn(s, make_float2(-tb.x, -tb.y)), __fadd2_rn(y, make_float2(-bp.x, -bp.y)));
+  s = t;
+  c = __fadd2_rn(c, err);
+}
+
 // The row's mean of squares ms = (s + c) / K (the compensated block sum of
 // x^2, divided in fp64 and rounded to fp32) and r = 1 / sqrt(ms + eps)
 // (correctly rounded fp32 square root and division), computed by one thread
@@ -119,84 +129,170 @@ struct Enc {
   float scale;
   float inv;
   int qt;
+  bool fma_quotient;  // FP8: the scale admits the FMA-corrected quotient (below)
 };
 
 __device__ __forceinline__ Enc make_enc(float amax, int qt) {
   const float scale = row_scale(amax, qt);
-  return {scale, __frcp_rn(scale), qt};
+  return {scale, __frcp_rn(scale), qt, scale >= 0x1p-100f && scale <= 0x1p100f};
 }
 
-// Code of v / scale.  Both types are decided on the IEEE quotient fl(v /
+// ---- paired fp32 arithmetic: sm_100's two-lane fp32 instructions, each lane
+// rounded exactly like its scalar counterpart (no contraction).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+
+// Codes of v / scale.  Both types are decided on the IEEE quotient fl(v /
 // scale), but most codes come from the product r = v * fl(1 / scale) instead:
 // r carries two roundings of relative size 2^-24 on top of the exact quotient,
 // so it lies within 2.5 units in the last place of fl(v / scale).
 //  * INT8: fl(v / scale) rounded to the nearest integer, ties to even, clamped
-//    to +-127.  For |r| < 256 r is within 5e-5 of the quotient, so wherever r
-//    is more than 1e-4 away from a half-integer both round to the same integer
-//    and r is used; otherwise (one code in ~5000, and NaN or out-of-range
-//    inputs) the quotient itself is computed.
-//  * FP8-E4M3: round to nearest even with saturation to +-448.  For magnitudes
-//    of at least 2^-6 (e4m3's normal range) the code keeps 3 of fp32's 23
-//    fraction bits, so r and the quotient give the same code unless the 20
-//    dropped bits of r lie within 8 units of the halfway pattern 0x80000; then,
-//    and below 2^-6 (e4m3 subnormals round at another bit) or for non-finite
-//    r, the quotient itself is computed.
+//    to +-127.  |v| <= absmax makes |r| <= 127 (1 + 2^-22), so r is within
+//    5e-5 of the quotient: wherever r is more than 1e-4 away from a
+//    half-integer both round to the same integer, which r + 1.5 * 2^23 gives
+//    (the sum's unit in the last place is 1, so the addition itself rounds r
+//    to an integer, ties to even; its low byte is the two's-complement code)
+//    and which needs no clamp.  Otherwise (one code in ~5000, and NaN inputs,
+//    whose distance to the integer is NaN) the quotient itself is computed.
+//  * FP8-E4M3: round to nearest even with saturation to +-448, applied to
+//    fl(v / scale) itself, which one correction step gives without a
+//    division: with inv = fl(1 / scale) (correctly rounded) and r = fl(v *
+//    inv) within an ulp of the quotient, the residual v - r * scale is exact
+//    in one FMA and fl(r + residual * inv) is the correctly rounded quotient
+//    (Markstein's theorem for FMA division, valid while nothing underflows or
+//    overflows: the scale lies in [2^-100, 2^100] and |quotient| <= 448, so
+//    only quotients far below e4m3's smallest subnormal, whose codes are 0
+//    either way, come near underflow).  The sign is copied from v, so that
+//    -0 keeps its sign.  Rows with a scale outside that range divide.  Two
+//    codes per conversion.
 // The codes are therefore those of the plain division.
-__device__ __forceinline__ uint8_t encode(float v, const Enc& e) {
-  const float r = __fmul_rn(v, e.inv);
-  if (e.qt == kQInt8) {
-    const float f = r - floorf(r);
-    const bool fast = fabsf(r) < 256.0f && fabsf(f - 0.5f) > 1e-4f;
-    int q = __float2int_rn(fast ? r : __fdiv_rn(v, e.scale));
-    q = max(-127, min(127, q));
-    return static_cast<uint8_t>(static_cast<int8_t>(q));
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ int i8_quotient_code(float v, const Enc& e) {
+  const int q = __float2int_rn(__fdiv_rn(v, e.scale));
+  return max(-127, min(127, q));
+}
+
+// Low bytes of four words -> one word (byte i from word i).
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// 8 INT8 codes of v (pairs in k order) packed in k order; q receives the
+// same codes as floats.
+__device__ __forceinline__ uint2 encode8_i8(const float2 (&v)[4], const Enc& e, float2 (&q)[4]) {
+  const float2 inv = splat2(e.inv), mg = splat2(kRoundMagic);
+  uint32_t b[8];
+  bool fast = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 r = mul2(v[i], inv);
+    const float2 t = add2(r, mg);
+    q[i] = sub2(t, mg);
+    const float2 d = sub2(r, q[i]);
+    fast = fast & (fabsf(d.x) < 0.4999f) & (fabsf(d.y) < 0.4999f);
+    b[2 * i] = __float_as_uint(t.x);
+    b[2 * i + 1] = __float_as_uint(t.y);
   }
-  const uint32_t b = __float_as_uint(r) & 0x7FFFFFFFu;
-  const bool fast = b >= 0x3C800000u && b < 0x7F800000u && ((b & 0xFFFFFu) - 0x7FFF8u) > 16u;
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(fast ? r : __fdiv_rn(v, e.scale), __NV_SATFINITE, __NV_E4M3));
+  if (!fast) {
+    float qs[8], vs[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qs[2 * i] = q[i].x;
+      qs[2 * i + 1] = q[i].y;
+      vs[2 * i] = v[i].x;
+      vs[2 * i + 1] = v[i].y;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!(fabsf(__fsub_rn(__fmul_rn(vs[j], e.inv), qs[j])) < 0.4999f)) {
+        const int c = i8_quotient_code(vs[j], e);
+        b[j] = static_cast<uint32_t>(c);
+        qs[j] = static_cast<float>(c);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = make_float2(qs[2 * i], qs[2 * i + 1]);
+  }
+  return make_uint2(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7]));
+}
+
+// 8 FP8-E4M3 codes of v (pairs in k order) packed in k order.
+__device__ __forceinline__ uint2 encode8_f8(const float2 (&v)[4], const Enc& e) {
+  uint32_t h[4];
+  if (e.fma_quotient) {
+    const float2 inv = splat2(e.inv), nscale = splat2(-e.scale);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 r = mul2(v[i], inv);
+      const float2 res = __ffma2_rn(r, nscale, v[i]);  // v - r * scale, exact
+      float2 q = __ffma2_rn(res, inv, r);
+      q.x = copysignf(q.x, v[i].x);
+      q.y = copysignf(q.y, v[i].y);
+      h[i] = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);  // .x in the low byte
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      h[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v[i].x, e.scale), __fdiv_rn(v[i].y, e.scale)),
+                                      __NV_SATFINITE, __NV_E4M3);
+  }
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+__device__ __forceinline__ uint2 encode8(const float2 (&v)[4], const Enc& en) {
+  if (en.qt == kQInt8) {
+    float2 q[4];
+    return encode8_i8(v, en, q);
+  }
+  return encode8_f8(v, en);
 }
 
 // 8 values -> 8 code bytes packed in a uint2 (little-endian byte order = k order).
 __device__ __forceinline__ uint2 encode8(const float (&v)[8], const Enc& en) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) lo |= static_cast<uint32_t>(encode(v[e], en)) << (8 * e);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) hi |= static_cast<uint32_t>(encode(v[4 + e], en)) << (8 * e);
-  return make_uint2(lo, hi);
+  const float2 p[4] = {make_float2(v[0], v[1]), make_float2(v[2], v[3]), make_float2(v[4], v[5]),
+                       make_float2(v[6], v[7])};
+  return encode8(p, en);
 }
 
 // Saturation of the sums of |code| (any value above 2^24 / 128 means
 // "accumulate in chunks" to the GEMM that reads them).
 constexpr int kAbsSumCap = 1 << 24;
 
-// Store 8 codes (and, for INT8 when x16 is given, the same 8 codes as fp16 --
-// exact, integers of magnitude <= 127 -- for the tensor-core GEMM to read).
-// Returns the sum of |code| and the sum of code^2 of the 8 INT8 codes when x16
-// is given, else zeros.
+// Sum of |code| and of code^2 of 8 INT8 codes: |c| = c * (+1 or -1), the
+// second factor's bytes 0x01 | the code's sign replicated (byte_perm selector
+// nibbles with bit 3 set copy the selected byte's sign bit).
+__device__ __forceinline__ int2 code_sums8(uint2 c) {
+  const int sx = static_cast<int>(__byte_perm(c.x, 0u, 0xBA98) | 0x01010101u);
+  const int sy = static_cast<int>(__byte_perm(c.y, 0u, 0xBA98) | 0x01010101u);
+  const int cx = static_cast<int>(c.x), cy = static_cast<int>(c.y);
+  return make_int2(__dp4a(cy, sy, __dp4a(cx, sx, 0)), __dp4a(cy, cy, __dp4a(cx, cx, 0)));
+}
+
+// Store the 8 codes of v (and, for INT8 when x16 is given, the same 8 codes
+// as fp16 -- exact, integers of magnitude <= 127 -- for the tensor-core GEMM
+// to read).  Returns the sum of |code| and the sum of code^2 of the 8 INT8
+// codes when x16 is given, else zeros.
 __device__ __forceinline__ int2 store8(uint8_t* __restrict__ q, uint8_t* __restrict__ x16, size_t idx,
-                                       const float (&v)[8], const Enc& en) {
-  const uint2 c = encode8(v, en);
+                                       const float2 (&v)[4], const Enc& en) {
+  if (en.qt != kQInt8) {
+    reinterpret_cast<uint2*>(q)[idx] = encode8_f8(v, en);
+    return make_int2(0, 0);
+  }
+  float2 qf[4];
+  const uint2 c = encode8_i8(v, en, qf);
   reinterpret_cast<uint2*>(q)[idx] = c;
   if (x16 == nullptr) return make_int2(0, 0);
-  {
-    // the same 8 codes as fp16, exactly: with u = c + 128 in [0, 255], the
-    // fp16 with bits 0x6400 | u is 1024 + u, and subtracting 1152 leaves c
-    const uint32_t w[2] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u};
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    uint32_t h[4];
+  uint32_t h[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t p = __byte_perm(w[e >> 1], 0x64646464u, (e & 1) ? 0x4342 : 0x4140);
-      const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&p), bias);
-      h[e] = *reinterpret_cast<const uint32_t*>(&d);
-    }
-    reinterpret_cast<uint4*>(x16)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+  for (int i = 0; i < 4; ++i) {
+    const __half2 p = __float22half2_rn(qf[i]);  // .x in the low half
+    h[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
-  const int a = static_cast<int>(__dp4a(__vabs4(c.y), 0x01010101u, __dp4a(__vabs4(c.x), 0x01010101u, 0u)));
-  const int sq = __dp4a(static_cast<int>(c.y), static_cast<int>(c.y), __dp4a(static_cast<int>(c.x),
-                                                                              static_cast<int>(c.x), 0));
-  return make_int2(a, sq);
+  reinterpret_cast<uint4*>(x16)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+  return code_sums8(c);
 }
 
 // Per-row sums of |code| (and of code^2) over the ranges of a CodeSums, in
@@ -241,6 +337,27 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
     x[2 * e] = __uint_as_float(w[e] << 16);
     x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
   }
+}
+
+__device__ __forceinline__ void bf16x8_to_f2(const uint4 u, float2 (&x)[4]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+}
+
+// Largest |x| of 8 bf16 values folded into m (two lanes; NaN never wins, as in fmaxf).
+__device__ __forceinline__ __nv_bfloat162 absmax_bf16x8(const uint4 u, __nv_bfloat162 m) {
+  const uint32_t w[4] = {u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu, u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+  return m;
+}
+
+// max |fl(a * pre)| over the values a whose largest magnitude is amax: rounding
+// is monotone, so it is fl(amax * |pre|) (and 0 for pre = 0, where non-finite
+// a would give NaN products, which a max ignores).
+__device__ __forceinline__ float scaled_absmax(float amax, float pre) {
+  return pre == 0.0f ? 0.0f : __fmul_rn(amax, fabsf(pre));
 }
 
 // Visit the 16-byte vectors idx = threadIdx.x + c * blockDim.x of a row: the
@@ -303,25 +420,23 @@ __device__ __forceinline__ void quant_act_row(int m, const __nv_bfloat16* __rest
   const int nvec = K >> 3;
   uint4 cache[NC];
   fill_cache(row, nvec, cache);
-  float amax = 0.0f;
-  for_vectors(row, nvec, cache, [&](const uint4 u, int) {
-    float x[8];
-    bf16x8_to_f32(u, x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(x[e], pre)));
-  });
+  // the largest |x| on the bf16 values themselves; the pre-scale is applied once
+  __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
+  for_vectors(row, nvec, cache, [&](const uint4 u, int) { m2 = absmax_bf16x8(u, m2); });
+  float amax = scaled_absmax(fmaxf(__bfloat162float(m2.x), __bfloat162float(m2.y)), pre);
   amax = block_reduce<true>(amax, sh.red);
   const Enc en = make_enc(amax, qt);
   if (threadIdx.x == 0) sx[m] = en.scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * K;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * K * 2 : nullptr;
+  const float2 pre2 = splat2(pre);
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
     int2 v = make_int2(0, 0);
     if (valid) {
-      float x[8];
-      bf16x8_to_f32(u, x);
+      float2 x[4];
+      bf16x8_to_f2(u, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], pre);
+      for (int e = 0; e < 4; ++e) x[e] = mul2(x[e], pre2);
       v = store8(out, out16, idx, x, en);
     }
     sums_add_warp(sh.cnt, sums, idx, v);
@@ -351,13 +466,16 @@ __device__ __forceinline__ void rmsnorm_quant_row(int m, const __nv_bfloat16* __
   // rounding of the mean to within ~2^-44 relative -- the same fp32 value a
   // plain fp64 sum gives, except when the mean lies that close to a rounding
   // midpoint.
-  float ss = 0.0f, sc = 0.0f;
+  float2 ss2 = make_float2(0.0f, 0.0f), sc2 = make_float2(0.0f, 0.0f);  // even / odd k
   for_vectors(row, nvec, cache, [&](const uint4 u, int) {
-    float x[8];
-    bf16x8_to_f32(u, x);
+    float2 x[4];
+    bf16x8_to_f2(u, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) two_sum_acc(ss, sc, __fmul_rn(x[e], x[e]));
+    for (int e = 0; e < 4; ++e) two_sum_acc2(ss2, sc2, mul2(x[e], x[e]));
   });
+  float ss = ss2.x, sc = sc2.x;
+  two_sum_acc(ss, sc, ss2.y);
+  sc = __fadd_rn(sc, sc2.y);
   // the gain of the vectors this thread normalises is read while the sums are reduced
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
@@ -368,19 +486,21 @@ __device__ __forceinline__ void rmsnorm_quant_row(int m, const __nv_bfloat16* __
   block_mean_sq(ss, sc, sh.red, K, eps, ms, r);
   if (threadIdx.x == 0 && ms_out) ms_out[m] = ms;
   // v = (x * r) * gamma'
-  auto normed = [&](const uint4 u, int idx, float (&x)[8]) {
-    bf16x8_to_f32(u, x);
+  const float2 r2 = splat2(r);
+  auto normed = [&](const uint4 u, int idx, float2 (&x)[4]) {
+    bf16x8_to_f2(u, x);
     const float4 ga = __ldg(g4 + 2 * idx), gb = __ldg(g4 + 2 * idx + 1);
-    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const float2 g[4] = {make_float2(ga.x, ga.y), make_float2(ga.z, ga.w), make_float2(gb.x, gb.y),
+                         make_float2(gb.z, gb.w)};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(__fmul_rn(x[e], r), g[e]);
+    for (int e = 0; e < 4; ++e) x[e] = mul2(mul2(x[e], r2), g[e]);
   };
   float amax = 0.0f;
   for_vectors(row, nvec, cache, [&](const uint4 u, int idx) {
-    float x[8];
+    float2 x[4];
     normed(u, idx, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(x[e].x), fabsf(x[e].y)));
   });
   amax = block_reduce<true>(amax, sh.red);
   const Enc en = make_enc(amax, qt);
@@ -390,7 +510,7 @@ __device__ __forceinline__ void rmsnorm_quant_row(int m, const __nv_bfloat16* __
   for_vectors_warp(row, nvec, cache, [&](const uint4 u, int idx, bool valid) {
     int2 v = make_int2(0, 0);
     if (valid) {
-      float x[8];
+      float2 x[4];
       normed(u, idx, x);
       v = store8(out, out16, idx, x, en);
     }
@@ -399,18 +519,21 @@ __device__ __forceinline__ void rmsnorm_quant_row(int m, const __nv_bfloat16* __
   sums_end(sh.cnt, sums, m);
 }
 
-__device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float (&h)[8]) {
-  float g[8], u[8];
-  bf16x8_to_f32(gu, g);
-  bf16x8_to_f32(uu, u);
+__device__ __forceinline__ float silu_ratio(float g, float den) {
+  return den < 0x1p126f ? __fdividef(g, den) : 0.0f;
+}
+
+__device__ __forceinline__ void silu_mul8(const uint4 gu, const uint4 uu, float2 (&h)[4]) {
+  float2 g[4], u[4];
+  bf16x8_to_f2(gu, g);
+  bf16x8_to_f2(uu, u);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+  for (int e = 0; e < 4; ++e) {
     // g / (1 + exp(-g)) to within ~2 units in the last place (h is held to a
     // relative 2e-6 of the exact value; the codes are decided on this h).  A
     // denominator beyond 2^126 (g < -87.3) makes |h| < 2e-36: 0.
-    const float den = __fadd_rn(1.0f, expf(-g[e]));
-    const float sg = den < 0x1p126f ? __fdividef(g[e], den) : 0.0f;
-    h[e] = __fmul_rn(sg, u[e]);
+    const float2 den = add2(splat2(1.0f), make_float2(expf(-g[e].x), expf(-g[e].y)));
+    h[e] = mul2(make_float2(silu_ratio(g[e].x, den.x), silu_ratio(g[e].y, den.y)), u[e]);
   }
 }
 
@@ -430,17 +553,18 @@ __device__ __forceinline__ void silu_mul_quant_row(int m, const __nv_bfloat16* _
   uint4 cg[NC], cu[NC];
   fill_cache(grow, nvec, cg);
   fill_cache(urow, nvec, cu);
-  // pass 1: h = silu(g) * u, kept in registers for the cached positions
-  float hc[NC][8];
+  // pass 1: h = silu(g) * u, kept in registers for the cached positions; the
+  // largest |h| (the pre-scale is applied to it once)
+  float2 hc[NC][4];
   float amax = 0.0f;
-  auto take = [&](const float (&h)[8], int idx) {
+  auto take = [&](const float2 (&h)[4], int idx) {
     if (h_out) {
       float4* ho = reinterpret_cast<float4*>(h_out + static_cast<size_t>(m) * I) + 2 * idx;
-      ho[0] = make_float4(h[0], h[1], h[2], h[3]);
-      ho[1] = make_float4(h[4], h[5], h[6], h[7]);
+      ho[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      ho[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(h[e], pre)));
+    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(h[e].x), fabsf(h[e].y)));
   };
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
@@ -451,21 +575,22 @@ __device__ __forceinline__ void silu_mul_quant_row(int m, const __nv_bfloat16* _
     }
   }
   for (int idx = threadIdx.x + NC * blockDim.x; idx < nvec; idx += blockDim.x) {
-    float h[8];
+    float2 h[4];
     silu_mul8(__ldg(grow + idx), __ldg(urow + idx), h);
     take(h, idx);
   }
-  amax = block_reduce<true>(amax, sh.red);
+  amax = block_reduce<true>(scaled_absmax(amax, pre), sh.red);
   const Enc en = make_enc(amax, qt);
   if (threadIdx.x == 0) sx[m] = en.scale;
   uint8_t* out = Xq + static_cast<size_t>(m) * I;
   uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
+  const float2 pre2 = splat2(pre);
   // pass 2: codes (warp-uniform steps, see for_vectors_warp)
-  auto put = [&](float (&h)[8], int idx, bool valid) {
+  auto put = [&](float2 (&h)[4], int idx, bool valid) {
     int2 v = make_int2(0, 0);
     if (valid) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = __fmul_rn(h[e], pre);
+      for (int e = 0; e < 4; ++e) h[e] = mul2(h[e], pre2);
       v = store8(out, out16, idx, h, en);
     }
     sums_add_warp(sh.cnt, sums, idx, v);
@@ -477,7 +602,7 @@ __device__ __forceinline__ void silu_mul_quant_row(int m, const __nv_bfloat16* _
   }
   for (int i0 = NC * blockDim.x + (threadIdx.x & ~31); i0 < nvec; i0 += blockDim.x) {
     const int idx = i0 + (threadIdx.x & 31);
-    float h[8] = {};
+    float2 h[4] = {};
     if (idx < nvec) silu_mul8(__ldg(grow + idx), __ldg(urow + idx), h);
     put(h, idx, idx < nvec);
   }
