@@ -623,6 +623,72 @@ def time_kv_cache(q, stream, pk, l2):
                          "timing": f"CUDA events around a graph of {R} calls rotating over {k} inputs"}}
 
 
+def nvfp4_bytes(M, K, N):
+    """Algorithmic bytes of one 4-bit linear: codes (half a byte a value) and block scales (one byte per 16
+    values) of both operands, fp32 row scales, bf16 Y."""
+    return (M + N) * K // 2 + (M + N) * K // 16 + 4 * (M + N) + 2 * M * N
+
+
+def time_nvfp4(q, stream, pk, l2):
+    """The 4-bit (NVFP4, W4A4) variant on the 32B-class projections: each
+    linear on its own (graph of calls rotating over enough weight sets), and
+    the row quantizer on activations and on fp32 weights.  The GEMM runs on the
+    fp16 tensor pipe (exact widening of the E2M1 x E4M3 values): its roofline
+    is the measured bf16 = fp16 dense rate; the nominal FP4 rate (6x bf16) is
+    reported beside it."""
+    model = "32b"
+    res = {"per_linear": {}}
+    for name, K, N in chain_shapes(model):
+        W = synth.weights(f"bench/nvfp4/{name}/W", N, K).cuda()
+        w0 = q.nvfp4_quant(W)
+        del W
+        k = n_sets(N * K // 2, l2)
+        sets = [w0] + [tuple(torch.roll(t, (i * 1009) % N, 0).contiguous() for t in w0) for i in range(1, k)]
+        for M in (256, 8192):
+            x = q.nvfp4_quant(synth.activations(f"bench/nvfp4/{name}/X/{M}", M, K).cuda(), S_UAQ)
+            ws = q.nvfp4_workspace(M, N, K)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            R = max(k, 4)
+
+            def calls(x=x, ws=ws, Y=Y, R=R):
+                for r in range(R):
+                    q.qurl_nvfp4_linear(x, sets[r % len(sets)], Y, ws)
+
+            g, nl = graph_of(calls, q)
+            g.replay()
+            us = time_graph(g, 3, stream) / R * 1e3
+            ops = 2 * M * N * K
+            t_fp16 = ops / (pk["bf16_tflops"] * 1e12)
+            nb = nvfp4_bytes(M, K, N)
+            t_h = nb / (pk["hbm_gbs"] * 1e9)
+            res["per_linear"][f"{name}/M{M}"] = {
+                "M": M, "K": K, "N": N, "us": us, "TOPS": ops / (us * 1e-6) / 1e12, "launches": nl // R,
+                "frac_fp16_path": max(t_fp16, t_h) / (us * 1e-6),
+                "frac_nvfp4_nominal": max(t_fp16 / 6, t_h) / (us * 1e-6), "weight_sets": k}
+            del g, x, ws, Y
+        del sets, w0
+        torch.cuda.empty_cache()
+    # the row quantizer: activations (bf16, M = 8192, K = 5120) and the gate_up weights (fp32 W')
+    for what, R_, K_, f32 in (("act/M8192/K5120", 8192, 5120, False), ("weights/gate_up", 55296, 5120, True)):
+        src = (synth.weights("bench/nvfp4/qw", R_, K_) if f32 else synth.activations("bench/nvfp4/qa", R_, K_)).cuda()
+        out = q.nvfp4_quant(src)
+
+        def qcalls(src=src, out=out):
+            for _ in range(4):
+                q.qurl_nvfp4_quant(src, 1.0, *out)
+
+        g, _ = graph_of(qcalls, q)
+        g.replay()
+        us = time_graph(g, 3, stream) / 4 * 1e3
+        nb = R_ * K_ * (4 if f32 else 2) + R_ * K_ // 2 + R_ * K_ // 16 + 4 * R_
+        res[f"quant/{what}"] = {"us": us, "GBps": nb / (us * 1e-6) / 1e9,
+                                "roofline_frac": nb / (pk["hbm_gbs"] * 1e9) / (us * 1e-6)}
+        del g, src, out
+        torch.cuda.empty_cache()
+    q.qurl_check_device_status()
+    return res
+
+
 def time_tensor_routes(q, stream, pk):
     """The rate of each tensor route an 8-bit product can take on this GPU, from
     the library's probe kernels (fixed instruction counts on zero operands),
@@ -905,6 +971,7 @@ def run_ours(args):
     acr = time_acr(q, stream, pk, rank == 0 and world == 1 and not args.no_cpu_baseline)
     routes = time_tensor_routes(q, stream, pk)
     kv = time_kv_cache(q, stream, pk, l2)
+    nvfp4 = time_nvfp4(q, stream, pk, l2)
 
     value = ops * world / (ms_step * 1e-3) / 1e12
     step_bytes = sum(alg_bytes(M, K, N) for qtype, M in passes for _, K, N in chain_shapes(model))
@@ -926,7 +993,7 @@ def run_ours(args):
             "clocks": clocks.summary(t0_wall, t1_wall, CLOCK_LEAD),
             "per_gemm": per_gemm, "per_quant": per_quant,
             "decode_7b": decode_7b, "chain_7b": chain_7b, "weight_requant": requant,
-            "acr_objective": acr, "tensor_routes": routes, "kv_cache_fp8": kv}
+            "acr_objective": acr, "tensor_routes": routes, "kv_cache_fp8": kv, "nvfp4_w4a4": nvfp4}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

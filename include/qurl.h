@@ -21,7 +21,8 @@
  *           token-level mean.
  *   [LIMITS] section "局限与展望": FP8 KV-cache quantization is not yet
  *           optimized in the rollout engine (page 5's FP8-RL entry quantizes
- *           the KV cache to FP8).
+ *           the KV cache to FP8); 4-bit quantization would speed the rollout
+ *           up further but was not explored (page 5's QeRL entry uses NVFP4).
  *
  * Conventions (all entry points):
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
@@ -267,6 +268,51 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
  */
 qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned long long* count,
                             qurl_stream_t stream);
+
+/*
+ * 4-bit variant (W4A4, NVFP4) of the linear layer ([LIMITS]: 4-bit named as
+ * the next speedup; the format itself is a reading, the pages do not define
+ * it).  A row (an output channel of W, a token of X) of K values, K a multiple
+ * of 16, is stored as
+ *   q4   [K/2] bytes: E2M1 codes (sign bit 3; magnitudes 0, 0.5, 1, 1.5, 2,
+ *        3, 4, 6 for codes 0..7), value 2j in the low nibble of byte j;
+ *   sblk [K/16] bytes: one OCP E4M3 scale per 16 consecutive values;
+ *   g    fp32: the row's second-level scale;
+ * and a value is dec(code) * dec(sblk) * g.  Quantization of a row v (IEEE
+ * fp32 throughout): A = max|v|; g = A / 2688 (6 * 448), 1 for an all-zero
+ * row; per block s = e4m3_RNE_satfinite(max|v_block| / fl(6 g)); step e =
+ * fl(dec(s) * g); code = e2m1_RNE_satfinite(v / e) with the sign of v kept
+ * (also on zero), and every code 0 where e = 0.
+ *
+ * qurl_nvfp4_quant: R rows of X ([R, ldx], bf16 with v = x * pre_scale, or
+ * fp32 with v = x -- the UAQ-folded master weights W' of qurl_prepare_weights)
+ * -> q4 [R, K/2], sblk [R, K/16], g [R], densely packed.  R = 0 is valid.
+ * One kernel launch.  Errors: INVALID_ARG (NULL, K <= 0, R < 0, ldx < K,
+ * non-finite pre_scale, unknown x_type), UNSUPPORTED (K % 16), ALIGNMENT (X,
+ * q4 not 16-byte aligned, ldx * element size not a multiple of 16).
+ *
+ * qurl_nvfp4_linear: Y [M, N] (bf16, row stride ldy) =
+ *   bf16_RNE(fl(fl(fp32(acc[m, n]) * gx[m]) * gw[n])),
+ *   acc[m, n] = sum_k dec(x code) dec(x block scale) dec(w code) dec(w block scale),
+ * accumulated in fp32 on the tensor cores (the products are exact; the
+ * order of the sum is the kernel's, like the FP8 GEMM's).  Both operands
+ * are widened to fp16 in the workspace (ws_bytes >= qurl_nvfp4_workspace_size
+ * (M, N, K), 16-byte aligned, contents undefined between calls), then one
+ * CTA-pair GEMM runs; K split (where the tiles leave SMs idle) adds a
+ * reduction kernel.  3-4 kernel launches.  qurl_nvfp4_gemm_acc writes the fp32
+ * sums acc [M, N] themselves (for tests).  Errors: INVALID_ARG (NULL, a
+ * non-positive size, ldy < N), UNSUPPORTED (K % 16), ALIGNMENT (q4x, q4w, Y,
+ * acc or the workspace not 16-byte aligned, ldy * 2 not a multiple of 16),
+ * WORKSPACE (ws_bytes too small).
+ */
+qurl_status qurl_nvfp4_quant(const void* X, qurl_ftype x_type, int R, int K, int ldx, float pre_scale, void* q4,
+                             void* sblk, float* g, qurl_stream_t stream);
+size_t qurl_nvfp4_workspace_size(int M, int N, int K);
+qurl_status qurl_nvfp4_linear(const void* q4x, const void* sbx, const float* gx, const void* q4w, const void* sbw,
+                              const float* gw, int M, int N, int K, void* Y, int ldy, void* workspace,
+                              size_t ws_bytes, qurl_stream_t stream);
+qurl_status qurl_nvfp4_gemm_acc(const void* q4x, const void* sbx, const void* q4w, const void* sbw, int M, int N,
+                                int K, float* acc, void* workspace, size_t ws_bytes, qurl_stream_t stream);
 
 /*
  * FP8 key/value cache quantization ([LIMITS]: section "局限与展望" names FP8

@@ -84,9 +84,17 @@ def lib():
                                             P, P, P]
             L.orc_kv_cache_quant.argtypes = [P, i, i, i, i, i, P, P, P, P, P]
             L.orc_kv_cache_dequant.argtypes = [P, P, P, i, i, i, P]
+            L.orc_e2m1_encode.restype = ctypes.c_uint8
+            L.orc_e2m1_encode.argtypes = [f]
+            L.orc_e2m1_decode.restype = ctypes.c_double
+            L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            L.orc_nvfp4_quant_rows_f32.argtypes = [P, i, i, i, P, P, P]
+            L.orc_nvfp4_quant_act.argtypes = [P, i, i, i, f, P, P, P]
+            L.orc_gemm_nvfp4.argtypes = [P, P, P, P, i, i, i, P, i]
             for name in ("orc_quant_rows_f32", "orc_quant_act", "orc_prepare_weights", "orc_rmsnorm_quant",
                          "orc_silu_mul_quant", "orc_gemm_i8", "orc_gemm_fp8", "orc_acr_objective",
-                         "orc_kv_cache_quant", "orc_kv_cache_dequant"):
+                         "orc_kv_cache_quant", "orc_kv_cache_dequant", "orc_nvfp4_quant_rows_f32",
+                         "orc_nvfp4_quant_act", "orc_gemm_nvfp4"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -277,6 +285,61 @@ def w8a8_linear(Xq, sx, Wq, sw, qtype, nthreads=1):
     Returns (Y bf16 bits [M,N], acc)."""
     acc = gemm_i8(Xq, Wq, nthreads) if qtype == INT8 else gemm_fp8(Xq, Wq, nthreads)
     return epilogue(acc, sx, sw), acc
+
+
+# ---------------------------------------------------------------- 4-bit variant (NVFP4)
+
+def e2m1_encode(v) -> np.ndarray:
+    """fp32 -> E2M1 codes (0..15; RNE, saturating at 6, sign kept)."""
+    L = lib()
+    v = _c(v, np.float32)
+    return np.array([L.orc_e2m1_encode(float(x)) for x in v.ravel()], np.uint8).reshape(v.shape)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    L = lib()
+    table = np.array([L.orc_e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8) & 15]
+
+
+def nvfp4_quant_rows(V):
+    """fp32 rows [R, K] -> (packed codes u8 [R, K/2], block scales e4m3 u8 [R, K/16], row scales f32 [R])."""
+    V = _c(V, np.float32)
+    R, K = V.shape
+    q4 = np.empty((R, K // 2), np.uint8)
+    sb = np.empty((R, K // 16), np.uint8)
+    g = np.empty(R, np.float32)
+    _check(lib().orc_nvfp4_quant_rows_f32(_p(V), R, K, K, _p(q4), _p(sb), _p(g)), "nvfp4_quant_rows")
+    return q4, sb, g
+
+
+def nvfp4_quant_act(X_bits, pre_scale=1.0):
+    """bf16 rows (uint16 bits) [M, K], v = x * pre_scale -> (codes, block scales, row scales)."""
+    X = _c(X_bits, np.uint16)
+    M, K = X.shape
+    q4 = np.empty((M, K // 2), np.uint8)
+    sb = np.empty((M, K // 16), np.uint8)
+    g = np.empty(M, np.float32)
+    _check(lib().orc_nvfp4_quant_act(_p(X), M, K, K, float(pre_scale), _p(q4), _p(sb), _p(g)), "nvfp4_quant_act")
+    return q4, sb, g
+
+
+def nvfp4_unpack(q4) -> np.ndarray:
+    """Packed codes [R, K/2] -> one code per value [R, K] (value 2j in the low nibble)."""
+    q4 = np.asarray(q4, np.uint8)
+    out = np.empty((q4.shape[0], q4.shape[1] * 2), np.uint8)
+    out[:, 0::2] = q4 & 15
+    out[:, 1::2] = q4 >> 4
+    return out
+
+
+def gemm_nvfp4(q4x, sbx, q4w, sbw, nthreads=1) -> np.ndarray:
+    """Exact acc[m, n] = sum_k x value * w value (block scales applied, row scales not), fp64."""
+    q4x, sbx, q4w, sbw = (_c(a, np.uint8) for a in (q4x, sbx, q4w, sbw))
+    M, N, K = q4x.shape[0], q4w.shape[0], q4x.shape[1] * 2
+    acc = np.empty((M, N), np.float64)
+    _check(lib().orc_gemm_nvfp4(_p(q4x), _p(sbx), _p(q4w), _p(sbw), M, N, K, _p(acc), nthreads), "gemm_nvfp4")
+    return acc
 
 
 def count_diff(a, b) -> int:

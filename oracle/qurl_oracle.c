@@ -22,6 +22,10 @@
  *     [NOTES/LIMITS] section "局限与展望": FP8 KV-cache quantization is named
  *                   as not yet optimized in the rollout engine (with page 5's
  *                   FP8-RL entry, which quantizes the KV cache to FP8).
+ *     [NOTES/LIMITS/4BIT] the same section: 4-bit quantization would speed
+ *                   the rollout up further but was not explored; page 5 (the
+ *                   fugumt summary of the QuRL paper, related-papers list,
+ *                   QeRL entry) pairs RL rollout with NVFP4 quantization.
  *     [NOTES/ACR]   section "方法详解 > 关键设计 > 自适应裁剪范围 (ACR)": the
  *                   decoupled-PPO objective of the quantized rollout, with the
  *                   truncated importance weight min(pi_prox / pi_behav, C) and
@@ -527,6 +531,186 @@ void orc_epilogue_f64(const double* acc, const float* sx, const float* sw, int M
             float y = t * sw[n];
             Y[(size_t)m * ldy + n] = orc_bf16_encode(y);
         }
+}
+
+/* ------------------------------------------------------------------------ */
+/* 4-bit W4A4 variant: NVFP4 rows [NOTES/LIMITS/4BIT]                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages name 4-bit quantization (NVFP4 through the QeRL entry) without
+ * defining it; the reading taken is NVIDIA's published NVFP4 layout with the
+ * pages' per-channel / per-token split for its second-level scale:
+ *   * element codes E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa
+ *     bit 0; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7;
+ *   * one E4M3 scale per 16 consecutive values of a row (a block);
+ *   * one fp32 scale g per row (an output channel of W, a token of X).
+ * A value is dec(code) * dec(block scale) * g.
+ *
+ * Quantizing a row v[0..K), K a multiple of 16 (every division IEEE fp32):
+ *   A = max |v|;  g = A / 2688 (6 * 448: the largest E2M1 magnitude times the
+ *   largest E4M3 scale), 1 for an all-zero row;  d6 = fl(6 * g);
+ *   block b: a_b = max of its |v|;  s_b = e4m3_RNE_satfinite(a_b / d6);
+ *   step e_b = fl(dec(s_b) * g);  code = e2m1_RNE_satfinite(v / e_b), with the
+ *   sign of v kept also where the magnitude rounds to 0 (as IEEE rounding
+ *   keeps the sign of zero); every code of a block with e_b = 0 is 0.
+ */
+static const double e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Round to the E2M1 grid: nearest magnitude, ties to the even code (mantissa
+ * bit 0), magnitudes >= 6 saturate to 6.  NaN is outside the domain (0). */
+uint8_t orc_e2m1_encode(float r) {
+    if (r != r) return 0;
+    double a = fabs((double)r);
+    int code = 7;
+    for (int i = 0; i < 7; ++i) {
+        double lo = e2m1_mag[i], hi = e2m1_mag[i + 1], mid = 0.5 * (lo + hi);
+        if (a < hi) {
+            if (a < mid) code = i;
+            else if (a > mid) code = i + 1;
+            else code = (i % 2 == 0) ? i : i + 1;
+            break;
+        }
+    }
+    if (a >= 6.0) code = 7;
+    return (uint8_t)((signbit(r) ? 8 : 0) | code);
+}
+
+double orc_e2m1_decode(uint8_t c) {
+    double m = e2m1_mag[c & 7];
+    return (c & 8) ? -m : m;
+}
+
+/* One row: q4[K/2] (value 2j in the low nibble of byte j), sblk[K/16], *g. */
+static void nvfp4_row(const float* v, int K, uint8_t* q4, uint8_t* sblk, float* g_out) {
+    float A = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        float t = fabsf(v[k]);
+        if (t > A) A = t;
+    }
+    float g = (A == 0.0f) ? 1.0f : A / 2688.0f;
+    float d6 = 6.0f * g;
+    memset(q4, 0, (size_t)K / 2);
+    for (int b = 0; b < K / 16; ++b) {
+        const float* vb = v + 16 * b;
+        float ab = 0.0f;
+        for (int k = 0; k < 16; ++k) {
+            float t = fabsf(vb[k]);
+            if (t > ab) ab = t;
+        }
+        uint8_t s = orc_e4m3_encode(ab / d6);
+        sblk[b] = s;
+        float eb = (float)orc_e4m3_decode(s) * g;
+        for (int k = 0; k < 16; ++k) {
+            uint8_t c = (eb == 0.0f) ? 0 : orc_e2m1_encode(vb[k] / eb);
+            int kk = 16 * b + k;
+            q4[kk / 2] |= (uint8_t)((kk & 1) ? (c << 4) : c);
+        }
+    }
+    *g_out = g;
+}
+
+/* Rows of fp32 values (weights: the UAQ-folded W'). */
+int orc_nvfp4_quant_rows_f32(const float* V, int R, int K, int ldv, uint8_t* q4, uint8_t* sblk, float* g) {
+    if (!V || !q4 || !sblk || !g || R < 0 || K <= 0 || K % 16 != 0 || ldv < K) return ORC_ERR_ARG;
+    for (int r = 0; r < R; ++r)
+        nvfp4_row(V + (size_t)r * ldv, K, q4 + (size_t)r * (K / 2), sblk + (size_t)r * (K / 16), g + r);
+    return ORC_OK;
+}
+
+/* Rows of bf16 activations with the UAQ pre-scale: v = fl(x * pre_scale). */
+int orc_nvfp4_quant_act(const uint16_t* X, int M, int K, int ldx, float pre_scale, uint8_t* q4, uint8_t* sblk,
+                        float* g) {
+    if (!X || !q4 || !sblk || !g || M < 0 || K <= 0 || K % 16 != 0 || ldx < K) return ORC_ERR_ARG;
+    float* v = (float*)malloc(sizeof(float) * (size_t)K);
+    if (!v) return ORC_ERR_ARG;
+    for (int m = 0; m < M; ++m) {
+        for (int k = 0; k < K; ++k) v[k] = orc_bf16_decode(X[(size_t)m * ldx + k]) * pre_scale;
+        nvfp4_row(v, K, q4 + (size_t)m * (K / 2), sblk + (size_t)m * (K / 16), g + m);
+    }
+    free(v);
+    return ORC_OK;
+}
+
+/*
+ * acc[m, n] = sum_k dec(x code) dec(x block scale) dec(w code) dec(w block
+ * scale), exactly: each factor dec(code) * dec(scale) is a multiple of 2^-10
+ * (E2M1 values are multiples of 1/2, E4M3 values of 2^-9) of magnitude at
+ * most 6 * 448, so each product is an integer multiple of 2^-20 below 2^43
+ * in those units, and the sum over K < 2^20 terms fits int64.  The int64 sum
+ * is converted to fp64 (exact below 2^53 units).  The row scales gx, gw
+ * enter the dequantizing epilogue (orc_epilogue_f64) as sx and sw.
+ */
+typedef struct {
+    const uint8_t *q4x, *sbx;
+    const int64_t* wf; /* [N][K] weight factors in units of 2^-10 */
+    int M, N, K, m0, m1;
+    double* acc;
+} nvfp4_job;
+
+static int64_t nvfp4_factor(const uint8_t* q4, const uint8_t* sb, int k) {
+    uint8_t c = (uint8_t)((k & 1) ? (q4[k / 2] >> 4) : (q4[k / 2] & 15));
+    /* 2 dec(code) and 2^9 dec(scale) are integers */
+    int64_t cv = (int64_t)(2.0 * orc_e2m1_decode(c));
+    int64_t sv = (int64_t)ldexp(orc_e4m3_decode(sb[k / 16]), 9);
+    return cv * sv;
+}
+
+static void* nvfp4_rows(void* p) {
+    nvfp4_job* j = (nvfp4_job*)p;
+    int K = j->K;
+    int64_t* xf = (int64_t*)malloc(sizeof(int64_t) * (size_t)K);
+    if (!xf) return (void*)1;
+    for (int m = j->m0; m < j->m1; ++m) {
+        for (int k = 0; k < K; ++k)
+            xf[k] = nvfp4_factor(j->q4x + (size_t)m * (K / 2), j->sbx + (size_t)m * (K / 16), k);
+        for (int n = 0; n < j->N; ++n) {
+            int64_t s = 0;
+            const int64_t* w = j->wf + (size_t)n * K;
+            for (int k = 0; k < K; ++k) s += xf[k] * w[k];
+            j->acc[(size_t)m * j->N + n] = ldexp((double)s, -20);
+        }
+    }
+    free(xf);
+    return NULL;
+}
+
+int orc_gemm_nvfp4(const uint8_t* q4x, const uint8_t* sbx, const uint8_t* q4w, const uint8_t* sbw, int M, int N,
+                   int K, double* acc, int nthreads) {
+    if (!q4x || !sbx || !q4w || !sbw || !acc || M < 0 || N < 0 || K <= 0 || K % 16 != 0 || K >= (1 << 20))
+        return ORC_ERR_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = M > 0 ? M : 1;
+    nvfp4_job* jobs = (nvfp4_job*)calloc((size_t)nthreads, sizeof(nvfp4_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    int64_t* wf = (int64_t*)malloc(sizeof(int64_t) * ((size_t)K * N + 1));
+    if (!jobs || !th || !wf) {
+        free(jobs);
+        free(th);
+        free(wf);
+        return ORC_ERR_ARG;
+    }
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            wf[(size_t)n * K + k] = nvfp4_factor(q4w + (size_t)n * (K / 2), sbw + (size_t)n * (K / 16), k);
+    int rc = ORC_OK;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (nvfp4_job){q4x, sbx, wf, M, N, K, (int)((long long)M * t / nthreads),
+                              (int)((long long)M * (t + 1) / nthreads), acc};
+        if (pthread_create(&th[t], NULL, nvfp4_rows, &jobs[t]) != 0) {
+            nvfp4_rows(&jobs[t]);
+            th[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        void* r = NULL;
+        if (th[t]) pthread_join(th[t], &r);
+        if (r) rc = ORC_ERR_ARG;
+    }
+    free(jobs);
+    free(th);
+    free(wf);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -82,6 +82,9 @@ def load() -> ctypes.CDLL:
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
             "qurl_set_fused_decode": [i, P],
+            "qurl_nvfp4_quant": [P, i, i, i, i, f, P, P, P, P],
+            "qurl_nvfp4_linear": [P, P, P, P, P, P, i, i, i, P, i, P, z, P],
+            "qurl_nvfp4_gemm_acc": [P, P, P, P, i, i, i, P, P, z, P],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
             "qurl_debug_mma_probe": [i, i, i, P, P],
             "qurl_acr_objective": [P, P, P, P, P, ctypes.c_longlong, f, f, i, P, P, P, P, z, P],
@@ -94,6 +97,8 @@ def load() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.qurl_workspace_size.argtypes = [i, i, i, i]
         L.qurl_workspace_size.restype = ctypes.c_size_t
+        L.qurl_nvfp4_workspace_size.argtypes = [i, i, i]
+        L.qurl_nvfp4_workspace_size.restype = ctypes.c_size_t
         L.qurl_acr_workspace_size.argtypes = []
         L.qurl_acr_workspace_size.restype = ctypes.c_size_t
         L.qurl_status_string.argtypes = [ctypes.c_int]
@@ -399,6 +404,71 @@ def count_diff(a, b, stream=None) -> torch.Tensor:
     c = torch.empty(1, dtype=torch.int64, device=a.device)
     qurl_count_diff(a, b, c, stream)
     return c
+
+
+# ---------------------------------------------------------------- 4-bit variant (NVFP4)
+
+def qurl_nvfp4_quant(X, pre_scale, q4, sblk, g, stream=None):
+    """Rows of X (bf16 times pre_scale, or fp32) -> E2M1 codes q4 [R, K/2], E4M3
+    block scales sblk [R, K/16], row scales g [R] (see include/qurl.h)."""
+    _dense(q4, sblk, g)
+    R, K = X.shape
+    xt = FP32 if X.dtype == torch.float32 else BF16
+    _ok(load().qurl_nvfp4_quant(_ptr(X), xt, R, K, _ld(X), float(pre_scale), _ptr(q4), _ptr(sblk), _ptr(g),
+                                _stream(stream)), "qurl_nvfp4_quant")
+
+
+def qurl_nvfp4_workspace_size(M, N, K) -> int:
+    return int(load().qurl_nvfp4_workspace_size(M, N, K))
+
+
+def qurl_nvfp4_linear(x, w, Y, workspace, stream=None):
+    """Y = the 4-bit linear of x = (q4, sblk, g) tokens and w = (q4, sblk, g) channels."""
+    (q4x, sbx, gx), (q4w, sbw, gw) = x, w
+    _dense(q4x, sbx, gx, q4w, sbw, gw, workspace)
+    M, N, K = q4x.shape[0], q4w.shape[0], q4x.shape[1] * 2
+    _ok(load().qurl_nvfp4_linear(_ptr(q4x), _ptr(sbx), _ptr(gx), _ptr(q4w), _ptr(sbw), _ptr(gw), M, N, K, _ptr(Y),
+                                 _ld(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "qurl_nvfp4_linear")
+
+
+def qurl_nvfp4_gemm_acc(x, w, acc, workspace, stream=None):
+    (q4x, sbx, _), (q4w, sbw, _) = x, w
+    _dense(q4x, sbx, q4w, sbw, acc, workspace)
+    M, N, K = q4x.shape[0], q4w.shape[0], q4x.shape[1] * 2
+    _ok(load().qurl_nvfp4_gemm_acc(_ptr(q4x), _ptr(sbx), _ptr(q4w), _ptr(sbw), M, N, K, _ptr(acc), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+        "qurl_nvfp4_gemm_acc")
+
+
+def nvfp4_quant(X, pre_scale=1.0, stream=None):
+    """Allocating wrapper: returns (q4 uint8 [R, K/2], sblk uint8 [R, K/16], g fp32 [R])."""
+    R, K = X.shape
+    q4 = torch.empty((R, K // 2), dtype=torch.uint8, device=X.device)
+    sb = torch.empty((R, K // 16), dtype=torch.uint8, device=X.device)
+    g = torch.empty(R, dtype=torch.float32, device=X.device)
+    qurl_nvfp4_quant(X, pre_scale, q4, sb, g, stream)
+    return q4, sb, g
+
+
+def nvfp4_workspace(M, N, K, device="cuda") -> torch.Tensor:
+    return torch.empty(max(qurl_nvfp4_workspace_size(M, N, K), 16), dtype=torch.uint8, device=device)
+
+
+def nvfp4_linear(x, w, ws=None, stream=None):
+    M, N = x[0].shape[0], w[0].shape[0]
+    ws = nvfp4_workspace(M, N, x[0].shape[1] * 2, x[0].device) if ws is None else ws
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=x[0].device)
+    qurl_nvfp4_linear(x, w, Y, ws, stream)
+    return Y
+
+
+def nvfp4_gemm_acc(x, w, ws=None, stream=None):
+    M, N = x[0].shape[0], w[0].shape[0]
+    ws = nvfp4_workspace(M, N, x[0].shape[1] * 2, x[0].device) if ws is None else ws
+    acc = torch.empty((M, N), dtype=torch.float32, device=x[0].device)
+    qurl_nvfp4_gemm_acc(x, w, acc, ws, stream)
+    return acc
 
 
 # ---------------------------------------------------------------- ACR objective

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libqurl.so")
 SOURCES = ["api.cu", "quant.cu", "gemm_common.cu", "gemm_fp8.cu", "gemm_fp8p.cu", "gemm_i8.cu", "gemm_i8t.cu", "gemm_i8w.cu", "objective.cu",
-           "static_scratch.cu", "probe.cu"]
+           "static_scratch.cu", "probe.cu", "nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -280,6 +280,66 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   return QURL_OK;
 }
 
+int device_sms() {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 160;  // no device visible: size for the largest SM count this library targets
+  }
+  return sms;
+}
+
+qurl_status check_nvfp4_rows(const void* q4, const void* sblk, const float* g, int R, int K) {
+  if (!q4 || !sblk || !g || !valid_dim(R) || !valid_dim(K)) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(q4)) return QURL_ERR_ALIGNMENT;
+  return QURL_OK;
+}
+
+// The 4-bit linear: both operands widened to fp16 in the workspace (exact),
+// then the CTA-pair GEMM in fp32 accumulation, with g_x and g_w as the token
+// and channel scales of its epilogue (Y), or the raw fp32 sums (acc).
+qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const void* q4w, const void* sbw,
+                      const float* gw, int M, int N, int K, void* Y, int ldy, float* acc, void* ws, size_t ws_bytes,
+                      cudaStream_t st) {
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  qurl::GemmPlan p{};
+  if (!ws || !qurl::plan_nvfp4(p, M, N, K, dev->num_sms, ws_bytes)) return QURL_ERR_WORKSPACE;
+  if (!aligned16(ws)) return QURL_ERR_ALIGNMENT;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  const bool split = p.splits > 1;
+  QURL_CUDA(qurl::launch_nvfp4_widen(q4x, sbx, M, K, ws, dev->num_sms, st));
+  QURL_CUDA(qurl::launch_nvfp4_widen(q4w, sbw, N, K, wsb + p.w16_off, dev->num_sms, st));
+  CUtensorMap ta, tb;
+  QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, 128, true, &ta));
+  QURL_TRY(byte_map(wsb + p.w16_off, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
+  qurl::GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_kb = p.num_kb;
+  a.kb_per_split = p.kb_per_split;
+  a.sx = gx;
+  a.sw = gw;
+  a.Y = reinterpret_cast<__nv_bfloat16*>(Y);
+  a.ldy = ldy;
+  a.status = dev->status;
+  a.w_prefetch = 0;
+  a.mode = (Y && !split) ? qurl::kModeBf16 : qurl::kModeAcc;
+  a.part = split ? static_cast<void*>(wsb + p.x16_bytes) : static_cast<void*>(acc);
+  a.acc_out = acc;
+  a.fault = g_inject_timeout.exchange(0);
+  a.scratch = reinterpret_cast<int*>(wsb + p.scratch_off);
+  a.float_acc = 1;
+  QURL_CUDA(qurl::launch_gemm_i8w(ta, tb, a, dim3(p.tiles_tok, p.tiles_ch, p.splits), st));
+  if (split)
+    QURL_CUDA(qurl::launch_splitk_reduce(qurl::kQFp8, wsb + p.x16_bytes, p.splits, M, N, gx, gw, Y, ldy,
+                                         Y ? nullptr : acc, dev->num_sms, st));
+  return QURL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -568,6 +628,51 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
   QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_count_diff(a, b, n, count, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
+}
+
+qurl_status qurl_nvfp4_quant(const void* X, qurl_ftype x_type, int R, int K, int ldx, float pre_scale, void* q4,
+                             void* sblk, float* g, qurl_stream_t stream) {
+  if (!X || !q4 || !sblk || !g || R < 0 || !valid_dim(K) || ldx < K || !std::isfinite(pre_scale))
+    return QURL_ERR_INVALID_ARG;
+  if (x_type != QURL_BF16 && x_type != QURL_FP32) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  const int esize = (x_type == QURL_FP32) ? 4 : 2;
+  if (!aligned16(X) || (static_cast<long long>(ldx) * esize) % 16 != 0 || !aligned16(q4)) return QURL_ERR_ALIGNMENT;
+  if (R == 0) return QURL_OK;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  QURL_CUDA(qurl::launch_nvfp4_quant(X, x_type == QURL_FP32, R, K, ldx, pre_scale, q4, sblk, g,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+size_t qurl_nvfp4_workspace_size(int M, int N, int K) {
+  if (!valid_dim(M) || !valid_dim(N) || !valid_dim(K)) return 0;
+  qurl::GemmPlan p{};
+  qurl::plan_nvfp4(p, M, N, K, device_sms(), static_cast<size_t>(-1));
+  return p.ws_bytes;
+}
+
+qurl_status qurl_nvfp4_linear(const void* q4x, const void* sbx, const float* gx, const void* q4w, const void* sbw,
+                              const float* gw, int M, int N, int K, void* Y, int ldy, void* workspace,
+                              size_t ws_bytes, qurl_stream_t stream) {
+  QURL_TRY(check_nvfp4_rows(q4x, sbx, gx, M, K));
+  QURL_TRY(check_nvfp4_rows(q4w, sbw, gw, N, K));
+  if (!Y || ldy < N) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (static_cast<long long>(ldy) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
+  return run_nvfp4(q4x, sbx, gx, q4w, sbw, gw, M, N, K, Y, ldy, nullptr, workspace, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+qurl_status qurl_nvfp4_gemm_acc(const void* q4x, const void* sbx, const void* q4w, const void* sbw, int M, int N,
+                                int K, float* acc, void* workspace, size_t ws_bytes, qurl_stream_t stream) {
+  static const float one = 1.0f;
+  QURL_TRY(check_nvfp4_rows(q4x, sbx, &one, M, K));
+  QURL_TRY(check_nvfp4_rows(q4w, sbw, &one, N, K));
+  if (!acc) return QURL_ERR_INVALID_ARG;
+  if (!aligned16(acc)) return QURL_ERR_ALIGNMENT;
+  return run_nvfp4(q4x, sbx, nullptr, q4w, sbw, nullptr, M, N, K, nullptr, N, acc, workspace, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 qurl_status qurl_kv_cache_quant(const void* qkv, int M, int ldq, int q_dim, int kv_heads, int head_dim,

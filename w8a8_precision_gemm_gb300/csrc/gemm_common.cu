@@ -65,6 +65,10 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
 
 GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
+bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
+  return plan_wide(p, M, N, K, num_sms, ws_avail);
+}
+
 GemmPlan plan_data(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan w{};
   if (qt == kQInt8 && M >= kWideMinM && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;

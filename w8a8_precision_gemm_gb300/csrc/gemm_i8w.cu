@@ -160,7 +160,9 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
     return j < kI8wModeUnits && ((bars.fast_bits[j >> 5] >> (j & 31)) & 1u) != 0;
   };
   // accumulation passes over a unit's k-blocks: one, or one per 1024-deep chunk
-  auto passes = [&](int j, int nkb) { return is_fast(j) ? 1 : (nkb + C::CHUNK_KB - 1) / C::CHUNK_KB; };
+  auto passes = [&](int j, int nkb) {
+    return (args.float_acc || is_fast(j)) ? 1 : (nkb + C::CHUNK_KB - 1) / C::CHUNK_KB;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -324,8 +326,9 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
           }
           uint32_t r[32];
           tmem_ld32(lane_base + b * C::BN + c0, r);
-          if (np == 1 && emode == kModeBf16) {
-            // one pass: the fp32 accumulator holds the exact integer; scale it as it is
+          if (np == 1 && (emode == kModeBf16 || args.float_acc)) {
+            // one pass: the fp32 accumulator holds the exact integer (or, for fp16 operands that
+            // are not integers, the fp32 sum itself); scale it, or write it as an fp32 partial
             float f[32];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(r[jj]);

@@ -82,6 +82,8 @@ struct GemmArgs {
   int* scratch;          // INT8: per CTA, the int32 running sum of a unit accumulated in chunks
   FusedQuant fq;         // decode fused entries: the quantizer this kernel runs first
   CodeSums fsums;        // ... and where it writes the code sums (INT8 decode)
+  int float_acc;         // fp16 operands that are not integers (the 4-bit variant): every unit in
+                         // one fp32 pass, fp32 partials
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -194,6 +196,9 @@ struct GemmPlan {
 // last kSyncBytes of the caller's workspace.
 constexpr size_t kSyncBytes = 256;
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
+// The 4-bit variant's plan: the CTA-pair layout of the INT8 prefill (both operands widened to fp16
+// in the workspace), for every M; false when ws_avail is short.
+bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
 
 // gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
 // (swap, bn) as a persistent grid.  grid = (token tiles, channel tiles, K
@@ -225,6 +230,13 @@ cudaError_t launch_widen_weights(const void* Wq, int N, int K, void* w16, unsign
                                  cudaStream_t st);
 // the CTAs an i8w launch of this plan runs (one per SM of the resident pairs), for sizing its scratch
 int i8w_max_ctas(int num_sms);
+
+// nvfp4.cu: the 4-bit variant's row quantizer (bf16 rows times pre, or fp32 rows) and the exact
+// widening of its rows to fp16.
+cudaError_t launch_nvfp4_quant(const void* X, bool x_f32, int R, int K, long long ldx, float pre, void* q4,
+                               void* sblk, float* g, cudaStream_t st);
+cudaError_t launch_nvfp4_widen(const void* q4, const void* sblk, int R, int K, void* out16, int num_sms,
+                               cudaStream_t st);
 // split-K reduction in split order: T = int (INT8) or float (FP8)
 cudaError_t launch_splitk_reduce(int qt, const void* part, int splits, int M, int N, const float* sx,
                                  const float* sw, void* Y, long long ldy, void* acc_out, int num_sms,
