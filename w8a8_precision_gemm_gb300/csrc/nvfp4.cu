@@ -35,8 +35,10 @@ namespace {
 
 constexpr int kNvThreads = 256;
 
-// fl(v / d) for a step d in [2^-100, 2^100] by one FMA correction of the
-// reciprocal product (correctly rounded: Markstein's theorem), sign of v kept.
+// fl(v / d) for a step d in [2^-80, 2^100] by one FMA correction of the
+// reciprocal product (correctly rounded by Markstein's theorem wherever the
+// residual does not underflow, |v| >= 2^-102: so for every quotient of 2^-3 or
+// more, all that can round to a nonzero E2M1 code), sign of v kept.
 __device__ __forceinline__ float2 quotient2(float2 v, float d, float inv) {
   const float2 r = __fmul2_rn(v, make_float2(inv, inv));
   const float2 res = __ffma2_rn(r, make_float2(-d, -d), v);
@@ -50,7 +52,7 @@ __device__ __forceinline__ float2 quotient2(float2 v, float d, float inv) {
 __device__ __forceinline__ uint2 e2m1_codes16(const float (&v)[16], float e) {
   uint32_t w[2] = {0u, 0u};
   if (e == 0.0f) return make_uint2(0u, 0u);
-  const bool fma_ok = e >= 0x1p-100f && e <= 0x1p100f;
+  const bool fma_ok = e >= 0x1p-80f && e <= 0x1p100f;
   const float inv = __frcp_rn(e);
 #pragma unroll
   for (int p = 0; p < 8; ++p) {

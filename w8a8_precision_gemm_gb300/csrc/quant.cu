@@ -98,13 +98,16 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
   const int n = blockIdx.x;
   const char* row = reinterpret_cast<const char*>(W) + static_cast<size_t>(n) * ldw * (kF32 ? 4 : 2);
   const int nvec = K >> 3;
-  // pass 1: absmax of W' = W / s (reads only)
+  // W' = W / s; s = 1 (the per-step re-quantization of the folded weights)
+  // divides exactly into w itself, so that case skips the division
+  const bool unit = (s == 1.0f);
+  // pass 1: absmax of W' (reads only)
   float amax = 0.0f;
   for (int idx = threadIdx.x; idx < nvec; idx += blockDim.x) {
     float w[8];
     load_w8<kF32>(row, idx, w);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fdiv_rn(w[e], s)));
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(unit ? w[e] : __fdiv_rn(w[e], s)));
   }
   amax = block_reduce<true>(amax, red);
   const Enc en = make_enc(amax, qt);
@@ -115,8 +118,10 @@ __global__ void __launch_bounds__(kRowThreads) prepare_weights_kernel(const void
   for (int idx = threadIdx.x; idx < nvec; idx += blockDim.x) {
     float w[8];
     load_w8<kF32>(row, idx, w);
+    if (!unit) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = __fdiv_rn(w[e], s);
+      for (int e = 0; e < 8; ++e) w[e] = __fdiv_rn(w[e], s);
+    }
     if (W_scaled) {
       float4* o = reinterpret_cast<float4*>(W_scaled + static_cast<size_t>(n) * K) + 2 * idx;
       o[0] = make_float4(w[0], w[1], w[2], w[3]);

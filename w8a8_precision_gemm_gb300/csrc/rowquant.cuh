@@ -134,7 +134,7 @@ struct Enc {
 
 __device__ __forceinline__ Enc make_enc(float amax, int qt) {
   const float scale = row_scale(amax, qt);
-  return {scale, __frcp_rn(scale), qt, scale >= 0x1p-100f && scale <= 0x1p100f};
+  return {scale, __frcp_rn(scale), qt, scale >= 0x1p-80f && scale <= 0x1p100f};
 }
 
 // ---- paired fp32 arithmetic: sm_100's two-lane fp32 instructions, each lane
@@ -161,12 +161,12 @@ __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 //    division: with inv = fl(1 / scale) (correctly rounded) and r = fl(v *
 //    inv) within an ulp of the quotient, the residual v - r * scale is exact
 //    in one FMA and fl(r + residual * inv) is the correctly rounded quotient
-//    (Markstein's theorem for FMA division, valid while nothing underflows or
-//    overflows: the scale lies in [2^-100, 2^100] and |quotient| <= 448, so
-//    only quotients far below e4m3's smallest subnormal, whose codes are 0
-//    either way, come near underflow).  The sign is copied from v, so that
-//    -0 keeps its sign.  Rows with a scale outside that range divide.  Two
-//    codes per conversion.
+//    (Markstein's theorem for FMA division, valid while the residual does not
+//    underflow, i.e. for |v| >= 2^-102: with the scale in [2^-80, 2^100] and
+//    |quotient| <= 448 every quotient of 2^-11 or more -- all that can give a
+//    nonzero code -- qualifies, and smaller ones, exact or not, encode to a
+//    signed zero).  The sign is copied from v, so that -0 keeps its sign.
+//    Rows with a scale outside that range divide.  Two codes per conversion.
 // The codes are therefore those of the plain division.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
