@@ -21,8 +21,9 @@ Reported beside it (not part of `value`): the 7B-class decode chain (M = 64 and
 256), the 7B-class chain at M = 512 and 4096 with the code flips of a weight
 update W' -> W' + dW' for s = 1 and s = 1.5, every GEMM and quantizer on its
 own against its roofline, the per-RL-step weight re-quantization, the ACR
-token objective, the end-to-end number through the C ABI with host buffers and
-the CPU oracle as a baseline.
+token objective, the tensor-rate probes, the FP8 KV-cache quantizer, the 4-bit
+(NVFP4) variant of the linear, the end-to-end number through the C ABI with
+host buffers and the CPU oracle as a baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
