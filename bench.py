@@ -268,12 +268,15 @@ class Layer:
     def __init__(self, q, qt, model, W, gammas, rotate=0):
         self.q, self.qt, self.model = q, qt, model
         self.w = {}
+        self.wide = {}
         for name, K, N in chain_shapes(model):
             Wd = rotated_rows(W[name].cuda(), N, rotate)
             g = gammas.get(name)
             Wq, sw, gf, _ = q.prepare_weights(Wd, qt, s=S_UAQ, gamma=None if g is None else g.cuda(),
                                               keep_scaled=False)
             self.w[name] = (Wq, sw, gf)
+            if qt == q.INT8:  # the fp16 copy the INT8 prefill GEMM reads, kept with the weights
+                self.wide[name] = q.wide_weights(Wq)
             del Wd
         torch.cuda.synchronize()
 
@@ -409,6 +412,8 @@ def time_per_gemm(q, qtype, layer, model, Ms, stream, pk, l2):
             Wq, sw, _ = layer.w[name]
             k = n_sets(N * K, l2)
             sets = rotated_codes(Wq, sw, k)
+            plan = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)
+            wides = [q.wide_weights(t[0]) for t in sets] if plan["kernel"] == 4 else []
             Xq, sx = q.quant_act(synth.activations(f"bench/{model}/{name}/Xg/{M}", M, K).cuda(), qt)
             ws = q.workspace(M, N, K, qt)
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
@@ -425,12 +430,11 @@ def time_per_gemm(q, qtype, layer, model, Ms, stream, pk, l2):
             nb = alg_bytes(M, K, N)
             t_t = ops / (tensor_peak(pk, qtype) * 1e12)
             t_h = nb / (pk["hbm_gbs"] * 1e9)
-            plan = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)
             res[f"{name}/M{M}"] = {"M": M, "K": K, "N": N, "us": us, "TOPS": ops / (us * 1e-6) / 1e12,
                                    "GBps": nb / (us * 1e-6) / 1e9, "bound": "tensor" if t_t >= t_h else "hbm",
                                    "roofline_frac": max(t_t, t_h) / (us * 1e-6), "launches": nl // R,
                                    "kernel": KERNEL_NAMES[plan["kernel"]], "weight_sets": k}
-            del g, sets, Xq, sx, ws, Y
+            del g, wides, sets, Xq, sx, ws, Y
     torch.cuda.empty_cache()
     return res
 
@@ -1052,6 +1056,7 @@ def run_single(args):
     W = synth.weights(f"single/{model}/{proj}/W", N, K).cuda()
     Wq, sw, _, _ = q.prepare_weights(W, qt, s=S_UAQ, keep_scaled=False)
     del W
+    wide = q.wide_weights(Wq) if qt == q.INT8 else None  # as the benchmark's layers keep it
     Xq, sx = q.quant_act(synth.activations(f"single/{model}/{proj}/X", M, K).cuda(), qt)
     ws = q.workspace(M, N, K, qt)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")

@@ -270,6 +270,31 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
                             qurl_stream_t stream);
 
 /*
+ * A persistent fp16 copy of an INT8 weight matrix for the prefill GEMM.  INT8
+ * products run on the fp16 tensor cores (the codes are exact in fp16); for
+ * large batches (the plan reported as kernel 4 by qurl_debug_plan) the GEMM
+ * reads an fp16 copy of Wq and the per-channel sums of code^2, which a linear
+ * call otherwise writes into its workspace every time (2 N K + 4 N bytes
+ * written, N K read).  qurl_widen_weights writes that copy into the caller's
+ * buffer `wide` (qurl_wide_weights_size(N, K) bytes, 16-byte aligned, owned by
+ * the caller) and attaches it to Wq: later linear calls on this Wq with the
+ * same N, K read it instead.  qurl_prepare_weights into an attached Wq (the
+ * per-RL-step re-quantization) refreshes the copy on the same stream; codes
+ * written into Wq by any other means require calling qurl_widen_weights
+ * again before the next linear call, or the copy is stale.
+ * qurl_detach_wide_weights(Wq) forgets the attachment; call it before
+ * freeing Wq or `wide` (the table is keyed by Wq's address and shape, so a
+ * later matrix allocated at that address would otherwise inherit the copy).
+ * Up to 1024 matrices are attached at a time (more: the call returns
+ * QURL_ERR_UNSUPPORTED).  Outputs are bit-identical either way.
+ * Errors: INVALID_ARG (NULL, a non-positive size), UNSUPPORTED (K % 16, table
+ * full), ALIGNMENT.  One kernel launch.
+ */
+size_t qurl_wide_weights_size(int N, int K);
+qurl_status qurl_widen_weights(const void* Wq, int N, int K, void* wide, qurl_stream_t stream);
+qurl_status qurl_detach_wide_weights(const void* Wq);
+
+/*
  * 4-bit variant (W4A4, NVFP4) of the linear layer ([LIMITS]: 4-bit named as
  * the next speedup; the format itself is a reading, the pages do not define
  * it).  A row (an output channel of W, a token of X) of K values, K a multiple

@@ -179,3 +179,40 @@ def test_wide_more_units_than_mode_slots():
     ref = oracle.gemm_i8(xq[rows].view(np.uint8), wq[cols].view(np.uint8), nthreads=NT)
     Yo = oracle.epilogue(ref, np.full(len(rows), 2.0 ** -10, np.float32), np.full(len(cols), 2.0 ** -8, np.float32))
     np.testing.assert_array_equal(got, Yo)
+
+
+def test_attached_wide_weights_bit_identical_and_refreshed():
+    """A call with the caller's persistent fp16 copy of the weights attached
+    (qurl_widen_weights) launches one kernel fewer than one that widens Wq into
+    its workspace and gives the same bits; re-quantizing the attached Wq in
+    place through qurl_prepare_weights refreshes the copy; after detaching,
+    calls widen again."""
+    M, N, K = 2048, 1024, 2048
+    X = synth.activations("gpu/i8w/att/X", M, K).cuda()
+    W = synth.weights("gpu/i8w/att/W", N, K).cuda()
+    Wq, sw, _, Wm = q.prepare_weights(W, q.INT8, s=1.5)
+    Xq, sx = q.quant_act(X, q.INT8)
+    ws = q.workspace(M, N, K, q.INT8)
+    assert q.plan(M, N, K, q.INT8, sms())["kernel"] == 4
+
+    def run():
+        n0 = q.qurl_kernel_launches()
+        Y = q.linear(Xq, sx, Wq, sw, q.INT8, ws)
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+        return Y, q.qurl_kernel_launches() - n0
+
+    Y0, n_plain = run()
+    wide = q.wide_weights(Wq)
+    Y1, n_att = run()
+    assert n_att == n_plain - 1 and torch.equal(Y0.view(torch.int16), Y1.view(torch.int16))
+    # the per-step re-quantization of an updated master, into the same Wq buffer
+    W2 = Wm + torch.randn_like(Wm) * 1e-3
+    q.qurl_prepare_weights(W2, None, 1.0, q.INT8, Wq, sw)
+    Y2, _ = run()
+    q.qurl_detach_wide_weights(Wq)
+    Y3, n_det = run()
+    assert n_det == n_plain
+    assert torch.equal(Y2.view(torch.int16), Y3.view(torch.int16))
+    assert not torch.equal(Y2.view(torch.int16), Y0.view(torch.int16))
+    del wide

@@ -21,6 +21,7 @@ import ctypes
 import os
 import re
 import threading
+import weakref
 
 import torch
 
@@ -82,6 +83,8 @@ def load() -> ctypes.CDLL:
             "qurl_check_device_status": [P],
             "qurl_debug_inject_timeout": [],
             "qurl_set_fused_decode": [i, P],
+            "qurl_widen_weights": [P, i, i, P, P],
+            "qurl_detach_wide_weights": [P],
             "qurl_nvfp4_quant": [P, i, i, i, i, f, P, P, P, P],
             "qurl_nvfp4_linear": [P, P, P, P, P, P, i, i, i, P, i, P, z, P],
             "qurl_nvfp4_gemm_acc": [P, P, P, P, i, i, i, P, P, z, P],
@@ -97,6 +100,8 @@ def load() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.qurl_workspace_size.argtypes = [i, i, i, i]
         L.qurl_workspace_size.restype = ctypes.c_size_t
+        L.qurl_wide_weights_size.argtypes = [i, i]
+        L.qurl_wide_weights_size.restype = ctypes.c_size_t
         L.qurl_nvfp4_workspace_size.argtypes = [i, i, i]
         L.qurl_nvfp4_workspace_size.restype = ctypes.c_size_t
         L.qurl_acr_workspace_size.argtypes = []
@@ -404,6 +409,32 @@ def count_diff(a, b, stream=None) -> torch.Tensor:
     c = torch.empty(1, dtype=torch.int64, device=a.device)
     qurl_count_diff(a, b, c, stream)
     return c
+
+
+# ---------------------------------------------------------------- attached fp16 weight copies
+
+def qurl_widen_weights(Wq, wide, stream=None):
+    """Write the fp16 copy of INT8 codes Wq [N, K] (and their per-channel sums
+    of squares) into `wide` and attach it to Wq (see include/qurl.h)."""
+    _dense(Wq, wide)
+    N, K = Wq.shape
+    _ok(load().qurl_widen_weights(_ptr(Wq), N, K, _ptr(wide), _stream(stream)), "qurl_widen_weights")
+
+
+def qurl_detach_wide_weights(Wq):
+    _ok(load().qurl_detach_wide_weights(_ptr(Wq)), "qurl_detach_wide_weights")
+
+
+def wide_weights(Wq, stream=None) -> torch.Tensor:
+    """Allocate, fill and attach the fp16 copy of INT8 codes Wq.  The returned
+    tensor holds a reference to Wq and detaches the copy when it is freed, so
+    neither buffer can be reused at its address while attached."""
+    N, K = Wq.shape
+    wide = torch.empty(int(load().qurl_wide_weights_size(N, K)), dtype=torch.uint8, device=Wq.device)
+    qurl_widen_weights(Wq, wide, stream)
+    wide._qurl_wq = Wq  # Wq outlives the attachment
+    weakref.finalize(wide, load().qurl_detach_wide_weights, ctypes.c_void_p(Wq.data_ptr()))
+    return wide
 
 
 # ---------------------------------------------------------------- 4-bit variant (NVFP4)

@@ -204,6 +204,30 @@ qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
 //              before that kernel ends.
 //   fq:        a fused entry's quantizer for the decode GEMM to run first (null:
 //              the activation codes are an input), writing its code sums to fsums.
+// ------------------------------------------------------------------ attached fp16 weight copies
+
+// INT8 weight matrices whose fp16 copy (and per-channel sums of code^2) the
+// caller keeps in its own buffer (qurl_widen_weights): the CTA-pair prefill
+// GEMM reads it instead of widening Wq into the workspace on every call.
+// Layout of an attached buffer: fp16 codes [N, K], then (256-aligned) the sums [N].
+struct WideEntry {
+  const void* wq = nullptr;
+  int N = 0, K = 0;
+  uint8_t* wide = nullptr;
+};
+constexpr int kWideSlots = 1024;
+std::mutex g_wide_mu;
+WideEntry g_wide[kWideSlots];
+
+size_t wide_qn_off(int N, int K) { return (static_cast<size_t>(N) * K * 2 + 255) & ~static_cast<size_t>(255); }
+
+uint8_t* find_wide(const void* wq, int N, int K) {
+  std::lock_guard<std::mutex> lock(g_wide_mu);
+  for (const WideEntry& e : g_wide)
+    if (e.wq == wq && e.N == N && e.K == K) return e.wide;
+  return nullptr;
+}
+
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
                      bool x16_ready = false, bool w_indep = false, const qurl::FusedQuant* fq = nullptr,
@@ -217,13 +241,22 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   const qurl::CodeSums sums = code_sums(p, ws);
   CUtensorMap ta, tb;
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  uint8_t* w16 = nullptr;
+  const unsigned* qn = nullptr;
   if (p.wide) {
     if (!x16_ready) QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
-    QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, wsb + p.w16_off, reinterpret_cast<unsigned*>(wsb + p.qn_off),
-                                         dev->num_sms, st));
-    w_indep = false;  // the GEMM reads the widened weights the kernel before it writes
+    uint8_t* att = find_wide(Wq, N, K);
+    if (att) {  // the caller's fp16 copy, kept current by qurl_widen_weights / qurl_prepare_weights
+      w16 = att;
+      qn = reinterpret_cast<const unsigned*>(att + wide_qn_off(N, K));
+    } else {
+      w16 = wsb + p.w16_off;
+      qn = reinterpret_cast<const unsigned*>(wsb + p.qn_off);
+      QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, w16, const_cast<unsigned*>(qn), dev->num_sms, st));
+    }
+    w_indep = false;
     QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, 128, true, &ta));
-    QURL_TRY(byte_map(wsb + p.w16_off, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
+    QURL_TRY(byte_map(w16, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
   } else if (p.tmem_a) {
     if (!x16_ready) {
       QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
@@ -255,7 +288,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.fault = g_inject_timeout.exchange(0);
   a.asum = sums.asum;
   a.qsum = sums.qsum;
-  a.qn = p.wide ? reinterpret_cast<const unsigned*>(wsb + p.qn_off) : nullptr;
+  a.qn = p.wide ? qn : nullptr;
   a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
   if (fq) {
     a.fq = *fq;
@@ -390,9 +423,12 @@ qurl_status qurl_prepare_weights(const void* W, qurl_ftype w_type, int N, int K,
     return QURL_ERR_INVALID_ARG;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  (void)dev;
   QURL_CUDA(qurl::launch_prepare_weights(W, w_type == QURL_FP32, N, K, ldw, gamma, s, qt, Wq, sw, gamma_folded,
                                          W_scaled, reinterpret_cast<cudaStream_t>(stream)));
+  // new codes in an attached INT8 matrix: refresh its fp16 copy (the next kernel in the stream)
+  if (uint8_t* att = (qt == QURL_INT8) ? find_wide(Wq, N, K) : nullptr)
+    QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, att, reinterpret_cast<unsigned*>(att + wide_qn_off(N, K)),
+                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
 
@@ -627,6 +663,51 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_count_diff(a, b, n, count, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+size_t qurl_wide_weights_size(int N, int K) {
+  if (!valid_dim(N) || !valid_dim(K)) return 0;
+  return wide_qn_off(N, K) + ((static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255));
+}
+
+qurl_status qurl_widen_weights(const void* Wq, int N, int K, void* wide, qurl_stream_t stream) {
+  if (!Wq || !wide || !valid_dim(N) || !valid_dim(K)) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(Wq) || !aligned16(wide)) return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  {
+    std::lock_guard<std::mutex> lock(g_wide_mu);
+    WideEntry* slot = nullptr;
+    for (WideEntry& e : g_wide)
+      if (e.wq == Wq) {
+        slot = &e;
+        break;
+      }
+    if (!slot)
+      for (WideEntry& e : g_wide)
+        if (!e.wq) {
+          slot = &e;
+          break;
+        }
+    if (!slot) return QURL_ERR_UNSUPPORTED;  // every slot taken: detach some first
+    slot->wq = Wq;
+    slot->N = N;
+    slot->K = K;
+    slot->wide = reinterpret_cast<uint8_t*>(wide);
+  }
+  uint8_t* w = reinterpret_cast<uint8_t*>(wide);
+  QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, w, reinterpret_cast<unsigned*>(w + wide_qn_off(N, K)),
+                                       dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_detach_wide_weights(const void* Wq) {
+  if (!Wq) return QURL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_wide_mu);
+  for (WideEntry& e : g_wide)
+    if (e.wq == Wq) e = WideEntry{};
   return QURL_OK;
 }
 
