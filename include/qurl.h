@@ -179,7 +179,8 @@ qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, co
 /*
  * qurl_w8a8_linear without a caller-provided workspace and without allocating:
  * the same computation and the same results as qurl_w8a8_linear given a
- * workspace of qurl_workspace_size(M, N, K, qt) bytes, but its scratch is a
+ * workspace (of the size the shape's plan asks for when no fp16 weight copy
+ * is attached, qurl_widen_weights), but its scratch is a
  * 32 MiB buffer compiled into the library (a file-scope device array), so
  * neither the caller nor the library has to allocate device memory for it.
  * The source pages have no counterpart to this entry point; it exists for
@@ -189,8 +190,8 @@ qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, co
  * cudaMalloc / cudaFree can bring in the middle of a decode loop, and foreign
  * callers that have no handle on the application's allocator.
  *
- *   - Limit: a shape whose qurl_workspace_size exceeds 32 MiB (33,554,432
- *     bytes) returns QURL_ERR_WORKSPACE and launches nothing.  Every 7B-class
+ *   - Limit: a shape whose plan needs more than 32 MiB (33,554,432 bytes)
+ *     returns QURL_ERR_WORKSPACE and launches nothing.  Every 7B-class
  *     decode projection up to M = 256 fits, and every 32B-class one but the
  *     INT8 down projection (K = 27648) at M = 256.
  *   - The buffer lives in a CUDA module of its own.  Under the CUDA runtime's
@@ -286,7 +287,10 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
  * freeing Wq or `wide` (the table is keyed by Wq's address and shape, so a
  * later matrix allocated at that address would otherwise inherit the copy).
  * Up to 1024 matrices are attached at a time (more: the call returns
- * QURL_ERR_UNSUPPORTED).  Outputs are bit-identical either way.
+ * QURL_ERR_UNSUPPORTED).  With a copy attached, INT8 calls above 128 tokens
+ * run on the CTA-pair kernel that reads it (qurl_workspace_size covers that
+ * plan); outputs are bit-identical either way.  Attaching or detaching must
+ * not run concurrently with calls on the same Wq.
  * Errors: INVALID_ARG (NULL, a non-positive size), UNSUPPORTED (K % 16, table
  * full), ALIGNMENT.  One kernel launch.
  */

@@ -189,9 +189,15 @@ def test_plan_workspace_and_fallbacks(L):
     import ctypes
     import w8a8_precision_gemm_gb300 as q
 
-    # the plan's workspace is what qurl_workspace_size reports (160 SMs without a device)
-    for M, N, K, qt in ((64, 4608, 3584, 0), (256, 37888, 3584, 0), (64, 3584, 18944, 1), (4096, 3584, 3584, 0)):
+    # the plan's workspace is what qurl_workspace_size reports (160 SMs without a device) -- for INT8
+    # above 128 tokens at least that, and enough for the CTA-pair plan of weights with an attached
+    # fp16 copy: the activations' fp16 copy, one 256 x 128 int32 region per SM, the counters
+    for M, N, K, qt in ((64, 4608, 3584, 0), (64, 3584, 18944, 1), (4096, 3584, 3584, 0), (256, 4608, 3584, 1)):
         assert q.plan(M, N, K, qt, 160)["ws_bytes"] == L.qurl_workspace_size(M, N, K, qt)
+    for M, N, K in ((256, 37888, 3584), (1024, 7168, 5120)):
+        ws = L.qurl_workspace_size(M, N, K, 0)
+        assert ws >= q.plan(M, N, K, 0, 160)["ws_bytes"]
+        assert ws >= M * K * 2 + 160 * 256 * 128 * 4 + 256
     # no workspace: INT8 widens both operands in shared memory and K is not split
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=0)
     assert p["kernel"] == 0 and p["splits"] == 1 and p["ws_bytes"] == 256  # (a fused call wants the counters)

@@ -216,3 +216,36 @@ def test_attached_wide_weights_bit_identical_and_refreshed():
     assert torch.equal(Y2.view(torch.int16), Y3.view(torch.int16))
     assert not torch.equal(Y2.view(torch.int16), Y0.view(torch.int16))
     del wide
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 4608, 3584), (256, 3584, 18944), (1024, 7168, 5120)])
+def test_attached_weights_take_the_pair_kernel_above_128_tokens(M, N, K):
+    """With an attached fp16 copy of the weights, INT8 batches above 128 tokens
+    run on the CTA-pair kernel (ragged M; K split at 256 x 3584 x 18944) and
+    give the bits of the TMEM-weight kernel that runs without it, and of the
+    oracle on a sample."""
+    X = synth.activations(f"gpu/i8w/mid/X/{M}", M, K).cuda()
+    W = synth.weights(f"gpu/i8w/mid/W/{N}", N, K).cuda()
+    Wq, sw, _, _ = q.prepare_weights(W, q.INT8, s=1.5, keep_scaled=False)
+    del W
+    Xq, sx = q.quant_act(X, q.INT8)
+    ws = q.workspace(M, N, K, q.INT8)
+    assert q.plan(M, N, K, q.INT8, sms())["kernel"] != 4
+    Y0 = q.linear(Xq, sx, Wq, sw, q.INT8, ws)
+    wide = q.wide_weights(Wq)
+    n0 = q.qurl_kernel_launches()
+    Y1 = q.linear(Xq, sx, Wq, sw, q.INT8, ws)
+    launched = q.qurl_kernel_launches() - n0
+    torch.cuda.synchronize()
+    q.qurl_check_device_status()
+    assert launched >= 2  # the activations' widening, the pair GEMM (and a reduction where K is split)
+    assert torch.equal(Y0.view(torch.int16), Y1.view(torch.int16))
+    g = np.random.Generator(np.random.PCG64(M + N))
+    rows = np.unique(np.concatenate([g.choice(M, 16, replace=False), [0, M - 1]]))
+    cols = np.unique(np.concatenate([g.choice(N, 64, replace=False), [0, N - 1]]))
+    xc = Xq.cpu().view(torch.uint8).numpy()
+    wc = Wq.cpu().view(torch.uint8).numpy()
+    ref = oracle.gemm_i8(xc[rows], wc[cols], nthreads=NT)
+    Yo = oracle.epilogue(ref, sx.cpu().numpy()[rows], sw.cpu().numpy()[cols])
+    np.testing.assert_array_equal(synth.bf16_bits(Y1.cpu())[np.ix_(rows, cols)], Yo)
+    del wide

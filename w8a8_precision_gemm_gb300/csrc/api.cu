@@ -228,13 +228,22 @@ uint8_t* find_wide(const void* wq, int N, int K) {
   return nullptr;
 }
 
+// The plan of a call: INT8 on a matrix with an attached fp16 copy (`att`)
+// takes the CTA-pair plan that reads it where that pays, else the shape's plan.
+qurl::GemmPlan choose_plan(int M, int N, int K, int qt, int sms, size_t ws_avail, const uint8_t* att) {
+  qurl::GemmPlan p{};
+  if (qt == QURL_INT8 && att && qurl::plan_attached(p, M, N, K, sms, ws_avail)) return p;
+  return qurl::plan_gemm(M, N, K, qt, sms, ws_avail);
+}
+
 qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K, int qt,
                      void* Y, int ldy, void* acc_out, void* ws, size_t ws_bytes, cudaStream_t st,
                      bool x16_ready = false, bool w_indep = false, const qurl::FusedQuant* fq = nullptr,
                      qurl::CodeSums fsums = qurl::CodeSums{}) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
+  uint8_t* att = (qt == QURL_INT8) ? find_wide(Wq, N, K) : nullptr;
+  const qurl::GemmPlan p = choose_plan(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0, att);
   const bool int8 = (qt == QURL_INT8);
   const bool split = p.splits > 1;
   uint8_t* part = reinterpret_cast<uint8_t*>(ws) + p.x16_bytes;
@@ -245,7 +254,6 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   const unsigned* qn = nullptr;
   if (p.wide) {
     if (!x16_ready) QURL_CUDA(qurl::launch_i8_to_f16(Xq, ws, M, K, sums, st));
-    uint8_t* att = find_wide(Wq, N, K);
     if (att) {  // the caller's fp16 copy, kept current by qurl_widen_weights / qurl_prepare_weights
       w16 = att;
       qn = reinterpret_cast<const unsigned*>(att + wide_qn_off(N, K));
@@ -374,6 +382,13 @@ qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const v
 }
 
 }  // namespace
+
+namespace qurl {
+size_t plain_workspace_bytes(int M, int N, int K, int qt) {
+  if (!valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt)) return 0;
+  return plan_gemm(M, N, K, qt, device_sms(), static_cast<size_t>(-1)).ws_bytes;
+}
+}  // namespace qurl
 
 extern "C" {
 
@@ -509,7 +524,11 @@ size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt) {
     cudaGetLastError();
     sms = 160;  // no device visible: size for the largest SM count this library targets
   }
-  return qurl::plan_gemm(M, N, K, qt, sms, static_cast<size_t>(-1)).ws_bytes;
+  size_t bytes = qurl::plan_gemm(M, N, K, qt, sms, static_cast<size_t>(-1)).ws_bytes;
+  qurl::GemmPlan a{};
+  if (qt == QURL_INT8 && qurl::plan_attached(a, M, N, K, sms, static_cast<size_t>(-1)))
+    bytes = std::max(bytes, a.ws_bytes);  // enough for the plan of a matrix with an attached fp16 copy too
+  return bytes;
 }
 
 qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N, int K,
@@ -554,11 +573,12 @@ bool in_gemm_pays(int kind, int qt, int M) {
   return false;
 }
 
-FusedAct fused_x16(int kind, int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
+FusedAct fused_x16(int kind, const void* Wq, int M, int N, int K, int qt, void* ws, size_t ws_bytes) {
   FusedAct f;
   DevState* dev = nullptr;
   if (device_state(&dev) != QURL_OK) return f;
-  const qurl::GemmPlan p = qurl::plan_gemm(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0);
+  const qurl::GemmPlan p = choose_plan(M, N, K, qt, dev->num_sms, ws ? ws_bytes : 0,
+                                       qt == QURL_INT8 ? find_wide(Wq, N, K) : nullptr);
   if (p.tmem_a || p.wide) {
     f.x16 = ws;
     f.sums = code_sums(p, ws);
@@ -611,7 +631,7 @@ qurl_status qurl_rmsnorm_quant_linear(const void* X, int ldx, const float* gamma
   if (!gamma_folded || !(eps >= 0.0f) || !std::isfinite(eps)) return QURL_ERR_INVALID_ARG;
   if (!aligned16(gamma_folded)) return QURL_ERR_ALIGNMENT;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(qurl::kFuseRmsNorm, M, N, K, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseRmsNorm, Wq, M, N, K, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseRmsNorm, X, ldx, gamma_folded, eps, 1.0f, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
                      sx_scratch, workspace, ws_bytes, st);
@@ -628,7 +648,7 @@ qurl_status qurl_quant_act_linear(const void* X, int ldx, float pre_scale, const
   QURL_TRY(check_fused_out(Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   if (!std::isfinite(pre_scale)) return QURL_ERR_INVALID_ARG;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(qurl::kFuseQuant, M, N, K, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseQuant, Wq, M, N, K, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseQuant, X, ldx, nullptr, 0.0f, pre_scale, Wq, sw, M, N, K, qt, Y, ldy, Xq_scratch,
                      sx_scratch, workspace, ws_bytes, st);
@@ -646,7 +666,7 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   if (!aligned16(GU) || (static_cast<long long>(ldgu) * 2) % 16 != 0) return QURL_ERR_ALIGNMENT;
   QURL_TRY(check_fused_out(Wq, sw, M, N, I, qt, Y, ldy, Xq_scratch, sx_scratch, workspace, ws_bytes));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const FusedAct f = fused_x16(qurl::kFuseSiluMul, M, N, I, qt, workspace, ws_bytes);
+  const FusedAct f = fused_x16(qurl::kFuseSiluMul, Wq, M, N, I, qt, workspace, ws_bytes);
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseSiluMul, GU, ldgu, nullptr, 0.0f, pre_scale, Wq, sw, M, N, I, qt, Y, ldy,
                      Xq_scratch, sx_scratch, workspace, ws_bytes, st);

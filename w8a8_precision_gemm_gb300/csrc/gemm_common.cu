@@ -22,9 +22,10 @@ namespace qurl {
 // takes its place (gate_up at M = 1024: 447-453 us against 399 us with small
 // activation codes and 780 us with normed ones).
 constexpr int kWideMinM = 2048;
+constexpr int kAttachedMinM = 128;
 
 // The INT8 plan on CTA pairs with widened operands, when the workspace holds it.
-bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
+bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, bool w_attached) {
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   p = GemmPlan{};
   p.wide = true;
@@ -46,8 +47,9 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
   splits = (p.num_kb + kps - 1) / kps;
   const size_t x16 = al(static_cast<size_t>(M) * K * 2);
   const size_t sums = al(static_cast<size_t>(M) * 4 * splits);
-  const size_t w16 = al(static_cast<size_t>(N) * K * 2);
-  const size_t qn = al(static_cast<size_t>(N) * 4);
+  // weights attached by the caller (their fp16 copy and sums live in the caller's buffer)
+  const size_t w16 = w_attached ? 0 : al(static_cast<size_t>(N) * K * 2);
+  const size_t qn = w_attached ? 0 : al(static_cast<size_t>(N) * 4);
   const size_t scratch = static_cast<size_t>(i8w_max_ctas(num_sms)) * 256 * 128 * 4;
   const size_t part = splits > 1 ? static_cast<size_t>(splits) * M * N * 4 : 0;
   p.kb_per_split = kps;
@@ -66,14 +68,26 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
 GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
 bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
-  return plan_wide(p, M, N, K, num_sms, ws_avail);
+  return plan_wide(p, M, N, K, num_sms, ws_avail, false);
+}
+
+// INT8 whose weights' fp16 copy the caller keeps (qurl_widen_weights): the
+// CTA-pair kernel above kAttachedMinM tokens.  It reads 2 bytes a weight, so
+// below that the TMEM-weight kernel, which streams the 1-byte codes, is
+// faster; above it the pair kernel's full-rate 256 x 256 tiles win (measured
+// on the 7B/32B shapes at M = 256 and 1024).
+bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
+  if (M <= kAttachedMinM || ws_avail < kSyncBytes) return false;
+  if (!plan_wide(p, M, N, K, num_sms, ws_avail - kSyncBytes, true)) return false;
+  p.ws_bytes += kSyncBytes;
+  return true;
 }
 
 GemmPlan plan_data(int M, int N, int K, int qt, int num_sms, size_t ws_avail) {
   GemmPlan w{};
-  if (qt == kQInt8 && M >= kWideMinM && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
+  if (qt == kQInt8 && M >= kWideMinM && plan_wide(w, M, N, K, num_sms, ws_avail, false)) return w;
   const GemmPlan p = plan_narrow(M, N, K, qt, num_sms, ws_avail);
-  if (p.tmem_a && p.pair && plan_wide(w, M, N, K, num_sms, ws_avail)) return w;
+  if (p.tmem_a && p.pair && plan_wide(w, M, N, K, num_sms, ws_avail, false)) return w;
   return p;
 }
 

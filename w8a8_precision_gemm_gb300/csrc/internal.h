@@ -199,6 +199,12 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 // The 4-bit variant's plan: the CTA-pair layout of the INT8 prefill (both operands widened to fp16
 // in the workspace), for every M; false when ws_avail is short.
 bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
+// INT8 with the weights' fp16 copy attached by the caller (no weight region in the workspace):
+// the CTA-pair plan for batches above 128 tokens; false otherwise or when ws_avail is short.
+bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
+// api.cu: the workspace the shape's plan asks for on the current device when no fp16 weight copy is
+// attached (0 for invalid arguments).
+size_t plain_workspace_bytes(int M, int N, int K, int qt);
 
 // gemm_fp8.cu / gemm_i8.cu / gemm_i8t.cu: launch the instantiation matching
 // (swap, bn) as a persistent grid.  grid = (token tiles, channel tiles, K

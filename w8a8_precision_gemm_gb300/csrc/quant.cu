@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kVPT = 8;           // 16-byte vectors cached per thread
 constexpr int kRowThreads = 512;  // most threads of a row CTA (register budget of the row kernels)
+constexpr int kSlimVPT = 5;       // e.g. the 5120-wide rows of the 32B class at 128 threads
 
 using rq::Enc;
 using rq::block_reduce;
@@ -38,17 +39,21 @@ using rq::warp_max;
 
 // ------------------------------------------------------------------ activation quant
 
+// NC: 16-byte vectors a thread caches (kVPT, or kSlimVPT for rows that need
+// no more: fewer registers, more resident CTAs).
+template <int NC>
 __global__ void __launch_bounds__(kRowThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx, float pre, int qt,
                                  uint8_t* __restrict__ Xq, float* __restrict__ sx, uint8_t* __restrict__ x16,
                                  const CodeSums sums) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ rq::RowScratch sh;
-  rq::quant_act_row<kVPT>(blockIdx.x, X, K, ldx, pre, qt, Xq, sx, x16, sums, sh);
+  rq::quant_act_row<NC>(blockIdx.x, X, K, ldx, pre, qt, Xq, sx, x16, sums, sh);
 }
 
 // ------------------------------------------------------------------ RMSNorm -> quant
 
+template <int NC>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_bfloat16* __restrict__ X, int K, long long ldx,
                                      const float* __restrict__ gamma, float eps, int qt, uint8_t* __restrict__ Xq,
                                      float* __restrict__ sx, float* __restrict__ ms_out, uint8_t* __restrict__ x16,
@@ -56,7 +61,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_kernel(const __nv_b
   griddep_wait();
   griddep_launch_dependents();
   __shared__ rq::RowScratch sh;
-  rq::rmsnorm_quant_row<kVPT>(blockIdx.x, X, K, ldx, gamma, eps, qt, Xq, sx, ms_out, x16, sums, sh);
+  rq::rmsnorm_quant_row<NC>(blockIdx.x, X, K, ldx, gamma, eps, qt, Xq, sx, ms_out, x16, sums, sh);
 }
 
 // ------------------------------------------------------------------ SiLU * up -> quant
@@ -68,6 +73,20 @@ __global__ void __launch_bounds__(kRowThreads, MINB) silu_mul_quant_kernel(const
                                       int qt, uint8_t* __restrict__ Xq, float* __restrict__ sx,
                                       float* __restrict__ h_out, uint8_t* __restrict__ x16,
                                       const CodeSums sums) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ rq::RowScratch sh;
+  rq::silu_mul_quant_row<kVPT / 2>(blockIdx.x, GU, I, ldgu, pre, qt, Xq, sx, h_out, x16, sums, sh);
+}
+
+// Rows of more than 2048 positions at more rows than SMs: 1024 threads (one
+// CTA per SM at 64 registers), so the register cache holds rows of up to 4096
+// positions whole and pass 2 recomputes none of them.
+__global__ void __launch_bounds__(1024, 1) silu_mul_quant_1k_kernel(const __nv_bfloat16* __restrict__ GU, int I,
+                                                                   long long ldgu, float pre, int qt,
+                                                                   uint8_t* __restrict__ Xq, float* __restrict__ sx,
+                                                                   float* __restrict__ h_out,
+                                                                   uint8_t* __restrict__ x16, const CodeSums sums) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ rq::RowScratch sh;
@@ -267,18 +286,20 @@ int row_threads(int nvec, int rows, int per = kVPT) {
 cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float pre, int qt, void* Xq, float* sx,
                              void* x16, CodeSums sums, cudaStream_t st) {
   if (x16 == nullptr) sums.asum = nullptr;
-  return launch_pdl(quant_act_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
-                    reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq), sx,
-                    reinterpret_cast<uint8_t*>(x16), sums);
+  const int t = row_threads(K / 8, M);
+  return launch_pdl(K / 8 <= kSlimVPT * t ? quant_act_kernel<kSlimVPT> : quant_act_kernel<kVPT>, dim3(M), dim3(t),
+                    0, st, reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, pre, qt, reinterpret_cast<uint8_t*>(Xq),
+                    sx, reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
                                  int qt, void* Xq, float* sx, float* ms_out, void* x16, CodeSums sums,
                                  cudaStream_t st) {
   if (x16 == nullptr) sums.asum = nullptr;
-  return launch_pdl(rmsnorm_quant_kernel, dim3(M), dim3(row_threads(K / 8, M)), 0, st,
-                    reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt, reinterpret_cast<uint8_t*>(Xq),
-                    sx, ms_out, reinterpret_cast<uint8_t*>(x16), sums);
+  const int t = row_threads(K / 8, M);
+  return launch_pdl(K / 8 <= kSlimVPT * t ? rmsnorm_quant_kernel<kSlimVPT> : rmsnorm_quant_kernel<kVPT>, dim3(M),
+                    dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(X), K, ldx, gamma, eps, qt,
+                    reinterpret_cast<uint8_t*>(Xq), sx, ms_out, reinterpret_cast<uint8_t*>(x16), sums);
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
@@ -289,6 +310,11 @@ cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, 
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
+  const int nvec = I / 8;
+  if (sms > 0 && M > sms && nvec > kRowThreads * (kVPT / 2) && nvec <= 1024 * (kVPT / 2))
+    return launch_pdl(silu_mul_quant_1k_kernel, dim3(M), dim3(1024), 0, st,
+                      reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq),
+                      sx, h_out, reinterpret_cast<uint8_t*>(x16), sums);
   auto* kern = (sms > 0 && M > sms) ? silu_mul_quant_kernel<2> : silu_mul_quant_kernel<1>;
   return launch_pdl(kern, dim3(M), dim3(t), 0, st, reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt,
                     reinterpret_cast<uint8_t*>(Xq), sx, h_out, reinterpret_cast<uint8_t*>(x16), sums);

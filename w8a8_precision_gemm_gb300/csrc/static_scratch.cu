@@ -20,6 +20,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "internal.h"
 #include "qurl.h"
 
 namespace {
@@ -63,8 +64,9 @@ extern "C" qurl_status qurl_w8a8_linear_static_scratch(const void* Xq, const flo
                                                        int ldy, qurl_stream_t stream) {
   if (!Xq || !sx || !Wq || !sw || !Y || M <= 0 || N <= 0 || K <= 0 || ldy < N) return QURL_ERR_INVALID_ARG;
   if (qt != QURL_INT8 && qt != QURL_FP8_E4M3) return QURL_ERR_INVALID_ARG;
-  // the scratch this shape uses at full speed (on the current device) must fit
-  if (qurl_workspace_size(M, N, K, qt) > kStaticScratchBytes) return QURL_ERR_WORKSPACE;
+  // the scratch this shape's plan uses (on the current device) must fit; an
+  // attached fp16 weight copy's plan that does not fit falls back to it
+  if (qurl::plain_workspace_bytes(M, N, K, qt) > kStaticScratchBytes) return QURL_ERR_WORKSPACE;
   void* scratch = nullptr;
   const qurl_status s = scratch_of_current_device(&scratch);
   if (s != QURL_OK) return s;
