@@ -413,10 +413,10 @@ def time_per_gemm(q, qtype, layer, model, Ms, stream, pk, l2):
             k = n_sets(N * K, l2)
             sets = rotated_codes(Wq, sw, k)
             plan = q.plan(M, N, K, qt, torch.cuda.get_device_properties(0).multi_processor_count)
-            # INT8 weights carry their fp16 copy as the benchmark's layers do; above 128 tokens the call
+            # INT8 weights carry their fp16 copy as the benchmark's layers do; above 256 tokens the call
             # then runs on the CTA-pair kernel that reads it
             wides = [q.wide_weights(t[0]) for t in sets] if qtype == "int8" else []
-            kernel = KERNEL_NAMES[4 if (qtype == "int8" and M > 128) else plan["kernel"]]
+            kernel = KERNEL_NAMES[4 if (qtype == "int8" and M > 256) else plan["kernel"]]
             Xq, sx = q.quant_act(synth.activations(f"bench/{model}/{name}/Xg/{M}", M, K).cuda(), qt)
             ws = q.workspace(M, N, K, qt)
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")

@@ -287,7 +287,7 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
  * freeing Wq or `wide` (the table is keyed by Wq's address and shape, so a
  * later matrix allocated at that address would otherwise inherit the copy).
  * Up to 1024 matrices are attached at a time (more: the call returns
- * QURL_ERR_UNSUPPORTED).  With a copy attached, INT8 calls above 128 tokens
+ * QURL_ERR_UNSUPPORTED).  With a copy attached, INT8 calls above 256 tokens
  * run on the CTA-pair kernel that reads it (qurl_workspace_size covers that
  * plan); outputs are bit-identical either way.  Attaching or detaching must
  * not run concurrently with calls on the same Wq.

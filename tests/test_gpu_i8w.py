@@ -218,12 +218,12 @@ def test_attached_wide_weights_bit_identical_and_refreshed():
     del wide
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 4608, 3584), (256, 3584, 18944), (1024, 7168, 5120)])
-def test_attached_weights_take_the_pair_kernel_above_128_tokens(M, N, K):
-    """With an attached fp16 copy of the weights, INT8 batches above 128 tokens
-    run on the CTA-pair kernel (ragged M; K split at 256 x 3584 x 18944) and
+@pytest.mark.parametrize("M,N,K", [(300, 4608, 3584), (264, 3584, 18944), (1024, 7168, 5120), (256, 4608, 3584)])
+def test_attached_weights_take_the_pair_kernel_above_256_tokens(M, N, K):
+    """With an attached fp16 copy of the weights, INT8 batches above 256 tokens
+    run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944) and
     give the bits of the TMEM-weight kernel that runs without it, and of the
-    oracle on a sample."""
+    oracle on a sample; at 256 tokens the TMEM-weight kernel keeps the call."""
     X = synth.activations(f"gpu/i8w/mid/X/{M}", M, K).cuda()
     W = synth.weights(f"gpu/i8w/mid/W/{N}", N, K).cuda()
     Wq, sw, _, _ = q.prepare_weights(W, q.INT8, s=1.5, keep_scaled=False)

@@ -22,7 +22,7 @@ namespace qurl {
 // takes its place (gate_up at M = 1024: 447-453 us against 399 us with small
 // activation codes and 780 us with normed ones).
 constexpr int kWideMinM = 2048;
-constexpr int kAttachedMinM = 128;
+constexpr int kAttachedMinM = 256;
 
 // The INT8 plan on CTA pairs with widened operands, when the workspace holds it.
 bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, bool w_attached) {
@@ -73,9 +73,10 @@ bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) 
 
 // INT8 whose weights' fp16 copy the caller keeps (qurl_widen_weights): the
 // CTA-pair kernel above kAttachedMinM tokens.  It reads 2 bytes a weight, so
-// below that the TMEM-weight kernel, which streams the 1-byte codes, is
-// faster; above it the pair kernel's full-rate 256 x 256 tiles win (measured
-// on the 7B/32B shapes at M = 256 and 1024).
+// up to there the TMEM-weight kernel, which streams the 1-byte codes, is
+// faster (32B-class qkv / o_proj at M = 256: 31 / 30 us against 44 / 42 us);
+// above it the pair kernel's full-rate 256 x 256 tiles win (M = 1024: qkv 69
+// -> 64 us, o_proj 68 -> 63, down 285 -> 273).
 bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
   if (M <= kAttachedMinM || ws_avail < kSyncBytes) return false;
   if (!plan_wide(p, M, N, K, num_sms, ws_avail - kSyncBytes, true)) return false;

@@ -200,7 +200,7 @@ GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 // in the workspace), for every M; false when ws_avail is short.
 bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
 // INT8 with the weights' fp16 copy attached by the caller (no weight region in the workspace):
-// the CTA-pair plan for batches above 128 tokens; false otherwise or when ws_avail is short.
+// the CTA-pair plan for batches above 256 tokens; false otherwise or when ws_avail is short.
 bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
 // api.cu: the workspace the shape's plan asks for on the current device when no fp16 weight copy is
 // attached (0 for invalid arguments).
