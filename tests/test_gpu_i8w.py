@@ -218,10 +218,12 @@ def test_attached_wide_weights_bit_identical_and_refreshed():
     del wide
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 4608, 3584), (264, 3584, 18944), (1024, 7168, 5120), (256, 4608, 3584)])
+@pytest.mark.parametrize("M,N,K", [(300, 4608, 3584), (264, 3584, 18944), (1024, 7168, 5120), (1024, 5120, 27648),
+                                   (256, 4608, 3584)])
 def test_attached_weights_take_the_pair_kernel_above_256_tokens(M, N, K):
     """With an attached fp16 copy of the weights, INT8 batches above 256 tokens
-    run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944) and
+    run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944 and,
+    by the planner's time model, at 1024 x 5120 x 27648) and
     give the bits of the TMEM-weight kernel that runs without it, and of the
     oracle on a sample; at 256 tokens the TMEM-weight kernel keeps the call."""
     X = synth.activations(f"gpu/i8w/mid/X/{M}", M, K).cuda()

@@ -40,10 +40,40 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, b
   const int slots = std::max(1, num_sms / 2);
   // K splits (ranges of a multiple of 4 k-blocks, 256 codes: the code sums' granularity) only when the
   // pair tiles leave the pairs mostly idle
+  const int cap = std::max(1, std::min(p.num_kb / 16, kMaxSums));
   int splits = 1;
-  if (tiles < slots) splits = std::max(1, std::min(static_cast<int>(slots / tiles), std::min(p.num_kb / 16, kMaxSums)));
-  int kps = (p.num_kb + splits - 1) / splits;
-  kps = (kps + 3) & ~3;
+  if (tiles < slots) splits = std::max(1, std::min(static_cast<int>(slots / tiles), cap));
+  // k-blocks per split for s splits (a multiple of 4: the code sums' granularity)
+  auto kps_of = [&](int s) { return ((p.num_kb + s - 1) / s + 3) & ~3; };
+  {
+    // Rough time of s splits, as for the other kernels: rounds of units over
+    // the pairs x (k-blocks per unit + pipeline fill and drain) x one 64-deep
+    // k-block of a 256 x 256 unit at the fp16 rate (0.33 us), plus the
+    // reduction (launch, s fp32/int32 partials read, bf16 written).  Taken
+    // over the rule above when predicted 10% faster: shapes whose units fill
+    // a last round of pairs barely (32B down at M = 1024: 80 units on 76
+    // pairs, four splits predicted 220 us against 291).
+    auto est = [&](int s) {
+      const int kps = kps_of(s);
+      const int ns = (p.num_kb + kps - 1) / kps;
+      const double rounds = static_cast<double>((tiles * ns + slots - 1) / slots);
+      double t = rounds * (kps + 9) * 0.33;
+      if (ns > 1) t += 3.0 + (static_cast<double>(ns) * M * N * 4 + static_cast<double>(M) * N * 2) / 4e6;
+      return t;
+    };
+    const double t_rule = est(splits);
+    int best = splits;
+    double t_best = t_rule;
+    for (int s = 1; s <= std::min(cap, 64); ++s) {
+      const double t = est(s);
+      if (t < t_best) {
+        t_best = t;
+        best = s;
+      }
+    }
+    if (t_best < 0.9 * t_rule) splits = best;
+  }
+  int kps = kps_of(splits);
   splits = (p.num_kb + kps - 1) / kps;
   const size_t x16 = al(static_cast<size_t>(M) * K * 2);
   const size_t sums = al(static_cast<size_t>(M) * 4 * splits);
