@@ -639,19 +639,20 @@ def nvfp4_bytes(M, K, N):
 
 def time_nvfp4(q, stream, pk, l2):
     """The 4-bit (NVFP4, W4A4) variant on the 32B-class projections: each
-    linear on its own (graph of calls rotating over enough weight sets), and
-    the row quantizer on activations and on fp32 weights.  The GEMM runs on the
-    fp16 tensor pipe (exact widening of the E2M1 x E4M3 values): its roofline
-    is the measured bf16 = fp16 dense rate; the nominal FP4 rate (6x bf16) is
-    reported beside it."""
+    linear on its own (graph of calls rotating over enough weight sets, each
+    with its fp16 copy attached), and the row quantizer on activations and on
+    fp32 weights.  The GEMM runs on the fp16 tensor pipe (exact widening of the
+    E2M1 x E4M3 values): its roofline is the measured bf16 = fp16 dense rate;
+    the nominal FP4 rate (6x bf16) is reported beside it."""
     model = "32b"
     res = {"per_linear": {}}
     for name, K, N in chain_shapes(model):
         W = synth.weights(f"bench/nvfp4/{name}/W", N, K).cuda()
         w0 = q.nvfp4_quant(W)
         del W
-        k = n_sets(N * K // 2, l2)
+        k = n_sets(N * K * 2, l2)  # the GEMM reads the weights' fp16 copy (attached, as for INT8)
         sets = [w0] + [tuple(torch.roll(t, (i * 1009) % N, 0).contiguous() for t in w0) for i in range(1, k)]
+        wides = [q.nvfp4_wide_weights(t) for t in sets]
         for M in (256, 8192):
             x = q.nvfp4_quant(synth.activations(f"bench/nvfp4/{name}/X/{M}", M, K).cuda(), S_UAQ)
             ws = q.nvfp4_workspace(M, N, K)
@@ -674,7 +675,7 @@ def time_nvfp4(q, stream, pk, l2):
                 "frac_fp16_path": max(t_fp16, t_h) / (us * 1e-6),
                 "frac_nvfp4_nominal": max(t_fp16 / 6, t_h) / (us * 1e-6), "weight_sets": k}
             del g, x, ws, Y
-        del sets, w0
+        del wides, sets, w0
         torch.cuda.empty_cache()
     # the row quantizer: activations (bf16, M = 8192, K = 5120) and the gate_up weights (fp32 W')
     for what, R_, K_, f32 in (("act/M8192/K5120", 8192, 5120, False), ("weights/gate_up", 55296, 5120, True)):

@@ -148,7 +148,9 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
  * activation codes (2 M K bytes) with per-token sums of |code| over each K
  * split, the int32 running sums of units accumulated in chunks (one region
  * per SM), and from 2048 tokens on an fp16 copy of the weight codes (2 N K
- * bytes) with their per-channel sums of squares.  The last 256 bytes of any
+ * bytes) with their per-channel sums of squares; above 256 tokens also enough
+ * for the plan that reads an attached fp16 weight copy (qurl_widen_weights)
+ * instead.  The last 256 bytes of any
  * workspace hold two counters through which the CTAs of a fused decode call
  * hand over (see the fused entries): they must be zero before the
  * workspace's first use by a fused entry, and every call leaves them zero.
@@ -167,10 +169,12 @@ size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt);
  * ldy.  workspace: device scratch of ws_bytes (may be NULL / 0).
  * INT8 runs on the fp16 tensor path: the codes are widened to fp16 (exact)
  * and accumulated in fp32, which is exact while every partial sum is an
- * integer of magnitude <= 2^24: a token tile whose tokens have sum |x| <=
- * 2^24 / 128 over the k range is accumulated in one pass, any other in
- * 1024-deep chunks (1024 * 128^2 = 2^24) added in int32.  The int32
- * accumulator and the bf16 Y are therefore exact for any codes.
+ * integer of magnitude <= 2^24: a tile is accumulated in one pass when its
+ * tokens have sum |x| <= 2^24 / 128 over the k range, or (on the CTA-pair
+ * kernel) when max over its tokens of sum x^2 times max over its channels of
+ * sum w^2 is <= 2^48 (Cauchy-Schwarz bounds every partial sum by 2^24), and
+ * in 1024-deep chunks (1024 * 128^2 = 2^24) added in int32 otherwise.  The
+ * int32 accumulator and the bf16 Y are therefore exact for any codes.
  */
 qurl_status qurl_w8a8_linear(const void* Xq, const float* sx, const void* Wq, const float* sw, int M, int N,
                              int K, qurl_qtype qt, void* Y, int ldy, void* workspace, size_t ws_bytes,
@@ -343,6 +347,16 @@ qurl_status qurl_nvfp4_linear(const void* q4x, const void* sbx, const float* gx,
 qurl_status qurl_nvfp4_gemm_acc(const void* q4x, const void* sbx, const void* q4w, const void* sbw, int M, int N,
                                 int K, float* acc, void* workspace, size_t ws_bytes, qurl_stream_t stream);
 
+/* As qurl_widen_weights for 4-bit weight rows: writes their fp16 values
+ * dec(code) * dec(block scale) [N, K] (2 N K bytes, 16-byte aligned, caller
+ * owned) into `wide` and attaches it to q4; qurl_nvfp4_linear / _gemm_acc on
+ * those weights then read it instead of widening them every call, and
+ * qurl_nvfp4_quant into attached rows refreshes it.  Detach with
+ * qurl_detach_wide_weights(q4) before freeing q4 or `wide`.  Errors and
+ * limits as for qurl_widen_weights.  One kernel launch. */
+qurl_status qurl_nvfp4_widen_weights(const void* q4, const void* sblk, int N, int K, void* wide,
+                                     qurl_stream_t stream);
+
 /*
  * FP8 key/value cache quantization ([LIMITS]: section "局限与展望" names FP8
  * KV-cache quantization as not yet optimized in the rollout engine; page 5's
@@ -464,9 +478,11 @@ qurl_status qurl_set_fused_decode(int on, int* previous);
  * GPU with `num_sms` SMs and `ws_bytes` of workspace (SIZE_MAX: as much as
  * qurl_workspace_size asks for).  Host-side only; no device is needed.  Not
  * a computation of the method: a window on the tiling, for tests and tuning.
+ * The plan is the one for weights without an attached fp16 copy.
  * out[0..7]: kernel (0 = operands staged in shared memory, INT8 widened
  * there; 1 = INT8 with the widened weights in TMEM; 2 = the same on CTA
- * pairs, 256 x 256 tiles; 3 = FP8 on CTA pairs), weights on the MMA M side
+ * pairs, 256 x 256 tiles; 3 = FP8 on CTA pairs; 4 = INT8 on CTA pairs with
+ * both operands widened to fp16 in the workspace), weights on the MMA M side
  * (1) or tokens (0), token tile width, token tiles, channel tiles, K splits,
  * k-blocks per split, workspace bytes the plan uses.  QURL_ERR_INVALID_ARG
  * for a null `out`, a non-positive size or SM count, or an unknown qt. */

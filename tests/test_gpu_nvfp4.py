@@ -136,3 +136,31 @@ def test_workspace_too_small_and_k_tail_rejected():
     rc = lib.qurl_nvfp4_linear(q._ptr(x[0]), q._ptr(x[1]), q._ptr(x[2]), q._ptr(w[0]), q._ptr(w[1]), q._ptr(w[2]),
                                64, 256, 504, q._ptr(Y), 256, q._ptr(ws), ws.numel(), None)
     assert q.STATUS[rc] == "QURL_ERR_UNSUPPORTED"  # K not a multiple of 16
+
+
+def test_attached_weight_copy_gives_identical_results_and_refreshes():
+    """With the weights' fp16 copy attached (qurl_nvfp4_widen_weights) the
+    linear launches one kernel fewer and gives the same bits; re-quantizing
+    attached rows in place refreshes the copy; detached, calls widen again."""
+    M, N, K = 512, 1024, 2048
+    x, w = _operands(M, N, K, "attach")
+    ws = q.nvfp4_workspace(M, N, K)
+
+    def run():
+        n0 = q.qurl_kernel_launches()
+        Y = q.nvfp4_linear(x, w, ws)
+        torch.cuda.synchronize()
+        q.qurl_check_device_status()
+        return Y.view(torch.int16).clone(), q.qurl_kernel_launches() - n0
+
+    Y0, n0 = run()
+    wide = q.nvfp4_wide_weights(w)
+    Y1, n1 = run()
+    assert n1 == n0 - 1 and torch.equal(Y0, Y1)
+    W2 = synth.weights("nvfp4/gemm/attach/W2", N, K).cuda()
+    q.qurl_nvfp4_quant(W2, 1.0, *w)  # new codes into the attached rows
+    Y2, _ = run()
+    q.qurl_detach_wide_weights(w[0])
+    Y3, n3 = run()
+    assert n3 == n0 and torch.equal(Y2, Y3) and not torch.equal(Y2, Y0)
+    del wide

@@ -86,6 +86,7 @@ def load() -> ctypes.CDLL:
             "qurl_widen_weights": [P, i, i, P, P],
             "qurl_detach_wide_weights": [P],
             "qurl_nvfp4_quant": [P, i, i, i, i, f, P, P, P, P],
+            "qurl_nvfp4_widen_weights": [P, P, i, i, P, P],
             "qurl_nvfp4_linear": [P, P, P, P, P, P, i, i, i, P, i, P, z, P],
             "qurl_nvfp4_gemm_acc": [P, P, P, P, i, i, i, P, P, z, P],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
@@ -480,6 +481,19 @@ def nvfp4_quant(X, pre_scale=1.0, stream=None):
     g = torch.empty(R, dtype=torch.float32, device=X.device)
     qurl_nvfp4_quant(X, pre_scale, q4, sb, g, stream)
     return q4, sb, g
+
+
+def nvfp4_wide_weights(w, stream=None) -> torch.Tensor:
+    """Allocate, fill and attach the fp16 copy of 4-bit weight rows w = (q4, sblk, g);
+    detached when the returned tensor is freed (it holds a reference to q4)."""
+    q4, sb, _ = w
+    N, K = q4.shape[0], q4.shape[1] * 2
+    wide = torch.empty(N * K * 2, dtype=torch.uint8, device=q4.device)
+    _ok(load().qurl_nvfp4_widen_weights(_ptr(q4), _ptr(sb), N, K, _ptr(wide), _stream(stream)),
+        "qurl_nvfp4_widen_weights")
+    wide._qurl_wq = q4
+    weakref.finalize(wide, load().qurl_detach_wide_weights, ctypes.c_void_p(q4.data_ptr()))
+    return wide
 
 
 def nvfp4_workspace(M, N, K, device="cuda") -> torch.Tensor:

@@ -210,9 +210,11 @@ qurl::CodeSums code_sums(const qurl::GemmPlan& p, void* ws) {
 // caller keeps in its own buffer (qurl_widen_weights): the CTA-pair prefill
 // GEMM reads it instead of widening Wq into the workspace on every call.
 // Layout of an attached buffer: fp16 codes [N, K], then (256-aligned) the sums [N].
+constexpr int kWideInt8 = 0;   // INT8 codes: fp16 codes, then the per-channel sums of code^2
+constexpr int kWideNvfp4 = 1;  // 4-bit rows: fp16 values dec(code) * dec(block scale)
 struct WideEntry {
   const void* wq = nullptr;
-  int N = 0, K = 0;
+  int N = 0, K = 0, kind = kWideInt8;
   uint8_t* wide = nullptr;
 };
 constexpr int kWideSlots = 1024;
@@ -221,11 +223,35 @@ WideEntry g_wide[kWideSlots];
 
 size_t wide_qn_off(int N, int K) { return (static_cast<size_t>(N) * K * 2 + 255) & ~static_cast<size_t>(255); }
 
-uint8_t* find_wide(const void* wq, int N, int K) {
+uint8_t* find_wide(const void* wq, int N, int K, int kind = kWideInt8) {
   std::lock_guard<std::mutex> lock(g_wide_mu);
   for (const WideEntry& e : g_wide)
-    if (e.wq == wq && e.N == N && e.K == K) return e.wide;
+    if (e.wq == wq && e.N == N && e.K == K && e.kind == kind) return e.wide;
   return nullptr;
+}
+
+// Record (or re-point) an attachment; false when every slot is taken.
+bool attach_wide(const void* wq, int N, int K, int kind, void* wide) {
+  std::lock_guard<std::mutex> lock(g_wide_mu);
+  WideEntry* slot = nullptr;
+  for (WideEntry& e : g_wide)
+    if (e.wq == wq) {
+      slot = &e;
+      break;
+    }
+  if (!slot)
+    for (WideEntry& e : g_wide)
+      if (!e.wq) {
+        slot = &e;
+        break;
+      }
+  if (!slot) return false;
+  slot->wq = wq;
+  slot->N = N;
+  slot->K = K;
+  slot->kind = kind;
+  slot->wide = reinterpret_cast<uint8_t*>(wide);
+  return true;
 }
 
 // The plan of a call: INT8 on a matrix with an attached fp16 copy (`att`)
@@ -346,16 +372,18 @@ qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const v
                       cudaStream_t st) {
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
+  uint8_t* att = find_wide(q4w, N, K, kWideNvfp4);  // the caller's fp16 copy of the weights, if attached
   qurl::GemmPlan p{};
-  if (!ws || !qurl::plan_nvfp4(p, M, N, K, dev->num_sms, ws_bytes)) return QURL_ERR_WORKSPACE;
+  if (!ws || !qurl::plan_nvfp4(p, M, N, K, dev->num_sms, ws_bytes, att != nullptr)) return QURL_ERR_WORKSPACE;
   if (!aligned16(ws)) return QURL_ERR_ALIGNMENT;
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
   const bool split = p.splits > 1;
+  uint8_t* w16 = att ? att : wsb + p.w16_off;
   QURL_CUDA(qurl::launch_nvfp4_widen(q4x, sbx, M, K, ws, dev->num_sms, st));
-  QURL_CUDA(qurl::launch_nvfp4_widen(q4w, sbw, N, K, wsb + p.w16_off, dev->num_sms, st));
+  if (!att) QURL_CUDA(qurl::launch_nvfp4_widen(q4w, sbw, N, K, w16, dev->num_sms, st));
   CUtensorMap ta, tb;
   QURL_TRY(byte_map(ws, M, 2LL * K, 2LL * K, 128, 128, true, &ta));
-  QURL_TRY(byte_map(wsb + p.w16_off, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
+  QURL_TRY(byte_map(w16, N, 2LL * K, 2LL * K, 128, 128, true, &tb));
   qurl::GemmArgs a{};
   a.M = M;
   a.N = N;
@@ -697,26 +725,7 @@ qurl_status qurl_widen_weights(const void* Wq, int N, int K, void* wide, qurl_st
   if (!aligned16(Wq) || !aligned16(wide)) return QURL_ERR_ALIGNMENT;
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
-  {
-    std::lock_guard<std::mutex> lock(g_wide_mu);
-    WideEntry* slot = nullptr;
-    for (WideEntry& e : g_wide)
-      if (e.wq == Wq) {
-        slot = &e;
-        break;
-      }
-    if (!slot)
-      for (WideEntry& e : g_wide)
-        if (!e.wq) {
-          slot = &e;
-          break;
-        }
-    if (!slot) return QURL_ERR_UNSUPPORTED;  // every slot taken: detach some first
-    slot->wq = Wq;
-    slot->N = N;
-    slot->K = K;
-    slot->wide = reinterpret_cast<uint8_t*>(wide);
-  }
+  if (!attach_wide(Wq, N, K, kWideInt8, wide)) return QURL_ERR_UNSUPPORTED;  // every slot taken
   uint8_t* w = reinterpret_cast<uint8_t*>(wide);
   QURL_CUDA(qurl::launch_widen_weights(Wq, N, K, w, reinterpret_cast<unsigned*>(w + wide_qn_off(N, K)),
                                        dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
@@ -744,6 +753,21 @@ qurl_status qurl_nvfp4_quant(const void* X, qurl_ftype x_type, int R, int K, int
   QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_nvfp4_quant(X, x_type == QURL_FP32, R, K, ldx, pre_scale, q4, sblk, g,
                                      reinterpret_cast<cudaStream_t>(stream)));
+  // new codes in attached rows: refresh their fp16 copy (the next kernel in the stream)
+  if (uint8_t* att = find_wide(q4, R, K, kWideNvfp4))
+    QURL_CUDA(qurl::launch_nvfp4_widen(q4, sblk, R, K, att, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QURL_OK;
+}
+
+qurl_status qurl_nvfp4_widen_weights(const void* q4, const void* sblk, int N, int K, void* wide,
+                                     qurl_stream_t stream) {
+  if (!q4 || !sblk || !wide || !valid_dim(N) || !valid_dim(K)) return QURL_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QURL_ERR_UNSUPPORTED;
+  if (!aligned16(q4) || !aligned16(wide)) return QURL_ERR_ALIGNMENT;
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
+  if (!attach_wide(q4, N, K, kWideNvfp4, wide)) return QURL_ERR_UNSUPPORTED;
+  QURL_CUDA(qurl::launch_nvfp4_widen(q4, sblk, N, K, wide, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
 

@@ -97,8 +97,8 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, b
 
 GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 
-bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
-  return plan_wide(p, M, N, K, num_sms, ws_avail, false);
+bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, bool w_attached) {
+  return plan_wide(p, M, N, K, num_sms, ws_avail, w_attached);
 }
 
 // INT8 whose weights' fp16 copy the caller keeps (qurl_widen_weights): the

@@ -198,7 +198,7 @@ constexpr size_t kSyncBytes = 256;
 GemmPlan plan_gemm(int M, int N, int K, int qt, int num_sms, size_t ws_avail);
 // The 4-bit variant's plan: the CTA-pair layout of the INT8 prefill (both operands widened to fp16
 // in the workspace), for every M; false when ws_avail is short.
-bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
+bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, bool w_attached = false);
 // INT8 with the weights' fp16 copy attached by the caller (no weight region in the workspace):
 // the CTA-pair plan for batches above 256 tokens; false otherwise or when ws_avail is short.
 bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail);
