@@ -219,11 +219,13 @@ def test_attached_wide_weights_bit_identical_and_refreshed():
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 4608, 3584), (264, 3584, 18944), (1024, 7168, 5120), (1024, 5120, 27648),
-                                   (256, 4608, 3584)])
+                                   (1024, 5120, 5120), (256, 4608, 3584)])
 def test_attached_weights_take_the_pair_kernel_above_256_tokens(M, N, K):
     """With an attached fp16 copy of the weights, INT8 batches above 256 tokens
     run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944 and,
-    by the planner's time model, at 1024 x 5120 x 27648) and
+    by the planner's time model, at 1024 x 5120 x 27648; at 1024 x 5120 x 5120
+    76 of the 80 tiles run whole and the last 4 split, reduced by their own
+    kernel -- raw int32 sums through qurl_w8a8_gemm_acc too) and
     give the bits of the TMEM-weight kernel that runs without it, and of the
     oracle on a sample; at 256 tokens the TMEM-weight kernel keeps the call."""
     X = synth.activations(f"gpu/i8w/mid/X/{M}", M, K).cuda()
@@ -250,4 +252,8 @@ def test_attached_weights_take_the_pair_kernel_above_256_tokens(M, N, K):
     ref = oracle.gemm_i8(xc[rows], wc[cols], nthreads=NT)
     Yo = oracle.epilogue(ref, sx.cpu().numpy()[rows], sw.cpu().numpy()[cols])
     np.testing.assert_array_equal(synth.bf16_bits(Y1.cpu())[np.ix_(rows, cols)], Yo)
+    acc = q.gemm_acc(Xq, Wq, q.INT8, ws)
+    torch.cuda.synchronize()
+    q.qurl_check_device_status()
+    np.testing.assert_array_equal(sampled(acc, rows, cols), ref)
     del wide

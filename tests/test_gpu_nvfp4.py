@@ -85,10 +85,12 @@ def _operands(M, N, K, tag):
     return x, w
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 520, 1040), (64, 4608, 3584), (256, 256, 8192)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 520, 1040), (64, 4608, 3584), (256, 256, 8192),
+                                   (1024, 5120, 5120)])
 def test_gemm_acc_and_linear(M, N, K):
-    """Tiles, ragged M/N, a K tail (1040 = 16.25 k-blocks of 64), and K split
-    eight ways (one 256 x 256 tile)."""
+    """Tiles, ragged M/N, a K tail (1040 = 16.25 k-blocks of 64), K split eight
+    ways (one 256 x 256 tile), and 80 tiles on 76 SM pairs: 76 whole, the last
+    4 split and reduced by their own kernel."""
     x, w = _operands(M, N, K, f"{M}/{N}/{K}")
     ws = q.nvfp4_workspace(M, N, K)
     acc = q.nvfp4_gemm_acc(x, w, ws)

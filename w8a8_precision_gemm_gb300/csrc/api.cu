@@ -324,6 +324,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.qsum = sums.qsum;
   a.qn = p.wide ? qn : nullptr;
   a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
+  a.whole_units = p.wide ? p.whole_units : 0;
   if (fq) {
     a.fq = *fq;
     a.fsums = fsums;
@@ -341,9 +342,17 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   else
     QURL_CUDA(int8 ? qurl::launch_gemm_i8(p.swap, p.bn, ta, tb, a, grid, st)
                    : qurl::launch_gemm_fp8(p.swap, p.bn, ta, tb, a, grid, st));
-  if (split)
+  if (split && a.whole_units > 0) {  // only the split tail needs reducing
+    qurl::GemmArgs r = a;
+    r.tiles_tok = p.tiles_tok;
+    r.tiles_ch = p.tiles_ch;
+    r.splits = p.splits;
+    r.part = part;
+    QURL_CUDA(qurl::launch_tail_reduce(int8, r, st));
+  } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qt, part, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
                                          dev->num_sms, st));
+  }
   return QURL_OK;
 }
 
@@ -402,10 +411,19 @@ qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const v
   a.fault = g_inject_timeout.exchange(0);
   a.scratch = reinterpret_cast<int*>(wsb + p.scratch_off);
   a.float_acc = 1;
+  a.whole_units = p.whole_units;
   QURL_CUDA(qurl::launch_gemm_i8w(ta, tb, a, dim3(p.tiles_tok, p.tiles_ch, p.splits), st));
-  if (split)
+  if (split && a.whole_units > 0) {  // only the split tail needs reducing
+    qurl::GemmArgs r = a;
+    r.tiles_tok = p.tiles_tok;
+    r.tiles_ch = p.tiles_ch;
+    r.splits = p.splits;
+    r.part = wsb + p.x16_bytes;
+    QURL_CUDA(qurl::launch_tail_reduce(false, r, st));
+  } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qurl::kQFp8, wsb + p.x16_bytes, p.splits, M, N, gx, gw, Y, ldy,
                                          Y ? nullptr : acc, dev->num_sms, st));
+  }
   return QURL_OK;
 }
 

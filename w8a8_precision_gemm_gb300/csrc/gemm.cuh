@@ -312,12 +312,14 @@ __device__ __forceinline__ float channel_scale(const GemmArgs& a, int mode, int 
 
 // Prefill orientation: write 32 accumulator values of one tile row.  i = row
 // of the A tile (TMEM lane = token), columns c0..c0+31 of the B tile.
+// (part_base, when given, replaces a.part: a whole-K unit of a call that also
+// has split units writes its raw sums straight to the accumulator output)
 template <int BN, typename T>
 __device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int b0, int split, int i, int c0,
-                                       const T (&v)[32]) {
+                                       const T (&v)[32], void* part_base = nullptr) {
   const int M = a.M, N = a.N;
   if (mode == kModeAcc) {
-    T* part = reinterpret_cast<T*>(a.part) + static_cast<size_t>(split) * M * N;
+    T* part = reinterpret_cast<T*>(part_base ? part_base : a.part) + static_cast<size_t>(split) * M * N;
     const int m = a0 + i;
     if (m < M) {
       T* dst = part + static_cast<size_t>(m) * N + (b0 + c0);

@@ -73,6 +73,30 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, b
     }
     if (t_best < 0.9 * t_rule) splits = best;
   }
+  // Hybrid: when whole-K units would leave a last round of pairs mostly idle
+  // (tiles a little above a multiple of the pairs), the tiles of that last
+  // round alone are split so that their pieces fill it, and a reduction kernel
+  // finishes only them (32B o_proj at M = 1024: 80 tiles on 76 pairs, 76 whole
+  // + 4 split five ways: 1.2 unit-times instead of 2).
+  int whole = 0;
+  if (splits == 1 && tiles > slots && tiles % slots != 0) {
+    const long long rem = tiles % slots;
+    const int st = std::min(static_cast<int>(slots / rem), cap);
+    if (st >= 2) {
+      const int kps_t = kps_of(st);
+      const int ns = (p.num_kb + kps_t - 1) / kps_t;
+      const double unit = (p.num_kb + 9) * 0.33;
+      const double t_plain = static_cast<double>((tiles + slots - 1) / slots) * unit;
+      const double t_hyb = static_cast<double>(tiles / slots) * unit +
+                           static_cast<double>((rem * ns + slots - 1) / slots) * (kps_t + 9) * 0.33 + 3.0 +
+                           static_cast<double>(rem) * 65536.0 * (4.0 * ns + 2.0) / 4e6;
+      if (t_hyb < 0.9 * t_plain) {
+        whole = static_cast<int>(tiles - rem);
+        splits = ns;
+      }
+    }
+  }
+  p.whole_units = whole;
   int kps = kps_of(splits);
   splits = (p.num_kb + kps - 1) / kps;
   const size_t x16 = al(static_cast<size_t>(M) * K * 2);

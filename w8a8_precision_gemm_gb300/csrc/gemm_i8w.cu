@@ -75,25 +75,44 @@ struct I8wBarriers {
 // Token tiles per group of the unit order below.
 constexpr int kI8wTokGroup = 16;
 
-// Tile coordinates of unit u.  Units run K split slowest, then groups of
-// kI8wTokGroup token tiles, then channel tiles, token tile fastest: the pairs
-// running together cover a few channel tiles of one token group, so a
-// channel tile's weights are read from HBM once per token group and the
-// group's activations (16 x 256 rows) stay in L2 while its channel tiles go by.
+// Tile v's coordinates in the unit order: groups of kI8wTokGroup token tiles,
+// then channel tiles, token tile fastest -- the pairs running together cover a
+// few channel tiles of one token group, so a channel tile's weights are read
+// from HBM once per token group and the group's activations (16 x 256 rows)
+// stay in L2 while its channel tiles go by.
+__host__ __device__ __forceinline__ void i8w_tile(int tiles_tok, int tiles_ch, int v, int& tok, int& ch) {
+  const int gi = v / (kI8wTokGroup * tiles_ch);  // only the last group can be short
+  const int gs = min(kI8wTokGroup, tiles_tok - gi * kI8wTokGroup);
+  const int r = v - gi * kI8wTokGroup * tiles_ch;
+  ch = r / gs;
+  tok = gi * kI8wTokGroup + (r - ch * gs);
+}
+
+// Unit u: the first whole_units units are tiles 0 .. whole_units - 1 over all
+// of K (sp = -1); the remaining tiles are split `splits` ways, split slowest
+// (so the pieces of one tile run on different pairs at the same time).  With
+// whole_units = 0 every tile is split.
 struct UnitCoords {
   int tok, ch, sp;
 };
 __device__ __forceinline__ UnitCoords i8w_coords(const GemmArgs& a, int u) {
-  const int per_split = a.tiles_tok * a.tiles_ch;
   UnitCoords c;
-  c.sp = u / per_split;
-  const int v = u - c.sp * per_split;
-  const int gi = v / (kI8wTokGroup * a.tiles_ch);  // only the last group can be short
-  const int gs = min(kI8wTokGroup, a.tiles_tok - gi * kI8wTokGroup);
-  const int r = v - gi * kI8wTokGroup * a.tiles_ch;
-  c.ch = r / gs;
-  c.tok = gi * kI8wTokGroup + (r - c.ch * gs);
+  int v;
+  if (u < a.whole_units) {
+    v = u;
+    c.sp = -1;
+  } else {
+    const int tail = a.tiles_tok * a.tiles_ch - a.whole_units;
+    const int w = u - a.whole_units;
+    c.sp = w / tail;
+    v = a.whole_units + (w - c.sp * tail);
+  }
+  i8w_tile(a.tiles_tok, a.tiles_ch, v, c.tok, c.ch);
   return c;
+}
+
+__device__ __forceinline__ int i8w_units(const GemmArgs& a) {
+  return a.whole_units + (a.tiles_tok * a.tiles_ch - a.whole_units) * a.splits;
 }
 
 // This CTA's part of unit u: token rows a0 .. a0 + 127, output channels
@@ -103,8 +122,8 @@ __device__ __forceinline__ Unit i8w_unit(const GemmArgs& a, int u, uint32_t rank
   Unit w;
   w.a0 = c.tok * 256 + static_cast<int>(rank) * 128;
   w.b0 = c.ch * 256;
-  w.kb0 = c.sp * a.kb_per_split;
-  w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
+  w.kb0 = c.sp < 0 ? 0 : c.sp * a.kb_per_split;
+  w.nkb = c.sp < 0 ? a.num_kb : min(a.num_kb - w.kb0, a.kb_per_split);
   w.split = c.sp;
   return w;
 }
@@ -124,7 +143,7 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   // the two CTAs of a cluster walk the same units
   const int u_begin = static_cast<int>(blockIdx.x >> 1), u_stride = static_cast<int>(gridDim.x >> 1);
-  const int u_end = args.tiles_tok * args.tiles_ch * args.splits;
+  const int u_end = i8w_units(args);
   int* status = args.status;
 
   if (threadIdx.x == 0) {
@@ -258,24 +277,37 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
       for (int u = u_begin, j = 0; u < u_end && j < kI8wModeUnits; u += u_stride, ++j) {
         const UnitCoords uc = i8w_coords(args, u);
         const int t = uc.tok, ch = uc.ch, sp = uc.sp;
-        int smax = 0;
-        unsigned qmax = 0, nmax = 0;
+        // a whole-K unit's sums are those of all the split ranges added (exact
+        // integers; a capped range makes the total exceed the bounds either way)
+        const int s0 = sp < 0 ? 0 : sp, s1 = sp < 0 ? args.splits : sp + 1;
+        unsigned long long smax = 0, qmax = 0;
+        unsigned nmax = 0;
         for (int c = lane; c < 256; c += 32) {
           const int m = t * 256 + c;
           if (m < args.M) {
-            const size_t k = static_cast<size_t>(m) * args.splits + sp;
-            smax = max(smax, __ldg(args.asum + k));
-            if (args.qsum) qmax = max(qmax, __ldg(args.qsum + k));
+            unsigned long long sa = 0, qa = 0;
+            for (int k = s0; k < s1; ++k) {
+              const size_t at = static_cast<size_t>(m) * args.splits + k;
+              sa += static_cast<unsigned long long>(__ldg(args.asum + at));
+              if (args.qsum) qa += __ldg(args.qsum + at);
+            }
+            smax = max(smax, sa);
+            qmax = max(qmax, qa);
           }
           const int n = ch * 256 + c;
           if (args.qn && n < args.N) nmax = max(nmax, __ldg(args.qn + n));
         }
-        smax = __reduce_max_sync(0xFFFFFFFFu, smax);
-        qmax = __reduce_max_sync(0xFFFFFFFFu, qmax);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, o));
+          qmax = max(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, o));
+        }
         nmax = __reduce_max_sync(0xFFFFFFFFu, nmax);
-        const bool fast = smax <= kFastAbsSum ||
-                          (args.qsum && args.qn &&
-                           static_cast<unsigned long long>(qmax) * static_cast<unsigned long long>(nmax) <= kFastSqProd);
+        // Q_t x Q_n <= 2^48, in exact 128-bit arithmetic
+        const unsigned long long lo = qmax * static_cast<unsigned long long>(nmax);
+        const unsigned long long hi = __umul64hi(qmax, static_cast<unsigned long long>(nmax));
+        const bool fast = smax <= static_cast<unsigned long long>(kFastAbsSum) ||
+                          (args.qsum && args.qn && hi == 0 && lo <= kFastSqProd);
         if (lane == 0) {
           if (fast) bars.fast_bits[j >> 5] |= 1u << (j & 31);
           st_release_cta(&bars.mode_count, static_cast<uint32_t>(j + 1));
@@ -293,7 +325,6 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t pempty0 = cluster_map(&bars.pempty[0], 0);
     int* scr = args.scratch + static_cast<size_t>(blockIdx.x) * C::SCRATCH_INTS + i;  // [column][row]
-    const int emode = args.mode;
     int nb[2] = {0, 0};
     int nextbuf = 0;
     bool ok = true;
@@ -303,6 +334,12 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
         ok = false;
         break;
       }
+      // a whole-K unit of a call with a split tail writes its result itself:
+      // scaled to Y, or as raw sums straight into the accumulator output
+      const bool whole = (w.split < 0);
+      const int emode = whole ? (args.Y ? kModeBf16 : kModeAcc) : args.mode;
+      const int esplit = whole ? 0 : w.split;
+      void* ebase = (whole && !args.Y) ? args.acc_out : nullptr;
       const int np = passes(j, w.nkb);
       for (int p = 0; p < np; ++p) {
         const int b = nextbuf;
@@ -332,7 +369,7 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
             float f[32];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(r[jj]);
-            emit32<C::BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, f);
+            emit32<C::BN, float>(args, emode, w.a0, w.b0, esplit, i, c0, f, ebase);
             continue;
           }
           int v[32];
@@ -349,7 +386,7 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
               continue;
             }
           }
-          emit32<C::BN, int>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+          emit32<C::BN, int>(args, emode, w.a0, w.b0, esplit, i, c0, v, ebase);
         }
         tc_fence_before();
         __syncwarp();
@@ -398,6 +435,39 @@ __global__ void __launch_bounds__(256) widen_weights_kernel(const uint8_t* __res
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
   if (lane == 0) qn[row] = static_cast<unsigned>(q < 0xFFFFFFFFull ? q : 0xFFFFFFFFull);
+}
+
+// The split tail of a hybrid plan: one CTA per 16 rows of a tail tile, one
+// thread per column; each output is the sum of its `splits` partials in split
+// order (int32: exact in any order; fp32: a fixed order), then the epilogue
+// y = bf16((fp32(sum) * sx[m]) * sw[n]), or the raw sum into acc_out.
+template <typename T>
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
+                                                          int tiles_tok, int tiles_ch, int whole_units,
+                                                          const float* __restrict__ sx, const float* __restrict__ sw,
+                                                          __nv_bfloat16* __restrict__ Y, long long ldy,
+                                                          T* __restrict__ acc_out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int v = whole_units + static_cast<int>(blockIdx.x >> 4);  // the tail tile
+  int tok, ch;
+  i8w_tile(tiles_tok, tiles_ch, v, tok, ch);
+  const int n = ch * 256 + static_cast<int>(threadIdx.x);
+  if (n >= N) return;
+  const size_t plane = static_cast<size_t>(M) * N;
+  const float swn = Y ? __ldg(sw + n) : 0.0f;
+  for (int r = 0; r < 16; ++r) {
+    const int m = tok * 256 + static_cast<int>(blockIdx.x & 15) * 16 + r;
+    if (m >= M) break;
+    const size_t at = static_cast<size_t>(m) * N + n;
+    T sum = T(0);
+    for (int z = 0; z < splits; ++z) sum += __ldcg(part + z * plane + at);
+    if (Y)
+      Y[static_cast<size_t>(m) * ldy + n] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(static_cast<float>(sum),
+                                                                                     __ldg(sx + m)), swn));
+    else
+      acc_out[at] = sum;
+  }
 }
 
 }  // namespace
@@ -452,12 +522,26 @@ cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, co
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(args.tiles_tok) * args.tiles_ch * args.splits;
+  const long long tiles = static_cast<long long>(args.tiles_tok) * args.tiles_ch;
+  const long long units = args.whole_units + (tiles - args.whole_units) * args.splits;
   // the scratch holds one region per CTA, sized for one CTA per SM
   const int pairs = static_cast<int>(
       std::max<long long>(1, std::min<long long>(std::min<long long>(units, max_pairs[dev]), sms / 2)));
   return launch_pdl_pair(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(C::NUM_THREADS), C::SMEM_BYTES, stream,
                          tx16, tw16, args);
+}
+
+cudaError_t launch_tail_reduce(bool int_partials, const GemmArgs& a, cudaStream_t st) {
+  const long long tail = static_cast<long long>(a.tiles_tok) * a.tiles_ch - a.whole_units;
+  if (tail <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(tail * 16));
+  if (int_partials)
+    return launch_pdl(tail_reduce_kernel<int>, grid, dim3(256), 0, st, reinterpret_cast<const int*>(a.part), a.splits,
+                      a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, a.sx, a.sw, a.Y, a.ldy,
+                      reinterpret_cast<int*>(a.acc_out));
+  return launch_pdl(tail_reduce_kernel<float>, grid, dim3(256), 0, st, reinterpret_cast<const float*>(a.part),
+                    a.splits, a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, a.sx, a.sw, a.Y, a.ldy,
+                    reinterpret_cast<float*>(a.acc_out));
 }
 
 }  // namespace qurl

@@ -84,6 +84,8 @@ struct GemmArgs {
   CodeSums fsums;        // ... and where it writes the code sums (INT8 decode)
   int float_acc;         // fp16 operands that are not integers (the 4-bit variant): every unit in
                          // one fp32 pass, fp32 partials
+  int whole_units;       // CTA-pair prefill kernel: the first whole_units tiles (in its unit order) run
+                         // over all of K as single units, only the rest are split `splits` ways (0: all)
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -189,6 +191,7 @@ struct GemmPlan {
   size_t w16_off;      // fp16 copy of the weight codes [N, K]
   size_t qn_off;       // per-channel sums of code^2 [N]
   size_t scratch_off;  // running sums of chunked units, one region per CTA
+  int whole_units;     // tiles that run unsplit before the split tail (GemmArgs::whole_units)
 };
 
 // gemm_common.cu.  ws_bytes of a plan includes kSyncBytes at the end of the
@@ -232,6 +235,9 @@ cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums 
 // 256-channel tiles, K splits), and the widening of the weight codes with their sums of code^2.
 cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
+// The reduction of a hybrid plan's split tail: the tiles after the first whole_units (in the CTA-pair
+// kernel's unit order) sum their s partials in split order and apply the epilogue (or write acc_out).
+cudaError_t launch_tail_reduce(bool int_partials, const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_widen_weights(const void* Wq, int N, int K, void* w16, unsigned* qn, int num_sms,
                                  cudaStream_t st);
 // the CTAs an i8w launch of this plan runs (one per SM of the resident pairs), for sizing its scratch
