@@ -437,10 +437,14 @@ __global__ void __launch_bounds__(256) widen_weights_kernel(const uint8_t* __res
   if (lane == 0) qn[row] = static_cast<unsigned>(q < 0xFFFFFFFFull ? q : 0xFFFFFFFFull);
 }
 
-// The split tail of a hybrid plan: one CTA per 16 rows of a tail tile, one
-// thread per column; each output is the sum of its `splits` partials in split
-// order (int32: exact in any order; fp32: a fixed order), then the epilogue
-// y = bf16((fp32(sum) * sx[m]) * sw[n]), or the raw sum into acc_out.
+// The split tail of a hybrid plan: one CTA per 4 rows of a tail tile, 64
+// threads a row, 4 adjacent columns a thread (one 16-byte load per split when
+// N is a multiple of 4).  Each output is the sum of its `splits` partials in
+// split order (int32: exact in any order; fp32: a fixed order), then the
+// epilogue y = bf16((fp32(sum) * sx[m]) * sw[n]), or the raw sum into acc_out.
+__device__ __forceinline__ void add_bits(int& s, uint32_t b) { s += static_cast<int>(b); }
+__device__ __forceinline__ void add_bits(float& s, uint32_t b) { s += __uint_as_float(b); }
+
 template <typename T>
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
                                                           int tiles_tok, int tiles_ch, int whole_units,
@@ -449,24 +453,35 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ 
                                                           T* __restrict__ acc_out) {
   griddep_wait();
   griddep_launch_dependents();
-  const int v = whole_units + static_cast<int>(blockIdx.x >> 4);  // the tail tile
+  const int v = whole_units + static_cast<int>(blockIdx.x >> 6);  // the tail tile
   int tok, ch;
   i8w_tile(tiles_tok, tiles_ch, v, tok, ch);
-  const int n = ch * 256 + static_cast<int>(threadIdx.x);
-  if (n >= N) return;
+  const int m = tok * 256 + static_cast<int>(blockIdx.x & 63) * 4 + static_cast<int>(threadIdx.x >> 6);
+  const int n = ch * 256 + static_cast<int>(threadIdx.x & 63) * 4;
+  if (m >= M || n >= N) return;
+  const int nc = min(4, N - n);
   const size_t plane = static_cast<size_t>(M) * N;
-  const float swn = Y ? __ldg(sw + n) : 0.0f;
-  for (int r = 0; r < 16; ++r) {
-    const int m = tok * 256 + static_cast<int>(blockIdx.x & 15) * 16 + r;
-    if (m >= M) break;
-    const size_t at = static_cast<size_t>(m) * N + n;
-    T sum = T(0);
-    for (int z = 0; z < splits; ++z) sum += __ldcg(part + z * plane + at);
-    if (Y)
-      Y[static_cast<size_t>(m) * ldy + n] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(static_cast<float>(sum),
-                                                                                     __ldg(sx + m)), swn));
-    else
-      acc_out[at] = sum;
+  const size_t at = static_cast<size_t>(m) * N + n;
+  T sum[4] = {T(0), T(0), T(0), T(0)};
+  if (nc == 4 && (N & 3) == 0) {
+#pragma unroll 4
+    for (int z = 0; z < splits; ++z) {
+      const uint4 w = __ldcg(reinterpret_cast<const uint4*>(part + z * plane + at));
+      const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) add_bits(sum[c], e[c]);
+    }
+  } else {
+    for (int z = 0; z < splits; ++z)
+      for (int c = 0; c < nc; ++c) sum[c] += __ldcg(part + z * plane + at + c);
+  }
+  if (Y) {
+    const float sxm = __ldg(sx + m);
+    for (int c = 0; c < nc; ++c)
+      Y[static_cast<size_t>(m) * ldy + n + c] =
+          __float2bfloat16_rn(__fmul_rn(__fmul_rn(static_cast<float>(sum[c]), sxm), __ldg(sw + n + c)));
+  } else {
+    for (int c = 0; c < nc; ++c) acc_out[at + c] = sum[c];
   }
 }
 
@@ -534,7 +549,7 @@ cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, co
 cudaError_t launch_tail_reduce(bool int_partials, const GemmArgs& a, cudaStream_t st) {
   const long long tail = static_cast<long long>(a.tiles_tok) * a.tiles_ch - a.whole_units;
   if (tail <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(tail * 16));
+  const dim3 grid(static_cast<unsigned>(tail * 64));
   if (int_partials)
     return launch_pdl(tail_reduce_kernel<int>, grid, dim3(256), 0, st, reinterpret_cast<const int*>(a.part), a.splits,
                       a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, a.sx, a.sw, a.Y, a.ldy,
