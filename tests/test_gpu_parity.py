@@ -174,7 +174,11 @@ def test_rmsnorm_quant(qt, M, K):
 
 
 @pytest.mark.parametrize("qt", QTS)
-@pytest.mark.parametrize("M,I", [(16, 256), (9, 18944), (3, 4096)])
+@pytest.mark.parametrize("M,I", [(16, 256), (9, 18944), (3, 4096),
+                                 # more rows than SMs, rows longer than 16384: the persistent kernel
+                                 # that streams each row into shared memory (one row on most CTAs; six
+                                 # or seven, both row buffers reused; the widest row it takes)
+                                 (153, 16400), (1000, 18944), (300, 27648)])
 def test_silu_mul_quant(qt, M, I):
     GU = synth.activations(f"gpu/silu/{M}/{I}", M, 2 * I, outlier_gain=4.0)
     GU[0, :4] = torch.tensor([0.0, -90.0, 60.0, -3.0])
@@ -619,6 +623,31 @@ def test_fused_rmsnorm_quant_linear(qt):
     qo, so, _, _ = oracle.rmsnorm_quant(bits(X), gfo, oqt(qt), eps=1e-6)
     Yo, _ = oracle.w8a8_linear(qo, so, Wo, swo, oqt(qt), nthreads=NT)
     assert max_abs_rel(oracle.bf16_decode(bits(Y)), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+@pytest.mark.parametrize("qt", QTS)
+def test_silu_stream_linear_matches_separate_calls(qt):
+    """SiLU*mul -> quant -> linear at a streamed row width (I = 27648, 300
+    rows): the fp16 codes and code sums the quantizer leaves for the INT8 GEMM
+    give the bits of the quantizer + linear called apart, and the codes are the
+    oracle's given the kernel's h."""
+    M, N, I = 300, 512, 27648
+    GU = synth.activations(f"gpu/fqs/GU/{M}", M, 2 * I, outlier_gain=4.0)
+    W = synth.weights("gpu/fqs/W", N, I)
+    Wq, sw, _, _ = q.prepare_weights(W.cuda(), qt, s=1.5)
+    cd = q.code_dtype(qt)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    xs = torch.empty((M, I), dtype=cd, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    q.qurl_silu_mul_quant_linear(GU.cuda(), 1.5, Wq, sw, qt, Y, xs, sx, q.workspace(M, N, I, qt))
+    Xq, s2, h = q.silu_mul_quant(GU.cuda(), qt, pre_scale=1.5, want_h=True)
+    R = q.linear(Xq, s2, Wq, sw, qt, q.workspace(M, N, I, qt))
+    sync_ok()
+    assert torch.equal(xs.view(torch.uint8), Xq.view(torch.uint8)) and torch.equal(sx, s2)
+    assert torch.equal(Y.view(torch.int16), R.view(torch.int16))
+    qo, so, _ = oracle.silu_mul_quant(bits(GU), oqt(qt), pre_scale=1.5, h_given=f32(h))
+    np.testing.assert_array_equal(codes(Xq), qo)
+    np.testing.assert_array_equal(f32(s2), so)
 
 
 @pytest.mark.parametrize("qt", QTS)

@@ -530,7 +530,7 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
   DevState* dev = nullptr;
   QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq, sx, h_out, nullptr,
-                                        qurl::CodeSums{},
+                                        qurl::CodeSums{}, dev->status,
                                         reinterpret_cast<cudaStream_t>(stream)));
   return QURL_OK;
 }
@@ -716,8 +716,10 @@ qurl_status qurl_silu_mul_quant_linear(const void* GU, int ldgu, float pre_scale
   if (f.in_gemm)
     return run_fused(f, qurl::kFuseSiluMul, GU, ldgu, nullptr, 0.0f, pre_scale, Wq, sw, M, N, I, qt, Y, ldy,
                      Xq_scratch, sx_scratch, workspace, ws_bytes, st);
+  DevState* dev = nullptr;
+  QURL_TRY(device_state(&dev));
   QURL_CUDA(qurl::launch_silu_mul_quant(GU, M, I, ldgu, pre_scale, qt, Xq_scratch, sx_scratch, nullptr, f.x16,
-                                        f.sums, st));
+                                        f.sums, dev->status, st));
   return run_gemm(Xq_scratch, sx_scratch, Wq, sw, M, N, I, qt, Y, ldy, nullptr, workspace, ws_bytes, st,
                   f.x16 != nullptr, true);
 }

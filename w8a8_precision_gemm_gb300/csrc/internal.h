@@ -152,8 +152,10 @@ cudaError_t launch_quant_act(const void* X, int M, int K, long long ldx, float p
 cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, const float* gamma, float eps,
                                  int qt, void* Xq, float* sx, float* ms_out, void* x16, CodeSums sums,
                                  cudaStream_t st);
+// status: the device status word, where the streaming SiLU kernel latches a
+// timed-out row copy (null: the row kernels, which wait on nothing, only).
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, CodeSums sums, cudaStream_t st);
+                                  float* sx, float* h_out, void* x16, CodeSums sums, int* status, cudaStream_t st);
 cudaError_t launch_prepare_weights(const void* W, bool w_f32, int N, int K, long long ldw, const float* gamma,
                                    float s, int qt, void* Wq, float* sw, float* gamma_folded, float* W_scaled,
                                    cudaStream_t st);

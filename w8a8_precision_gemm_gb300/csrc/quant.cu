@@ -93,6 +93,122 @@ __global__ void __launch_bounds__(1024, 1) silu_mul_quant_1k_kernel(const __nv_b
   rq::silu_mul_quant_row<kVPT / 2>(blockIdx.x, GU, I, ldgu, pre, qt, Xq, sx, h_out, x16, sums, sh);
 }
 
+// Rows of 8192 .. kSiluStreamMaxI positions at more rows than SMs: one
+// persistent CTA of 1024 threads per SM walks rows blockIdx.x + j gridDim.x.
+// Each gate | up row arrives in shared memory by one bulk copy, two rows
+// ahead: while a row is computed, reduced and its codes stored, the next one
+// is already in flight, so the SM keeps reading HBM through the arithmetic,
+// the block reductions and the stores (one resident row kernel per SM leaves
+// HBM idle across each of those phases).  Same arithmetic, in the same order,
+// as the row kernels above.
+constexpr int kSiluStreamNC = 4;  // vectors of h a thread holds: rows of up to 4 x 1024 x 8 positions
+constexpr int kSiluStreamMaxI = 27648;  // two gate | up rows of bf16: 8 I bytes of shared memory
+
+__device__ __forceinline__ void drain_bulk(uint64_t* bar, uint32_t parity, int* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, kDevOk, kDevTimeout);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024, 1) silu_mul_quant_stream_kernel(const __nv_bfloat16* __restrict__ GU, int M,
+                                                                       int I, long long ldgu, float pre, int qt,
+                                                                       uint8_t* __restrict__ Xq, float* __restrict__ sx,
+                                                                       float* __restrict__ h_out,
+                                                                       uint8_t* __restrict__ x16, const CodeSums sums,
+                                                                       int* status) {
+  extern __shared__ __align__(16) uint8_t rows_smem[];  // [2][gate I | up I] bf16
+  __shared__ rq::RowScratch sh;
+  __shared__ uint64_t full[2];
+  __shared__ int stop;
+  const uint32_t row_bytes = 4u * static_cast<uint32_t>(I);
+  const int nvec = I >> 3;
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_barrier_init();
+    stop = 0;
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  int issued[2] = {0, 0};  // copies issued per buffer (thread 0)
+  auto issue = [&](int j) {
+    const int m = blockIdx.x + j * static_cast<int>(gridDim.x);
+    if (m >= M) return;
+    mbar_arrive_expect_tx(&full[j & 1], row_bytes);
+    bulk_load_1d(rows_smem + (j & 1) * row_bytes, GU + static_cast<size_t>(m) * ldgu, row_bytes, &full[j & 1]);
+    ++issued[j & 1];
+  };
+  if (threadIdx.x == 0) {
+    issue(0);
+    issue(1);
+  }
+  const float2 pre2 = rq::splat2(pre);
+  int j = 0;
+  for (;; ++j) {
+    const int m = blockIdx.x + j * static_cast<int>(gridDim.x);
+    if (m >= M) break;
+    if (threadIdx.x == 0 && !mbar_wait(&full[j & 1], (j >> 1) & 1, status)) stop = 1;
+    __syncthreads();  // also: the previous row's sums are written before the counters are reset
+    if (stop) break;
+    rq::sums_begin(sh.cnt, sums);
+    const uint4* g = reinterpret_cast<const uint4*>(rows_smem + (j & 1) * row_bytes);
+    const uint4* u = g + nvec;
+    // pass 1: h = silu(g) * u into registers; the largest |h|
+    float2 hc[kSiluStreamNC][4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kSiluStreamNC; ++c) {
+      const int idx = threadIdx.x + c * 1024;
+      if (idx < nvec) {
+        rq::silu_mul8(g[idx], u[idx], hc[c]);
+        if (h_out) {
+          float4* ho = reinterpret_cast<float4*>(h_out + static_cast<size_t>(m) * I) + 2 * idx;
+          ho[0] = make_float4(hc[c][0].x, hc[c][0].y, hc[c][1].x, hc[c][1].y);
+          ho[1] = make_float4(hc[c][2].x, hc[c][2].y, hc[c][3].x, hc[c][3].y);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(hc[c][e].x), fabsf(hc[c][e].y)));
+      }
+    }
+    amax = block_reduce<true>(rq::scaled_absmax(amax, pre), sh.red);
+    // every thread has read this buffer: the row after next streams into it
+    if (threadIdx.x == 0) {
+      fence_proxy_async_smem();
+      issue(j + 2);
+    }
+    const Enc en = make_enc(amax, qt);
+    if (threadIdx.x == 0) sx[m] = en.scale;
+    uint8_t* out = Xq + static_cast<size_t>(m) * I;
+    uint8_t* out16 = x16 ? x16 + static_cast<size_t>(m) * I * 2 : nullptr;
+    // pass 2: codes (warp-uniform steps: the code sums reduce over the warp)
+#pragma unroll
+    for (int c = 0; c < kSiluStreamNC; ++c) {
+      const int idx = threadIdx.x + c * 1024;
+      int2 v = make_int2(0, 0);
+      if (idx < nvec) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hc[c][e] = rq::mul2(hc[c][e], pre2);
+        v = rq::store8(out, out16, idx, hc[c], en);
+      }
+      rq::sums_add_warp(sh.cnt, sums, idx, v);
+    }
+    rq::sums_end(sh.cnt, sums, m);
+  }
+  if (stop && threadIdx.x == 0) {
+    // a copy timed out (the status is latched): wait, bounded, for the copies
+    // still in flight before the shared memory is released
+    for (int b = 0; b < 2; ++b) {
+      const int consumed = (j + 1 - b) / 2;  // rows 0 .. j - 1 of buffer b (j & 1 == b)
+      if (issued[b] > consumed) drain_bulk(&full[b], (issued[b] - 1) & 1, status);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ weight fold + quant
 
 // Loads 8 consecutive weights of a row as fp32 (bf16 or fp32 storage).
@@ -303,7 +419,7 @@ cudaError_t launch_rmsnorm_quant(const void* X, int M, int K, long long ldx, con
 }
 
 cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, float pre, int qt, void* Xq,
-                                  float* sx, float* h_out, void* x16, CodeSums sums, cudaStream_t st) {
+                                  float* sx, float* h_out, void* x16, CodeSums sums, int* status, cudaStream_t st) {
   if (x16 == nullptr) sums.asum = nullptr;
   // two vectors (gate, up) are cached per position: half as many per thread
   const int t = row_threads(I / 8, M, kVPT / 2);
@@ -311,6 +427,21 @@ cudaError_t launch_silu_mul_quant(const void* GU, int M, int I, long long ldgu, 
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
   const int nvec = I / 8;
+  if (sms > 0 && M > sms && status != nullptr && nvec > kRowThreads * (kVPT / 2) && I <= kSiluStreamMaxI &&
+      dev >= 0 && dev < 64) {
+    static bool attr_done[64] = {};
+    const size_t smem = 8 * static_cast<size_t>(I);
+    if (!attr_done[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(silu_mul_quant_stream_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(8 * kSiluStreamMaxI));
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
+    return launch_pdl(silu_mul_quant_stream_kernel, dim3(sms), dim3(1024), smem, st,
+                      reinterpret_cast<const __nv_bfloat16*>(GU), M, I, ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq),
+                      sx, h_out, reinterpret_cast<uint8_t*>(x16), sums, status);
+  }
   if (sms > 0 && M > sms && nvec > kRowThreads * (kVPT / 2) && nvec <= 1024 * (kVPT / 2))
     return launch_pdl(silu_mul_quant_1k_kernel, dim3(M), dim3(1024), 0, st,
                       reinterpret_cast<const __nv_bfloat16*>(GU), I, ldgu, pre, qt, reinterpret_cast<uint8_t*>(Xq),
