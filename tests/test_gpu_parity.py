@@ -110,6 +110,46 @@ def test_quant_act_fp8_midpoint_quotients():
 
 
 @pytest.mark.parametrize("qt", QTS)
+@pytest.mark.parametrize("M,K,ldx", [(3000, 5120, 7168), (4100, 3584, 3584)])
+def test_quantizers_on_streamed_rows(qt, M, K, ldx):
+    """Prefill-sized batches (thousands of rows, several waves of row CTAs):
+    per-token quant (rows strided as the q slice of a qkv output) and RMSNorm
+    -> quant stay exact against the oracle, and the fp16 codes and code sums
+    they leave for the INT8 GEMM give the bits of the separate quantizer +
+    linear calls."""
+    big = synth.activations(f"gpu/stream/{M}/{K}", M, ldx)
+    X = big[:, :K].contiguous()
+    g = synth.gamma(f"gpu/stream/g/{K}", K) * 1.5
+    Xq, sx = q.quant_act(big.cuda()[:, :K], qt, pre_scale=1.5)
+    Xr, sr, ms = q.rmsnorm_quant(X.cuda(), g.cuda(), qt, eps=1e-6, want_ms=True)
+    sync_ok()
+    qo, so = oracle.quant_act(bits(X), oqt(qt), pre_scale=1.5)
+    np.testing.assert_array_equal(codes(Xq), qo)
+    np.testing.assert_array_equal(f32(sx), so)
+    ms_d = f32(ms)
+    np.testing.assert_allclose(ms_d, oracle.rms_ms(bits(X)), rtol=2e-7)
+    qo, so, _, _ = oracle.rmsnorm_quant(bits(X), g.numpy(), oqt(qt), eps=1e-6, ms_given=ms_d)
+    np.testing.assert_array_equal(codes(Xr), qo)
+    np.testing.assert_array_equal(f32(sr), so)
+    N = 256
+    Wq, sw, gf, _ = q.prepare_weights(synth.weights(f"gpu/stream/W/{K}", N, K).cuda(), qt, s=1.5,
+                                      gamma=synth.gamma(f"gpu/stream/g/{K}", K).cuda())
+    cd = q.code_dtype(qt)
+    Y1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    xs = torch.empty((M, K), dtype=cd, device="cuda")
+    ss = torch.empty(M, dtype=torch.float32, device="cuda")
+    q.qurl_quant_act_linear(big.cuda()[:, :K], 1.5, Wq, sw, qt, Y1, xs, ss, q.workspace(M, N, K, qt))
+    R1 = q.linear(Xq, sx, Wq, sw, qt, q.workspace(M, N, K, qt))
+    q.qurl_rmsnorm_quant_linear(X.cuda(), gf, 1e-6, Wq, sw, qt, Y2, xs, ss, q.workspace(M, N, K, qt))
+    X2, s2 = q.rmsnorm_quant(X.cuda(), gf, qt, eps=1e-6)
+    R2 = q.linear(X2, s2, Wq, sw, qt, q.workspace(M, N, K, qt))
+    sync_ok()
+    assert torch.equal(Y1.view(torch.int16), R1.view(torch.int16))
+    assert torch.equal(Y2.view(torch.int16), R2.view(torch.int16))
+
+
+@pytest.mark.parametrize("qt", QTS)
 def test_quant_act_strided_rows(qt):
     """The o_proj input is a column slice of the qkv output (row stride 4608)."""
     big = synth.activations("gpu/act/strided", 37, 4608)
@@ -623,6 +663,24 @@ def test_fused_rmsnorm_quant_linear(qt):
     qo, so, _, _ = oracle.rmsnorm_quant(bits(X), gfo, oqt(qt), eps=1e-6)
     Yo, _ = oracle.w8a8_linear(qo, so, Wo, swo, oqt(qt), nthreads=NT)
     assert max_abs_rel(oracle.bf16_decode(bits(Y)), oracle.bf16_decode(Yo)) <= 1e-2
+
+
+def test_silu_over_every_bf16_gate():
+    """h = silu(g) * u for every finite bf16 g in [-120, 120] (u = 1 and -3):
+    within the relative 2e-6 the codes are decided on across the whole range of
+    the exponential -- both tails, the reduction's boundaries at every multiple
+    of ln 2 / 2, and the flush to 0 below g = -87.3."""
+    v = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    g = v[torch.isfinite(v) & (v.abs() <= 120)]
+    I = ((g.numel() + 15) // 16) * 16
+    gate = torch.zeros(I)
+    gate[: g.numel()] = g
+    GU = torch.stack([torch.cat([gate, torch.ones(I)]), torch.cat([gate, torch.full((I,), -3.0)])])
+    GU = GU.to(torch.bfloat16)
+    _, _, h = q.silu_mul_quant(GU.cuda(), q.FP8_E4M3, pre_scale=1.0, want_h=True)
+    sync_ok()
+    _, _, ho = oracle.silu_mul_quant(bits(GU), oracle.FP8_E4M3, pre_scale=1.0)
+    np.testing.assert_allclose(f32(h), ho, rtol=2e-6, atol=1e-35)
 
 
 @pytest.mark.parametrize("qt", QTS)
