@@ -559,6 +559,35 @@ def test_gemm_acc_fp8(M, N, K):
     assert float((err / (absref + 1e-30)).max()) < 1e-4
 
 
+@pytest.mark.parametrize("M,N,K", [(1024, 5120, 27648), (1000, 5000, 12288)])
+def test_fp8_pair_whole_units_and_split_tail(M, N, K):
+    """FP8 prefill on CTA pairs with 80 tiles on 76 pairs: 76 tiles run over
+    all of K and write their results themselves, the last 4 (the last channel
+    tile of every token tile; ragged in both at 1000 x 5000) are split 18 and
+    16 ways and reduced by their own kernel.  Raw accumulators (sampled,
+    against the oracle within the fp32 summation bound) and the bf16 linear
+    (bits of the accumulators through the epilogue the oracle applies)."""
+    xq = random_codes(q.FP8_E4M3, (M, K), M * 5 + K)
+    wq = random_codes(q.FP8_E4M3, (N, K), N * 3 + K)
+    ws = q.workspace(M, N, K, q.FP8_E4M3)
+    X, W = to_dev(xq, q.FP8_E4M3), to_dev(wq, q.FP8_E4M3)
+    acc = q.gemm_acc(X, W, q.FP8_E4M3, ws)
+    sx = torch.rand(M, device="cuda") + 0.5
+    sw = torch.rand(N, device="cuda") + 0.5
+    Y = q.linear(X, sx, W, sw, q.FP8_E4M3, ws)
+    sync_ok()
+    g = np.random.Generator(np.random.PCG64(M + N + K))
+    rows = np.unique(np.concatenate([g.choice(M, 24, replace=False), [0, 255, 256, M - 1]]))
+    # columns of whole tiles and of the split tail (the last 256-channel tile)
+    cols = np.unique(np.concatenate([g.choice(N, 96, replace=False), [0, 255, 256, 4863, 4864, N - 1]]))
+    ref = oracle.gemm_fp8(xq[rows], wq[cols], nthreads=NT)
+    absref = oracle.gemm_fp8(xq[rows] & np.uint8(0x7F), wq[cols] & np.uint8(0x7F), nthreads=NT)
+    a = acc.cpu().numpy()[np.ix_(rows, cols)].astype(np.float64)
+    assert np.all(np.abs(a - ref) <= absref * (K * 2.0 ** -23) + 1e-30)
+    Yo = oracle.epilogue(acc.cpu().numpy()[np.ix_(rows, cols)], f32(sx)[rows], f32(sw)[cols])
+    np.testing.assert_array_equal(bits(Y)[np.ix_(rows, cols)], Yo)
+
+
 def _random_shapes(n, seed):
     """Seeded shapes across the decode and prefill ranges: any M and N, K a
     multiple of 16 (the row-stride rule of the codes), some with code

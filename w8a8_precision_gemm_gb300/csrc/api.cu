@@ -324,7 +324,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.qsum = sums.qsum;
   a.qn = p.wide ? qn : nullptr;
   a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
-  a.whole_units = p.wide ? p.whole_units : 0;
+  a.whole_units = p.whole_units;
   if (fq) {
     a.fq = *fq;
     a.fsums = fsums;
@@ -348,7 +348,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
     r.tiles_ch = p.tiles_ch;
     r.splits = p.splits;
     r.part = part;
-    QURL_CUDA(qurl::launch_tail_reduce(int8, r, st));
+    QURL_CUDA(qurl::launch_tail_reduce(int8, !p.wide, r, st));
   } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qt, part, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
                                          dev->num_sms, st));
@@ -419,7 +419,7 @@ qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const v
     r.tiles_ch = p.tiles_ch;
     r.splits = p.splits;
     r.part = wsb + p.x16_bytes;
-    QURL_CUDA(qurl::launch_tail_reduce(false, r, st));
+    QURL_CUDA(qurl::launch_tail_reduce(false, false, r, st));
   } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qurl::kQFp8, wsb + p.x16_bytes, p.splits, M, N, gx, gw, Y, ldy,
                                          Y ? nullptr : acc, dev->num_sms, st));

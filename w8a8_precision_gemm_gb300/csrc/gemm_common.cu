@@ -45,22 +45,21 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, b
   if (tiles < slots) splits = std::max(1, std::min(static_cast<int>(slots / tiles), cap));
   // k-blocks per split for s splits (a multiple of 4: the code sums' granularity)
   auto kps_of = [&](int s) { return ((p.num_kb + s - 1) / s + 3) & ~3; };
+  // Rough time of s splits, as for the other kernels: rounds of units over
+  // the pairs x (k-blocks per unit + pipeline fill and drain) x one 64-deep
+  // k-block of a 256 x 256 unit at the fp16 rate (0.33 us), plus the
+  // reduction (launch, s fp32/int32 partials read, bf16 written).  Taken over
+  // the rule above when predicted 10% faster: shapes whose units fill a last
+  // round of pairs barely.
+  auto est = [&](int s) {
+    const int kps = kps_of(s);
+    const int ns = (p.num_kb + kps - 1) / kps;
+    const double rounds = static_cast<double>((tiles * ns + slots - 1) / slots);
+    double t = rounds * (kps + 9) * 0.33;
+    if (ns > 1) t += 3.0 + (static_cast<double>(ns) * M * N * 4 + static_cast<double>(M) * N * 2) / 4e6;
+    return t;
+  };
   {
-    // Rough time of s splits, as for the other kernels: rounds of units over
-    // the pairs x (k-blocks per unit + pipeline fill and drain) x one 64-deep
-    // k-block of a 256 x 256 unit at the fp16 rate (0.33 us), plus the
-    // reduction (launch, s fp32/int32 partials read, bf16 written).  Taken
-    // over the rule above when predicted 10% faster: shapes whose units fill
-    // a last round of pairs barely (32B down at M = 1024: 80 units on 76
-    // pairs, four splits predicted 220 us against 291).
-    auto est = [&](int s) {
-      const int kps = kps_of(s);
-      const int ns = (p.num_kb + kps - 1) / kps;
-      const double rounds = static_cast<double>((tiles * ns + slots - 1) / slots);
-      double t = rounds * (kps + 9) * 0.33;
-      if (ns > 1) t += 3.0 + (static_cast<double>(ns) * M * N * 4 + static_cast<double>(M) * N * 2) / 4e6;
-      return t;
-    };
     const double t_rule = est(splits);
     int best = splits;
     double t_best = t_rule;
@@ -76,21 +75,25 @@ bool plan_wide(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, b
   // Hybrid: when whole-K units would leave a last round of pairs mostly idle
   // (tiles a little above a multiple of the pairs), the tiles of that last
   // round alone are split so that their pieces fill it, and a reduction kernel
-  // finishes only them (32B o_proj at M = 1024: 80 tiles on 76 pairs, 76 whole
-  // + 4 split five ways: 1.2 unit-times instead of 2).
+  // finishes only them.  Taken over the plan above when the model says it
+  // saves 3% and 8 us (below that the first round's start-up, which the model
+  // leaves out, ate the gain: 32B qkv at M = 1024, predicted 4 us faster,
+  // measured 1 us slower).  Measured: 32B o_proj at M = 1024, 76 whole + 4
+  // tiles split five ways, 60.6 us a call against 64.9; 32B down at M = 8192,
+  // 608 whole + 32 split two ways, 1169 us against 1212.
   int whole = 0;
-  if (splits == 1 && tiles > slots && tiles % slots != 0) {
+  if (tiles > slots && tiles % slots != 0) {
+    const double t_cur = est(splits);
     const long long rem = tiles % slots;
     const int st = std::min(static_cast<int>(slots / rem), cap);
     if (st >= 2) {
       const int kps_t = kps_of(st);
       const int ns = (p.num_kb + kps_t - 1) / kps_t;
       const double unit = (p.num_kb + 9) * 0.33;
-      const double t_plain = static_cast<double>((tiles + slots - 1) / slots) * unit;
       const double t_hyb = static_cast<double>(tiles / slots) * unit +
                            static_cast<double>((rem * ns + slots - 1) / slots) * (kps_t + 9) * 0.33 + 3.0 +
                            static_cast<double>(rem) * 65536.0 * (4.0 * ns + 2.0) / 4e6;
-      if (t_hyb < 0.9 * t_plain) {
+      if (t_hyb < 0.97 * t_cur && t_cur - t_hyb > 8.0) {
         whole = static_cast<int>(tiles - rem);
         splits = ns;
       }
@@ -244,6 +247,30 @@ GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail) 
       }
     }
     if (t_best < 0.9 * t_rule) splits = best;
+    // FP8 prefill on CTA pairs: whole-K units plus a split tail, as for the
+    // INT8 prefill kernel, when the last round of pair units would be mostly
+    // idle and the model saves 3% and 15 us (32B down at M = 1024: 80 tiles on
+    // 76 pairs, 76 whole + 4 split 18 ways, 93 us a call against 124 with K
+    // split four ways; 32B o_proj at M = 1024, predicted 10 us faster, measured
+    // 3 us slower: the few units of a last round run faster alone than the
+    // model's shared rate says, more so for short K)
+    if (!int8 && p.pair && !p.swap && tiles > slots && tiles % slots != 0) {
+      const double t_cur = est(splits);
+      const long long rem = tiles % slots;
+      const int st = std::min(static_cast<int>(slots / rem), cap);
+      if (st >= 2) {
+        const int kps_t = (p.num_kb + st - 1) / st;
+        const int ns = (p.num_kb + kps_t - 1) / kps_t;
+        const double unit = (p.num_kb + fill) * stage_us;
+        const double t_hyb = static_cast<double>(tiles / slots) * unit +
+                             static_cast<double>((rem * ns + slots - 1) / slots) * (kps_t + fill) * stage_us + 3.0 +
+                             static_cast<double>(rem) * 65536.0 * (4.0 * ns + 2.0) / 4e6;
+        if (t_hyb < 0.97 * t_cur && t_cur - t_hyb > 15.0) {
+          p.whole_units = static_cast<int>(tiles - rem);
+          splits = ns;
+        }
+      }
+    }
   }
   const size_t per_split = static_cast<size_t>(M) * N * 4;
   // workspace for s splits: [fp16 codes, code sums (INT8 decode)][s partials if s > 1]
@@ -251,6 +278,7 @@ GemmPlan plan_narrow(int M, int N, int K, int qt, int num_sms, size_t ws_avail) 
     return (p.tmem_a ? x16 + sums(s) + scratch : 0) + (s > 1 ? static_cast<size_t>(s) * per_split : 0);
   };
   while (splits > 1 && need(splits) > ws_avail) --splits;
+  if (splits == 1) p.whole_units = 0;
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.x16_bytes = p.tmem_a ? x16 + sums(p.splits) + scratch : 0;

@@ -56,22 +56,33 @@ struct Fp8PairBarriers {
 // This CTA's part of unit u: A rows a0 .. a0 + 127 (rank r takes the r-th
 // half of the pair's 256), B columns b0 .. b0 + BN - 1 of the output, of which
 // it stages rows b0 + r BN / 2 ...  Prefill: A = tokens, B = channels;
-// SWAP: A = channels, B = tokens.  Units are numbered token tile fastest.
+// SWAP: A = channels, B = tokens.  Tiles are numbered token tile fastest; the
+// first whole_units units (prefill only) are tiles 0 .. whole_units - 1 over
+// all of K (split -1), the remaining tiles are split `splits` ways, split
+// slowest (with whole_units = 0 every tile is split).
 struct PairUnit {
   int a0, b0, kb0, nkb, split;
 };
 
 template <bool SWAP, int BN>
 __device__ __forceinline__ PairUnit pair_unit(const GemmArgs& a, int u, uint32_t rank) {
-  const int tok = u % a.tiles_tok;
-  const int rest = u / a.tiles_tok;
-  const int ch = rest % a.tiles_ch;
-  const int sp = rest / a.tiles_ch;
+  int v, sp;
+  if (u < a.whole_units) {
+    v = u;
+    sp = -1;
+  } else {
+    const int tail = a.tiles_tok * a.tiles_ch - a.whole_units;
+    const int w = u - a.whole_units;
+    sp = w / tail;
+    v = a.whole_units + (w - sp * tail);
+  }
+  const int tok = v % a.tiles_tok;
+  const int ch = v / a.tiles_tok;
   PairUnit w;
   w.a0 = (SWAP ? ch : tok) * 256 + static_cast<int>(rank) * 128;
   w.b0 = (SWAP ? tok : ch) * BN;
-  w.kb0 = sp * a.kb_per_split;
-  w.nkb = min(a.num_kb - w.kb0, a.kb_per_split);
+  w.kb0 = sp < 0 ? 0 : sp * a.kb_per_split;
+  w.nkb = sp < 0 ? a.num_kb : min(a.num_kb - w.kb0, a.kb_per_split);
   w.split = sp;
   return w;
 }
@@ -92,7 +103,8 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t rank = cluster_ctarank();
   // the two CTAs of a cluster walk the same units
   const int u_begin = static_cast<int>(blockIdx.x >> 1), u_stride = static_cast<int>(gridDim.x >> 1);
-  const int u_end = args.tiles_tok * args.tiles_ch * args.splits;
+  const int tiles = args.tiles_tok * args.tiles_ch;
+  const int u_end = args.whole_units + (tiles - args.whole_units) * args.splits;  // as the launch counts them
   int* status = args.status;
 
   if (threadIdx.x == 0) {
@@ -255,10 +267,15 @@ __global__ void __launch_bounds__(192, 1)
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
-        if constexpr (SWAP)
+        if constexpr (SWAP) {
           emit32_swap<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
-        else
-          emit32<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v);
+        } else {
+          // a whole-K unit of a call with a split tail writes its result itself:
+          // scaled to Y, or as raw sums straight into the accumulator output
+          const bool whole = w.split < 0;
+          emit32<BN, float>(args, whole ? (args.Y ? kModeBf16 : kModeAcc) : emode, w.a0, w.b0, whole ? 0 : w.split,
+                            i, c0, v, (whole && !args.Y) ? args.acc_out : nullptr);
+        }
         sx_lane = sx_next;
       }
       tc_fence_before();
@@ -317,7 +334,8 @@ cudaError_t launch_pair_inst(const CUtensorMap& ta, const CUtensorMap& tb, const
   args.tiles_tok = grid.x;
   args.tiles_ch = grid.y;
   args.splits = grid.z;
-  const long long units = static_cast<long long>(args.tiles_tok) * args.tiles_ch * args.splits;
+  const long long tiles = static_cast<long long>(args.tiles_tok) * args.tiles_ch;
+  const long long units = args.whole_units + (tiles - args.whole_units) * args.splits;
   const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(units, max_pairs[dev])));
   return launch_pdl_pair(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(C::NUM_THREADS), C::SMEM_BYTES, stream,
                          ta, tb, args);

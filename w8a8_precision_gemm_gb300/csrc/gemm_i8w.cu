@@ -448,14 +448,20 @@ __device__ __forceinline__ void add_bits(float& s, uint32_t b) { s += __uint_as_
 template <typename T>
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
                                                           int tiles_tok, int tiles_ch, int whole_units,
-                                                          const float* __restrict__ sx, const float* __restrict__ sw,
+                                                          bool tok_fastest, const float* __restrict__ sx,
+                                                          const float* __restrict__ sw,
                                                           __nv_bfloat16* __restrict__ Y, long long ldy,
                                                           T* __restrict__ acc_out) {
   griddep_wait();
   griddep_launch_dependents();
   const int v = whole_units + static_cast<int>(blockIdx.x >> 6);  // the tail tile
   int tok, ch;
-  i8w_tile(tiles_tok, tiles_ch, v, tok, ch);
+  if (tok_fastest) {
+    tok = v % tiles_tok;
+    ch = v / tiles_tok;
+  } else {
+    i8w_tile(tiles_tok, tiles_ch, v, tok, ch);
+  }
   const int m = tok * 256 + static_cast<int>(blockIdx.x & 63) * 4 + static_cast<int>(threadIdx.x >> 6);
   const int n = ch * 256 + static_cast<int>(threadIdx.x & 63) * 4;
   if (m >= M || n >= N) return;
@@ -546,16 +552,16 @@ cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, co
                          tx16, tw16, args);
 }
 
-cudaError_t launch_tail_reduce(bool int_partials, const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_tail_reduce(bool int_partials, bool tok_fastest, const GemmArgs& a, cudaStream_t st) {
   const long long tail = static_cast<long long>(a.tiles_tok) * a.tiles_ch - a.whole_units;
   if (tail <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(tail * 64));
   if (int_partials)
     return launch_pdl(tail_reduce_kernel<int>, grid, dim3(256), 0, st, reinterpret_cast<const int*>(a.part), a.splits,
-                      a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, a.sx, a.sw, a.Y, a.ldy,
+                      a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_fastest, a.sx, a.sw, a.Y, a.ldy,
                       reinterpret_cast<int*>(a.acc_out));
   return launch_pdl(tail_reduce_kernel<float>, grid, dim3(256), 0, st, reinterpret_cast<const float*>(a.part),
-                    a.splits, a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, a.sx, a.sw, a.Y, a.ldy,
+                    a.splits, a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_fastest, a.sx, a.sw, a.Y, a.ldy,
                     reinterpret_cast<float*>(a.acc_out));
 }
 

@@ -84,7 +84,7 @@ struct GemmArgs {
   CodeSums fsums;        // ... and where it writes the code sums (INT8 decode)
   int float_acc;         // fp16 operands that are not integers (the 4-bit variant): every unit in
                          // one fp32 pass, fp32 partials
-  int whole_units;       // CTA-pair prefill kernel: the first whole_units tiles (in its unit order) run
+  int whole_units;       // CTA-pair prefill kernels: the first whole_units tiles (in their unit order) run
                          // over all of K as single units, only the rest are split `splits` ways (0: all)
 };
 
@@ -238,8 +238,9 @@ cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums 
 cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
 // The reduction of a hybrid plan's split tail: the tiles after the first whole_units (in the CTA-pair
-// kernel's unit order) sum their s partials in split order and apply the epilogue (or write acc_out).
-cudaError_t launch_tail_reduce(bool int_partials, const GemmArgs& a, cudaStream_t st);
+// kernel's tile order: the INT8 prefill kernel's token groups, or token tile fastest for the FP8 pair
+// kernel) sum their s partials in split order and apply the epilogue (or write acc_out).
+cudaError_t launch_tail_reduce(bool int_partials, bool tok_fastest, const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_widen_weights(const void* Wq, int N, int K, void* w16, unsigned* qn, int num_sms,
                                  cudaStream_t st);
 // the CTAs an i8w launch of this plan runs (one per SM of the resident pairs), for sizing its scratch
