@@ -48,7 +48,7 @@ struct I8wCfg {
   static constexpr int BK = 64;              // k per k-block: 128 bytes of fp16 per row
   static constexpr int A_STAGE = BM * 128;   // 16 KB
   static constexpr int B_STAGE = BNH * 128;  // 16 KB
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = 7;
   static constexpr int PAIR_TX = 2 * (A_STAGE + B_STAGE);  // bytes rank 0's barrier counts per stage
   static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024;
   static constexpr int NUM_THREADS = 352;    // producer, MMA, mode, 8 epilogue warps
