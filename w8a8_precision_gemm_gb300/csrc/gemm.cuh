@@ -370,6 +370,41 @@ __device__ __forceinline__ void emit32(const GemmArgs& a, int mode, int a0, int 
   }
 }
 
+// The dequantizing write of 32 columns of one tile row whose scales are
+// already in registers (loaded while the accumulator filled): sxm = sx[m],
+// sw_lane = sw[n0 + lane] (0 past N).  The same products in the same order as
+// emit32's; every lane of the warp calls it (the channel scales are shuffled).
+template <typename T>
+__device__ __forceinline__ void emit32_prescaled(const GemmArgs& a, int m, int n0, const T (&v)[32], float sxm,
+                                                 float sw_lane) {
+  const bool row = m < a.M;
+  const int nvalid = min(32, a.N - n0);
+  __nv_bfloat16* dst = a.Y + static_cast<size_t>(row ? m : 0) * a.ldy + n0;
+  if (nvalid == 32) {
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float s0 = __shfl_sync(0xFFFFFFFFu, sw_lane, j), s1 = __shfl_sync(0xFFFFFFFFu, sw_lane, j + 1);
+      const float y0 = __fmul_rn(__fmul_rn(static_cast<float>(v[j]), sxm), s0);
+      const float y1 = __fmul_rn(__fmul_rn(static_cast<float>(v[j + 1]), sxm), s1);
+      __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
+      packed[j / 2] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    if (row) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4*>(dst)[q] =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float sj = __shfl_sync(0xFFFFFFFFu, sw_lane, j);
+      if (row && j < nvalid) dst[j] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(static_cast<float>(v[j]), sxm), sj));
+    }
+  }
+}
+
 template <int QT, bool SWAP, int BN, int STAGES>
 __global__ void __launch_bounds__(GemmCfg<QT, SWAP, BN, STAGES>::NUM_THREADS, 1)
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

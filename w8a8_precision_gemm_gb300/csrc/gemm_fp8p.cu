@@ -256,12 +256,22 @@ __global__ void __launch_bounds__(192, 1)
       // 32-token block, loaded while the accumulator is being filled
       const float sw_lane = SWAP ? channel_scale(args, emode, w.a0 + i) : 0.0f;
       const float sx_first = SWAP ? token_scale(args, emode, w.b0 + lane) : 0.0f;
+      // prefill: the unit's mode, and for the dequantizing epilogue this lane's
+      // token scale and its channel's scale in the first 32-column group,
+      // loaded while the accumulator fills
+      const bool whole = !SWAP && w.split < 0;
+      const int umode = whole ? (args.Y ? kModeBf16 : kModeAcc) : emode;
+      const float sxm = (!SWAP && umode == kModeBf16 && w.a0 + i < args.M) ? __ldg(args.sx + w.a0 + i) : 0.0f;
+      float swc = (!SWAP && umode == kModeBf16) ? channel_scale(args, kModeBf16, w.b0 + lane) : 0.0f;
       if (!warp_wait(&bars.pfull[buf], (cg >> 1) & 1, status)) break;
       tc_fence_after();
       float sx_lane = sx_first;
 #pragma unroll 1
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         const float sx_next = (SWAP && c0 + 32 < C::BN) ? token_scale(args, emode, w.b0 + c0 + 32 + lane) : 0.0f;
+        const float sw_next =
+            (!SWAP && umode == kModeBf16 && c0 + 32 < C::BN) ? channel_scale(args, kModeBf16, w.b0 + c0 + 32 + lane)
+                                                              : 0.0f;
         uint32_t p[32];
         tmem_ld32(lane_base + buf * C::BN + c0, p);
         float v[32];
@@ -269,14 +279,16 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
         if constexpr (SWAP) {
           emit32_swap<BN, float>(args, emode, w.a0, w.b0, w.split, i, c0, v, sx_lane, sw_lane);
+        } else if (umode == kModeBf16) {
+          emit32_prescaled<float>(args, w.a0 + i, w.b0 + c0, v, sxm, swc);
         } else {
-          // a whole-K unit of a call with a split tail writes its result itself:
-          // scaled to Y, or as raw sums straight into the accumulator output
-          const bool whole = w.split < 0;
-          emit32<BN, float>(args, whole ? (args.Y ? kModeBf16 : kModeAcc) : emode, w.a0, w.b0, whole ? 0 : w.split,
-                            i, c0, v, (whole && !args.Y) ? args.acc_out : nullptr);
+          // a whole-K unit of a call with a split tail writes its raw sums
+          // straight into the accumulator output
+          emit32<BN, float>(args, umode, w.a0, w.b0, whole ? 0 : w.split, i, c0, v,
+                            (whole && !args.Y) ? args.acc_out : nullptr);
         }
         sx_lane = sx_next;
+        swc = sw_next;
       }
       tc_fence_before();
       __syncwarp();

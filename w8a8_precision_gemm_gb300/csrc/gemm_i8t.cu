@@ -331,9 +331,11 @@ __global__ void __launch_bounds__(512, 1)
         const int t = u % args.tiles_tok;
         const int sp = u / (args.tiles_tok * args.tiles_ch);
         int mx = 0;
-        for (int c = lane; c < BN; c += 32) {
-          const int m = t * BN + c;
-          if (m < args.M) mx = max(mx, __ldcg(args.asum + static_cast<size_t>(m) * args.splits + sp));
+#pragma unroll  // the tile's loads all in flight before the first is used
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          const int m = t * BN + c0 + lane;
+          if (c0 + lane < BN && m < args.M)
+            mx = max(mx, __ldcg(args.asum + static_cast<size_t>(m) * args.splits + sp));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
         if (lane == 0) {
@@ -774,9 +776,11 @@ __global__ void __launch_bounds__(512, 1)
         const int t = u % args.tiles_tok;
         const int sp = u / (args.tiles_tok * args.tiles_ch);
         int mx = 0;
-        for (int c = lane; c < C::BN; c += 32) {
-          const int m = t * C::BN + c;
-          if (m < args.M) mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
+#pragma unroll  // the tile's loads all in flight before the first is used
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          const int m = t * C::BN + c0 + lane;
+          if (c0 + lane < C::BN && m < args.M)
+            mx = max(mx, __ldg(args.asum + static_cast<size_t>(m) * args.splits + sp));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
         if (lane == 0) {

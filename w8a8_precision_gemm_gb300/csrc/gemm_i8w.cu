@@ -280,22 +280,49 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
         // a whole-K unit's sums are those of all the split ranges added (exact
         // integers; a capped range makes the total exceed the bounds either way)
         const int s0 = sp < 0 ? 0 : sp, s1 = sp < 0 ? args.splits : sp + 1;
+        // eight token rows and eight channels a lane
         unsigned long long smax = 0, qmax = 0;
         unsigned nmax = 0;
-        for (int c = lane; c < 256; c += 32) {
-          const int m = t * 256 + c;
-          if (m < args.M) {
-            unsigned long long sa = 0, qa = 0;
-            for (int k = s0; k < s1; ++k) {
-              const size_t at = static_cast<size_t>(m) * args.splits + k;
-              sa += static_cast<unsigned long long>(__ldg(args.asum + at));
-              if (args.qsum) qa += __ldg(args.qsum + at);
-            }
-            smax = max(smax, sa);
-            qmax = max(qmax, qa);
+        if (s1 - s0 == 1) {
+          // one split range (every unit of an unsplit call): all sixteen or
+          // twenty-four loads are issued before any is used, so the first
+          // unit's mode, which the MMA waits for, costs one load latency
+          unsigned long long sa[8], qa[8];
+          unsigned nq[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int m = t * 256 + lane + 32 * r;
+            const int n = ch * 256 + lane + 32 * r;
+            const size_t at = static_cast<size_t>(m) * args.splits + s0;
+            sa[r] = m < args.M ? static_cast<unsigned long long>(__ldg(args.asum + at)) : 0ull;
+            qa[r] = (args.qsum && m < args.M) ? __ldg(args.qsum + at) : 0ull;
+            nq[r] = (args.qn && n < args.N) ? __ldg(args.qn + n) : 0u;
           }
-          const int n = ch * 256 + c;
-          if (args.qn && n < args.N) nmax = max(nmax, __ldg(args.qn + n));
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            smax = max(smax, sa[r]);
+            qmax = max(qmax, qa[r]);
+            nmax = max(nmax, nq[r]);
+          }
+        } else {
+          // a whole-K unit of a call with a split tail: its row sums add all
+          // the split ranges, row by row (batching four ranges of the eight
+          // rows measured slower at eighteen ranges: 32B down, M = 1024)
+          for (int c = lane; c < 256; c += 32) {
+            const int m = t * 256 + c;
+            if (m < args.M) {
+              unsigned long long sa = 0, qa = 0;
+              for (int k = s0; k < s1; ++k) {
+                const size_t at = static_cast<size_t>(m) * args.splits + k;
+                sa += static_cast<unsigned long long>(__ldg(args.asum + at));
+                if (args.qsum) qa += __ldg(args.qsum + at);
+              }
+              smax = max(smax, sa);
+              qmax = max(qmax, qa);
+            }
+            const int n = ch * 256 + c;
+            if (args.qn && n < args.N) nmax = max(nmax, __ldg(args.qn + n));
+          }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -341,6 +368,19 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
       const int esplit = whole ? 0 : w.split;
       void* ebase = (whole && !args.Y) ? args.acc_out : nullptr;
       const int np = passes(j, w.nkb);
+      // the dequantizing epilogue's scales, loaded while the accumulator fills:
+      // this lane's token row and its channel in each of the warp's 32-column
+      // groups
+      float sxm = 0.0f, swr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (emode == kModeBf16) {
+        const int m = w.a0 + i;
+        sxm = m < args.M ? __ldg(args.sx + m) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int n = w.b0 + cbeg + 32 * k + lane;
+          swr[k] = n < args.N ? __ldg(args.sw + n) : 0.0f;
+        }
+      }
       for (int p = 0; p < np; ++p) {
         const int b = nextbuf;
         nextbuf ^= 1;
@@ -369,7 +409,13 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
             float f[32];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(r[jj]);
-            emit32<C::BN, float>(args, emode, w.a0, w.b0, esplit, i, c0, f, ebase);
+            if (emode == kModeBf16) {
+              const int k = (c0 - cbeg) >> 5;
+              const float swk = k == 0 ? swr[0] : (k == 1 ? swr[1] : (k == 2 ? swr[2] : swr[3]));
+              emit32_prescaled<float>(args, w.a0 + i, w.b0 + c0, f, sxm, swk);
+            } else {
+              emit32<C::BN, float>(args, emode, w.a0, w.b0, esplit, i, c0, f, ebase);
+            }
             continue;
           }
           int v[32];
@@ -386,7 +432,13 @@ __global__ void __launch_bounds__(I8wCfg::NUM_THREADS, 1)
               continue;
             }
           }
-          emit32<C::BN, int>(args, emode, w.a0, w.b0, esplit, i, c0, v, ebase);
+          if (emode == kModeBf16) {
+            const int k = (c0 - cbeg) >> 5;
+            const float swk = k == 0 ? swr[0] : (k == 1 ? swr[1] : (k == 2 ? swr[2] : swr[3]));
+            emit32_prescaled<int>(args, w.a0 + i, w.b0 + c0, v, sxm, swk);
+          } else {
+            emit32<C::BN, int>(args, emode, w.a0, w.b0, esplit, i, c0, v, ebase);
+          }
         }
         tc_fence_before();
         __syncwarp();
