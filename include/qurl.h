@@ -488,6 +488,16 @@ qurl_status qurl_set_fused_decode(int on, int* previous);
  * for a null `out`, a non-positive size or SM count, or an unknown qt. */
 qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, long long* out);
 
+/* The same window with the plan's schedule of units and, with `attached`
+ * nonzero, the INT8 plan a call takes when the weights carry an fp16 copy
+ * (qurl_widen_weights).  out[0..7] as qurl_debug_plan; out[8]: whole-K units
+ * -- with K splits > 1, the first out[8] tiles (in the kernel's unit order)
+ * run over all of K and write their own results, and only the remaining
+ * tiles are split out[5] ways and reduced (0: every tile is split, or none
+ * when out[5] = 1).  Host-side only; errors as qurl_debug_plan. */
+qurl_status qurl_debug_plan_ex(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, int attached,
+                               long long* out);
+
 /* Tensor-rate probe (not a computation of the method: it measures the
  * denominators of the roofline).  Launches, asynchronously on `stream`, a
  * kernel that issues `iters` multiply-accumulate instructions of one kind on

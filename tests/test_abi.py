@@ -185,6 +185,46 @@ def test_plan_routing_and_coverage(M, N, K, qt, kernel):
     assert (p["splits"] - 1) * p["kb_per_split"] < num_kb <= p["splits"] * p["kb_per_split"]
 
 
+def _check_schedule(p, K, qt, slots):
+    """A plan's units cover every tile's K range once: all tiles split, or the
+    first whole_units whole (full rounds of SM pairs) and the rest split."""
+    tiles = p["tiles_tok"] * p["tiles_ch"]
+    bk = 64 if (qt == 0 and p["kernel"] == 4) else (256 if p["kernel"] in (1, 2) else (64 if qt == 0 else 128))
+    num_kb = -(-K // bk)
+    assert (p["splits"] - 1) * p["kb_per_split"] < num_kb <= p["splits"] * p["kb_per_split"]
+    w = p["whole_units"]
+    if w:
+        assert p["kernel"] in (3, 4) and not p["swap"] and p["splits"] >= 2
+        assert 0 < w < tiles and w % slots == 0
+        assert tiles - w < slots  # the split tail is the last round's tiles alone
+        units = w + (tiles - w) * p["splits"]
+        assert units > tiles
+
+
+@pytest.mark.parametrize("qt", [0, 1])
+@pytest.mark.parametrize("attached", [False, True])
+def test_plan_split_tails_cover_every_tile(L, qt, attached):
+    """Over a sweep of prefill shapes and SM counts, every plan with a split
+    tail keeps whole rounds of whole-K units and covers K once per tile; and the
+    32B-class projections take the schedules measured fastest on 152 SMs."""
+    import w8a8_precision_gemm_gb300 as q
+
+    for sms in (132, 148, 152, 160):
+        for M in (300, 777, 1024, 2048, 4096, 8192):
+            for N, K in ((7168, 5120), (5120, 5120), (55296, 5120), (5120, 27648), (3584, 18944), (5000, 12288)):
+                _check_schedule(q.plan(M, N, K, qt, sms, attached=attached), K, qt, sms // 2)
+    if attached and qt == 0:  # INT8 with persistent fp16 weight copies, as the benchmark's layers keep them
+        expect = {(1024, 5120, 5120): 76, (1024, 7168, 5120): 0, (1024, 5120, 27648): 76, (8192, 5120, 27648): 608,
+                  (8192, 55296, 5120): 0}
+    elif qt == 1:
+        expect = {(1024, 5120, 5120): 0, (1024, 5120, 27648): 76, (8192, 5120, 27648): 608, (8192, 55296, 5120): 0}
+    else:
+        expect = {}
+    for (M, N, K), w in expect.items():
+        p = q.plan(M, N, K, qt, 152, attached=attached)
+        assert p["whole_units"] == w, ((M, N, K), p)
+
+
 def test_plan_workspace_and_fallbacks(L):
     import ctypes
     import w8a8_precision_gemm_gb300 as q
@@ -217,3 +257,5 @@ def test_plan_workspace_and_fallbacks(L):
     assert L.qurl_debug_plan(64, 4608, 3584, 0, 0, 0, out) == 1
     assert L.qurl_debug_plan(64, 4608, 3584, 7, 152, 0, out) == 1
     assert L.qurl_debug_plan(64, 4608, 3584, 0, 152, 0, None) == 1
+    assert L.qurl_debug_plan_ex(64, 4608, 3584, 0, 0, 0, 1, out) == 1
+    assert L.qurl_debug_plan_ex(64, 4608, 3584, 0, 152, 0, 0, None) == 1

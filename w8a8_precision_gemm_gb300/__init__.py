@@ -90,6 +90,7 @@ def load() -> ctypes.CDLL:
             "qurl_nvfp4_linear": [P, P, P, P, P, P, i, i, i, P, i, P, z, P],
             "qurl_nvfp4_gemm_acc": [P, P, P, P, i, i, i, P, P, z, P],
             "qurl_debug_plan": [i, i, i, i, i, z, P],
+            "qurl_debug_plan_ex": [i, i, i, i, i, z, i, P],
             "qurl_debug_mma_probe": [i, i, i, P, P],
             "qurl_acr_objective": [P, P, P, P, P, ctypes.c_longlong, f, f, i, P, P, P, P, z, P],
             "qurl_kv_cache_quant": [P, i, i, i, i, i, P, ctypes.c_longlong, P, P, P, P, P],
@@ -298,12 +299,14 @@ def qurl_check_device_status(stream=None):
     _ok(load().qurl_check_device_status(_stream(stream)), "qurl_check_device_status")
 
 
-def plan(M, N, K, qt, num_sms, ws_bytes=None):
-    """The GEMM plan for a shape (host-side; see qurl_debug_plan)."""
-    out = (ctypes.c_longlong * 8)()
+def plan(M, N, K, qt, num_sms, ws_bytes=None, attached=False):
+    """The GEMM plan for a shape (host-side; see qurl_debug_plan_ex): with
+    `attached`, the INT8 plan of weights that carry an fp16 copy;
+    "whole_units" counts the tiles that run unsplit before a split tail."""
+    out = (ctypes.c_longlong * 9)()
     ws = ctypes.c_size_t(-1).value if ws_bytes is None else ws_bytes
-    _ok(load().qurl_debug_plan(M, N, K, qt, num_sms, ws, out), "qurl_debug_plan")
-    keys = ("kernel", "swap", "bn", "tiles_tok", "tiles_ch", "splits", "kb_per_split", "ws_bytes")
+    _ok(load().qurl_debug_plan_ex(M, N, K, qt, num_sms, ws, 1 if attached else 0, out), "qurl_debug_plan_ex")
+    keys = ("kernel", "swap", "bn", "tiles_tok", "tiles_ch", "splits", "kb_per_split", "ws_bytes", "whole_units")
     return dict(zip(keys, list(out)))
 
 

@@ -561,6 +561,25 @@ qurl_status qurl_debug_plan(int M, int N, int K, qurl_qtype qt, int num_sms, siz
   return QURL_OK;
 }
 
+qurl_status qurl_debug_plan_ex(int M, int N, int K, qurl_qtype qt, int num_sms, size_t ws_bytes, int attached,
+                               long long* out) {
+  if (!out || !valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt) || num_sms <= 0)
+    return QURL_ERR_INVALID_ARG;
+  qurl::GemmPlan p{};
+  if (!(attached && qt == QURL_INT8 && qurl::plan_attached(p, M, N, K, num_sms, ws_bytes)))
+    p = qurl::plan_gemm(M, N, K, qt, num_sms, ws_bytes);
+  out[0] = p.wide ? 4 : p.tmem_a ? (p.pair ? 2 : 1) : (p.pair ? 3 : 0);
+  out[1] = p.swap ? 1 : 0;
+  out[2] = p.bn;
+  out[3] = p.tiles_tok;
+  out[4] = p.tiles_ch;
+  out[5] = p.splits;
+  out[6] = p.kb_per_split;
+  out[7] = static_cast<long long>(p.ws_bytes);
+  out[8] = p.whole_units;
+  return QURL_OK;
+}
+
 size_t qurl_workspace_size(int M, int N, int K, qurl_qtype qt) {
   if (!valid_dim(M) || !valid_dim(N) || !valid_dim(K) || !valid_qt(qt)) return 0;
   int sms = 0;
