@@ -230,14 +230,15 @@ def test_plan_workspace_and_fallbacks(L):
     import w8a8_precision_gemm_gb300 as q
 
     # the plan's workspace is what qurl_workspace_size reports (160 SMs without a device) -- for INT8
-    # above 256 tokens at least that, and enough for the CTA-pair plan of weights with an attached
-    # fp16 copy: the activations' fp16 copy, one 256 x 128 int32 region per SM, the counters
-    for M, N, K, qt in ((64, 4608, 3584, 0), (256, 37888, 3584, 0), (64, 3584, 18944, 1), (4096, 3584, 3584, 0),
+    # above 256 tokens (and from 129 tokens for weights of 2^26 codes or more) at least that, and enough
+    # for the CTA-pair plan of weights with an attached fp16 copy: the activations' fp16 copy, one
+    # 256 x 128 int32 region per SM, the counters
+    for M, N, K, qt in ((64, 4608, 3584, 0), (256, 4608, 3584, 0), (64, 3584, 18944, 1), (4096, 3584, 3584, 0),
                         (256, 4608, 3584, 1)):
         assert q.plan(M, N, K, qt, 160)["ws_bytes"] == L.qurl_workspace_size(M, N, K, qt)
-    for M, N, K in ((512, 37888, 3584), (1024, 7168, 5120)):
+    for M, N, K in ((512, 37888, 3584), (1024, 7168, 5120), (256, 37888, 3584)):
         ws = L.qurl_workspace_size(M, N, K, 0)
-        assert ws >= q.plan(M, N, K, 0, 160)["ws_bytes"]
+        assert ws == max(q.plan(M, N, K, 0, 160)["ws_bytes"], q.plan(M, N, K, 0, 160, attached=True)["ws_bytes"])
         assert ws >= M * K * 2 + 160 * 256 * 128 * 4 + 256
     # no workspace: INT8 widens both operands in shared memory and K is not split
     p = q.plan(64, 4608, 3584, 0, 152, ws_bytes=0)

@@ -219,15 +219,19 @@ def test_attached_wide_weights_bit_identical_and_refreshed():
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 4608, 3584), (264, 3584, 18944), (1024, 7168, 5120), (1024, 5120, 27648),
-                                   (1024, 5120, 5120), (256, 4608, 3584)])
+                                   (1024, 5120, 5120), (256, 4608, 3584), (256, 5120, 27648), (200, 55296, 5120)])
 def test_attached_weights_take_the_pair_kernel_above_256_tokens(M, N, K):
     """With an attached fp16 copy of the weights, INT8 batches above 256 tokens
-    run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944 and,
-    by the planner's time model, at 1024 x 5120 x 27648; at 1024 x 5120 x 5120
-    76 of the 80 tiles run whole and the last 4 split, reduced by their own
-    kernel -- raw int32 sums through qurl_w8a8_gemm_acc too) and
-    give the bits of the TMEM-weight kernel that runs without it, and of the
-    oracle on a sample; at 256 tokens the TMEM-weight kernel keeps the call."""
+    run on the CTA-pair kernel (ragged M; K split at 264 x 3584 x 18944; at
+    1024 x 5120 x 5120 and 1024 x 5120 x 27648 76 of the 80 tiles run whole and
+    the last 4 split, reduced by their own kernel -- raw int32 sums through
+    qurl_w8a8_gemm_acc too), and so do batches of 129 to 256 tokens on weights
+    of 2^26 codes or more (one token tile, partly empty); all give the bits of
+    the TMEM-weight kernel that runs without the copy, and of the oracle on a
+    sample.  At 256 tokens on smaller weights the TMEM-weight kernel keeps the
+    call."""
+    big = M > 128 and N * K >= (1 << 26)
+    assert q.plan(M, N, K, q.INT8, sms(), attached=True)["kernel"] == (4 if (M > 256 or big) else 1)
     X = synth.activations(f"gpu/i8w/mid/X/{M}", M, K).cuda()
     W = synth.weights(f"gpu/i8w/mid/W/{N}", N, K).cuda()
     Wq, sw, _, _ = q.prepare_weights(W, q.INT8, s=1.5, keep_scaled=False)

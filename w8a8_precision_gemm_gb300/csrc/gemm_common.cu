@@ -129,13 +129,22 @@ bool plan_nvfp4(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail, 
 }
 
 // INT8 whose weights' fp16 copy the caller keeps (qurl_widen_weights): the
-// CTA-pair kernel above kAttachedMinM tokens.  It reads 2 bytes a weight, so
-// up to there the TMEM-weight kernel, which streams the 1-byte codes, is
-// faster (32B-class qkv / o_proj at M = 256: 31 / 30 us against 44 / 42 us);
-// above it the pair kernel's full-rate 256 x 256 tiles win (M = 1024: qkv 69
+// CTA-pair kernel above kAttachedMinM tokens, and from kAttachedBigMinM tokens
+// for weights of at least kAttachedBigCodes codes.  It reads 2 bytes a weight,
+// so for the smaller projections at up to 256 tokens the TMEM-weight kernel,
+// which streams the 1-byte codes, is faster (32B-class qkv / o_proj at
+// M = 256: 28.5 / 27.8 us against 35.4 / 32.9; 7B qkv 23.5 against 27.3);
+// for the large ones the pair kernel's full-rate 256 x 256 tiles win even half
+// empty (M = 256: 32B gate_up 109.6 against 125.9, down 79.8 against 88.5, 7B
+// gate_up 59.5 against 65.6, down 53.4 against 54.2; gate_up at M = 160 105.8
+// against 126.3), and above 256 tokens for every projection (M = 1024: qkv 69
 // -> 64 us, o_proj 68 -> 63, down 285 -> 273).
+constexpr int kAttachedBigMinM = 129;
+constexpr long long kAttachedBigCodes = 1LL << 26;
+
 bool plan_attached(GemmPlan& p, int M, int N, int K, int num_sms, size_t ws_avail) {
-  if (M <= kAttachedMinM || ws_avail < kSyncBytes) return false;
+  const bool big = M >= kAttachedBigMinM && static_cast<long long>(N) * K >= kAttachedBigCodes;
+  if ((M <= kAttachedMinM && !big) || ws_avail < kSyncBytes) return false;
   if (!plan_wide(p, M, N, K, num_sms, ws_avail - kSyncBytes, true)) return false;
   p.ws_bytes += kSyncBytes;
   return true;
