@@ -325,6 +325,16 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
   a.qn = p.wide ? qn : nullptr;
   a.scratch = (p.wide || p.tmem_a) ? reinterpret_cast<int*>(wsb + p.scratch_off) : nullptr;
   a.whole_units = p.whole_units;
+  // FP8 prefill pairs whose activations do not fit in L2 beside the weights
+  // (more than 48 MB of codes): token groups of about 48 MB of activation tiles
+  // (256 rows x K codes), at most 16 tiles.  32B down at M = 8192 (226 MB of
+  // activations, groups of 7): 655 us a call against 698, DRAM reads 1.76 GB
+  // against 2.55; smaller activations keep token tile fastest over all
+  // (o_proj at M = 8192, 42 MB: 127.0 us against 128.8 grouped)
+  const bool big_act = static_cast<long long>(M) * K > (48LL << 20);
+  a.tok_group = (p.pair && !p.swap && !p.wide && !p.tmem_a && big_act)
+                    ? std::max(1, std::min(16, static_cast<int>((48LL << 20) / (256LL * K))))
+                    : 0;
   if (fq) {
     a.fq = *fq;
     a.fsums = fsums;
@@ -348,7 +358,7 @@ qurl_status run_gemm(const void* Xq, const float* sx, const void* Wq, const floa
     r.tiles_ch = p.tiles_ch;
     r.splits = p.splits;
     r.part = part;
-    QURL_CUDA(qurl::launch_tail_reduce(int8, !p.wide, r, st));
+    QURL_CUDA(qurl::launch_tail_reduce(int8, p.wide ? qurl::kWideTokGroup : a.tok_group, r, st));
   } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qt, part, p.splits, M, N, sx, sw, Y, ldy, Y ? nullptr : acc_out,
                                          dev->num_sms, st));
@@ -419,7 +429,7 @@ qurl_status run_nvfp4(const void* q4x, const void* sbx, const float* gx, const v
     r.tiles_ch = p.tiles_ch;
     r.splits = p.splits;
     r.part = wsb + p.x16_bytes;
-    QURL_CUDA(qurl::launch_tail_reduce(false, false, r, st));
+    QURL_CUDA(qurl::launch_tail_reduce(false, qurl::kWideTokGroup, r, st));
   } else if (split) {
     QURL_CUDA(qurl::launch_splitk_reduce(qurl::kQFp8, wsb + p.x16_bytes, p.splits, M, N, gx, gw, Y, ldy,
                                          Y ? nullptr : acc, dev->num_sms, st));

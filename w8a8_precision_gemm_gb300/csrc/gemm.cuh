@@ -45,6 +45,21 @@ namespace qurl {
 // One work unit of a persistent GEMM CTA: a 128 x BN accumulator tile over
 // one K split.  Units are numbered token tile fastest, so CTAs running at the
 // same time share weight tiles (L2 reuse when there are several token tiles).
+// Tile v's coordinates in the unit order of the CTA-pair prefill kernels:
+// groups of `group` token tiles, then channel tiles, token tile fastest -- the
+// pairs running together cover a few channel tiles of one token group, so a
+// channel tile's weights are read from HBM once per token group and the
+// group's activations stay in L2 while its channel tiles go by.  Only the last
+// group can be short; group >= tiles_tok is token tile fastest over all.
+__host__ __device__ __forceinline__ void group_tile(int tiles_tok, int tiles_ch, int group, int v, int& tok,
+                                                    int& ch) {
+  const int gi = v / (group * tiles_ch);
+  const int gs = min(group, tiles_tok - gi * group);
+  const int r = v - gi * group * tiles_ch;
+  ch = r / gs;
+  tok = gi * group + (r - ch * gs);
+}
+
 struct Unit {
   int a0, b0;    // first row of the A tile / of the B tile
   int kb0, nkb;  // k-block range

@@ -56,10 +56,11 @@ struct Fp8PairBarriers {
 // This CTA's part of unit u: A rows a0 .. a0 + 127 (rank r takes the r-th
 // half of the pair's 256), B columns b0 .. b0 + BN - 1 of the output, of which
 // it stages rows b0 + r BN / 2 ...  Prefill: A = tokens, B = channels;
-// SWAP: A = channels, B = tokens.  Tiles are numbered token tile fastest; the
-// first whole_units units (prefill only) are tiles 0 .. whole_units - 1 over
-// all of K (split -1), the remaining tiles are split `splits` ways, split
-// slowest (with whole_units = 0 every tile is split).
+// SWAP: A = channels, B = tokens.  Tiles are numbered token tile fastest
+// (prefill: within groups of tok_group token tiles, group_tile); the first
+// whole_units units (prefill only) are tiles 0 .. whole_units - 1 over all of
+// K (split -1), the remaining tiles are split `splits` ways, split slowest
+// (with whole_units = 0 every tile is split).
 struct PairUnit {
   int a0, b0, kb0, nkb, split;
 };
@@ -76,8 +77,13 @@ __device__ __forceinline__ PairUnit pair_unit(const GemmArgs& a, int u, uint32_t
     sp = w / tail;
     v = a.whole_units + (w - sp * tail);
   }
-  const int tok = v % a.tiles_tok;
-  const int ch = v / a.tiles_tok;
+  int tok, ch;
+  if (SWAP) {
+    tok = v % a.tiles_tok;
+    ch = v / a.tiles_tok;
+  } else {
+    group_tile(a.tiles_tok, a.tiles_ch, a.tok_group > 0 ? a.tok_group : a.tiles_tok, v, tok, ch);
+  }
   PairUnit w;
   w.a0 = (SWAP ? ch : tok) * 256 + static_cast<int>(rank) * 128;
   w.b0 = (SWAP ? tok : ch) * BN;

@@ -72,22 +72,6 @@ struct I8wBarriers {
   uint32_t tmem_base;
 };
 
-// Token tiles per group of the unit order below.
-constexpr int kI8wTokGroup = 16;
-
-// Tile v's coordinates in the unit order: groups of kI8wTokGroup token tiles,
-// then channel tiles, token tile fastest -- the pairs running together cover a
-// few channel tiles of one token group, so a channel tile's weights are read
-// from HBM once per token group and the group's activations (16 x 256 rows)
-// stay in L2 while its channel tiles go by.
-__host__ __device__ __forceinline__ void i8w_tile(int tiles_tok, int tiles_ch, int v, int& tok, int& ch) {
-  const int gi = v / (kI8wTokGroup * tiles_ch);  // only the last group can be short
-  const int gs = min(kI8wTokGroup, tiles_tok - gi * kI8wTokGroup);
-  const int r = v - gi * kI8wTokGroup * tiles_ch;
-  ch = r / gs;
-  tok = gi * kI8wTokGroup + (r - ch * gs);
-}
-
 // Unit u: the first whole_units units are tiles 0 .. whole_units - 1 over all
 // of K (sp = -1); the remaining tiles are split `splits` ways, split slowest
 // (so the pieces of one tile run on different pairs at the same time).  With
@@ -107,7 +91,7 @@ __device__ __forceinline__ UnitCoords i8w_coords(const GemmArgs& a, int u) {
     c.sp = w / tail;
     v = a.whole_units + (w - c.sp * tail);
   }
-  i8w_tile(a.tiles_tok, a.tiles_ch, v, c.tok, c.ch);
+  group_tile(a.tiles_tok, a.tiles_ch, kWideTokGroup, v, c.tok, c.ch);
   return c;
 }
 
@@ -500,7 +484,7 @@ __device__ __forceinline__ void add_bits(float& s, uint32_t b) { s += __uint_as_
 template <typename T>
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ part, int splits, int M, int N,
                                                           int tiles_tok, int tiles_ch, int whole_units,
-                                                          bool tok_fastest, const float* __restrict__ sx,
+                                                          int tok_group, const float* __restrict__ sx,
                                                           const float* __restrict__ sw,
                                                           __nv_bfloat16* __restrict__ Y, long long ldy,
                                                           T* __restrict__ acc_out) {
@@ -508,12 +492,7 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const T* __restrict__ 
   griddep_launch_dependents();
   const int v = whole_units + static_cast<int>(blockIdx.x >> 6);  // the tail tile
   int tok, ch;
-  if (tok_fastest) {
-    tok = v % tiles_tok;
-    ch = v / tiles_tok;
-  } else {
-    i8w_tile(tiles_tok, tiles_ch, v, tok, ch);
-  }
+  group_tile(tiles_tok, tiles_ch, tok_group, v, tok, ch);
   const int m = tok * 256 + static_cast<int>(blockIdx.x & 63) * 4 + static_cast<int>(threadIdx.x >> 6);
   const int n = ch * 256 + static_cast<int>(threadIdx.x & 63) * 4;
   if (m >= M || n >= N) return;
@@ -604,16 +583,17 @@ cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, co
                          tx16, tw16, args);
 }
 
-cudaError_t launch_tail_reduce(bool int_partials, bool tok_fastest, const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_tail_reduce(bool int_partials, int tok_group, const GemmArgs& a, cudaStream_t st) {
   const long long tail = static_cast<long long>(a.tiles_tok) * a.tiles_ch - a.whole_units;
   if (tail <= 0) return cudaSuccess;
+  if (tok_group <= 0) tok_group = a.tiles_tok;
   const dim3 grid(static_cast<unsigned>(tail * 64));
   if (int_partials)
     return launch_pdl(tail_reduce_kernel<int>, grid, dim3(256), 0, st, reinterpret_cast<const int*>(a.part), a.splits,
-                      a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_fastest, a.sx, a.sw, a.Y, a.ldy,
+                      a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_group, a.sx, a.sw, a.Y, a.ldy,
                       reinterpret_cast<int*>(a.acc_out));
   return launch_pdl(tail_reduce_kernel<float>, grid, dim3(256), 0, st, reinterpret_cast<const float*>(a.part),
-                    a.splits, a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_fastest, a.sx, a.sw, a.Y, a.ldy,
+                    a.splits, a.M, a.N, a.tiles_tok, a.tiles_ch, a.whole_units, tok_group, a.sx, a.sw, a.Y, a.ldy,
                     reinterpret_cast<float*>(a.acc_out));
 }
 

@@ -20,6 +20,8 @@ constexpr int kDevBadIndex = 1;  // QURL_ERR_INVALID_ARG: an index read on the d
 constexpr int kQInt8 = 0;  // QURL_INT8
 constexpr int kQFp8 = 1;   // QURL_FP8_E4M3
 
+// Token tiles per group of the INT8 CTA-pair prefill kernel's tile order.
+constexpr int kWideTokGroup = 16;
 constexpr int kModeBf16 = 0;  // GEMM epilogue dequantizes and writes Y
 constexpr int kModeAcc = 1;   // GEMM writes the raw accumulator of its split to part
 
@@ -86,6 +88,7 @@ struct GemmArgs {
                          // one fp32 pass, fp32 partials
   int whole_units;       // CTA-pair prefill kernels: the first whole_units tiles (in their unit order) run
                          // over all of K as single units, only the rest are split `splits` ways (0: all)
+  int tok_group;         // FP8 CTA-pair prefill: token tiles per group of its tile order (group_tile)
 };
 
 // Number of kernels this library has launched in the process (api.cu).
@@ -238,9 +241,9 @@ cudaError_t launch_i8_to_f16(const void* src, void* dst, int M, int K, CodeSums 
 cudaError_t launch_gemm_i8w(const CUtensorMap& tx16, const CUtensorMap& tw16, const GemmArgs& a, dim3 grid,
                             cudaStream_t st);
 // The reduction of a hybrid plan's split tail: the tiles after the first whole_units (in the CTA-pair
-// kernel's tile order: the INT8 prefill kernel's token groups, or token tile fastest for the FP8 pair
-// kernel) sum their s partials in split order and apply the epilogue (or write acc_out).
-cudaError_t launch_tail_reduce(bool int_partials, bool tok_fastest, const GemmArgs& a, cudaStream_t st);
+// kernels' tile order, groups of tok_group token tiles: group_tile in gemm.cuh) sum their s partials
+// in split order and apply the epilogue (or write acc_out).
+cudaError_t launch_tail_reduce(bool int_partials, int tok_group, const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_widen_weights(const void* Wq, int N, int K, void* w16, unsigned* qn, int num_sms,
                                  cudaStream_t st);
 // the CTAs an i8w launch of this plan runs (one per SM of the resident pairs), for sizing its scratch
