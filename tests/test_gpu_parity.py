@@ -559,14 +559,17 @@ def test_gemm_acc_fp8(M, N, K):
     assert float((err / (absref + 1e-30)).max()) < 1e-4
 
 
-@pytest.mark.parametrize("M,N,K", [(1024, 5120, 27648), (1000, 5000, 12288)])
+@pytest.mark.parametrize("M,N,K", [(1024, 5120, 27648), (1000, 5000, 12288), (2048, 5120, 27648)])
 def test_fp8_pair_whole_units_and_split_tail(M, N, K):
     """FP8 prefill on CTA pairs with 80 tiles on 76 pairs: 76 tiles run over
     all of K and write their results themselves, the last 4 (the last channel
     tile of every token tile; ragged in both at 1000 x 5000) are split 18 and
-    16 ways and reduced by their own kernel.  Raw accumulators (sampled,
-    against the oracle within the fp32 summation bound) and the bf16 linear
-    (bits of the accumulators through the epilogue the oracle applies)."""
+    16 ways and reduced by their own kernel; at 2048 x 5120 x 27648 (160
+    tiles: 152 whole, 8 split) the 56 MB of activations also put the tiles in
+    groups of 7 token tiles (the last group short).  Raw accumulators
+    (sampled, against the oracle within the fp32 summation bound) and the bf16
+    linear (bits of the accumulators through the epilogue the oracle
+    applies)."""
     xq = random_codes(q.FP8_E4M3, (M, K), M * 5 + K)
     wq = random_codes(q.FP8_E4M3, (N, K), N * 3 + K)
     ws = q.workspace(M, N, K, q.FP8_E4M3)
