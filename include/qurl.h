@@ -148,9 +148,10 @@ qurl_status qurl_silu_mul_quant(const void* GU, int M, int I, int ldgu, float pr
  * activation codes (2 M K bytes) with per-token sums of |code| over each K
  * split, the int32 running sums of units accumulated in chunks (one region
  * per SM), and from 2048 tokens on an fp16 copy of the weight codes (2 N K
- * bytes) with their per-channel sums of squares; above 256 tokens also enough
- * for the plan that reads an attached fp16 weight copy (qurl_widen_weights)
- * instead.  The last 256 bytes of any
+ * bytes) with their per-channel sums of squares; above 256 tokens (and from
+ * 129 tokens for weights of 2^26 codes or more) also enough for the plan that
+ * reads an attached fp16 weight copy (qurl_widen_weights) instead.  The last
+ * 256 bytes of any
  * workspace hold two counters through which the CTAs of a fused decode call
  * hand over (see the fused entries): they must be zero before the
  * workspace's first use by a fused entry, and every call leaves them zero.
@@ -291,9 +292,10 @@ qurl_status qurl_count_diff(const void* a, const void* b, size_t n, unsigned lon
  * freeing Wq or `wide` (the table is keyed by Wq's address and shape, so a
  * later matrix allocated at that address would otherwise inherit the copy).
  * Up to 1024 matrices are attached at a time (more: the call returns
- * QURL_ERR_UNSUPPORTED).  With a copy attached, INT8 calls above 256 tokens
- * run on the CTA-pair kernel that reads it (qurl_workspace_size covers that
- * plan); outputs are bit-identical either way.  Attaching or detaching must
+ * QURL_ERR_UNSUPPORTED).  With a copy attached, INT8 calls above 256 tokens,
+ * and from 129 tokens on weights of 2^26 codes or more, run on the CTA-pair
+ * kernel that reads it (qurl_workspace_size covers that plan); outputs are
+ * bit-identical either way.  Attaching or detaching must
  * not run concurrently with calls on the same Wq.
  * Errors: INVALID_ARG (NULL, a non-positive size), UNSUPPORTED (K % 16, table
  * full), ALIGNMENT.  One kernel launch.
